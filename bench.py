@@ -1,0 +1,445 @@
+"""MoE block-verify benchmark on GB300: per-layer us and achieved HBM GB/s vs the
+block size k, and the verify/decode latency ratio.
+
+Workload (one "step"): a block of k=16 positions verified through 40 MoE layers
+of the Qwen3-A3B-like shape (d=2048, 128 experts, top-8, d_ff=768, bf16, SwiGLU,
+independent seeded weights per layer, 48 GB in HBM), each layer called through
+the C ABI (router + top-8 + woken union + grouped expert FFN + combine).  The
+40 distinct weight sets are far larger than L2, so no step reads weights from
+L2.  `value` = algorithmic HBM bytes (woken experts x expert bytes + router
+bytes, summed over the layers) / device time, in GB/s.
+
+Also reported: the k=1 decode pass (verify/decode ratio against the woken-byte
+ratio), a k=1..16 sweep for repeated-token and independent blocks, the 40-layer
+pre-norm residual stack with greedy acceptance on logits[17, 151936], per-kernel
+roofline of the dominant kernel, an end-to-end number through the host-buffer
+entry point, and the CPU oracle on a bounded sample.
+
+python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "MoE block-verify layer µs and HBM GB/s (% of roofline) vs k; verify/decode ratio"
+N_LAYERS = 40
+KBLOCK = 16
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return PEAKS_FALLBACK, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.05)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- reference arm (CPU oracle)
+
+
+def oracle_layer_sample(n_threads: int, budget_s: float, k: int = KBLOCK, min_calls: int = 1, max_calls: int = 8):
+    """Time the CPU oracle on config-2 layers at block k: returns (GB/s, calls, seconds, threads)."""
+    import oracle
+    from speculative_decoding_moe_gb300 import inputs
+    from tests._util import np_of, oracle_layer
+    oracle.build()
+    total_bytes, total_s, calls = 0.0, 0.0, 0
+    while calls < max_calls and (calls < min_calls or total_s < budget_s):
+        lw = inputs.make_layer(inputs.A3B, seed=9000 + calls)
+        ol = oracle_layer(lw)
+        x = np_of(inputs.make_hidden(k, inputs.A3B.d, "bf16", seed=9100 + calls))
+        _, idx, _ = oracle.route(ol, x)
+        W = len(oracle.woken(idx, inputs.A3B.n_experts)[0])
+        t0 = time.perf_counter()
+        oracle.moe_forward(ol, x, nthreads=n_threads)
+        total_s += time.perf_counter() - t0
+        total_bytes += W * lw.expert_bytes() + lw.router_bytes()
+        calls += 1
+    return total_bytes / total_s / 1e9, calls, total_s
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from speculative_decoding_moe_gb300 import inputs
+    from tests._util import np_of, oracle_layer
+    oracle.build()
+    nthr = host_threads()
+    lw = inputs.make_layer(inputs.A3B, seed=9000)
+    ol = oracle_layer(lw)
+    x = np_of(inputs.make_hidden(KBLOCK, inputs.A3B.d, "bf16", seed=9100))
+    _, idx, _ = oracle.route(ol, x)
+    W = len(oracle.woken(idx, inputs.A3B.n_experts)[0])
+    step_bytes = W * lw.expert_bytes() + lw.router_bytes()
+    for _ in range(args.warmup):
+        oracle.moe_forward(ol, x, nthreads=nthr)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.moe_forward(ol, x, nthreads=nthr)
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = step_bytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": nthr, "kind": "oracle",
+                         "sample": "one Qwen3-A3B-like layer (d=2048, E=128, top-8, d_ff=768, bf16 weights) at k=16 "
+                                   "per step, W=%d woken experts, oracle moe_forward on %d host threads" % (W, nthr)},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config():
+    return {"workload": "qwen3-a3b-like MoE layer x %d (d=2048, E=128, top-8, d_ff=768, bf16, SwiGLU), "
+                        "k=16 verify block" % N_LAYERS,
+            "d": 2048, "n_experts": 128, "top_k": 8, "d_ff": 768, "k": KBLOCK, "layers_per_step": N_LAYERS,
+            "weights_gb": None,
+            "l2": "inputs larger than L2: 40 distinct layer weight sets (48 GB), each step streams every woken "
+                  "expert from HBM"}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+
+def graph_time(fn, warmup: int, steps: int, barrier=None, sampler=None):
+    """Capture one step into a CUDA graph, replay `warmup` untimed then `steps`
+    timed replays bracketed by CUDA events; returns ms per step."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        a.record()
+        for _ in range(steps):
+            g.replay()
+        b.record()
+        b.synchronize()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return a.elapsed_time(b) / steps
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def stream_time(fn, warmup: int, steps: int):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_gpu(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+        def barrier():
+            dist.barrier()
+    else:
+        barrier = None
+
+    from speculative_decoding_moe_gb300 import build as bld
+    bld.build()
+    from speculative_decoding_moe_gb300 import dfv, inputs
+
+    peaks, peak_kind = load_peaks()
+    shape = inputs.A3B
+    t_gen = time.time()
+    layers = [inputs.make_layer(shape, seed=1000 * rank + l, device=dev) for l in range(N_LAYERS)]
+    torch.cuda.synchronize()
+    t_gen = time.time() - t_gen
+    Ls = [dfv.Layer(w) for w in layers]
+    exp_bytes = layers[0].expert_bytes()
+    router_bytes = layers[0].router_bytes()
+    ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], KBLOCK), device=dev)
+
+    def make_pass(k, mode="independent", seed=5):
+        x = inputs.make_hidden(k, shape.d, "bf16", seed=seed + 100 * rank, mode=mode, device=dev)
+        out = torch.empty_like(x)
+        nws = torch.zeros(N_LAYERS, dtype=torch.int32, device=dev)
+
+        def fn():
+            for l in range(N_LAYERS):
+                dfv.moe_block_forward(Ls[l], x, ws, out=out, n_woken=nws[l:l + 1])
+        return fn, nws
+
+    def pass_bytes(nws):
+        W = nws.to(torch.int64).cpu()
+        return float(W.sum().item() * exp_bytes + N_LAYERS * router_bytes), W
+
+    # ---- headline: k=16 verify pass over 40 layers (CUDA graph replay)
+    fn16, nw16 = make_pass(KBLOCK)
+    sampler = ClockSampler(local)
+    ms16 = graph_time(fn16, args.warmup, args.steps, barrier, sampler)
+    clocks = sampler.summary()
+    bytes16, W16 = pass_bytes(nw16)
+    ms_max = ms16
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms16], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * bytes16 / (ms_max * 1e-3) / 1e9
+
+    # ---- decode: k=1 pass, same layers
+    fn1, nw1 = make_pass(1, seed=6)
+    ms1 = graph_time(fn1, args.warmup, args.steps, barrier)
+    bytes1, W1 = pass_bytes(nw1)
+
+    # ---- stream-launch numbers (no graph) for context
+    ms16_stream = stream_time(fn16, 2, max(3, args.steps // 4))
+    ms1_stream = stream_time(fn1, 2, max(3, args.steps // 4))
+
+    # ---- per-kernel timing with CUDA events (dominant kernel = gate/up)
+    x16 = inputs.make_hidden(KBLOCK, shape.d, "bf16", seed=5 + 100 * rank, device=dev)
+    out16 = torch.empty_like(x16)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(N_LAYERS)]
+    reps = 3
+    t_router = t_gate = t_down = 0.0
+    for r in range(reps + 1):
+        for l in range(N_LAYERS):
+            dfv.profile_set_events(evs[l])
+            dfv.moe_block_forward(Ls[l], x16, ws, out=out16)
+        dfv.profile_set_events(None)
+        torch.cuda.synchronize()
+        if r == 0:
+            continue
+        for l in range(N_LAYERS):
+            e = evs[l]
+            t_router += e[0].elapsed_time(e[1])
+            t_gate += e[1].elapsed_time(e[2])
+            t_down += e[2].elapsed_time(e[3])
+    n_launch = reps * N_LAYERS
+    gate_bytes = float(W16.sum().item()) * (2 * shape.d_ff * shape.d * 2) / N_LAYERS  # per launch
+    down_bytes = float(W16.sum().item()) * (shape.d * shape.d_ff * 2) / N_LAYERS
+    gate_ms = t_gate / n_launch
+    down_ms = t_down / n_launch
+    router_ms = t_router / n_launch
+    gate_gbs = gate_bytes / (gate_ms * 1e-3) / 1e9
+    peak_bw = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    roofline = {"bound": "hbm", "kernel": "gateup_bf16_kernel<2> (k=16)", "achieved": gate_gbs, "peak": peak_bw,
+                "unit": "GB/s", "frac": gate_gbs / peak_bw, "traffic": None,
+                "peak_kind": peak_kind + " (STREAM-style copy, burst)",
+                "per_launch_us": {"router": router_ms * 1e3, "gate_up": gate_ms * 1e3, "down_combine": down_ms * 1e3},
+                "down_achieved_gbs": down_bytes / (down_ms * 1e-3) / 1e9,
+                "algorithmic_bytes_per_launch": {"gate_up": gate_bytes, "down": down_bytes}}
+
+    # ---- k sweep (repeated-token vs independent blocks)
+    sweep = {}
+    if not args.no_sweep:
+        for mode in ("repeated", "independent"):
+            rows = []
+            for k in range(1, 17):
+                fnk, nwk = make_pass(k, mode=mode, seed=50 + k)
+                msk = graph_time(fnk, 2, max(3, args.steps // 4))
+                bk, Wk = pass_bytes(nwk)
+                rows.append({"k": k, "woken_mean": float(Wk.double().mean().item()),
+                             "layer_us": msk * 1e3 / N_LAYERS, "gbs": bk / (msk * 1e-3) / 1e9})
+            sweep[mode] = rows
+
+    # ---- 40-layer pre-norm residual stack + greedy acceptance (one verify cycle)
+    stack = None
+    if not args.no_stack:
+        V = 151936
+        xs0 = inputs.make_hidden(KBLOCK, shape.d, "bf16", seed=7 + 100 * rank, device=dev)
+        xs = xs0.clone()
+        logits, toks = inputs.spiked_logits(KBLOCK + 1, V, "bf16", 2.0, seed=8, device=dev)
+        nacc = 5
+        draft = toks[:KBLOCK].clone()
+        draft[nacc] = (draft[nacc] + 1) % V
+        aws = dfv.alloc_workspace(dfv.accept_workspace_size(KBLOCK, V), device=dev)
+        tau = torch.zeros(1, dtype=torch.int32, device=dev)
+        com = torch.zeros(KBLOCK + 1, dtype=torch.int32, device=dev)
+
+        def fn_stack():
+            xs.copy_(xs0)
+            dfv.moe_stack_forward(Ls, xs, ws)
+            dfv.accept_greedy(logits, draft, aws, tau=tau, committed=com)
+
+        ms_stack = graph_time(fn_stack, 2, max(3, args.steps // 4))
+        stack = {"ms": ms_stack, "layer_us": ms_stack * 1e3 / N_LAYERS, "tau": int(tau.item()),
+                 "tau_expected": nacc + 1, "finite": bool(torch.isfinite(xs.float()).all().item())}
+
+    # ---- end to end through the host-buffer entry point (plain stream launches)
+    hx = x16.cpu().pin_memory()
+    ho = torch.empty_like(hx).pin_memory()
+
+    def fn_e2e():
+        for l in range(N_LAYERS):
+            dfv.moe_block_forward_host(Ls[l], hx, ho, ws)
+        _ = None
+
+    e2e_ms = stream_time(fn_e2e, 2, max(3, args.steps // 2))
+    e2e = {"value": world * bytes16 / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": N_LAYERS * hx.numel() * hx.element_size(),
+           "d2h_bytes_per_step": N_LAYERS * ho.numel() * ho.element_size(), "ms_per_step": e2e_ms,
+           "api": "dfv_moe_block_forward_host per layer, pinned host buffers"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        nthr = host_threads()
+        gbs, calls, secs = oracle_layer_sample(nthr, budget_s=args.cpu_budget)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": nthr, "kind": "oracle",
+               "sample": "%d Qwen3-A3B-like layer call(s) at k=16 (oracle moe_forward, fp64, %d threads, %.1f s)"
+                         % (calls, nthr, secs)}
+
+    ratio = ms16 / ms1
+    byte_ratio = bytes16 / bytes1
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and hidden rows)",
+        "config": dict(workload_config(), weights_gb=round(N_LAYERS * (exp_bytes * 128 + router_bytes) / 1e9, 2)),
+        "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS,
+                     "k16_stream": ms16_stream * 1e3 / N_LAYERS, "k1_stream": ms1_stream * 1e3 / N_LAYERS},
+        "frac_of_hbm_peak": {"measured": value / world / peak_bw, "nominal_8tbs": value / world / 8000.0},
+        "woken_mean": {"k16": float(W16.double().mean().item()), "k1": float(W1.double().mean().item())},
+        "verify_decode": {"latency_ratio": ratio, "woken_byte_ratio": byte_ratio,
+                          "quotient": byte_ratio / ratio},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 3 * N_LAYERS * args.steps, "clocks": clocks,
+        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dfv", choices=["dfv", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

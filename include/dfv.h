@@ -1,0 +1,205 @@
+/*
+ * dfv.h -- C ABI of the GB300 (sm_103a) MoE block-verify library, libdfv.so.
+ *
+ * The target model's verify step in DFlash-style speculative decoding over a
+ * Mixture-of-Experts model: a block of k drafted positions goes through each
+ * MoE layer together, and greedy acceptance turns the target's logits into the
+ * committed length tau.
+ *
+ * Sources (page titles and sections of the method's write-ups):
+ *   "Speculating on a Strix Halo", section "Speculative decoding": the target
+ *       checks the whole draft in one pass; under greedy decoding it accepts
+ *       only tokens it would have produced itself; a cycle commits the accepted
+ *       draft prefix plus one token of the target's own (tau).
+ *   same page, section "What the pieces cost": each token of the block routes
+ *       to its own experts, so the block wakes the union of its rows' experts;
+ *       reference 1 (model card): 8 routed experts of 256.
+ *   same page, section "The verify's own cost": tokens are sorted by expert
+ *       and each projection runs as one grouped launch.
+ *   "Speculating on a Strix Halo (part 2)", section "The verification cog":
+ *       the verifier is the base model run over the draft; expert weight
+ *       streaming is what makes verify cost more than decode.
+ *   same page, section "Why drafter performance doesn't really matter": the
+ *       n-th drafted token is accepted only if the n-1 before it were.
+ *   the MI355X / vLLM write-up (allbreaknews.com/?p=4397), sections "Why
+ *       Quantize the Target Model on Top?" and "Results: Quantizing the Target
+ *       Model": mxfp4 target weights, used natively, never re-materialised.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named in the signatures are DEVICE pointers, owned by the
+ *     caller, unless a comment says "host".  Tensors are row-major and
+ *     contiguous.  Every pointer must be 16-byte aligned; the workspace
+ *     256-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on it and returns; nothing is synchronised and
+ *     nothing is allocated.  Arguments are validated on the host before any
+ *     launch; on a non-zero status nothing was enqueued (except DFV_ERR_CUDA,
+ *     where a launch itself failed).
+ *   - Workspaces are caller-owned device memory of at least the size the
+ *     matching *_workspace_size() reports.  A workspace must be ZERO-FILLED
+ *     before its first use (e.g. cudaMemset); every call leaves it zero-ready
+ *     for the next one.  Calls that share a workspace must be ordered (same
+ *     stream, or synchronised): concurrent use races.
+ *   - Returns DFV_OK (0) or a DFV_ERR_* status; dfv_status_string() names it
+ *     and dfv_last_error_detail() gives the last failure's detail text
+ *     (thread-local).
+ */
+#ifndef DFV_H
+#define DFV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFV_VERSION 1
+
+enum {
+  DFV_OK = 0,
+  DFV_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, size out of range  */
+  DFV_ERR_UNSUPPORTED = 2,  /* dtype combination or shape not supported   */
+  DFV_ERR_WORKSPACE = 3,    /* workspace too small or misaligned          */
+  DFV_ERR_CUDA = 4          /* a CUDA launch or copy failed               */
+};
+
+typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2 } dfv_dtype;
+
+/* Limits of this implementation. */
+#define DFV_MAX_BLOCK 16      /* k: positions in one verify block          */
+#define DFV_MAX_EXPERTS 256   /* E                                          */
+#define DFV_MAX_TOPK 8        /* K                                          */
+
+/*
+ * One MoE layer.  All weights are caller-owned device memory.
+ *   w_router  [E, d]            router weights, r_dtype (F32 or BF16)
+ *   w_gate    [E, d_ff, d]      gate projection of every expert
+ *   w_up      [E, d_ff, d]      up projection
+ *   w_down    [E, d, d_ff]      down projection
+ * For w_dtype = DFV_MXFP4 the three expert matrices hold packed E2M1 codes,
+ * two per byte, low nibble = even column ([E, d_ff, d/2], [E, d, d_ff/2]
+ * bytes), and s_gate/s_up/s_down hold one E8M0 scale byte per 32 consecutive
+ * elements of a row ([E, d_ff, d/32], [E, d_ff, d/32], [E, d, d_ff/32]);
+ * element value = e2m1(code) * 2^(scale - 127).  Scale 255 (NaN) is not
+ * supported.  For F32/BF16 weights the scale pointers are ignored.
+ * norm_topk: 1 renormalises the K selected routing weights to sum 1
+ * (w_s = p_s / sum p), 0 keeps the softmax probabilities p_s.
+ * Supported combinations (w_dtype, r_dtype, activations):
+ *   (BF16, BF16, BF16), (MXFP4, BF16, BF16), (F32, F32, F32).
+ * Shapes: 1 <= K <= min(E, 8), E <= 256, d % 32 == 0, d_ff % 32 == 0
+ * (MXFP4: d % 64 == 0 and d_ff % 64 == 0).
+ */
+typedef struct dfv_moe_layer {
+  int d, n_experts, top_k, d_ff, norm_topk;
+  int w_dtype; /* dfv_dtype of the expert weights */
+  int r_dtype; /* dfv_dtype of the router weights */
+  const void *w_router;
+  const void *w_gate, *w_up, *w_down;
+  const uint8_t *s_gate, *s_up, *s_down;
+} dfv_moe_layer;
+
+/* Bytes of workspace dfv_route_topk / dfv_moe_block_forward /
+ * dfv_moe_stack_forward need for blocks of up to k_max positions
+ * (0 on invalid arguments). */
+size_t dfv_moe_workspace_size(const dfv_moe_layer *layer, int k_max);
+
+/*
+ * Router of one layer for a block of k positions ("What the pieces cost":
+ * each token routes to its own experts; the block wakes their union).
+ *   hidden    [k, d] activations (act = BF16 or F32, matching the layer)
+ * Outputs (device, caller-owned; any may be NULL except n_woken):
+ *   topk_idx  [k, K] int32   experts of each row, by descending router logit,
+ *                            equal logits ordered by lower expert index
+ *   topk_w    [k, K] fp32    routing weights (softmax over all E logits,
+ *                            renormalised over the K when norm_topk)
+ *   woken     [min(E, k*K)]  int32, ascending ids of the woken experts
+ *   n_woken   [1]  int32     W, the number of woken experts
+ *   offsets   [W + 1] int32  exclusive prefix sum of per-expert pair counts
+ *   gather    [k*K] int32    flat pair ids t*K+s ordered by (expert, t)
+ * Logits are fp32 dot products of the given operands; selection compares
+ * those fp32 values exactly.
+ */
+int dfv_route_topk(const dfv_moe_layer *layer, const void *hidden, int act, int k,
+                   int32_t *topk_idx, float *topk_w, int32_t *woken, int32_t *n_woken,
+                   int32_t *offsets, int32_t *gather, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Routed expert output of one MoE layer for a block of k positions: router,
+ * top-K, woken-expert union and per-expert token gather, SwiGLU expert FFN
+ *   y = W_down (silu(W_gate x) * (W_up x)),  silu(z) = z / (1 + e^-z),
+ * and the routing-weighted combine out[t] = sum_s w[t,s] y_{idx[t,s]}(x[t]),
+ * summed in slot order ("What the pieces cost"; "The verify's own cost").
+ * The residual and any shared expert are not included.
+ *   hidden  [k, d] act   input rows
+ *   out     [k, d] act   routed output (bf16 or fp32, same dtype as hidden)
+ *   opt_topk_idx [k, K] int32 and opt_n_woken [1] int32: optional copies of
+ *           the routing decision (NULL to skip).
+ * Accumulation is fp32.  Each weight byte of a woken expert is read from HBM
+ * once per call; experts no row selected are not read.
+ */
+int dfv_moe_block_forward(const dfv_moe_layer *layer, const void *hidden, int act, int k,
+                          void *out, int32_t *opt_topk_idx, int32_t *opt_n_woken,
+                          void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Same as dfv_moe_block_forward, but `hidden_host` and `out_host` are HOST
+ * buffers (pinned memory gives asynchronous copies).  The call enqueues the
+ * host->device copy of hidden into the workspace, the layer, and the
+ * device->host copy of out; the caller synchronises the stream before reading
+ * out_host.  The workspace must be sized with dfv_moe_workspace_size.
+ */
+int dfv_moe_block_forward_host(const dfv_moe_layer *layer, const void *hidden_host, int act, int k,
+                               void *out_host, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Pre-norm residual stack of MoE layers over a bf16 residual stream, in place:
+ *   n_l     = bf16(x_l / sqrt(mean(x_l^2) + eps))      (RMSNorm, unit gain)
+ *   x_{l+1} = bf16(x_l + MoE_l(n_l))                    (one rounding)
+ *   layers  host array of n_layers layer descriptors (BF16 or MXFP4 experts,
+ *           BF16 router), all with the same d
+ *   x       [k, d] bf16 device buffer, input and output
+ */
+int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, int k, float eps,
+                          void *ws, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace dfv_accept_greedy needs for up to k_max drafted tokens
+ * over a vocabulary of V (0 on invalid arguments). */
+size_t dfv_accept_workspace_size(int k_max, int V);
+
+/*
+ * Greedy acceptance ("Speculative decoding": the target accepts only tokens it
+ * would have produced itself and commits the accepted prefix plus one token of
+ * its own; part 2, "Why drafter performance doesn't really matter": the n-th
+ * draft is accepted only if the n-1 before it were).
+ *   logits    [k+1, V] (BF16 or F32) target logits at the k+1 positions
+ *   draft     [k] int32 drafted tokens, 0 <= k <= 16
+ *   a[i]      = argmax_v logits[i, v], equal values to the lowest v
+ *               (+0 and -0 compare equal; logits must not be NaN)
+ *   n         = largest j <= k with draft[i] == a[i] for all i < j
+ *   tau       [1] int32  = n + 1
+ *   committed [k+1] int32 or NULL: a[0..n], then -1
+ */
+int dfv_accept_greedy(const void *logits, int dtype, int k, int V, const int32_t *draft,
+                      int32_t *tau, int32_t *committed, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Profiling hook (no counterpart on the method's pages; used to time each
+ * kernel of the layer with CUDA events).  With a non-NULL array of 4
+ * cudaEvent_t handles, every later layer call made from this host thread
+ * records events[0] before the router launch, events[1] after it, events[2]
+ * after the gate/up launch and events[3] after the down/combine launch, on the
+ * call's stream.  NULL turns it off.  The events are caller-owned; recording
+ * them between launches keeps the launches in stream order but removes the
+ * overlap of one kernel's start with the previous kernel's tail.
+ */
+int dfv_profile_set_events(void *const *events, int n_events);
+
+const char *dfv_status_string(int status);
+const char *dfv_last_error_detail(void);
+int dfv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFV_H */

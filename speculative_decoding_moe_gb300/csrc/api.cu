@@ -1,0 +1,323 @@
+// api.cu -- the C ABI of libdfv.so: argument validation, workspace layout and
+// launch order.  Every entry point validates on the host, then only enqueues
+// kernels (and, for the host-buffer variant, copies) on the caller's stream.
+#include <mutex>
+#include <map>
+#include <string>
+#include <tuple>
+#include <cstdarg>
+#include <cstdio>
+
+#include "dfv_internal.cuh"
+
+namespace {
+
+thread_local std::string g_detail;
+thread_local cudaEvent_t g_events[4];
+thread_local bool g_profile = false;
+
+inline void mark(int i, cudaStream_t s) {
+  if (g_profile) cudaEventRecord(g_events[i], s);
+}
+
+int fail(int status, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+  return fail(DFV_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t act_size(int act) { return act == DFV_BF16 ? 2 : 4; }
+
+// Workspace sections, in order; base == nullptr only measures.
+dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
+  dfv::Workspace w = {};
+  const size_t E = L->n_experts, K = L->top_k, d = L->d, I = L->d_ff, km = k_max;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void * {
+    void *p = base ? (void *)((char *)base + off) : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  w.logits = (float *)take(km * E * 4);
+  w.topk_idx = (int32_t *)take(km * K * 4);
+  w.topk_w = (float *)take(km * K * 4);
+  w.woken = (int32_t *)take(E * 4);
+  w.n_woken = (int32_t *)take(4);
+  w.offsets = (int32_t *)take((E + 1) * 4);
+  w.gather = (int32_t *)take(km * K * 4);
+  w.router_cnt = (unsigned *)take(4);
+  w.down_cnt = (unsigned *)take(((d + dfv::kDownTile - 1) / dfv::kDownTile) * 4);
+  w.xn = take(km * d * 4);
+  w.h = (float *)take(km * K * I * 4);
+  w.ys = (float *)take(km * K * d * 4);
+  w.xio = take(km * d * 4);
+  w.oio = take(km * d * 4);
+  w.bytes = off;
+  return w;
+}
+
+int check_layer(const dfv_moe_layer *L, int act) {
+  if (!L) return fail(DFV_ERR_INVALID_ARG, "layer is NULL");
+  if (L->d <= 0 || L->n_experts <= 0 || L->top_k <= 0 || L->d_ff <= 0)
+    return fail(DFV_ERR_INVALID_ARG, "non-positive layer size");
+  if (L->n_experts > DFV_MAX_EXPERTS) return fail(DFV_ERR_UNSUPPORTED, "n_experts %d > %d", L->n_experts, DFV_MAX_EXPERTS);
+  if (L->top_k > DFV_MAX_TOPK || L->top_k > L->n_experts)
+    return fail(DFV_ERR_UNSUPPORTED, "top_k %d outside 1..min(E, %d)", L->top_k, DFV_MAX_TOPK);
+  if (L->d % 32 || L->d_ff % 32) return fail(DFV_ERR_UNSUPPORTED, "d and d_ff must be multiples of 32");
+  const bool ok = (L->w_dtype == DFV_BF16 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
+                  (L->w_dtype == DFV_F32 && L->r_dtype == DFV_F32 && act == DFV_F32);
+  if (!ok)
+    return fail(DFV_ERR_UNSUPPORTED, "unsupported dtype combination (experts %d, router %d, act %d)", L->w_dtype,
+                L->r_dtype, act);
+  if (!L->w_router || !L->w_gate || !L->w_up || !L->w_down) return fail(DFV_ERR_INVALID_ARG, "NULL weight pointer");
+  if (!aligned(L->w_router, 16) || !aligned(L->w_gate, 16) || !aligned(L->w_up, 16) || !aligned(L->w_down, 16))
+    return fail(DFV_ERR_INVALID_ARG, "weight pointers must be 16-byte aligned");
+  return DFV_OK;
+}
+
+int check_ws(const dfv_moe_layer *L, int k, void *ws, size_t ws_bytes) {
+  if (!ws) return fail(DFV_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(DFV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  const size_t need = layout(L, k, nullptr).bytes;
+  if (ws_bytes < need) return fail(DFV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  return DFV_OK;
+}
+
+// Occupancy-limited persistent grid sizes, cached per (dtype, k<=8, d, I, which).
+int grid_limit(int w_dtype, int k, int d, int I, int which) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int, int>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto key = std::make_tuple(dev, w_dtype, k <= 8 ? 1 : 2, d, I, which);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int g = dfv::ffn_grid_limit(w_dtype, k, d, I, which);
+  if (g > 0) cache[key] = g;
+  return g;
+}
+
+dfv::RouterParams router_params(const dfv_moe_layer *L, const void *x, int act, int k, const dfv::Workspace &w) {
+  dfv::RouterParams p = {};
+  p.x = x;
+  p.wr = L->w_router;
+  p.k = k;
+  p.d = L->d;
+  p.E = L->n_experts;
+  p.K = L->top_k;
+  p.norm_topk = L->norm_topk ? 1 : 0;
+  p.act = act;
+  p.rdt = L->r_dtype;
+  p.ws = w;
+  return p;
+}
+
+int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, const void *residual,
+              bool fuse_norm, float eps, int32_t *u_idx, int32_t *u_nw, const dfv::Workspace &w, cudaStream_t s) {
+  dfv::RouterParams rp = router_params(L, x, act, k, w);
+  rp.fuse_norm = fuse_norm ? 1 : 0;
+  rp.eps = eps;
+  rp.u_idx = u_idx;
+  rp.u_nw = u_nw;
+  mark(0, s);
+  cudaError_t e = dfv::launch_router(rp, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
+  mark(1, s);
+
+  dfv::FfnParams fp = {};
+  fp.x = fuse_norm ? w.xn : x;
+  fp.wg = L->w_gate;
+  fp.wu = L->w_up;
+  fp.wd = L->w_down;
+  fp.sg = L->s_gate;
+  fp.su = L->s_up;
+  fp.sd = L->s_down;
+  fp.residual = residual;
+  fp.out = out;
+  fp.k = k;
+  fp.d = L->d;
+  fp.I = L->d_ff;
+  fp.E = L->n_experts;
+  fp.K = L->top_k;
+  fp.act = act;
+  fp.swz_x = (L->d % 64 == 0) ? 4 : 0;
+  fp.swz_h = (L->d_ff % 64 == 0) ? 4 : 0;
+  fp.ws = w;
+  const int maxW = L->n_experts < k * L->top_k ? L->n_experts : k * L->top_k;
+  const int units_g = maxW * (L->d_ff / dfv::kGateTile);
+  const int units_d = maxW * ((L->d + dfv::kDownTile - 1) / dfv::kDownTile);
+  const int lim_g = grid_limit(L->w_dtype, k, L->d, L->d_ff, 0);
+  const int lim_d = grid_limit(L->w_dtype, k, L->d, L->d_ff, 1);
+  if (lim_g <= 0 || lim_d <= 0) return fail(DFV_ERR_CUDA, "expert FFN kernels cannot be resident (occupancy 0)");
+  const int gg = units_g < lim_g ? units_g : lim_g;
+  const int gd = units_d < lim_d ? units_d : lim_d;
+  e = dfv::launch_ffn_phase(fp, L->w_dtype, 0, gg, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
+  mark(2, s);
+  e = dfv::launch_ffn_phase(fp, L->w_dtype, 1, gd, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "expert down/combine launch");
+  mark(3, s);
+  return DFV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dfv_version(void) { return DFV_VERSION; }
+
+const char *dfv_status_string(int status) {
+  switch (status) {
+    case DFV_OK: return "DFV_OK";
+    case DFV_ERR_INVALID_ARG: return "DFV_ERR_INVALID_ARG";
+    case DFV_ERR_UNSUPPORTED: return "DFV_ERR_UNSUPPORTED";
+    case DFV_ERR_WORKSPACE: return "DFV_ERR_WORKSPACE";
+    case DFV_ERR_CUDA: return "DFV_ERR_CUDA";
+    default: return "DFV_ERR_UNKNOWN";
+  }
+}
+
+const char *dfv_last_error_detail(void) { return g_detail.c_str(); }
+
+int dfv_profile_set_events(void *const *events, int n_events) {
+  if (!events) {
+    g_profile = false;
+    return DFV_OK;
+  }
+  if (n_events < 4) return fail(DFV_ERR_INVALID_ARG, "need 4 events, got %d", n_events);
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return fail(DFV_ERR_INVALID_ARG, "event %d is NULL", i);
+    g_events[i] = (cudaEvent_t)events[i];
+  }
+  g_profile = true;
+  return DFV_OK;
+}
+
+size_t dfv_moe_workspace_size(const dfv_moe_layer *layer, int k_max) {
+  if (!layer || k_max < 1 || k_max > DFV_MAX_BLOCK || layer->n_experts <= 0 || layer->top_k <= 0 ||
+      layer->d <= 0 || layer->d_ff <= 0)
+    return 0;
+  return layout(layer, k_max, nullptr).bytes;
+}
+
+int dfv_route_topk(const dfv_moe_layer *layer, const void *hidden, int act, int k, int32_t *topk_idx,
+                   float *topk_w, int32_t *woken, int32_t *n_woken, int32_t *offsets, int32_t *gather, void *ws,
+                   size_t ws_bytes, void *stream) {
+  int st = check_layer(layer, act);
+  if (st) return st;
+  if (k < 1 || k > DFV_MAX_BLOCK) return fail(DFV_ERR_INVALID_ARG, "k=%d outside 1..%d", k, DFV_MAX_BLOCK);
+  if (!hidden || !aligned(hidden, 16)) return fail(DFV_ERR_INVALID_ARG, "hidden NULL or not 16-byte aligned");
+  if (!n_woken) return fail(DFV_ERR_INVALID_ARG, "n_woken is NULL");
+  if ((st = check_ws(layer, k, ws, ws_bytes))) return st;
+  const dfv::Workspace w = layout(layer, k, ws);
+  dfv::RouterParams rp = router_params(layer, hidden, act, k, w);
+  rp.u_idx = topk_idx;
+  rp.u_w = topk_w;
+  rp.u_woken = woken;
+  rp.u_nw = n_woken;
+  rp.u_offs = offsets;
+  rp.u_gather = gather;
+  cudaError_t e = dfv::launch_router(rp, (cudaStream_t)stream, true);
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
+  return DFV_OK;
+}
+
+int dfv_moe_block_forward(const dfv_moe_layer *layer, const void *hidden, int act, int k, void *out,
+                          int32_t *opt_topk_idx, int32_t *opt_n_woken, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_layer(layer, act);
+  if (st) return st;
+  if (k < 1 || k > DFV_MAX_BLOCK) return fail(DFV_ERR_INVALID_ARG, "k=%d outside 1..%d", k, DFV_MAX_BLOCK);
+  if (!hidden || !out || !aligned(hidden, 16) || !aligned(out, 16))
+    return fail(DFV_ERR_INVALID_ARG, "hidden/out NULL or not 16-byte aligned");
+  if ((st = check_ws(layer, k, ws, ws_bytes))) return st;
+  const dfv::Workspace w = layout(layer, k, ws);
+  return run_layer(layer, hidden, act, k, out, nullptr, false, 0.f, opt_topk_idx, opt_n_woken, w,
+                   (cudaStream_t)stream);
+}
+
+int dfv_moe_block_forward_host(const dfv_moe_layer *layer, const void *hidden_host, int act, int k, void *out_host,
+                               void *ws, size_t ws_bytes, void *stream) {
+  int st = check_layer(layer, act);
+  if (st) return st;
+  if (k < 1 || k > DFV_MAX_BLOCK) return fail(DFV_ERR_INVALID_ARG, "k=%d outside 1..%d", k, DFV_MAX_BLOCK);
+  if (!hidden_host || !out_host) return fail(DFV_ERR_INVALID_ARG, "host buffers must not be NULL");
+  if ((st = check_ws(layer, k, ws, ws_bytes))) return st;
+  const dfv::Workspace w = layout(layer, k, ws);
+  const size_t bytes = (size_t)k * layer->d * act_size(act);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(w.xio, hidden_host, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "host->device copy of hidden");
+  if ((st = run_layer(layer, w.xio, act, k, w.oio, nullptr, false, 0.f, nullptr, nullptr, w, s))) return st;
+  e = cudaMemcpyAsync(out_host, w.oio, bytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "device->host copy of out");
+  return DFV_OK;
+}
+
+int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, int k, float eps, void *ws,
+                          size_t ws_bytes, void *stream) {
+  if (!layers || n_layers < 1) return fail(DFV_ERR_INVALID_ARG, "no layers");
+  if (k < 1 || k > DFV_MAX_BLOCK) return fail(DFV_ERR_INVALID_ARG, "k=%d outside 1..%d", k, DFV_MAX_BLOCK);
+  if (!x || !aligned(x, 16)) return fail(DFV_ERR_INVALID_ARG, "x NULL or not 16-byte aligned");
+  if (!(eps >= 0.f)) return fail(DFV_ERR_INVALID_ARG, "eps must be >= 0");
+  for (int l = 0; l < n_layers; ++l) {
+    int st = check_layer(&layers[l], DFV_BF16);
+    if (st) return fail(st, "layer %d: %s", l, g_detail.c_str());
+    if (layers[l].d != layers[0].d) return fail(DFV_ERR_INVALID_ARG, "layer %d: d differs from layer 0", l);
+    if ((st = check_ws(&layers[l], k, ws, ws_bytes))) return fail(st, "layer %d: %s", l, g_detail.c_str());
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const dfv::Workspace w = layout(&layers[l], k, ws);
+    int st = run_layer(&layers[l], x, DFV_BF16, k, x, x, true, eps, nullptr, nullptr, w, (cudaStream_t)stream);
+    if (st) return st;
+  }
+  return DFV_OK;
+}
+
+size_t dfv_accept_workspace_size(int k_max, int V) {
+  if (k_max < 0 || k_max > DFV_MAX_BLOCK || V < 1) return 0;
+  return align256(sizeof(unsigned)) + align256((size_t)(k_max + 1) * 304 * 8);
+}
+
+int dfv_accept_greedy(const void *logits, int dtype, int k, int V, const int32_t *draft, int32_t *tau,
+                      int32_t *committed, void *ws, size_t ws_bytes, void *stream) {
+  if (k < 0 || k > DFV_MAX_BLOCK) return fail(DFV_ERR_INVALID_ARG, "k=%d outside 0..%d", k, DFV_MAX_BLOCK);
+  if (V < 1) return fail(DFV_ERR_INVALID_ARG, "V=%d < 1", V);
+  if (dtype != DFV_BF16 && dtype != DFV_F32) return fail(DFV_ERR_UNSUPPORTED, "logits dtype %d", dtype);
+  if (!logits || !aligned(logits, 16) || !tau || (k > 0 && !draft))
+    return fail(DFV_ERR_INVALID_ARG, "logits/tau/draft NULL or logits not 16-byte aligned");
+  if (!ws || !aligned(ws, 256)) return fail(DFV_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < dfv_accept_workspace_size(k, V))
+    return fail(DFV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, dfv_accept_workspace_size(k, V));
+  dfv::AcceptParams p = {};
+  p.logits = logits;
+  p.draft = draft;
+  p.tau = tau;
+  p.committed = committed;
+  p.k = k;
+  p.V = V;
+  p.dtype = dtype;
+  int chunks = (304 + k) / (k + 1);  // about two CTAs per SM in total
+  const int maxc = (V + 1023) / 1024;
+  if (chunks > maxc) chunks = maxc;
+  if (chunks < 1) chunks = 1;
+  p.chunks = chunks;
+  p.cnt = (unsigned *)ws;
+  p.partial = (unsigned long long *)((char *)ws + align256(sizeof(unsigned)));
+  cudaError_t e = dfv::launch_accept(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "accept launch");
+  return DFV_OK;
+}
+
+}  // extern "C"

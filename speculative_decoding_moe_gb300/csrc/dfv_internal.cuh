@@ -1,0 +1,148 @@
+// dfv_internal.cuh -- device helpers, kernel parameter blocks and the
+// workspace layout shared by the kernels of libdfv.so (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dfv.h"
+
+namespace dfv {
+
+constexpr int kMaxBlock = DFV_MAX_BLOCK;
+constexpr int kMaxExperts = DFV_MAX_EXPERTS;
+constexpr int kMaxTopK = DFV_MAX_TOPK;
+constexpr int kDownTile = 64;   // d-rows per down-projection unit (4 warps x 16)
+constexpr int kGateTile = 8;    // d_ff rows per gate/up unit (8 gate + 8 up = one m16 tile)
+
+// ---------------------------------------------------------------- workspace
+// Every section is 256-byte aligned.  Counters must start at zero; the kernel
+// that uses a counter returns it to zero.
+struct Workspace {
+  float *logits;      // [k_max][E]
+  int32_t *topk_idx;  // [k_max][K]
+  float *topk_w;      // [k_max][K]
+  int32_t *woken;     // [E]
+  int32_t *n_woken;   // [1]
+  int32_t *offsets;   // [E + 1]
+  int32_t *gather;    // [k_max * K]   pair ids t*K+s sorted by (expert, t)
+  unsigned *router_cnt;  // [1]
+  unsigned *down_cnt;    // [ceil(d / kDownTile)]
+  void *xn;           // [k_max][d] activations staged for the expert FFN (act dtype)
+  float *h;           // [k_max * K][d_ff]  SwiGLU activations, by sorted pair position
+  float *ys;          // [k_max * K][d]     weighted expert outputs, by pair id
+  void *xio;          // [k_max][d] host-variant input staging (4-byte elements)
+  void *oio;          // [k_max][d] host-variant output staging
+  size_t bytes;
+};
+
+// ---------------------------------------------------------------- parameters
+struct RouterParams {
+  const void *x;        // [k][d] act (input rows; when norm: residual stream)
+  const void *wr;       // [E][d]
+  int k, d, E, K, norm_topk, act, rdt;
+  int fuse_norm;        // 1: route RMSNorm(x) rounded to act, and stage it in ws.xn
+  int stage_x;          // 1: copy x into ws.xn (block 0) for the FFN kernels
+  float eps;
+  Workspace ws;
+  // optional user copies of the routing decision
+  int32_t *u_idx;
+  float *u_w;
+  int32_t *u_woken, *u_nw, *u_offs, *u_gather;
+};
+
+struct FfnParams {
+  const void *x;        // [k][d] rows the experts see (bf16 / f32)
+  const void *wg, *wu, *wd;
+  const uint8_t *sg, *su, *sd;
+  const void *residual; // [k][d] or null: added in the combine
+  void *out;            // [k][d] act dtype
+  int k, d, I, E, K, act;
+  int swz_x;            // XOR swizzle mask for staged x rows (0 or 4)
+  int swz_h;            // XOR swizzle mask for staged h rows (0 or 4)
+  Workspace ws;
+};
+
+struct AcceptParams {
+  const void *logits;   // [k+1][V]
+  const int32_t *draft; // [k]
+  int32_t *tau, *committed;
+  int k, V, dtype, chunks;  // chunks: CTAs per row
+  unsigned long long *partial;  // [(k+1) * chunks]
+  unsigned *cnt;                // [1]
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// 128-bit streaming load through the non-coherent path, not kept in L1.
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D += A * B with fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Load element i of an activation row (bf16 or f32) as float.
+__device__ __forceinline__ float load_act(const void *p, size_t i, int act) {
+  if (act == DFV_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+  return reinterpret_cast<const float *>(p)[i];
+}
+
+__device__ __forceinline__ void store_act(void *p, size_t i, int act, float v) {
+  if (act == DFV_BF16)
+    reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float *>(p)[i] = v;
+}
+
+// Monotone unsigned key of a float: a < b  <=>  key(a) < key(b), with -0 == +0.
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) == 0) u = 0;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace dfv
+
+// Launch entry points implemented in the .cu files (host side).
+namespace dfv {
+cudaError_t launch_router(const RouterParams &p, cudaStream_t s, bool pdl);
+// phase 0: gate/up, phase 1: down + combine
+cudaError_t launch_ffn_phase(const FfnParams &p, int w_dtype, int phase, int grid, cudaStream_t s, bool pdl);
+int ffn_grid_limit(int w_dtype, int k, int d, int I, int which);
+cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);
+}  // namespace dfv

@@ -1,0 +1,200 @@
+"""Python binding of libdfv.so (ctypes).  Argument marshalling only: every step
+of the block-verify path runs in the library's CUDA kernels.  Tensors must be
+CUDA tensors; calls enqueue work on torch's current CUDA stream."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from .inputs import LayerWeights
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdfv.so")
+
+F32, BF16, MXFP4 = 0, 1, 2
+_NAMES = {"f32": F32, "bf16": BF16, "mxfp4": MXFP4}
+EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_profile_set_events",
+           "dfv_moe_workspace_size",
+           "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
+           "dfv_accept_workspace_size", "dfv_accept_greedy")
+
+
+class DfvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _load()
+        super().__init__("%s: %s: %s" % (where, lib.dfv_status_string(status).decode(),
+                                         lib.dfv_last_error_detail().decode()))
+        self.status = status
+
+
+class CLayer(ctypes.Structure):
+    _fields_ = [
+        ("d", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+        ("d_ff", ctypes.c_int), ("norm_topk", ctypes.c_int),
+        ("w_dtype", ctypes.c_int), ("r_dtype", ctypes.c_int),
+        ("w_router", ctypes.c_void_p), ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+        ("w_down", ctypes.c_void_p), ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p),
+        ("s_down", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libdfv.so is not built (%s); run speculative_decoding_moe_gb300.build.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.dfv_version.restype = I
+        L.dfv_status_string.restype = ctypes.c_char_p
+        L.dfv_status_string.argtypes = [I]
+        L.dfv_last_error_detail.restype = ctypes.c_char_p
+        L.dfv_moe_workspace_size.restype = S
+        L.dfv_moe_workspace_size.argtypes = [P, I]
+        L.dfv_route_topk.argtypes = [P, P, I, I, P, P, P, P, P, P, P, S, P]
+        L.dfv_moe_block_forward.argtypes = [P, P, I, I, P, P, P, P, S, P]
+        L.dfv_moe_block_forward_host.argtypes = [P, P, I, I, P, P, S, P]
+        L.dfv_moe_stack_forward.argtypes = [P, I, P, I, ctypes.c_float, P, S, P]
+        L.dfv_accept_workspace_size.restype = S
+        L.dfv_accept_workspace_size.argtypes = [I, I]
+        L.dfv_accept_greedy.argtypes = [P, I, I, I, P, P, P, P, S, P]
+        L.dfv_profile_set_events.argtypes = [P, I]
+        _lib = L
+    return _lib
+
+
+def lib():
+    return _load()
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _act(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("activations must be bf16 or fp32, got %s" % t.dtype)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise DfvError(status, where)
+
+
+class Layer:
+    """A layer descriptor over device-resident weights (keeps them alive)."""
+
+    def __init__(self, w: LayerWeights):
+        for t in (w.w_router, w.w_gate, w.w_up, w.w_down):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("layer weights must be contiguous CUDA tensors")
+        s = w.shape
+        self.w = w
+        self.shape = s
+        self.c = CLayer(s.d, s.n_experts, s.top_k, s.d_ff, s.norm_topk, _NAMES[s.w_dtype], _NAMES[s.r_dtype],
+                        w.w_router.data_ptr(), w.w_gate.data_ptr(), w.w_up.data_ptr(), w.w_down.data_ptr(),
+                        None if w.s_gate is None else w.s_gate.data_ptr(),
+                        None if w.s_up is None else w.s_up.data_ptr(),
+                        None if w.s_down is None else w.s_down.data_ptr())
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def workspace_size(layer: Layer, k_max: int) -> int:
+    return int(_load().dfv_moe_workspace_size(layer.ref, int(k_max)))
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace (the library requires zeros before first use)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def route_topk(layer: Layer, hidden: torch.Tensor, ws: torch.Tensor, stream=None):
+    k = hidden.shape[0]
+    s = layer.shape
+    dev = hidden.device
+    idx = torch.empty(k, s.top_k, dtype=torch.int32, device=dev)
+    w = torch.empty(k, s.top_k, dtype=torch.float32, device=dev)
+    woken = torch.empty(min(s.n_experts, k * s.top_k), dtype=torch.int32, device=dev)
+    nw = torch.empty(1, dtype=torch.int32, device=dev)
+    offs = torch.empty(min(s.n_experts, k * s.top_k) + 1, dtype=torch.int32, device=dev)
+    gat = torch.empty(k * s.top_k, dtype=torch.int32, device=dev)
+    st = _load().dfv_route_topk(layer.ref, _p(hidden), _act(hidden), k, _p(idx), _p(w), _p(woken), _p(nw), _p(offs),
+                                _p(gat), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dfv_route_topk")
+    return dict(topk_idx=idx, topk_w=w, woken=woken, n_woken=nw, offsets=offs, gather=gat)
+
+
+def moe_block_forward(layer: Layer, hidden: torch.Tensor, ws: torch.Tensor, out: Optional[torch.Tensor] = None,
+                      topk_idx: Optional[torch.Tensor] = None, n_woken: Optional[torch.Tensor] = None, stream=None):
+    k = hidden.shape[0]
+    if out is None:
+        out = torch.empty_like(hidden)
+    st = _load().dfv_moe_block_forward(layer.ref, _p(hidden), _act(hidden), k, _p(out), _p(topk_idx), _p(n_woken),
+                                       _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dfv_moe_block_forward")
+    return out
+
+
+def moe_block_forward_host(layer: Layer, hidden_host: torch.Tensor, out_host: torch.Tensor, ws: torch.Tensor,
+                           stream=None):
+    """hidden_host / out_host: CPU tensors (pinned for asynchronous copies)."""
+    k = hidden_host.shape[0]
+    st = _load().dfv_moe_block_forward_host(layer.ref, _p(hidden_host), _act(hidden_host), k, _p(out_host), _p(ws),
+                                            ws.numel(), _stream(stream))
+    _check(st, "dfv_moe_block_forward_host")
+    return out_host
+
+
+def moe_stack_forward(layers: Sequence[Layer], x: torch.Tensor, ws: torch.Tensor, eps: float = 1e-6, stream=None):
+    arr = (CLayer * len(layers))(*[L.c for L in layers])
+    st = _load().dfv_moe_stack_forward(arr, len(layers), _p(x), x.shape[0], float(eps), _p(ws), ws.numel(),
+                                       _stream(stream))
+    _check(st, "dfv_moe_stack_forward")
+    return x
+
+
+def accept_workspace_size(k_max: int, V: int) -> int:
+    return int(_load().dfv_accept_workspace_size(int(k_max), int(V)))
+
+
+def accept_greedy(logits: torch.Tensor, draft: torch.Tensor, ws: torch.Tensor, tau: Optional[torch.Tensor] = None,
+                  committed: Optional[torch.Tensor] = None, stream=None):
+    rows, V = logits.shape
+    k = rows - 1
+    dev = logits.device
+    if tau is None:
+        tau = torch.empty(1, dtype=torch.int32, device=dev)
+    if committed is None:
+        committed = torch.empty(k + 1, dtype=torch.int32, device=dev)
+    st = _load().dfv_accept_greedy(_p(logits), _act(logits), k, V, _p(draft), _p(tau), _p(committed), _p(ws),
+                                   ws.numel(), _stream(stream))
+    _check(st, "dfv_accept_greedy")
+    return tau, committed
+
+
+def profile_set_events(events: Optional[Sequence[torch.cuda.Event]]):
+    """Record the 4 phase-boundary events in later layer calls (None: off)."""
+    if events is None:
+        _check(_load().dfv_profile_set_events(None, 0), "dfv_profile_set_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(_load().dfv_profile_set_events(arr, len(events)), "dfv_profile_set_events")
