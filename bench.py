@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 METRIC = "MoE block-verify layer µs and HBM GB/s (% of roofline) vs k; verify/decode ratio"
-N_LAYERS = 40
+N_LAYERS = 40   # layers per step (--layers overrides, for profiling runs only)
 KBLOCK = 16
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
@@ -433,7 +433,10 @@ def main():
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=40, help="layers per step (profiling runs only)")
     args = ap.parse_args()
+    global N_LAYERS
+    N_LAYERS = args.layers
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -38,8 +38,10 @@
  *   - Workspaces are caller-owned device memory of at least the size the
  *     matching *_workspace_size() reports.  A workspace must be ZERO-FILLED
  *     before its first use (e.g. cudaMemset); every call leaves it zero-ready
- *     for the next one.  Calls that share a workspace must be ordered (same
- *     stream, or synchronised): concurrent use races.
+ *     for the next one (the counters that must start at zero live at fixed
+ *     offsets, so one workspace serves any k and, for d <= 61440, any layer).
+ *     Calls that share a workspace must be ordered (same stream, or
+ *     synchronised): concurrent use races.
  *   - Returns DFV_OK (0) or a DFV_ERR_* status; dfv_status_string() names it
  *     and dfv_last_error_detail() gives the last failure's detail text
  *     (thread-local).

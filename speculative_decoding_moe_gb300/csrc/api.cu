@@ -49,6 +49,14 @@ dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
     off += align256(bytes);
     return p;
   };
+  // counters first: their offsets depend only on d, never on the call's k, so
+  // calls with different block sizes sharing one workspace see the same zeroed
+  // counters
+  w.router_cnt = (unsigned *)take(4);
+  // a fixed 4 KB holds the counters of any d <= 61440, so layers of different
+  // widths may share a workspace too
+  const size_t tiles = (d + dfv::kDownTile - 1) / dfv::kDownTile;
+  w.down_cnt = (unsigned *)take(tiles * 4 > 3840 ? tiles * 4 : 3840);
   w.logits = (float *)take(km * E * 4);
   w.topk_idx = (int32_t *)take(km * K * 4);
   w.topk_w = (float *)take(km * K * 4);
@@ -56,8 +64,6 @@ dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
   w.n_woken = (int32_t *)take(4);
   w.offsets = (int32_t *)take((E + 1) * 4);
   w.gather = (int32_t *)take(km * K * 4);
-  w.router_cnt = (unsigned *)take(4);
-  w.down_cnt = (unsigned *)take(((d + dfv::kDownTile - 1) / dfv::kDownTile) * 4);
   w.xn = take(km * d * 4);
   w.h = (float *)take(km * K * I * 4);
   w.ys = (float *)take(km * K * d * 4);

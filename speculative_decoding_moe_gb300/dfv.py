@@ -196,5 +196,8 @@ def profile_set_events(events: Optional[Sequence[torch.cuda.Event]]):
     if events is None:
         _check(_load().dfv_profile_set_events(None, 0), "dfv_profile_set_events")
         return
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event on first record
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(_load().dfv_profile_set_events(arr, len(events)), "dfv_profile_set_events")
