@@ -68,6 +68,14 @@ enum {
 
 typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2 } dfv_dtype;
 
+/* Device-side error bits a kernel may set in the workspace (see
+ * dfv_read_device_error).  Every wait inside a kernel is bounded; a wait that
+ * runs out sets one of these bits and the kernel returns early (its outputs
+ * are then invalid). */
+#define DFV_DEVERR_STAGE_WAIT 0x1u   /* a consumer gave up waiting for a weight tile */
+#define DFV_DEVERR_SLOT_WAIT 0x2u    /* the producer gave up waiting for a free stage */
+#define DFV_DEVERR_DRAIN_WAIT 0x4u   /* copies still in flight at exit after a timeout */
+
 /* Limits of this implementation. */
 #define DFV_MAX_BLOCK 16      /* k: positions in one verify block          */
 #define DFV_MAX_EXPERTS 256   /* E                                          */
@@ -125,6 +133,16 @@ size_t dfv_moe_workspace_size(const dfv_moe_layer *layer, int k_max);
 int dfv_route_topk(const dfv_moe_layer *layer, const void *hidden, int act, int k,
                    int32_t *topk_idx, float *topk_w, int32_t *woken, int32_t *n_woken,
                    int32_t *offsets, int32_t *gather, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Enqueue a copy of the workspace's device error word (DFV_DEVERR_* bits, 0 =
+ * no error) to host memory `err_host` on `stream`; read it after the stream
+ * has synchronised.  The bits are sticky: after a non-zero word the outputs of
+ * the calls since the workspace was zero-filled are invalid, and the
+ * workspace must be zero-filled again before reuse.  (No counterpart on the
+ * method's pages: the bounded waits of the TMA-staged kernels report here.)
+ */
+int dfv_read_device_error(const void *ws, uint32_t *err_host, void *stream);
 
 /*
  * Routed expert output of one MoE layer for a block of k positions: router,

@@ -49,14 +49,13 @@ dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
     off += align256(bytes);
     return p;
   };
-  // counters first: their offsets depend only on d, never on the call's k, so
-  // calls with different block sizes sharing one workspace see the same zeroed
-  // counters
+  // counters and the error word first, at offsets that depend on nothing but d
+  // (a fixed 4 KB for d <= 14336): calls of any k, and layers of any width in
+  // that range, can share a workspace
   w.router_cnt = (unsigned *)take(4);
-  // a fixed 4 KB holds the counters of any d <= 61440, so layers of different
-  // widths may share a workspace too
-  const size_t tiles = (d + dfv::kDownTile - 1) / dfv::kDownTile;
-  w.down_cnt = (unsigned *)take(tiles * 4 > 3840 ? tiles * 4 : 3840);
+  w.err = (unsigned *)take(4);
+  const size_t tiles = (d + 15) / 16;
+  w.down_cnt = (unsigned *)take(tiles * 4 > 3584 ? tiles * 4 : 3584);
   w.logits = (float *)take(km * E * 4);
   w.topk_idx = (int32_t *)take(km * K * 4);
   w.topk_w = (float *)take(km * K * 4);
@@ -115,6 +114,20 @@ int grid_limit(int w_dtype, int k, int d, int I, int which) {
   return g;
 }
 
+int sm_count() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev] = n;
+  return n;
+}
+
 dfv::RouterParams router_params(const dfv_moe_layer *L, const void *x, int act, int k, const dfv::Workspace &w) {
   dfv::RouterParams p = {};
   p.x = x;
@@ -162,6 +175,21 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
   fp.swz_h = (L->d_ff % 64 == 0) ? 4 : 0;
   fp.ws = w;
   const int maxW = L->n_experts < k * L->top_k ? L->n_experts : k * L->top_k;
+  dfv::TmaPlan plan;
+  if (dfv::tma_plan(L->w_dtype, k, L->d, L->d_ff, &plan)) {
+    // TMA-staged kernels: one persistent CTA per SM
+    const int sms = sm_count();
+    if (sms <= 0) return fail(DFV_ERR_CUDA, "cannot query the SM count");
+    const int units_g = maxW * (L->d_ff / dfv::kGateTile);
+    const int units_d = maxW * ((L->d + plan.rs - 1) / plan.rs);
+    e = dfv::launch_ffn_tma(fp, L->w_dtype, 0, plan, units_g < sms ? units_g : sms, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
+    mark(2, s);
+    e = dfv::launch_ffn_tma(fp, L->w_dtype, 1, plan, units_d < sms ? units_d : sms, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "expert down/combine launch");
+    mark(3, s);
+    return DFV_OK;
+  }
   const int units_g = maxW * (L->d_ff / dfv::kGateTile);
   const int units_d = maxW * ((L->d + dfv::kDownTile - 1) / dfv::kDownTile);
   const int lim_g = grid_limit(L->w_dtype, k, L->d, L->d_ff, 0);
@@ -288,6 +316,15 @@ int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, in
     int st = run_layer(&layers[l], x, DFV_BF16, k, x, x, true, eps, nullptr, nullptr, w, (cudaStream_t)stream);
     if (st) return st;
   }
+  return DFV_OK;
+}
+
+int dfv_read_device_error(const void *ws, uint32_t *err_host, void *stream) {
+  if (!ws || !err_host) return fail(DFV_ERR_INVALID_ARG, "ws and err_host must not be NULL");
+  if (!aligned(ws, 256)) return fail(DFV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaError_t e = cudaMemcpyAsync(err_host, (const char *)ws + 256, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "device->host copy of the error word");
   return DFV_OK;
 }
 

@@ -29,7 +29,8 @@ struct Workspace {
   int32_t *offsets;   // [E + 1]
   int32_t *gather;    // [k_max * K]   pair ids t*K+s sorted by (expert, t)
   unsigned *router_cnt;  // [1]
-  unsigned *down_cnt;    // [ceil(d / kDownTile)]
+  unsigned *err;         // [1] device error bits (DFV_DEVERR_*), sticky until cleared
+  unsigned *down_cnt;    // [ceil(d / 16)] one ticket per down tile
   void *xn;           // [k_max][d] activations staged for the expert FFN (act dtype)
   float *h;           // [k_max * K][d_ff]  SwiGLU activations, by sorted pair position
   float *ys;          // [k_max * K][d]     weighted expert outputs, by pair id
@@ -62,6 +63,11 @@ struct FfnParams {
   int k, d, I, E, K, act;
   int swz_x;            // XOR swizzle mask for staged x rows (0 or 4)
   int swz_h;            // XOR swizzle mask for staged h rows (0 or 4)
+  // TMA-staged kernels only
+  int ks;               // gate/up: k-columns per stage slice
+  int nslices;          // gate/up: slices per unit (d / ks)
+  int stages;           // ring depth
+  int rs;               // down: rows per unit
   Workspace ws;
 };
 
@@ -136,6 +142,87 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// ---------------------------------------------------------------- combine
+// out[t][r] = residual[t][r] + sum_s ys[t*K+s][r] (slot order) for rows
+// [r0, r0+rows) of every token, by threads tid = 0..nthr-1.
+__device__ __forceinline__ void combine_rows(const void *residual, void *out, const float *ys, int k, int K, int d,
+                                             int act, int r0, int rows, int tid, int nthr) {
+  for (int idx = tid; idx < k * rows; idx += nthr) {
+    const int t = idx / rows, r = r0 + idx % rows;
+    float s = 0.f;
+    for (int sl = 0; sl < K; ++sl) s += __ldcg(ys + (size_t)(t * K + sl) * d + r);
+    if (residual) s = load_act(residual, (size_t)t * d + r, act) + s;
+    store_act(out, (size_t)t * d + r, act, s);
+  }
+}
+
+// ---------------------------------------------------------------- TMA / mbarrier
+constexpr unsigned long long kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of `bar` with the given parity.  Gives up when *abort is
+// set by another thread of the CTA, or after kWaitNs (then records `code` in
+// *err and sets *abort); returns false when it gave up.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err, unsigned code,
+                                       volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitNs) {
+      atomicOr(err, code);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Named barrier over the first n threads of the CTA (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void bar_sync_n(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 }  // namespace dfv
 
 // Launch entry points implemented in the .cu files (host side).
@@ -144,5 +231,13 @@ cudaError_t launch_router(const RouterParams &p, cudaStream_t s, bool pdl);
 // phase 0: gate/up, phase 1: down + combine
 cudaError_t launch_ffn_phase(const FfnParams &p, int w_dtype, int phase, int grid, cudaStream_t s, bool pdl);
 int ffn_grid_limit(int w_dtype, int k, int d, int I, int which);
+// TMA-staged expert FFN: geometry for a layer shape, 0 if it does not fit.
+struct TmaPlan {
+  int ks, nslices, stages_g, rs, stages_d;
+  size_t smem_g, smem_d;
+};
+bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
+cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
+                           bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);
 }  // namespace dfv

@@ -1,0 +1,433 @@
+// ffn_tma.cu -- TMA-staged grouped SwiGLU expert FFN and combine (bf16
+// weights), one persistent CTA per SM.
+//
+// Same arithmetic as the register-direct kernels in ffn.cu ("Speculating on a
+// Strix Halo", sections "What the pieces cost" and "The verify's own cost":
+// tokens sorted by expert, one grouped launch per projection, the block's
+// output the routing-weighted sum of each token's K experts), with the weight
+// stream decoupled from the arithmetic:
+//
+//   * warp 8 is the producer: one thread walks the CTA's units and, for each
+//     stage of a ring in shared memory, waits for the stage to be free, posts
+//     the expected byte count on the stage's "full" mbarrier and issues 1-D
+//     bulk copies (cp.async.bulk, the untiled TMA) of the weight rows;
+//   * warps 0-7 consume: wait on "full", run the m16n8k16 MMAs from shared
+//     memory, release the stage on its "empty" mbarrier, and do the per-unit
+//     epilogues (cross-warp reduction, SwiGLU, weighted scatter, combine)
+//     while the producer keeps the next stages loading.
+//
+// Every weight byte of a woken expert crosses HBM once.  Row pieces land in
+// shared memory with a row stride of 64 mod 128 bytes, so the fragment loads
+// of two neighbouring rows fall on disjoint bank halves.  Every mbarrier wait
+// is bounded (2 s); a timeout sets a bit in the workspace error word, the CTA
+// stops, and the producer waits (bounded) for its copies in flight first.
+#include "dfv_internal.cuh"
+
+namespace dfv {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTmaThreads = kConsumers + 32;
+constexpr int kBarConsumers = 1;  // named barrier id for the consumer warps
+
+__device__ __forceinline__ int pad_to_64mod128(int bytes) { return (bytes % 128 == 0) ? bytes + 64 : bytes; }
+
+__device__ __forceinline__ void unit_range_tma(int U, int &lo, int &hi) {
+  lo = (int)(((long long)blockIdx.x * U) / gridDim.x);
+  hi = (int)(((long long)(blockIdx.x + 1) * U) / gridDim.x);
+}
+
+// Wait (bounded) until the copies of the last min(issued, S) stage fills have
+// landed, so no bulk copy targets this CTA's shared memory after it exits.
+__device__ void drain_stages(uint32_t full0, int issued, int S, unsigned *err) {
+  volatile int never = 0;  // the drain ignores the CTA's abort flag
+  for (int j = issued - S < 0 ? 0 : issued - S; j < issued; ++j)
+    if (!mbar_wait(full0 + 8 * (j % S), (j / S) & 1, err, DFV_DEVERR_DRAIN_WAIT, &never)) return;
+}
+
+// ----------------------------------------------------------------------------
+// gate/up.  Unit = (woken expert, 8 d_ff rows); stage = that unit's 8 gate and
+// 8 up rows over `ks` columns (nslices stages per unit).
+// Shared memory: stages[S][16][rsg] | xs[NT*8][rsx] | red[8][NT][32][4] f32 |
+// full[S] | empty[S]
+template <int NT>
+__global__ void __launch_bounds__(kTmaThreads, 1) gateup_tma_kernel(FfnParams p) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int d = p.d, I = p.I, K = p.K, ks = p.ks, S = p.stages, nsl = p.nslices;
+  const int rsg = pad_to_64mod128(ks * 2);
+  const int rsx = pad_to_64mod128(d * 2);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t stage_bytes = 16u * rsg;
+  const uint32_t xbase = sbase + S * stage_bytes;
+  float *red = reinterpret_cast<float *>(smem + S * stage_bytes + (size_t)NT * 8 * rsx);
+  const uint32_t full0 = smem_u32(red + kConsumerWarps * NT * 32 * 4);
+  const uint32_t empty0 = full0 + 8 * S;
+  __shared__ int s_tok[16];
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_abort = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  const int nW = *p.ws.n_woken;
+  const int tiles = I / kGateTile;
+  int lo, hi;
+  unit_range_tma(nW * tiles, lo, hi);
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer
+    if (lane == 0) {
+      const uint16_t *wg = reinterpret_cast<const uint16_t *>(p.wg);
+      const uint16_t *wu = reinterpret_cast<const uint16_t *>(p.wu);
+      int it = 0;
+      bool ok = true;
+      for (int u = lo; u < hi && ok; ++u) {
+        const int e = p.ws.woken[u / tiles], i0 = (u % tiles) * kGateTile;
+        for (int sl = 0; sl < nsl; ++sl, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * s, dst = sbase + s * stage_bytes;
+          mbar_expect_tx(fb, 16u * ks * 2);
+          for (int r = 0; r < 8; ++r) {
+            const size_t row = ((size_t)e * I + i0 + r) * d + (size_t)sl * ks;
+            bulk_g2s(dst + r * rsg, wg + row, ks * 2, fb);
+            bulk_g2s(dst + (8 + r) * rsg, wu + row, ks * 2, fb);
+          }
+        }
+      }
+      drain_stages(full0, it, S, p.ws.err);
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int g = lane >> 2, c = lane & 3;
+  const int cps = ks / 32;  // 32-column chunks per slice
+  const int c0 = warp * cps / kConsumerWarps, c1 = (warp + 1) * cps / kConsumerWarps;
+  const uint16_t *xg = reinterpret_cast<const uint16_t *>(p.x);
+  const int cpr = d / 8;
+  int cur = -1, m = 0, off = 0, it = 0;
+  bool dead = false;  // after a failed wait: keep the barrier schedule, skip the work
+  for (int u = lo; u < hi; ++u) {
+    const int wi = u / tiles, i0 = (u % tiles) * kGateTile;
+    if (wi != cur) {
+      bar_sync_n(kBarConsumers, kConsumers);
+      cur = wi;
+      off = p.ws.offsets[wi];
+      m = p.ws.offsets[wi + 1] - off;
+      if (tid < m) s_tok[tid] = p.ws.gather[off + tid] / K;
+      bar_sync_n(kBarConsumers, kConsumers);
+      for (int idx = tid; idx < m * cpr; idx += kConsumers) {
+        const int j = idx / cpr, q = idx % cpr;
+        const uint4 v = *reinterpret_cast<const uint4 *>(xg + (size_t)s_tok[j] * d + q * 8);
+        *reinterpret_cast<uint4 *>(smem + (xbase - sbase) + (size_t)j * rsx + q * 16) = v;
+      }
+      bar_sync_n(kBarConsumers, kConsumers);
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+
+    for (int sl = 0; sl < nsl; ++sl, ++it) {
+      const int s = it % S;
+      if (!dead && !mbar_wait(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+      if (dead) continue;
+      const uint32_t st = sbase + s * stage_bytes;
+      for (int ch = c0; ch < c1; ++ch) {
+        const uint32_t q16 = (ch * 4 + c) * 16;
+        const uint4 ag = lds128(st + g * rsg + q16);
+        const uint4 au = lds128(st + (8 + g) * rsg + q16);
+        const uint32_t xq = (uint32_t)(sl * (ks / 8) + ch * 4 + c) * 16;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (nt * 8 < m) {
+            const int row = nt * 8 + g;
+            uint4 b = make_uint4(0u, 0u, 0u, 0u);
+            if (row < m) b = lds128(xbase + row * rsx + xq);
+            mma_bf16(acc[nt], ag.x, au.x, ag.y, au.y, b.x, b.y);
+            mma_bf16(acc[nt], ag.z, au.z, ag.w, au.w, b.z, b.w);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      *reinterpret_cast<float4 *>(red + ((warp * NT + nt) * 32 + lane) * 4) =
+          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    bar_sync_n(kBarConsumers, kConsumers);
+    if (tid < NT * 64) {
+      const int nt = tid >> 6, ln = (tid >> 1) & 31, q = tid & 1;
+      const int tok = nt * 8 + 2 * (ln & 3) + q;
+      if (tok < m) {
+        float gs = 0.f, us = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          gs += red[((w * NT + nt) * 32 + ln) * 4 + q];
+          us += red[((w * NT + nt) * 32 + ln) * 4 + q + 2];
+        }
+        p.ws.h[(size_t)(off + tok) * I + i0 + (ln >> 2)] = silu(gs) * us;
+      }
+    }
+    bar_sync_n(kBarConsumers, kConsumers);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// down + combine.  Unit = (woken expert, rs rows of d); stage = those rows over
+// the full d_ff.  Consumers: 2 row-tiles of 16 x 4 k-quarters (rs = 32) or
+// 1 x 8 (rs = 16).  h of the expert's tokens is staged as a bf16 hi/lo pair.
+// Shared memory: stages[S][rs][rsd] | hh[NT*8][rsh] | hl[NT*8][rsh] |
+// red[8][NT][32][4] f32 | full[S] | empty[S]
+template <int NT>
+__global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int d = p.d, I = p.I, K = p.K, S = p.stages, RS = p.rs;
+  const int rsd = pad_to_64mod128(I * 2);
+  const int rsh = pad_to_64mod128(I * 2);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t stage_bytes = (uint32_t)RS * rsd;
+  const uint32_t hhb = sbase + S * stage_bytes;
+  const uint32_t hlb = hhb + NT * 8 * rsh;
+  float *red = reinterpret_cast<float *>(smem + S * stage_bytes + (size_t)2 * NT * 8 * rsh);
+  const uint32_t full0 = smem_u32(red + kConsumerWarps * NT * 32 * 4);
+  const uint32_t empty0 = full0 + 8 * S;
+  __shared__ unsigned s_last;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_abort = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  const int nW = *p.ws.n_woken;
+  const int tiles = (d + RS - 1) / RS;
+  int lo, hi;
+  unit_range_tma(nW * tiles, lo, hi);
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
+      int it = 0;
+      for (int u = lo; u < hi; ++u, ++it) {
+        const int e = p.ws.woken[u / tiles], r0 = (u % tiles) * RS;
+        const int rows = min(RS, d - r0);
+        const int s = it % S;
+        if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) break;
+        const uint32_t fb = full0 + 8 * s, dst = sbase + s * stage_bytes;
+        mbar_expect_tx(fb, (uint32_t)rows * I * 2);
+        for (int r = 0; r < rows; ++r) bulk_g2s(dst + r * rsd, wd + ((size_t)e * d + r0 + r) * I, I * 2, fb);
+      }
+      drain_stages(full0, it, S, p.ws.err);
+    }
+    return;
+  }
+
+  const int g = lane >> 2, c = lane & 3;
+  const int rtiles = RS / 16;                   // row tiles per unit (2 or 1)
+  const int kparts = kConsumerWarps / rtiles;   // k parts (4 or 8)
+  const int rw = warp % rtiles, kq = warp / rtiles;
+  const int C = I / 32;
+  const int c0 = kq * C / kparts, c1 = (kq + 1) * C / kparts;
+  const int cpr = I / 8;
+  int cur = -1, m = 0, off = 0, it = 0;
+  bool dead = false;  // after a failed wait: keep the barrier schedule, skip the work
+  for (int u = lo; u < hi; ++u, ++it) {
+    const int wi = u / tiles, dt = u % tiles, r0 = dt * RS;
+    const int rows = min(RS, d - r0);
+    if (wi != cur) {
+      bar_sync_n(kBarConsumers, kConsumers);
+      cur = wi;
+      off = p.ws.offsets[wi];
+      m = p.ws.offsets[wi + 1] - off;
+      for (int idx = tid; idx < m * cpr; idx += kConsumers) {
+        const int j = idx / cpr, q = idx % cpr;
+        const float4 *src = reinterpret_cast<const float4 *>(p.ws.h + (size_t)(off + j) * I + q * 8);
+        const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t h2[4], l2[4];
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          const __nv_bfloat16 a = __float2bfloat16_rn(v[2 * q2]), b = __float2bfloat16_rn(v[2 * q2 + 1]);
+          const __nv_bfloat16 la = __float2bfloat16_rn(v[2 * q2] - __bfloat162float(a));
+          const __nv_bfloat16 lb = __float2bfloat16_rn(v[2 * q2 + 1] - __bfloat162float(b));
+          h2[q2] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+          l2[q2] = (uint32_t)__bfloat16_as_ushort(la) | ((uint32_t)__bfloat16_as_ushort(lb) << 16);
+        }
+        *reinterpret_cast<uint4 *>(smem + (hhb - sbase) + (size_t)j * rsh + q * 16) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+        *reinterpret_cast<uint4 *>(smem + (hlb - sbase) + (size_t)j * rsh + q * 16) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+      }
+      bar_sync_n(kBarConsumers, kConsumers);
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+
+    const int s = it % S;
+    if (!dead && !mbar_wait(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+    const uint32_t st = sbase + s * stage_bytes;
+    if (!dead && rw * 16 < rows) {
+      for (int ch = c0; ch < c1; ++ch) {
+        const uint32_t q16 = (ch * 4 + c) * 16;
+        const uint4 a0 = lds128(st + (rw * 16 + g) * rsd + q16);
+        const uint4 a1 = lds128(st + (rw * 16 + g + 8) * rsd + q16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (nt * 8 < m) {
+            const int row = nt * 8 + g;
+            uint4 bh = make_uint4(0u, 0u, 0u, 0u), bl = bh;
+            if (row < m) {
+              bh = lds128(hhb + row * rsh + q16);
+              bl = lds128(hlb + row * rsh + q16);
+            }
+            mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bh.x, bh.y);
+            mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bh.z, bh.w);
+            mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bl.x, bl.y);
+            mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bl.z, bl.w);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      *reinterpret_cast<float4 *>(red + ((warp * NT + nt) * 32 + lane) * 4) =
+          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    bar_sync_n(kBarConsumers, kConsumers);
+    // y[row][tok] = sum over k parts (fixed order); weighted by the pair's routing weight
+    for (int idx = tid; idx < rtiles * NT * 128; idx += kConsumers) {
+      const int q4 = idx & 3, ln = (idx >> 2) & 31, nt = (idx >> 7) % NT, rt = idx / (128 * NT);
+      const int row = r0 + rt * 16 + (ln >> 2) + ((q4 & 2) ? 8 : 0);
+      const int tok = nt * 8 + 2 * (ln & 3) + (q4 & 1);
+      if (tok < m && row < d) {
+        float y = 0.f;
+        for (int kp = 0; kp < kparts; ++kp) y += red[(((kp * rtiles + rt) * NT + nt) * 32 + ln) * 4 + q4];
+        const int pair = p.ws.gather[off + tok];
+        p.ws.ys[(size_t)pair * d + row] = p.ws.topk_w[pair] * y;
+      }
+    }
+    // ticket for this row tile; the last unit to finish it runs the combine
+    bar_sync_n(kBarConsumers, kConsumers);
+    if (tid == 0) {
+      __threadfence();
+      s_last = (!s_abort && atomicAdd(p.ws.down_cnt + dt, 1u) == (unsigned)(nW - 1)) ? 1u : 0u;
+    }
+    bar_sync_n(kBarConsumers, kConsumers);
+    if (s_last) {
+      __threadfence();
+      combine_rows(p.residual, p.out, p.ws.ys, p.k, K, d, p.act, r0, rows, tid, kConsumers);
+      bar_sync_n(kBarConsumers, kConsumers);
+      if (tid == 0) p.ws.down_cnt[dt] = 0u;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+namespace {
+int pad_host(int bytes) { return (bytes % 128 == 0) ? bytes + 64 : bytes; }
+constexpr size_t kSmemBudget = 220 * 1024;
+}  // namespace
+
+bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan) {
+  if (w_dtype != DFV_BF16) return false;
+  const int NT = k <= 8 ? 1 : 2;
+  // gate/up: slice width ks = d / nslices with ks % 32 == 0 and ks <= 1024
+  const int C = d / 32;
+  int nsl = (d + 1023) / 1024;
+  while (nsl <= C && (C % nsl) != 0) ++nsl;
+  if (nsl > C) return false;
+  const int ks = d / nsl;
+  const size_t xg = (size_t)NT * 8 * pad_host(d * 2);
+  const size_t redb = (size_t)kConsumerWarps * NT * 32 * 16;
+  int Sg = 4;
+  size_t smg = 0;
+  for (; Sg >= 2; --Sg) {
+    smg = (size_t)Sg * 16 * pad_host(ks * 2) + xg + redb + 16 * Sg;
+    if (smg <= kSmemBudget) break;
+  }
+  if (Sg < 2) return false;
+  // down: rs rows of the full d_ff per stage
+  const size_t hb = (size_t)2 * NT * 8 * pad_host(I * 2);
+  int rs = 32, Sd = 0;
+  size_t smd = 0;
+  for (; rs >= 16; rs /= 2) {
+    for (Sd = 4; Sd >= 2; --Sd) {
+      smd = (size_t)Sd * rs * pad_host(I * 2) + hb + redb + 16 * Sd;
+      if (smd <= kSmemBudget) break;
+    }
+    if (Sd >= 2) break;
+  }
+  if (rs < 16 || Sd < 2) return false;
+  plan->ks = ks;
+  plan->nslices = nsl;
+  plan->stages_g = Sg;
+  plan->rs = rs;
+  plan->stages_d = Sd;
+  plan->smem_g = smg;
+  plan->smem_d = smd;
+  return true;
+}
+
+namespace {
+template <typename F>
+cudaError_t launch_tma(F kern, int grid, size_t smem, const FfnParams &p, cudaStream_t s, bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTmaThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+}  // namespace
+
+cudaError_t launch_ffn_tma(const FfnParams &p0, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
+                           bool pdl) {
+  if (w_dtype != DFV_BF16) return cudaErrorInvalidValue;
+  FfnParams p = p0;
+  p.ks = plan.ks;
+  p.nslices = plan.nslices;
+  p.rs = plan.rs;
+  if (phase == 0) {
+    p.stages = plan.stages_g;
+    return p.k <= 8 ? launch_tma(gateup_tma_kernel<1>, grid, plan.smem_g, p, s, pdl)
+                    : launch_tma(gateup_tma_kernel<2>, grid, plan.smem_g, p, s, pdl);
+  }
+  p.stages = plan.stages_d;
+  return p.k <= 8 ? launch_tma(down_tma_kernel<1>, grid, plan.smem_d, p, s, pdl)
+                  : launch_tma(down_tma_kernel<2>, grid, plan.smem_d, p, s, pdl);
+}
+
+}  // namespace dfv

@@ -76,6 +76,7 @@ def test_bf16_layer_parity_small(dfv, shape, k):
     _check_routing(dfv, L, ol, xg, ws)
     out = dfv.moe_block_forward(L, xg, ws)
     torch.cuda.synchronize()
+    assert dfv.read_device_error(ws) == 0
     ref = oracle.moe_forward(ol, np_of(x), nthreads=8)
     assert _max_rel_err(_gpu_out_np(out), ref) <= TOL_BF16
 
@@ -115,6 +116,7 @@ def test_a3b_layer_full_size(dfv, a3b, k, mode):
     out = dfv.moe_block_forward(L, xg, ws, n_woken=nw)
     torch.cuda.synchronize()
     assert int(nw.item()) == W
+    assert dfv.read_device_error(ws) == 0
     ref = oracle.moe_forward(ol, np_of(x), nthreads=oracle.num_threads_available())
     assert _max_rel_err(_gpu_out_np(out), ref) <= TOL_BF16
 
