@@ -191,7 +191,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Wait for the phase of `bar` with the given parity.  Gives up when *abort is
 // set by another thread of the CTA, or after kWaitNs (then records `code` in
 // *err and sets *abort); returns false when it gave up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err, unsigned code,
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err, unsigned code,
                                        volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
