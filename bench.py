@@ -305,39 +305,49 @@ def run_gpu(args):
     ms16_stream = stream_time(fn16, 2, max(3, args.steps // 4))
     ms1_stream = stream_time(fn1, 2, max(3, args.steps // 4))
 
-    # ---- per-kernel timing with CUDA events (dominant kernel = gate/up)
+    # ---- per-launch timing with CUDA events.  The fused path runs one kernel per
+    # layer (the dominant and only kernel); the multi-kernel path is timed too.
     x16 = inputs.make_hidden(KBLOCK, shape.d, "bf16", seed=5 + 100 * rank, device=dev)
     out16 = torch.empty_like(x16)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(N_LAYERS)]
-    reps = 3
-    t_router = t_gate = t_down = 0.0
-    for r in range(reps + 1):
-        for l in range(N_LAYERS):
-            dfv.profile_set_events(evs[l])
-            dfv.moe_block_forward(Ls[l], x16, ws, out=out16)
-        dfv.profile_set_events(None)
-        torch.cuda.synchronize()
-        if r == 0:
-            continue
-        for l in range(N_LAYERS):
-            e = evs[l]
-            t_router += e[0].elapsed_time(e[1])
-            t_gate += e[1].elapsed_time(e[2])
-            t_down += e[2].elapsed_time(e[3])
-    n_launch = reps * N_LAYERS
-    gate_bytes = float(W16.sum().item()) * (2 * shape.d_ff * shape.d * 2) / N_LAYERS  # per launch
+
+    def per_phase(reps=3):
+        tot = [0.0, 0.0, 0.0]
+        for r in range(reps + 1):
+            for l in range(N_LAYERS):
+                dfv.profile_set_events(evs[l])
+                dfv.moe_block_forward(Ls[l], x16, ws, out=out16)
+            dfv.profile_set_events(None)
+            torch.cuda.synchronize()
+            if r == 0:
+                continue
+            for l in range(N_LAYERS):
+                e = evs[l]
+                tot[0] += e[0].elapsed_time(e[1])
+                tot[1] += e[1].elapsed_time(e[2])
+                tot[2] += e[2].elapsed_time(e[3])
+        n = reps * N_LAYERS
+        return [t / n for t in tot]
+
+    layer_bytes = float(W16.sum().item()) * exp_bytes / N_LAYERS + router_bytes  # per launch
+    ph = per_phase()
+    fused_ms = ph[0] + ph[1] + ph[2]
+    fused_gbs = layer_bytes / (fused_ms * 1e-3) / 1e9
+    dfv.set_path(False)
+    phm = per_phase()
+    ms16_multi = graph_time(fn16, 2, max(3, args.steps // 4))
+    dfv.set_path(True)
+    gate_bytes = float(W16.sum().item()) * (2 * shape.d_ff * shape.d * 2) / N_LAYERS
     down_bytes = float(W16.sum().item()) * (shape.d * shape.d_ff * 2) / N_LAYERS
-    gate_ms = t_gate / n_launch
-    down_ms = t_down / n_launch
-    router_ms = t_router / n_launch
-    gate_gbs = gate_bytes / (gate_ms * 1e-3) / 1e9
     peak_bw = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
-    roofline = {"bound": "hbm", "kernel": "gateup_bf16_kernel<2> (k=16)", "achieved": gate_gbs, "peak": peak_bw,
-                "unit": "GB/s", "frac": gate_gbs / peak_bw, "traffic": None,
+    roofline = {"bound": "hbm", "kernel": "moe_fused_kernel<2> (one launch per layer, k=16)", "achieved": fused_gbs,
+                "peak": peak_bw, "unit": "GB/s", "frac": fused_gbs / peak_bw, "traffic": None,
                 "peak_kind": peak_kind + " (STREAM-style copy, burst)",
-                "per_launch_us": {"router": router_ms * 1e3, "gate_up": gate_ms * 1e3, "down_combine": down_ms * 1e3},
-                "down_achieved_gbs": down_bytes / (down_ms * 1e-3) / 1e9,
-                "algorithmic_bytes_per_launch": {"gate_up": gate_bytes, "down": down_bytes}}
+                "per_launch_us": fused_ms * 1e3, "algorithmic_bytes_per_launch": layer_bytes,
+                "multi_kernel_per_launch_us": {"router": phm[0] * 1e3, "gate_up": phm[1] * 1e3,
+                                               "down_combine": phm[2] * 1e3},
+                "multi_kernel_gate_up_gbs": gate_bytes / (phm[1] * 1e-3) / 1e9,
+                "multi_kernel_down_gbs": down_bytes / (phm[2] * 1e-3) / 1e9}
 
     # ---- k sweep (repeated-token vs independent blocks)
     sweep = {}
@@ -406,13 +416,14 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and hidden rows)",
         "config": dict(workload_config(), weights_gb=round(N_LAYERS * (exp_bytes * 128 + router_bytes) / 1e9, 2)),
         "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS,
+                     "k16_multi_kernel": ms16_multi * 1e3 / N_LAYERS,
                      "k16_stream": ms16_stream * 1e3 / N_LAYERS, "k1_stream": ms1_stream * 1e3 / N_LAYERS},
         "frac_of_hbm_peak": {"measured": value / world / peak_bw, "nominal_8tbs": value / world / 8000.0},
         "woken_mean": {"k16": float(W16.double().mean().item()), "k1": float(W1.double().mean().item())},
         "verify_decode": {"latency_ratio": ratio, "woken_byte_ratio": byte_ratio,
                           "quotient": byte_ratio / ratio},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 3 * N_LAYERS * args.steps, "clocks": clocks,
+        "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
         "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen,
     }
     if rank == 0:

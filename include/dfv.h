@@ -39,7 +39,7 @@
  *     matching *_workspace_size() reports.  A workspace must be ZERO-FILLED
  *     before its first use (e.g. cudaMemset); every call leaves it zero-ready
  *     for the next one (the counters that must start at zero live at fixed
- *     offsets, so one workspace serves any k and, for d <= 61440, any layer).
+ *     offsets, so one workspace serves any k and, for d <= 13312, any layer).
  *     Calls that share a workspace must be ordered (same stream, or
  *     synchronised): concurrent use races.
  *   - Returns DFV_OK (0) or a DFV_ERR_* status; dfv_status_string() names it
@@ -75,6 +75,7 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2 } dfv_dtype;
 #define DFV_DEVERR_STAGE_WAIT 0x1u   /* a consumer gave up waiting for a weight tile */
 #define DFV_DEVERR_SLOT_WAIT 0x2u    /* the producer gave up waiting for a free stage */
 #define DFV_DEVERR_DRAIN_WAIT 0x4u   /* copies still in flight at exit after a timeout */
+#define DFV_DEVERR_GRID_WAIT 0x8u    /* a CTA gave up waiting at a grid-wide barrier */
 
 /* Limits of this implementation. */
 #define DFV_MAX_BLOCK 16      /* k: positions in one verify block          */
@@ -214,6 +215,17 @@ int dfv_accept_greedy(const void *logits, int dtype, int k, int V, const int32_t
  * overlap of one kernel's start with the previous kernel's tail.
  */
 int dfv_profile_set_events(void *const *events, int n_events);
+
+/*
+ * Kernel path for later layer calls from this host thread (no counterpart on
+ * the method's pages).  1 (default): bf16 layers whose shape fits run as one
+ * cooperative persistent launch per layer (router, routing, gate/up, down and
+ * combine separated by grid-wide barriers); the others, and 0, use the
+ * multi-kernel path (router launch, then gate/up and down/combine launches).
+ * Both compute the same function.  With the fused path the profiling events
+ * 1-3 are recorded together after the single launch.
+ */
+int dfv_set_path(int path);
 
 const char *dfv_status_string(int status);
 const char *dfv_last_error_detail(void);

@@ -50,12 +50,13 @@ dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
     return p;
   };
   // counters and the error word first, at offsets that depend on nothing but d
-  // (a fixed 4 KB for d <= 14336): calls of any k, and layers of any width in
+  // (a fixed 4 KB for d <= 13312): calls of any k, and layers of any width in
   // that range, can share a workspace
   w.router_cnt = (unsigned *)take(4);
   w.err = (unsigned *)take(4);
+  w.sync = (unsigned *)take(16);
   const size_t tiles = (d + 15) / 16;
-  w.down_cnt = (unsigned *)take(tiles * 4 > 3584 ? tiles * 4 : 3584);
+  w.down_cnt = (unsigned *)take(tiles * 4 > 3328 ? tiles * 4 : 3328);
   w.logits = (float *)take(km * E * 4);
   w.topk_idx = (int32_t *)take(km * K * 4);
   w.topk_w = (float *)take(km * K * 4);
@@ -143,8 +144,69 @@ dfv::RouterParams router_params(const dfv_moe_layer *L, const void *x, int act, 
   return p;
 }
 
+// Single-launch fused layer (bf16 weights): grid = SM count, cooperative.
+// Returns -1 when the shape or the device does not allow it (the caller then
+// uses the multi-kernel path), else a DFV status.
+int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void *out, const void *residual,
+                    bool fuse_norm, float eps, int32_t *u_idx, int32_t *u_nw, const dfv::Workspace &w,
+                    cudaStream_t s) {
+  if (L->w_dtype != DFV_BF16 || L->r_dtype != DFV_BF16 || act != DFV_BF16) return -1;
+  dfv::FusedPlan plan;
+  if (!dfv::fused_plan(k, L->d, L->d_ff, L->n_experts, &plan)) return -1;
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int grid;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_tuple(dev, k <= 8 ? 1 : 2, plan.smem);
+    auto it = cache.find(key);
+    if (it == cache.end()) it = cache.emplace(key, dfv::fused_max_grid(plan, k)).first;
+    grid = it->second;
+  }
+  if (grid <= 0) return -1;
+  dfv::FusedParams fp = {};
+  fp.x = x;
+  fp.residual = residual;
+  fp.out = out;
+  fp.wr = L->w_router;
+  fp.wg = L->w_gate;
+  fp.wu = L->w_up;
+  fp.wd = L->w_down;
+  fp.k = k;
+  fp.d = L->d;
+  fp.I = L->d_ff;
+  fp.E = L->n_experts;
+  fp.K = L->top_k;
+  fp.norm_topk = L->norm_topk ? 1 : 0;
+  fp.fuse_norm = fuse_norm ? 1 : 0;
+  fp.swz_x = (L->d % 64 == 0) ? 4 : 0;
+  fp.eps = eps;
+  fp.ws = w;
+  fp.u_idx = u_idx;
+  fp.u_nw = u_nw;
+  mark(0, s);
+  cudaError_t e = dfv::launch_fused(fp, plan, grid, s, true);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear, and retry without programmatic serialisation
+    e = dfv::launch_fused(fp, plan, grid, s, false);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "fused layer launch");
+  mark(1, s);
+  mark(2, s);
+  mark(3, s);
+  return DFV_OK;
+}
+
+thread_local bool g_fused_enabled = true;
+
 int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, const void *residual,
               bool fuse_norm, float eps, int32_t *u_idx, int32_t *u_nw, const dfv::Workspace &w, cudaStream_t s) {
+  if (g_fused_enabled) {
+    const int st = run_layer_fused(L, x, act, k, out, residual, fuse_norm, eps, u_idx, u_nw, w, s);
+    if (st >= 0) return st;
+  }
   dfv::RouterParams rp = router_params(L, x, act, k, w);
   rp.fuse_norm = fuse_norm ? 1 : 0;
   rp.eps = eps;
@@ -316,6 +378,12 @@ int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, in
     int st = run_layer(&layers[l], x, DFV_BF16, k, x, x, true, eps, nullptr, nullptr, w, (cudaStream_t)stream);
     if (st) return st;
   }
+  return DFV_OK;
+}
+
+int dfv_set_path(int path) {
+  if (path != 0 && path != 1) return fail(DFV_ERR_INVALID_ARG, "path must be 0 (multi-kernel) or 1 (fused)");
+  g_fused_enabled = path == 1;
   return DFV_OK;
 }
 

@@ -30,9 +30,11 @@ struct Workspace {
   int32_t *gather;    // [k_max * K]   pair ids t*K+s sorted by (expert, t)
   unsigned *router_cnt;  // [1]
   unsigned *err;         // [1] device error bits (DFV_DEVERR_*), sticky until cleared
+  unsigned *sync;        // [4] fused kernel: grid-barrier count, exit ticket, abort flag
   unsigned *down_cnt;    // [ceil(d / 16)] one ticket per down tile
   void *xn;           // [k_max][d] activations staged for the expert FFN (act dtype)
   float *h;           // [k_max * K][d_ff]  SwiGLU activations, by sorted pair position
+                      // (fused kernel: bf16 hi [kK][d_ff] then bf16 lo [kK][d_ff])
   float *ys;          // [k_max * K][d]     weighted expert outputs, by pair id
   void *xio;          // [k_max][d] host-variant input staging (4-byte elements)
   void *oio;          // [k_max][d] host-variant output staging
@@ -69,6 +71,23 @@ struct FfnParams {
   int stages;           // ring depth
   int rs;               // down: rows per unit
   Workspace ws;
+};
+
+struct FusedParams {
+  const void *x;         // [k][d] bf16 rows (the residual stream when fuse_norm)
+  const void *residual;  // [k][d] bf16 or null: added in the combine
+  void *out;             // [k][d] bf16
+  const void *wr, *wg, *wu, *wd;
+  int k, d, I, E, K, norm_topk, fuse_norm, swz_x;
+  float eps;
+  int ks, nsl, slot, scratch;  // filled from the plan
+  Workspace ws;
+  int32_t *u_idx, *u_nw;
+};
+
+struct FusedPlan {
+  int ks, nsl, slot, scratch;
+  size_t smem;
 };
 
 struct AcceptParams {
@@ -237,6 +256,10 @@ struct TmaPlan {
   size_t smem_g, smem_d;
 };
 bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
+// Fused single-launch layer (bf16): plan, grid (0 = cannot run) and launch.
+bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
+int fused_max_grid(const FusedPlan &plan, int k);
+cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);

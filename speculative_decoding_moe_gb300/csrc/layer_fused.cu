@@ -1,0 +1,630 @@
+// layer_fused.cu -- one MoE layer of a verify block in a single persistent,
+// cooperative launch (bf16 experts and router, bf16 activations).
+//
+// "Speculating on a Strix Halo", section "What the pieces cost": every token of
+// the block routes to its own top-K experts and the block wakes their union;
+// section "The verify's own cost": tokens are sorted by expert and each
+// projection runs grouped.  Part 2, section "The verification cog": the cost is
+// streaming the woken experts' weights, so every weight byte of a woken expert
+// crosses HBM exactly once.
+//
+// One CTA per SM (grid = SM count, co-residency guaranteed by the cooperative
+// launch); 16 consumer warps and one producer warp.  Phases:
+//   P0  router GEMV (optionally on RMSNorm(x) rounded to bf16): CTA b computes
+//       the logits of experts b, b+G, ...; fixed-order reductions.
+//       -- grid barrier 1 --
+//   P1  every CTA derives the whole routing decision itself from the logits:
+//       top-K per row (warp per row, redux max/min: largest logit, lowest id
+//       among equals), routing weights, woken union, per-expert pair offsets
+//       (block scan) and the (expert, token)-sorted pair list.
+//   P2  gate/up: unit = (woken expert, 8 d_ff rows).  The producer streams
+//       stages of 8 gate + 8 up rows x `ks` columns (1-D bulk copies into an
+//       mbarrier ring); the 16 consumer warps split the columns, run
+//       m16n8k16 MMAs (gate rows = M 0-7, up rows = M 8-15, tokens = N) and
+//       reduce across warps in fixed order; h = silu(g) * u is written as a
+//       bf16 hi/lo pair.  The producer then runs ahead into P3's weights.
+//       -- grid barrier 2 (consumers only) --
+//   P3  down: CTA b owns 16-row tiles b, b+G, ... of d; for each it streams
+//       the tile's rows of every woken expert (one contiguous copy each); two
+//       groups of 8 warps take alternate experts, reduce within the group,
+//       and scatter w[t,s] * y into a per-tile slot table in shared memory;
+//       the tile's outputs are summed over the K slots in slot order (+ the
+//       residual) and written once.  No cross-CTA reduction, no atomics on
+//       the output: the result of a token depends only on its own row, so a
+//       block and k single-token calls agree bit for bit.
+// Every wait is bounded (2 s) and reports through the workspace error word.
+#include "dfv_internal.cuh"
+
+namespace dfv {
+
+constexpr int kFW = 16;           // consumer warps
+constexpr int kFC = kFW * 32;     // consumer threads
+constexpr int kFT = kFC + 32;     // + producer warp
+constexpr int kBarAll = 1;        // named barrier: all consumers
+constexpr int kBarGroup = 2;      // named barriers 2, 3: consumer groups of 8 warps
+constexpr int kRing = 4;          // ring stages (even: P3 gives each group two)
+
+__device__ __forceinline__ int fpad(int bytes) { return (bytes % 128 == 0) ? bytes + 64 : bytes; }
+
+__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(n) : "memory");
+}
+
+// Grid barrier, one thread per CTA.  ctr counts arrivals over the whole launch;
+// barrier number `nb` (1-based) completes when ctr reaches nb * G.  Gives up
+// when another CTA aborted or after kWaitNs.
+__device__ bool grid_sync(const FusedParams &p, unsigned nb) {
+  unsigned *ctr = p.ws.sync, *gabort = p.ws.sync + 2;
+  red_release_add(ctr, 1u);
+  const unsigned target = nb * gridDim.x;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire(ctr) < target) {
+    if (ld_relaxed(gabort)) return false;
+    if (global_ns() - t0 > kWaitNs) {
+      atomicOr(p.ws.err, DFV_DEVERR_GRID_WAIT);
+      atomicExch(gabort, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Sum of 16 per-lane values over the warp with 16 shuffles: lane l ends with the
+// total of value index ((l>>4)&1)*8 + ((l>>3)&1)*4 + ((l>>2)&1)*2 + ((l>>1)&1).
+__device__ __forceinline__ float warp_sum16(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int h = 8, o = 16; h >= 1; h >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+__device__ __forceinline__ int warp_sum16_index(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
+__device__ __forceinline__ void load8_bf16(const void *base, size_t elem, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(base) + elem);
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ float rnd_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+template <int NT>
+__global__ void __maxnreg__(112) moe_fused_kernel(FusedParams p) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int k = p.k, d = p.d, I = p.I, E = p.E, K = p.K, ks = p.ks, nsl = p.nsl;
+  const int G = gridDim.x;
+  const int rsg = fpad(ks * 2);        // gate/up stage row stride
+  const int rsx = d * 2;               // staged x row stride (16B chunks XOR-swizzled)
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t slot = p.slot;
+  unsigned char *scratch = smem + kRing * slot;           // x rows / logits / slot table
+  float *red = reinterpret_cast<float *>(scratch + p.scratch);  // [16][NT][32][4]
+  const uint32_t full0 = smem_u32(red + kFW * NT * 32 * 4);
+  const uint32_t empty0 = full0 + 8 * kRing;
+
+  __shared__ int s_idx[kMaxBlock * kMaxTopK];
+  __shared__ float s_w[kMaxBlock * kMaxTopK];
+  __shared__ int s_woken[kMaxExperts];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_eoff[kMaxExperts];
+  __shared__ int s_gat[kMaxBlock * kMaxTopK];
+  __shared__ unsigned s_mask[kMaxBlock * (kMaxExperts / 32)];
+  __shared__ float s_part[kFW][16];
+  __shared__ float s_inv[kMaxBlock];
+  __shared__ int s_wsum[kFW], s_csum[kFW];
+  __shared__ int s_tok[16];
+  __shared__ int s_nw;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kFW);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  const bool consumer = warp < kFW;
+  // ------------------------------------------------------------------ P0: router GEMV
+  if (consumer) {
+    if (p.fuse_norm) {
+      float ss[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) ss[t] = 0.f;
+      for (int c = tid; c < d / 8; c += kFC) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          if (t < k) {
+            float f[8];
+            load8_bf16(p.x, (size_t)t * d + c * 8, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ss[t] = fmaf(f[q], f[q], ss[t]);
+          }
+        }
+      }
+      const float r = warp_sum16(ss);
+      if ((lane & 1) == 0) s_part[warp][warp_sum16_index(lane)] = r;
+      bar_sync_n(kBarAll, kFC);
+      if (tid < k) {
+        float a = 0.f;
+        for (int w = 0; w < kFW; ++w) a += s_part[w][tid];
+        s_inv[tid] = 1.0f / sqrtf(a / (float)d + p.eps);
+      }
+      bar_sync_n(kBarAll, kFC);
+    }
+    for (int e = blockIdx.x; e < E; e += G) {
+      float acc[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+      for (int c = tid; c < d / 8; c += kFC) {
+        float w8[8];
+        load8_bf16(p.wr, (size_t)e * d + c * 8, w8);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          if (t < k) {
+            float f[8];
+            load8_bf16(p.x, (size_t)t * d + c * 8, f);
+            if (p.fuse_norm) {
+              const float inv = s_inv[t];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) f[q] = rnd_bf16(f[q] * inv);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[t] = fmaf(f[q], w8[q], acc[t]);
+          }
+        }
+      }
+      const float r = warp_sum16(acc);
+      if ((lane & 1) == 0) s_part[warp][warp_sum16_index(lane)] = r;
+      bar_sync_n(kBarAll, kFC);
+      if (tid < k) {
+        float a = 0.f;
+        for (int w = 0; w < kFW; ++w) a += s_part[w][tid];
+        p.ws.logits[(size_t)tid * E + e] = a;
+      }
+      bar_sync_n(kBarAll, kFC);
+    }
+    // ---- grid barrier 1: every CTA's logits are published
+    if (tid == 0 && !grid_sync(p, 1)) s_abort = 1;
+    bar_sync_n(kBarAll, kFC);
+
+    // ---------------------------------------------------------------- P1: routing
+    float *lg = reinterpret_cast<float *>(scratch);
+    for (int i = tid; i < k * E; i += kFC) lg[i] = __ldcg(p.ws.logits + i);
+    for (int i = tid; i < kMaxExperts; i += kFC) s_eoff[i] = 0;
+    for (int i = tid; i < kMaxBlock * (kMaxExperts / 32); i += kFC) s_mask[i] = 0u;
+    bar_sync_n(kBarAll, kFC);
+    if (warp < k) {
+      // lane owns experts lane + 32 q; keys are monotone in the logit, 0 = taken/empty
+      const int t = warp;
+      uint32_t key[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = lane + 32 * q;
+        key[q] = (e < E) ? max(float_key(lg[t * E + e]), 1u) : 0u;
+      }
+      for (int s = 0; s < K; ++s) {
+        uint32_t bk = 0;
+        int bq = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (key[q] > bk) { bk = key[q]; bq = q; }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t cand = (bk == m) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu;
+        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+        if ((int)(win & 31) == lane) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q == (int)(win >> 5)) key[q] = 0u;
+        }
+        if (lane == 0) s_idx[t * K + s] = (int)win;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const float m0 = lg[t * E + s_idx[t * K]];
+        float denom = 0.f;
+        if (p.norm_topk) {
+          for (int s = 0; s < K; ++s) denom += expf(lg[t * E + s_idx[t * K + s]] - m0);
+        } else {
+          for (int j = 0; j < E; ++j) denom += expf(lg[t * E + j] - m0);
+        }
+        for (int s = 0; s < K; ++s) s_w[t * K + s] = expf(lg[t * E + s_idx[t * K + s]] - m0) / denom;
+      }
+    }
+    bar_sync_n(kBarAll, kFC);
+    for (int q = tid; q < k * K; q += kFC) {
+      const int t = q / K, ex = s_idx[q];
+      atomicAdd(&s_eoff[ex], 1);
+      atomicOr(&s_mask[t * (kMaxExperts / 32) + (ex >> 5)], 1u << (ex & 31));
+    }
+    bar_sync_n(kBarAll, kFC);
+    {
+      // exclusive scans over experts (E <= 256 <= 8 warps of threads)
+      int flag = 0, cnt = 0;
+      if (tid < E) { cnt = s_eoff[tid]; flag = cnt > 0; }
+      int fi = flag, ci = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, fi, o), b = __shfl_up_sync(0xffffffffu, ci, o);
+        if (lane >= o) { fi += a; ci += b; }
+      }
+      if (lane == 31) { s_wsum[warp] = fi; s_csum[warp] = ci; }
+      bar_sync_n(kBarAll, kFC);
+      int wb = 0, cb = 0, nW = 0;
+      for (int w = 0; w < kFW; ++w) {
+        if (w < warp) { wb += s_wsum[w]; cb += s_csum[w]; }
+        nW += s_wsum[w];
+      }
+      const int wpos = wb + fi - flag, off = cb + ci - cnt;
+      if (tid < E) s_eoff[tid] = off;
+      if (flag) { s_woken[wpos] = tid; s_off[wpos] = off; }
+      if (tid == 0) { s_off[nW] = k * K; s_nw = nW; }
+    }
+    bar_sync_n(kBarAll, kFC);
+    for (int q = tid; q < k * K; q += kFC) {
+      const int t = q / K, ex = s_idx[q];
+      int rank = 0;
+      for (int t2 = 0; t2 < t; ++t2) rank += (s_mask[t2 * (kMaxExperts / 32) + (ex >> 5)] >> (ex & 31)) & 1u;
+      s_gat[s_eoff[ex] + rank] = q;
+    }
+    bar_sync_n(kBarAll, kFC);
+    if (blockIdx.x == 0) {
+      const int nW = s_nw;
+      for (int q = tid; q < k * K; q += kFC) {
+        p.ws.topk_idx[q] = s_idx[q];
+        p.ws.topk_w[q] = s_w[q];
+        p.ws.gather[q] = s_gat[q];
+        if (p.u_idx) p.u_idx[q] = s_idx[q];
+      }
+      for (int i = tid; i < nW; i += kFC) { p.ws.woken[i] = s_woken[i]; p.ws.offsets[i] = s_off[i]; }
+      if (tid == 0) {
+        p.ws.offsets[nW] = s_off[nW];
+        *p.ws.n_woken = nW;
+        if (p.u_nw) *p.u_nw = nW;
+      }
+    }
+  }
+  __syncthreads();  // routing tables visible to the producer
+
+  const int nW = s_nw;
+  const int tiles_g = I / kGateTile;
+  int lo_g, hi_g;
+  {
+    const int U = nW * tiles_g;
+    lo_g = (int)(((long long)blockIdx.x * U) / G);
+    hi_g = (int)(((long long)(blockIdx.x + 1) * U) / G);
+  }
+  const int tiles_d = d / 16;
+
+  if (!consumer) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && !s_abort) {
+      const uint16_t *wg = reinterpret_cast<const uint16_t *>(p.wg);
+      const uint16_t *wu = reinterpret_cast<const uint16_t *>(p.wu);
+      const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
+      int it = 0;
+      bool ok = true;
+      for (int u = lo_g; u < hi_g && ok; ++u) {
+        const int e = s_woken[u / tiles_g], i0 = (u % tiles_g) * kGateTile;
+        for (int sl = 0; sl < nsl; ++sl, ++it) {
+          const int s = it % kRing;
+          if (!mbar_wait(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * s, dst = sbase + s * slot;
+          mbar_expect_tx(fb, 16u * ks * 2);
+          for (int r = 0; r < 8; ++r) {
+            const size_t row = ((size_t)e * I + i0 + r) * d + (size_t)sl * ks;
+            bulk_g2s(dst + r * rsg, wg + row, ks * 2, fb);
+            bulk_g2s(dst + (8 + r) * rsg, wu + row, ks * 2, fb);
+          }
+        }
+      }
+      for (int tl = blockIdx.x; tl < tiles_d && ok; tl += G) {
+        for (int wi = 0; wi < nW; ++wi, ++it) {
+          const int s = it % kRing;
+          if (!mbar_wait(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * s;
+          mbar_expect_tx(fb, 16u * I * 2);
+          bulk_g2s(sbase + s * slot, wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb);
+        }
+      }
+      // no copy may land after the CTA exits
+      volatile int never = 0;
+      for (int j = it - kRing < 0 ? 0 : it - kRing; j < it; ++j)
+        if (!mbar_wait(full0 + 8 * (j % kRing), (j / kRing) & 1, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never)) break;
+    }
+  } else {
+    // ---------------------------------------------------------------- P2: gate/up
+    const int g = lane >> 2, c = lane & 3;
+    const int cps = ks / 32;
+    const int c0 = warp * cps / kFW, c1 = (warp + 1) * cps / kFW;
+    const uint16_t *xg = reinterpret_cast<const uint16_t *>(p.x);
+    const int cpr = d / 8;
+    uint16_t *hhi = reinterpret_cast<uint16_t *>(p.ws.h);
+    uint16_t *hlo = hhi + (size_t)k * K * I;
+    const uint32_t xs = sbase + kRing * slot;
+    int cur = -1, m = 0, off = 0, it = 0;
+    bool dead = s_abort != 0;
+    for (int u = lo_g; u < hi_g; ++u) {
+      const int wi = u / tiles_g, i0 = (u % tiles_g) * kGateTile;
+      if (wi != cur) {
+        bar_sync_n(kBarAll, kFC);
+        cur = wi;
+        off = s_off[wi];
+        m = s_off[wi + 1] - off;
+        if (tid < m) s_tok[tid] = s_gat[off + tid] / K;
+        bar_sync_n(kBarAll, kFC);
+        for (int idx = tid; idx < m * cpr; idx += kFC) {
+          const int j = idx / cpr, q = idx % cpr, t = s_tok[j];
+          uint4 v = *reinterpret_cast<const uint4 *>(xg + (size_t)t * d + q * 8);
+          if (p.fuse_norm) {
+            const float inv = s_inv[t];
+            uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float a = rnd_bf16(bf16_lo(w4[h]) * inv), b = rnd_bf16(bf16_hi(w4[h]) * inv);
+              w4[h] = (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xffff0000u);
+            }
+            v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          *reinterpret_cast<uint4 *>(scratch + (size_t)j * rsx + ((q ^ ((j & 1) ? p.swz_x : 0)) * 16)) = v;
+        }
+        bar_sync_n(kBarAll, kFC);
+      }
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+      for (int sl = 0; sl < nsl; ++sl, ++it) {
+        const int s = it % kRing;
+        if (!dead && !mbar_wait(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        if (!dead) {
+          const uint32_t st = sbase + s * slot;
+          for (int ch = c0; ch < c1; ++ch) {
+            const uint32_t q16 = (ch * 4 + c) * 16;
+            const uint4 ag = lds128(st + g * rsg + q16);
+            const uint4 au = lds128(st + (8 + g) * rsg + q16);
+            const int xq = sl * (ks / 8) + ch * 4 + c;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              if (nt * 8 < m) {
+                const int row = nt * 8 + g;
+                uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                if (row < m) b = lds128(xs + row * rsx + (xq ^ ((row & 1) ? p.swz_x : 0)) * 16);
+                mma_bf16(acc[nt], ag.x, au.x, ag.y, au.y, b.x, b.y);
+                mma_bf16(acc[nt], ag.z, au.z, ag.w, au.w, b.z, b.w);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float4 *>(red + ((warp * NT + nt) * 32 + lane) * 4) =
+            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+      bar_sync_n(kBarAll, kFC);
+      if (tid < NT * 64) {
+        const int nt = tid >> 6, ln = (tid >> 1) & 31, q = tid & 1;
+        const int tok = nt * 8 + 2 * (ln & 3) + q;
+        if (tok < m) {
+          float gs = 0.f, us = 0.f;
+          for (int w = 0; w < kFW; ++w) {
+            gs += red[((w * NT + nt) * 32 + ln) * 4 + q];
+            us += red[((w * NT + nt) * 32 + ln) * 4 + q + 2];
+          }
+          const float hv = silu(gs) * us;
+          const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+          const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
+          const size_t o = (size_t)(off + tok) * I + i0 + (ln >> 2);
+          hhi[o] = __bfloat16_as_ushort(hb);
+          hlo[o] = __bfloat16_as_ushort(lb);
+        }
+      }
+      bar_sync_n(kBarAll, kFC);
+    }
+    // ---- grid barrier 2: every h row is written
+    if (tid == 0 && !grid_sync(p, 2)) s_abort = 1;
+    bar_sync_n(kBarAll, kFC);
+    dead = dead || s_abort != 0;
+
+    // ---------------------------------------------------------------- P3: down + combine
+    const int grp = warp >> 3, wg = warp & 7;
+    const int C = I / 32;
+    const int d0 = wg * C / 8, d1 = (wg + 1) * C / 8;
+    const int rsd = I * 2;
+    float *ysl = reinterpret_cast<float *>(scratch);  // [k*K][16]
+    float *redg = red + grp * 8 * NT * 32 * 4;         // this group's [8][NT][32][4]
+    int jd = 0;
+    for (int tl = blockIdx.x; tl < tiles_d; tl += G) {
+      const int r0 = tl * 16;
+      for (int wi = 0; wi < nW; ++wi, ++jd, ++it) {
+        if ((jd & 1) != grp) continue;
+        const int s = it % kRing;
+        const int eoff = s_off[wi], em = s_off[wi + 1] - eoff;
+        // B fragments (h hi/lo of this expert's tokens) straight from L2
+        uint4 bh[3][NT], bl[3][NT];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            bh[j][nt] = make_uint4(0u, 0u, 0u, 0u);
+            bl[j][nt] = bh[j][nt];
+            const int row = nt * 8 + g, ch = d0 + j;
+            if (!dead && ch < d1 && row < em) {
+              const size_t o = (size_t)(eoff + row) * I + ch * 32 + c * 8;
+              bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hhi + o));
+              bl[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hlo + o));
+            }
+          }
+        }
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+        if (!dead && !mbar_wait(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        if (!dead) {
+          const uint32_t st = sbase + s * slot;
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int ch = d0 + j;
+            if (ch < d1) {
+              const uint32_t q16 = (ch * 4 + c) * 16;
+              const uint4 a0 = lds128(st + g * rsd + q16);
+              const uint4 a1 = lds128(st + (g + 8) * rsd + q16);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (nt * 8 < em) {
+                  mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bh[j][nt].x, bh[j][nt].y);
+                  mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bh[j][nt].z, bh[j][nt].w);
+                  mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bl[j][nt].x, bl[j][nt].y);
+                  mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bl[j][nt].z, bl[j][nt].w);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_n(empty0 + 8 * s, 2);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
+              make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+        bar_sync_n(kBarGroup + grp, 256);
+        const int gt = tid & 255;
+        if (gt < NT * 128) {
+          const int q4 = gt & 3, ln = (gt >> 2) & 31, nt = gt >> 7;
+          const int tok = nt * 8 + 2 * (ln & 3) + (q4 & 1);
+          if (tok < em) {
+            float y = 0.f;
+            for (int w = 0; w < 8; ++w) y += redg[((w * NT + nt) * 32 + ln) * 4 + q4];
+            const int pair = s_gat[eoff + tok];
+            ysl[pair * 16 + (ln >> 2) + ((q4 & 2) ? 8 : 0)] = s_w[pair] * y;
+          }
+        }
+        bar_sync_n(kBarGroup + grp, 256);
+      }
+      bar_sync_n(kBarAll, kFC);
+      if (!dead) {
+        for (int idx = tid; idx < k * 16; idx += kFC) {
+          const int t = idx >> 4, rr = idx & 15, r = r0 + rr;
+          float sum = 0.f;
+          for (int sl = 0; sl < K; ++sl) sum += ysl[(t * K + sl) * 16 + rr];
+          if (p.residual) sum = load_act(p.residual, (size_t)t * d + r, DFV_BF16) + sum;
+          store_act(p.out, (size_t)t * d + r, DFV_BF16, sum);
+        }
+      }
+      bar_sync_n(kBarAll, kFC);
+    }
+  }
+
+  // exit ticket: the last CTA out resets the grid-barrier count for the next launch
+  __syncthreads();
+  if (tid == 0) {
+    if (atomicAdd(p.ws.sync + 1, 1u) == (unsigned)(G - 1)) {
+      atomicExch(p.ws.sync, 0u);
+      atomicExch(p.ws.sync + 1, 0u);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
+  if (d % 32 || I % 32 || I > 768 || k < 1 || k > kMaxBlock) return false;  // P3 holds <= 3 k-chunks per warp
+  const int NT = k <= 8 ? 1 : 2;
+  const int C = d / 32;
+  int nsl = (d + 1023) / 1024;
+  while (nsl <= C && (C % nsl) != 0) ++nsl;
+  if (nsl > C) return false;
+  const int ks = d / nsl;
+  auto pad = [](int b) { return (b % 128 == 0) ? b + 64 : b; };
+  const size_t gslot = (size_t)16 * pad(ks * 2);
+  const size_t dslot = (size_t)16 * I * 2;
+  size_t slot = gslot > dslot ? gslot : dslot;
+  slot = (slot + 127) & ~(size_t)127;
+  size_t scratch = (size_t)NT * 8 * d * 2;
+  const size_t lgb = (size_t)k * E * 4, ysb = (size_t)k * 8 * 16 * 4;
+  if (lgb > scratch) scratch = lgb;
+  if (ysb > scratch) scratch = ysb;
+  scratch = (scratch + 127) & ~(size_t)127;
+  const size_t redb = (size_t)kFW * NT * 32 * 16;
+  const size_t smem = kRing * slot + scratch + redb + 16 * kRing;
+  if (smem > 220 * 1024) return false;
+  plan->ks = ks;
+  plan->nsl = nsl;
+  plan->slot = (int)slot;
+  plan->scratch = (int)scratch;
+  plan->smem = smem;
+  return true;
+}
+
+cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
+  FusedParams p = p0;
+  p.ks = plan.ks;
+  p.nsl = plan.nsl;
+  p.slot = plan.slot;
+  p.scratch = plan.scratch;
+  auto kern = p.k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFT);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+int fused_max_grid(const FusedPlan &plan, int k) {
+  int dev = 0, sms = 0, per = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  auto kern = k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, kFT, plan.smem) != cudaSuccess) return 0;
+  return per >= 1 ? sms : 0;
+}
+
+}  // namespace dfv

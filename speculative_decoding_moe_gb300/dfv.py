@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libdfv.so")
 F32, BF16, MXFP4 = 0, 1, 2
 _NAMES = {"f32": F32, "bf16": BF16, "mxfp4": MXFP4}
 EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_profile_set_events",
-           "dfv_read_device_error",
+           "dfv_read_device_error", "dfv_set_path",
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
            "dfv_accept_workspace_size", "dfv_accept_greedy")
@@ -67,6 +67,7 @@ def _load():
         L.dfv_accept_greedy.argtypes = [P, I, I, I, P, P, P, P, S, P]
         L.dfv_profile_set_events.argtypes = [P, I]
         L.dfv_read_device_error.argtypes = [P, P, P]
+        L.dfv_set_path.argtypes = [I]
         _lib = L
     return _lib
 
@@ -211,3 +212,8 @@ def read_device_error(ws: torch.Tensor, stream=None) -> int:
     _check(_load().dfv_read_device_error(_p(ws), ctypes.byref(out), _stream(stream)), "dfv_read_device_error")
     (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return int(out.value)
+
+
+def set_path(fused: bool):
+    """Select the fused single-launch layer kernel (default) or the multi-kernel path."""
+    _check(_load().dfv_set_path(1 if fused else 0), "dfv_set_path")

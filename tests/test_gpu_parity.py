@@ -62,9 +62,16 @@ SMALL = [
 ]
 
 
+@pytest.fixture(params=["fused", "multi"])
+def path(request, dfv):
+    dfv.set_path(request.param == "fused")
+    yield request.param
+    dfv.set_path(True)
+
+
 @pytest.mark.parametrize("shape", SMALL)
 @pytest.mark.parametrize("k", [1, 3, 8, 9, 16])
-def test_bf16_layer_parity_small(dfv, shape, k):
+def test_bf16_layer_parity_small(dfv, path, shape, k):
     d, E, K, I = shape
     s = inputs.LayerShape(d=d, n_experts=E, top_k=K, d_ff=I)
     lw = inputs.make_layer(s, seed=100 + k)
@@ -103,7 +110,7 @@ def a3b(dfv):
 
 
 @pytest.mark.parametrize("k,mode", [(1, "independent"), (16, "independent"), (16, "repeated"), (7, "independent")])
-def test_a3b_layer_full_size(dfv, a3b, k, mode):
+def test_a3b_layer_full_size(dfv, a3b, path, k, mode):
     lw, ol, L = a3b
     x = hidden_without_near_ties(ol, k, "bf16", seed=300 + k, mode=mode)
     ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
@@ -121,7 +128,7 @@ def test_a3b_layer_full_size(dfv, a3b, k, mode):
     assert _max_rel_err(_gpu_out_np(out), ref) <= TOL_BF16
 
 
-def test_block_rows_equal_single_token_calls(dfv, a3b):
+def test_block_rows_equal_single_token_calls(dfv, a3b, path):
     """Losslessness on the GPU: row t of a 16-row block is bit-identical to the
     k=1 call on that row (fixed per-element summation order)."""
     lw, ol, L = a3b
@@ -164,7 +171,7 @@ def test_signed_zeros_do_not_change_results(dfv):
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
 
-def test_workspace_reuse_and_host_variant(dfv, a3b):
+def test_workspace_reuse_and_host_variant(dfv, a3b, path):
     lw, ol, L = a3b
     ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
     xa = inputs.make_hidden(16, 2048, "bf16", seed=14, device="cuda")
@@ -227,7 +234,7 @@ def test_accept_geometric_planted_lengths(dfv):
 # ---------------------------------------------------------------- stack
 
 
-def test_stack_teacher_forced_and_fused(dfv):
+def test_stack_teacher_forced_and_fused(dfv, path):
     """Pre-norm residual stack: each GPU layer checked against the oracle on the
     GPU's own layer input; the one-call stack equals the layer-by-layer calls."""
     shape = inputs.LayerShape(d=512, n_experts=32, top_k=4, d_ff=128)
@@ -262,3 +269,22 @@ def test_stack_teacher_forced_and_fused(dfv):
     dfv.moe_stack_forward(Ls, xs, ws)
     torch.cuda.synchronize()
     assert torch.equal(xs, x)
+
+
+def test_fused_and_multikernel_paths_agree(dfv, a3b):
+    """Both kernel paths compute the same function: equal routing, outputs
+    within the bf16 tolerance of each other."""
+    lw, ol, L = a3b
+    x = inputs.make_hidden(16, 2048, "bf16", seed=16, device="cuda")
+    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
+    outs, idxs = [], []
+    for fused in (True, False):
+        dfv.set_path(fused)
+        idx = torch.empty(16, 8, dtype=torch.int32, device="cuda")
+        outs.append(dfv.moe_block_forward(L, x, ws, topk_idx=idx).clone())
+        idxs.append(idx)
+    dfv.set_path(True)
+    assert torch.equal(idxs[0], idxs[1])
+    a, b = outs[0].double(), outs[1].double()
+    assert (a - b).abs().max().item() <= TOL_BF16 * b.abs().max().item()
+    assert dfv.read_device_error(ws) == 0
