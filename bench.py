@@ -331,6 +331,7 @@ def run_gpu(args):
 
     layer_bytes = float(W16.sum().item()) * exp_bytes / N_LAYERS + router_bytes  # per launch
     ph = per_phase()
+    fused_used = dfv.last_layer_path() == 1
     fused_ms = ph[0] + ph[1] + ph[2]
     fused_gbs = layer_bytes / (fused_ms * 1e-3) / 1e9
     dfv.set_path(False)
@@ -422,6 +423,7 @@ def run_gpu(args):
         "woken_mean": {"k16": float(W16.double().mean().item()), "k1": float(W1.double().mean().item())},
         "verify_decode": {"latency_ratio": ratio, "woken_byte_ratio": byte_ratio,
                           "quotient": byte_ratio / ratio},
+        "kernel_path": {"fused": fused_used, "why_not": dfv.fused_unavailable_reason()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
         "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen,

@@ -227,6 +227,14 @@ int dfv_profile_set_events(void *const *events, int n_events);
  */
 int dfv_set_path(int path);
 
+/* Path the last layer call from this host thread took: 1 fused, 0
+ * multi-kernel, -1 none yet. */
+int dfv_last_layer_path(void);
+
+/* Why the fused path could not be set up on this device (empty if it could,
+ * or if it was never tried). */
+const char *dfv_fused_unavailable_reason(void);
+
 const char *dfv_status_string(int status);
 const char *dfv_last_error_detail(void);
 int dfv_version(void);

@@ -15,6 +15,8 @@ namespace {
 thread_local std::string g_detail;
 thread_local cudaEvent_t g_events[4];
 thread_local bool g_profile = false;
+thread_local int g_last_path = -1;
+std::string g_fused_why;  // why the fused path is unavailable (first failure)
 
 inline void mark(int i, cudaStream_t s) {
   if (g_profile) cudaEventRecord(g_events[i], s);
@@ -162,7 +164,12 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
     std::lock_guard<std::mutex> lock(mu);
     auto key = std::make_tuple(dev, k <= 8 ? 1 : 2, plan.smem);
     auto it = cache.find(key);
-    if (it == cache.end()) it = cache.emplace(key, dfv::fused_max_grid(plan, k)).first;
+    if (it == cache.end()) {
+      char why[256] = {0};
+      const int gmax = dfv::fused_max_grid(plan, k, why, sizeof why);
+      if (gmax <= 0 && g_fused_why.empty()) g_fused_why = why;
+      it = cache.emplace(key, gmax).first;
+    }
     grid = it->second;
   }
   if (grid <= 0) return -1;
@@ -205,8 +212,12 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
               bool fuse_norm, float eps, int32_t *u_idx, int32_t *u_nw, const dfv::Workspace &w, cudaStream_t s) {
   if (g_fused_enabled) {
     const int st = run_layer_fused(L, x, act, k, out, residual, fuse_norm, eps, u_idx, u_nw, w, s);
-    if (st >= 0) return st;
+    if (st >= 0) {
+      g_last_path = 1;
+      return st;
+    }
   }
+  g_last_path = 0;
   dfv::RouterParams rp = router_params(L, x, act, k, w);
   rp.fuse_norm = fuse_norm ? 1 : 0;
   rp.eps = eps;
@@ -380,6 +391,10 @@ int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, in
   }
   return DFV_OK;
 }
+
+int dfv_last_layer_path(void) { return g_last_path; }
+
+const char *dfv_fused_unavailable_reason(void) { return g_fused_why.c_str(); }
 
 int dfv_set_path(int path) {
   if (path != 0 && path != 1) return fail(DFV_ERR_INVALID_ARG, "path must be 0 (multi-kernel) or 1 (fused)");

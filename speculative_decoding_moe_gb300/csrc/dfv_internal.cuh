@@ -258,7 +258,7 @@ struct TmaPlan {
 bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
 // Fused single-launch layer (bf16): plan, grid (0 = cannot run) and launch.
 bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
-int fused_max_grid(const FusedPlan &plan, int k);
+int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
 cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);

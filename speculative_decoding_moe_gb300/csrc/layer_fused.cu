@@ -33,6 +33,8 @@
 //       the output: the result of a token depends only on its own row, so a
 //       block and k single-token calls agree bit for bit.
 // Every wait is bounded (2 s) and reports through the workspace error word.
+#include <cstdio>
+
 #include "dfv_internal.cuh"
 
 namespace dfv {
@@ -617,14 +619,31 @@ cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid,
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-int fused_max_grid(const FusedPlan &plan, int k) {
+int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
   int dev = 0, sms = 0, per = 0;
   cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    snprintf(why, why_len, "SM count query: %s", cudaGetErrorString(e));
+    return 0;
+  }
   auto kern = k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, kFT, plan.smem) != cudaSuccess) return 0;
-  return per >= 1 ? sms : 0;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    snprintf(why, why_len, "shared memory %zu B: %s", plan.smem, cudaGetErrorString(e));
+    return 0;
+  }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, kFT, plan.smem);
+  if (e != cudaSuccess || per < 1) {
+    cudaGetLastError();
+    cudaFuncAttributes fa;
+    cudaFuncGetAttributes(&fa, kern);
+    snprintf(why, why_len, "occupancy %d (%s): regs %d, static smem %zu, max threads %d, dyn smem %zu", per,
+             cudaGetErrorString(e), fa.numRegs, fa.sharedSizeBytes, fa.maxThreadsPerBlock, plan.smem);
+    return 0;
+  }
+  return sms;
 }
 
 }  // namespace dfv

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libdfv.so")
 F32, BF16, MXFP4 = 0, 1, 2
 _NAMES = {"f32": F32, "bf16": BF16, "mxfp4": MXFP4}
 EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_profile_set_events",
-           "dfv_read_device_error", "dfv_set_path",
+           "dfv_read_device_error", "dfv_set_path", "dfv_last_layer_path", "dfv_fused_unavailable_reason",
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
            "dfv_accept_workspace_size", "dfv_accept_greedy")
@@ -68,6 +68,8 @@ def _load():
         L.dfv_profile_set_events.argtypes = [P, I]
         L.dfv_read_device_error.argtypes = [P, P, P]
         L.dfv_set_path.argtypes = [I]
+        L.dfv_last_layer_path.restype = I
+        L.dfv_fused_unavailable_reason.restype = ctypes.c_char_p
         _lib = L
     return _lib
 
@@ -217,3 +219,12 @@ def read_device_error(ws: torch.Tensor, stream=None) -> int:
 def set_path(fused: bool):
     """Select the fused single-launch layer kernel (default) or the multi-kernel path."""
     _check(_load().dfv_set_path(1 if fused else 0), "dfv_set_path")
+
+
+def last_layer_path() -> int:
+    """1 if the last layer call from this thread ran the fused kernel, 0 if multi-kernel."""
+    return int(_load().dfv_last_layer_path())
+
+
+def fused_unavailable_reason() -> str:
+    return _load().dfv_fused_unavailable_reason().decode()

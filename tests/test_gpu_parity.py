@@ -122,6 +122,7 @@ def test_a3b_layer_full_size(dfv, a3b, path, k, mode):
     nw = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = dfv.moe_block_forward(L, xg, ws, n_woken=nw)
     torch.cuda.synchronize()
+    assert dfv.last_layer_path() == (1 if path == "fused" else 0), dfv.fused_unavailable_reason()
     assert int(nw.item()) == W
     assert dfv.read_device_error(ws) == 0
     ref = oracle.moe_forward(ol, np_of(x), nthreads=oracle.num_threads_available())
