@@ -112,7 +112,7 @@ __device__ __forceinline__ void load8_bf16(const void *base, size_t elem, float 
 __device__ __forceinline__ float rnd_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 template <int NT>
-__global__ void __maxnreg__(112) moe_fused_kernel(FusedParams p) {
+__global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(128) unsigned char smem[];
