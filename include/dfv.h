@@ -235,6 +235,27 @@ int dfv_last_layer_path(void);
  * or if it was never tried). */
 const char *dfv_fused_unavailable_reason(void);
 
+/*
+ * Allocation-free greedy acceptance.  The method's pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory (a
+ * runtime with a fixed memory budget, or plain C host code with no allocator
+ * of its own to create the workspace dfv_accept_greedy needs).  It computes
+ * exactly what dfv_accept_greedy computes, with the same arguments minus the
+ * workspace; logits, draft, tau and committed are still the caller's device
+ * buffers.
+ * Its scratch is a fixed device array inside libdfv.so (about 41 KB, enough
+ * for every k <= 16 and any V) that each GPU holds until the process exits.
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * Each call clears the array's ticket with cudaMemsetAsync on `stream` and
+ * allocates nothing.  All calls share the array: calls whose kernels overlap
+ * on the GPU race; order them (one stream, or synchronise).
+ * Returns DFV_ERR_UNSUPPORTED if a launch would need more vocabulary slices
+ * than the array holds (cannot happen within the documented limits).
+ */
+int dfv_accept_greedy_noalloc(const void *logits, int dtype, int k, int V, const int32_t *draft,
+                              int32_t *tau, int32_t *committed, void *stream);
+
 const char *dfv_status_string(int status);
 const char *dfv_last_error_detail(void);
 int dfv_version(void);

@@ -11,6 +11,8 @@
 // the largest logit with the lowest column among equals.  The last CTA to
 // finish (atomic ticket, no waiting) reduces the slices of every row, matches
 // the draft prefix and writes tau and the committed tokens.
+#include <mutex>
+
 #include "dfv_internal.cuh"
 
 namespace dfv {
@@ -124,4 +126,48 @@ cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, accept_kernel, p);
 }
 
+}  // namespace dfv
+
+// ----------------------------------------------------------------------------
+// Allocation-free variant of the acceptance launch.
+//
+// Some callers cannot allocate device memory: a runtime that hands the
+// library a fixed memory budget, a caller that owns no allocator (plain C host
+// code without access to the framework's caching allocator), or code that must
+// not call cudaMalloc on its path.  For them the acceptance kernel's scratch
+// (one 64-bit partial per CTA plus the last-CTA ticket) lives in this
+// file-scope device array instead of a caller-provided workspace.  Every GPU
+// that loads the library keeps the array (about 41 KB) until the process
+// exits.  All calls share it: calls whose kernels overlap on the GPU race, so
+// such calls must be ordered (one stream, or synchronised).
+namespace dfv {
+namespace {
+constexpr int kNoAllocMaxChunks = 304;
+constexpr size_t kNoAllocPartials = (size_t)(kMaxBlock + 1) * kNoAllocMaxChunks;
+// [0, 32): ticket counter (first 4 bytes); [32, 32 + kNoAllocPartials): partials
+static __device__ __align__(256) unsigned long long g_accept_scratch[32 + kNoAllocPartials];
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[256];  // per device ordinal, set up once
+}  // namespace
+
+cudaError_t accept_noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *ptr = nullptr;
+    // The array's name is only a host-side stand-in: the device address of
+    // this device's copy has to be looked up with the device current.
+    e = cudaGetSymbolAddress(&ptr, g_accept_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+int accept_noalloc_max_chunks() { return kNoAllocMaxChunks; }
 }  // namespace dfv

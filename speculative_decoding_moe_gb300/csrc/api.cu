@@ -446,4 +446,41 @@ int dfv_accept_greedy(const void *logits, int dtype, int k, int V, const int32_t
   return DFV_OK;
 }
 
+int dfv_accept_greedy_noalloc(const void *logits, int dtype, int k, int V, const int32_t *draft, int32_t *tau,
+                              int32_t *committed, void *stream) {
+  if (k < 0 || k > DFV_MAX_BLOCK) return fail(DFV_ERR_INVALID_ARG, "k=%d outside 0..%d", k, DFV_MAX_BLOCK);
+  if (V < 1) return fail(DFV_ERR_INVALID_ARG, "V=%d < 1", V);
+  if (dtype != DFV_BF16 && dtype != DFV_F32) return fail(DFV_ERR_UNSUPPORTED, "logits dtype %d", dtype);
+  if (!logits || !aligned(logits, 16) || !tau || (k > 0 && !draft))
+    return fail(DFV_ERR_INVALID_ARG, "logits/tau/draft NULL or logits not 16-byte aligned");
+  int chunks = (304 + k) / (k + 1);
+  const int maxc = (V + 1023) / 1024;
+  if (chunks > maxc) chunks = maxc;
+  if (chunks < 1) chunks = 1;
+  if (chunks > dfv::accept_noalloc_max_chunks())
+    return fail(DFV_ERR_UNSUPPORTED, "%d vocabulary slices exceed the fixed scratch (%d)", chunks,
+                dfv::accept_noalloc_max_chunks());
+  void *scratch = nullptr;
+  cudaError_t e = dfv::accept_noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "fixed scratch lookup (cudaGetSymbolAddress)");
+  cudaStream_t s = (cudaStream_t)stream;
+  // the ticket must start at zero: clear it in stream order (no allocation)
+  e = cudaMemsetAsync(scratch, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch ticket");
+  dfv::AcceptParams p = {};
+  p.logits = logits;
+  p.draft = draft;
+  p.tau = tau;
+  p.committed = committed;
+  p.k = k;
+  p.V = V;
+  p.dtype = dtype;
+  p.chunks = chunks;
+  p.cnt = (unsigned *)scratch;
+  p.partial = (unsigned long long *)scratch + 32;
+  e = dfv::launch_accept(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "accept launch");
+  return DFV_OK;
+}
+
 }  // extern "C"

@@ -263,4 +263,7 @@ cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, 
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);
+// device address of the fixed acceptance scratch array on the current device
+cudaError_t accept_noalloc_scratch(void **out);
+int accept_noalloc_max_chunks();
 }  // namespace dfv

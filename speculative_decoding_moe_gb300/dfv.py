@@ -18,6 +18,7 @@ F32, BF16, MXFP4 = 0, 1, 2
 _NAMES = {"f32": F32, "bf16": BF16, "mxfp4": MXFP4}
 EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_profile_set_events",
            "dfv_read_device_error", "dfv_set_path", "dfv_last_layer_path", "dfv_fused_unavailable_reason",
+           "dfv_accept_greedy_noalloc",
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
            "dfv_accept_workspace_size", "dfv_accept_greedy")
@@ -66,6 +67,7 @@ def _load():
         L.dfv_accept_workspace_size.argtypes = [I, I]
         L.dfv_accept_greedy.argtypes = [P, I, I, I, P, P, P, P, S, P]
         L.dfv_profile_set_events.argtypes = [P, I]
+        L.dfv_accept_greedy_noalloc.argtypes = [P, I, I, I, P, P, P, P]
         L.dfv_read_device_error.argtypes = [P, P, P]
         L.dfv_set_path.argtypes = [I]
         L.dfv_last_layer_path.restype = I
@@ -228,3 +230,19 @@ def last_layer_path() -> int:
 
 def fused_unavailable_reason() -> str:
     return _load().dfv_fused_unavailable_reason().decode()
+
+
+def accept_greedy_noalloc(logits: torch.Tensor, draft: torch.Tensor, tau: Optional[torch.Tensor] = None,
+                          committed: Optional[torch.Tensor] = None, stream=None):
+    """Greedy acceptance with the library's fixed device scratch (no workspace)."""
+    rows, V = logits.shape
+    k = rows - 1
+    dev = logits.device
+    if tau is None:
+        tau = torch.empty(1, dtype=torch.int32, device=dev)
+    if committed is None:
+        committed = torch.empty(k + 1, dtype=torch.int32, device=dev)
+    st = _load().dfv_accept_greedy_noalloc(_p(logits), _act(logits), k, V, _p(draft), _p(tau), _p(committed),
+                                           _stream(stream))
+    _check(st, "dfv_accept_greedy_noalloc")
+    return tau, committed
