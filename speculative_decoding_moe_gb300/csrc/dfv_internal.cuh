@@ -225,6 +225,13 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uns
     }
   }
 }
+// mbar_wait with the ready case inlined (no call when the phase is complete).
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, unsigned *err, unsigned code,
+                                               volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity, err, code, abort);
+}
+
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {

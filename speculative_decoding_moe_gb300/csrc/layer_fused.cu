@@ -21,8 +21,8 @@
 //       stages of 8 gate + 8 up rows x `ks` columns (1-D bulk copies into an
 //       mbarrier ring); the 16 consumer warps split the columns, run
 //       m16n8k16 MMAs (gate rows = M 0-7, up rows = M 8-15, tokens = N) and
-//       reduce across warps in fixed order; h = silu(g) * u is written as a
-//       bf16 hi/lo pair.  The producer then runs ahead into P3's weights.
+//       reduce across warps in fixed order; h = silu(g) * u is written in
+//       bf16.  The producer then runs ahead into P3's weights.
 //       -- grid barrier 2 (consumers only) --
 //   P3  down: CTA b owns 16-row tiles b, b+G, ... of d; for each it streams
 //       the tile's rows of every woken expert (one contiguous copy each); two
@@ -45,6 +45,7 @@ constexpr int kFT = kFC + 32;     // + producer warp
 constexpr int kBarAll = 1;        // named barrier: all consumers
 constexpr int kBarGroup = 2;      // named barriers 2, 3: consumer groups of 8 warps
 constexpr int kRing = 4;          // ring stages (even: P3 gives each group two)
+constexpr int kMaxChunksP2 = 2;   // 32-column chunks per consumer warp per gate/up stage (ks <= 1024)
 
 __device__ __forceinline__ int fpad(int bytes) { return (bytes % 128 == 0) ? bytes + 64 : bytes; }
 
@@ -84,26 +85,6 @@ __device__ bool grid_sync(const FusedParams &p, unsigned nb) {
   return true;
 }
 
-// Sum of 16 per-lane values over the warp with 16 shuffles: lane l ends with the
-// total of value index ((l>>4)&1)*8 + ((l>>3)&1)*4 + ((l>>2)&1)*2 + ((l>>1)&1).
-__device__ __forceinline__ float warp_sum16(float (&v)[16]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int h = 8, o = 16; h >= 1; h >>= 1, o >>= 1) {
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < h; ++i) {
-      const float send = up ? v[i] : v[i + h];
-      const float keep = up ? v[i + h] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-__device__ __forceinline__ int warp_sum16_index(int lane) {
-  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-}
-
 __device__ __forceinline__ void load8_bf16(const void *base, size_t elem, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(base) + elem);
   f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
@@ -134,7 +115,6 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   __shared__ int s_eoff[kMaxExperts];
   __shared__ int s_gat[kMaxBlock * kMaxTopK];
   __shared__ unsigned s_mask[kMaxBlock * (kMaxExperts / 32)];
-  __shared__ float s_part[kFW][16];
   __shared__ float s_inv[kMaxBlock];
   __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_tok[16];
@@ -154,116 +134,112 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 
   const bool consumer = warp < kFW;
   // ------------------------------------------------------------------ P0: router GEMV
+  // Warp t computes token t's logits for this CTA's experts: lane-sequential
+  // products over its 16-byte chunks, then a fixed butterfly.  A token's logit
+  // therefore depends on nothing but its own row (the same in every block).
   if (consumer) {
-    if (p.fuse_norm) {
-      float ss[16];
+    if (warp < k) {
+      const int t = warp;
+      const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
+      float inv = 1.f;
+      if (p.fuse_norm) {
+        float ss = 0.f;
+        for (int c = lane; c < d / 8; c += 32) {
+          float f[8];
+          load8_bf16(xr, (size_t)c * 8, f);
 #pragma unroll
-      for (int t = 0; t < 16; ++t) ss[t] = 0.f;
-      for (int c = tid; c < d / 8; c += kFC) {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          if (t < k) {
-            float f[8];
-            load8_bf16(p.x, (size_t)t * d + c * 8, f);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) ss[t] = fmaf(f[q], f[q], ss[t]);
-          }
+          for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        inv = 1.0f / sqrtf(ss / (float)d + p.eps);
+        if (lane == 0) s_inv[t] = inv;
       }
-      const float r = warp_sum16(ss);
-      if ((lane & 1) == 0) s_part[warp][warp_sum16_index(lane)] = r;
-      bar_sync_n(kBarAll, kFC);
-      if (tid < k) {
-        float a = 0.f;
-        for (int w = 0; w < kFW; ++w) a += s_part[w][tid];
-        s_inv[tid] = 1.0f / sqrtf(a / (float)d + p.eps);
-      }
-      bar_sync_n(kBarAll, kFC);
-    }
-    for (int e = blockIdx.x; e < E; e += G) {
-      float acc[16];
+      for (int e = blockIdx.x; e < E; e += G) {
+        const uint16_t *wr = reinterpret_cast<const uint16_t *>(p.wr) + (size_t)e * d;
+        float acc = 0.f;
+        for (int c = lane; c < d / 8; c += 32) {
+          float f[8], w8[8];
+          load8_bf16(xr, (size_t)c * 8, f);
+          load8_bf16(wr, (size_t)c * 8, w8);
+          if (p.fuse_norm) {
 #pragma unroll
-      for (int t = 0; t < 16; ++t) acc[t] = 0.f;
-      for (int c = tid; c < d / 8; c += kFC) {
-        float w8[8];
-        load8_bf16(p.wr, (size_t)e * d + c * 8, w8);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          if (t < k) {
-            float f[8];
-            load8_bf16(p.x, (size_t)t * d + c * 8, f);
-            if (p.fuse_norm) {
-              const float inv = s_inv[t];
-#pragma unroll
-              for (int q = 0; q < 8; ++q) f[q] = rnd_bf16(f[q] * inv);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[t] = fmaf(f[q], w8[q], acc[t]);
+            for (int q = 0; q < 8; ++q) f[q] = rnd_bf16(f[q] * inv);
           }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc = fmaf(f[q], w8[q], acc);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) p.ws.logits[(size_t)t * E + e] = acc;
       }
-      const float r = warp_sum16(acc);
-      if ((lane & 1) == 0) s_part[warp][warp_sum16_index(lane)] = r;
-      bar_sync_n(kBarAll, kFC);
-      if (tid < k) {
-        float a = 0.f;
-        for (int w = 0; w < kFW; ++w) a += s_part[w][tid];
-        p.ws.logits[(size_t)tid * E + e] = a;
-      }
-      bar_sync_n(kBarAll, kFC);
     }
+    for (int i = tid; i < kMaxBlock * (kMaxExperts / 32); i += kFC) s_mask[i] = 0u;
+    bar_sync_n(kBarAll, kFC);
     // ---- grid barrier 1: every CTA's logits are published
     if (tid == 0 && !grid_sync(p, 1)) s_abort = 1;
     bar_sync_n(kBarAll, kFC);
 
     // ---------------------------------------------------------------- P1: routing
-    float *lg = reinterpret_cast<float *>(scratch);
-    for (int i = tid; i < k * E; i += kFC) lg[i] = __ldcg(p.ws.logits + i);
-    for (int i = tid; i < kMaxExperts; i += kFC) s_eoff[i] = 0;
-    for (int i = tid; i < kMaxBlock * (kMaxExperts / 32); i += kFC) s_mask[i] = 0u;
-    bar_sync_n(kBarAll, kFC);
+    // Warp t: top-K of row t (lane holds experts lane + 32 q), then the routing
+    // weights in parallel over the K lanes.
     if (warp < k) {
-      // lane owns experts lane + 32 q; keys are monotone in the logit, 0 = taken/empty
       const int t = warp;
       uint32_t key[8];
+      float val[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int e = lane + 32 * q;
-        key[q] = (e < E) ? max(float_key(lg[t * E + e]), 1u) : 0u;
+        val[q] = (e < E) ? __ldcg(p.ws.logits + (size_t)t * E + e) : 0.f;
+        key[q] = (e < E) ? max(float_key(val[q]), 1u) : 0u;
       }
+      int sel_id = 0;
+      float sel_val = 0.f;
       for (int s = 0; s < K; ++s) {
         uint32_t bk = 0;
         int bq = 0;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           if (key[q] > bk) { bk = key[q]; bq = q; }
+        float bv = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q == bq) bv = val[q];
         const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
         const uint32_t cand = (bk == m) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu;
         const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+        const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31));
         if ((int)(win & 31) == lane) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             if (q == (int)(win >> 5)) key[q] = 0u;
         }
-        if (lane == 0) s_idx[t * K + s] = (int)win;
+        if (lane == s) { sel_id = (int)win; sel_val = wv; }
       }
-      __syncwarp();
-      if (lane == 0) {
-        const float m0 = lg[t * E + s_idx[t * K]];
-        float denom = 0.f;
-        if (p.norm_topk) {
-          for (int s = 0; s < K; ++s) denom += expf(lg[t * E + s_idx[t * K + s]] - m0);
-        } else {
-          for (int j = 0; j < E; ++j) denom += expf(lg[t * E + j] - m0);
-        }
-        for (int s = 0; s < K; ++s) s_w[t * K + s] = expf(lg[t * E + s_idx[t * K + s]] - m0) / denom;
+      const float m0 = __shfl_sync(0xffffffffu, sel_val, 0);
+      const float z = (lane < K) ? expf(sel_val - m0) : 0.f;
+      float den = 0.f;
+      if (p.norm_topk) {
+        den = z;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (lane + 32 * q < E) den += expf(val[q] - m0);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      if (lane < K) {
+        s_idx[t * K + lane] = sel_id;
+        s_w[t * K + lane] = z / den;
+        atomicOr(&s_mask[t * (kMaxExperts / 32) + (sel_id >> 5)], 1u << (sel_id & 31));
       }
     }
     bar_sync_n(kBarAll, kFC);
-    for (int q = tid; q < k * K; q += kFC) {
-      const int t = q / K, ex = s_idx[q];
-      atomicAdd(&s_eoff[ex], 1);
-      atomicOr(&s_mask[t * (kMaxExperts / 32) + (ex >> 5)], 1u << (ex & 31));
+    // per-expert pair counts from the row masks
+    if (tid < E) {
+      int cnt = 0;
+      for (int t = 0; t < k; ++t) cnt += (s_mask[t * (kMaxExperts / 32) + (tid >> 5)] >> (tid & 31)) & 1u;
+      s_eoff[tid] = cnt;
     }
     bar_sync_n(kBarAll, kFC);
     {
@@ -336,7 +312,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
         const int e = s_woken[u / tiles_g], i0 = (u % tiles_g) * kGateTile;
         for (int sl = 0; sl < nsl; ++sl, ++it) {
           const int s = it % kRing;
-          if (!mbar_wait(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+          if (!mbar_wait_fast(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
             ok = false;
             break;
           }
@@ -352,7 +328,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
       for (int tl = blockIdx.x; tl < tiles_d && ok; tl += G) {
         for (int wi = 0; wi < nW; ++wi, ++it) {
           const int s = it % kRing;
-          if (!mbar_wait(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+          if (!mbar_wait_fast(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
             ok = false;
             break;
           }
@@ -373,8 +349,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
     const int c0 = warp * cps / kFW, c1 = (warp + 1) * cps / kFW;
     const uint16_t *xg = reinterpret_cast<const uint16_t *>(p.x);
     const int cpr = d / 8;
-    uint16_t *hhi = reinterpret_cast<uint16_t *>(p.ws.h);
-    uint16_t *hlo = hhi + (size_t)k * K * I;
+    uint16_t *hbf = reinterpret_cast<uint16_t *>(p.ws.h);  // h rounded to bf16, [k*K][d_ff]
     const uint32_t xs = sbase + kRing * slot;
     int cur = -1, m = 0, off = 0, it = 0;
     bool dead = s_abort != 0;
@@ -411,28 +386,41 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
         for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
       for (int sl = 0; sl < nsl; ++sl, ++it) {
         const int s = it % kRing;
-        if (!dead && !mbar_wait(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        // A fragments go to registers first and the slot is released at once,
+        // so the producer refills it while the MMAs run
+        uint4 ag[kMaxChunksP2], au[kMaxChunksP2];
         if (!dead) {
           const uint32_t st = sbase + s * slot;
-          for (int ch = c0; ch < c1; ++ch) {
-            const uint32_t q16 = (ch * 4 + c) * 16;
-            const uint4 ag = lds128(st + g * rsg + q16);
-            const uint4 au = lds128(st + (8 + g) * rsg + q16);
-            const int xq = sl * (ks / 8) + ch * 4 + c;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              if (nt * 8 < m) {
-                const int row = nt * 8 + g;
-                uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                if (row < m) b = lds128(xs + row * rsx + (xq ^ ((row & 1) ? p.swz_x : 0)) * 16);
-                mma_bf16(acc[nt], ag.x, au.x, ag.y, au.y, b.x, b.y);
-                mma_bf16(acc[nt], ag.z, au.z, ag.w, au.w, b.z, b.w);
-              }
+          for (int j = 0; j < kMaxChunksP2; ++j) {
+            if (c0 + j < c1) {
+              const uint32_t q16 = ((c0 + j) * 4 + c) * 16;
+              ag[j] = lds128(st + g * rsg + q16);
+              au[j] = lds128(st + (8 + g) * rsg + q16);
             }
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (!dead) {
+#pragma unroll
+          for (int j = 0; j < kMaxChunksP2; ++j) {
+            if (c0 + j < c1) {
+              const int xq = sl * (ks / 8) + (c0 + j) * 4 + c;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (nt * 8 < m) {
+                  const int row = nt * 8 + g;
+                  uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                  if (row < m) b = lds128(xs + row * rsx + (xq ^ ((row & 1) ? p.swz_x : 0)) * 16);
+                  mma_bf16(acc[nt], ag[j].x, au[j].x, ag[j].y, au[j].y, b.x, b.y);
+                  mma_bf16(acc[nt], ag[j].z, au[j].z, ag[j].w, au[j].w, b.z, b.w);
+                }
+              }
+            }
+          }
+        }
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -448,12 +436,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
             gs += red[((w * NT + nt) * 32 + ln) * 4 + q];
             us += red[((w * NT + nt) * 32 + ln) * 4 + q + 2];
           }
-          const float hv = silu(gs) * us;
-          const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-          const __nv_bfloat16 lb = __float2bfloat16_rn(hv - __bfloat162float(hb));
           const size_t o = (size_t)(off + tok) * I + i0 + (ln >> 2);
-          hhi[o] = __bfloat16_as_ushort(hb);
-          hlo[o] = __bfloat16_as_ushort(lb);
+          hbf[o] = __bfloat16_as_ushort(__float2bfloat16_rn(silu(gs) * us));
         }
       }
       bar_sync_n(kBarAll, kFC);
@@ -477,20 +461,17 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
         if ((jd & 1) != grp) continue;
         const int s = it % kRing;
         const int eoff = s_off[wi], em = s_off[wi + 1] - eoff;
-        // B fragments (h hi/lo of this expert's tokens) straight from L2
-        uint4 bh[3][NT], bl[3][NT];
+        // B fragments (h of this expert's tokens, bf16) straight from L2,
+        // issued before the stage wait so the two latencies overlap
+        uint4 bh[3][NT];
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             bh[j][nt] = make_uint4(0u, 0u, 0u, 0u);
-            bl[j][nt] = bh[j][nt];
             const int row = nt * 8 + g, ch = d0 + j;
-            if (!dead && ch < d1 && row < em) {
-              const size_t o = (size_t)(eoff + row) * I + ch * 32 + c * 8;
-              bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hhi + o));
-              bl[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hlo + o));
-            }
+            if (!dead && ch < d1 && row < em)
+              bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hbf + (size_t)(eoff + row) * I + ch * 32 + c * 8));
           }
         }
         float acc[NT][4];
@@ -498,30 +479,35 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-        if (!dead && !mbar_wait(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        uint4 a0[3], a1[3];
         if (!dead) {
           const uint32_t st = sbase + s * slot;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
-            const int ch = d0 + j;
-            if (ch < d1) {
-              const uint32_t q16 = (ch * 4 + c) * 16;
-              const uint4 a0 = lds128(st + g * rsd + q16);
-              const uint4 a1 = lds128(st + (g + 8) * rsd + q16);
+            if (d0 + j < d1) {
+              const uint32_t q16 = ((d0 + j) * 4 + c) * 16;
+              a0[j] = lds128(st + g * rsd + q16);
+              a1[j] = lds128(st + (g + 8) * rsd + q16);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_n(empty0 + 8 * s, 2);  // released before the MMAs
+        if (!dead) {
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            if (d0 + j < d1) {
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 if (nt * 8 < em) {
-                  mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bh[j][nt].x, bh[j][nt].y);
-                  mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bh[j][nt].z, bh[j][nt].w);
-                  mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bl[j][nt].x, bl[j][nt].y);
-                  mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bl[j][nt].z, bl[j][nt].w);
+                  mma_bf16(acc[nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
+                  mma_bf16(acc[nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
                 }
               }
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_n(empty0 + 8 * s, 2);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
