@@ -80,13 +80,13 @@ struct FusedParams {
   const void *wr, *wg, *wu, *wd;
   int k, d, I, E, K, norm_topk, fuse_norm, swz_x;
   float eps;
-  int ks, nsl, slot, scratch;  // filled from the plan
+  int ks, nsl, slot, scratch, ring;  // filled from the plan
   Workspace ws;
   int32_t *u_idx, *u_nw;
 };
 
 struct FusedPlan {
-  int ks, nsl, slot, scratch;
+  int ks, nsl, slot, scratch, ring;
   size_t smem;
 };
 
@@ -238,6 +238,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+// Hint: stream `bytes` from global memory into L2 (no completion tracking).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 // Named barrier over the first n threads of the CTA (id 1; id 0 is __syncthreads).
 __device__ __forceinline__ void bar_sync_n(int id, int n) {

@@ -44,7 +44,7 @@ constexpr int kFC = kFW * 32;     // consumer threads
 constexpr int kFT = kFC + 32;     // + producer warp
 constexpr int kBarAll = 1;        // named barrier: all consumers
 constexpr int kBarGroup = 2;      // named barriers 2, 3: consumer groups of 8 warps
-constexpr int kRing = 4;          // ring stages (even: P3 gives each group two)
+constexpr int kMaxRing = 8;       // upper bound of ring stages (barrier arrays)
 constexpr int kMaxChunksP2 = 2;   // 32-column chunks per consumer warp per gate/up stage (ks <= 1024)
 
 __device__ __forceinline__ int fpad(int bytes) { return (bytes % 128 == 0) ? bytes + 64 : bytes; }
@@ -99,14 +99,15 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, E = p.E, K = p.K, ks = p.ks, nsl = p.nsl;
   const int G = gridDim.x;
-  const int rsg = fpad(ks * 2);        // gate/up stage row stride
+  const int rsg = ks * 2;              // gate/up stage row stride (2-way conflicts are cheap)
   const int rsx = d * 2;               // staged x row stride (16B chunks XOR-swizzled)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t slot = p.slot;
-  unsigned char *scratch = smem + kRing * slot;           // x rows / logits / slot table
+  const int SH = p.ring;                                   // ring stages the launch reserved
+  unsigned char *scratch = smem + SH * slot;               // x rows / logits / slot table
   float *red = reinterpret_cast<float *>(scratch + p.scratch);  // [16][NT][32][4]
   const uint32_t full0 = smem_u32(red + kFW * NT * 32 * 4);
-  const uint32_t empty0 = full0 + 8 * kRing;
+  const uint32_t empty0 = full0 + 8 * kMaxRing;
 
   __shared__ int s_idx[kMaxBlock * kMaxTopK];
   __shared__ float s_w[kMaxBlock * kMaxTopK];
@@ -118,13 +119,13 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   __shared__ float s_inv[kMaxBlock];
   __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_tok[16];
-  __shared__ int s_nw;
+  __shared__ int s_nw, s_ring;
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_abort = 0;
-    for (int s = 0; s < kRing; ++s) {
+    for (int s = 0; s <= SH; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kFW);
     }
@@ -272,6 +273,13 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
       s_gat[s_eoff[ex] + rank] = q;
     }
     bar_sync_n(kBarAll, kFC);
+    if (tid == 0) {
+      // with at most 8 tokens per expert the staged-x rows 8..15 are unused:
+      // they become one more ring stage
+      int mmax = 0;
+      for (int i = 0; i < s_nw; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
+      s_ring = (NT == 2 && mmax <= 8 && (uint32_t)(8 * rsx) >= slot && SH < kMaxRing) ? SH + 1 : SH;
+    }
     if (blockIdx.x == 0) {
       const int nW = s_nw;
       for (int q = tid; q < k * K; q += kFC) {
@@ -291,6 +299,11 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   __syncthreads();  // routing tables visible to the producer
 
   const int nW = s_nw;
+  const int S = s_ring;
+  // stage s lives in the reserved ring, or (s == SH) in staged-x rows 8..15
+  auto slot_addr = [&](int st) -> uint32_t {
+    return st < SH ? sbase + (uint32_t)st * slot : sbase + (uint32_t)SH * slot + 8u * rsx;
+  };
   const int tiles_g = I / kGateTile;
   int lo_g, hi_g;
   {
@@ -311,12 +324,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
       for (int u = lo_g; u < hi_g && ok; ++u) {
         const int e = s_woken[u / tiles_g], i0 = (u % tiles_g) * kGateTile;
         for (int sl = 0; sl < nsl; ++sl, ++it) {
-          const int s = it % kRing;
-          if (!mbar_wait_fast(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+          const int s = it % S;
+          if (!mbar_wait_fast(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full0 + 8 * s, dst = sbase + s * slot;
+          const uint32_t fb = full0 + 8 * s, dst = slot_addr(s);
           mbar_expect_tx(fb, 16u * ks * 2);
           for (int r = 0; r < 8; ++r) {
             const size_t row = ((size_t)e * I + i0 + r) * d + (size_t)sl * ks;
@@ -327,20 +340,20 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
       }
       for (int tl = blockIdx.x; tl < tiles_d && ok; tl += G) {
         for (int wi = 0; wi < nW; ++wi, ++it) {
-          const int s = it % kRing;
-          if (!mbar_wait_fast(empty0 + 8 * s, ((it / kRing) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+          const int s = it % S;
+          if (!mbar_wait_fast(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * s;
           mbar_expect_tx(fb, 16u * I * 2);
-          bulk_g2s(sbase + s * slot, wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb);
+          bulk_g2s(slot_addr(s), wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb);
         }
       }
       // no copy may land after the CTA exits
       volatile int never = 0;
-      for (int j = it - kRing < 0 ? 0 : it - kRing; j < it; ++j)
-        if (!mbar_wait(full0 + 8 * (j % kRing), (j / kRing) & 1, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never)) break;
+      for (int j = it - S < 0 ? 0 : it - S; j < it; ++j)
+        if (!mbar_wait(full0 + 8 * (j % S), (j / S) & 1, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never)) break;
     }
   } else {
     // ---------------------------------------------------------------- P2: gate/up
@@ -350,7 +363,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
     const uint16_t *xg = reinterpret_cast<const uint16_t *>(p.x);
     const int cpr = d / 8;
     uint16_t *hbf = reinterpret_cast<uint16_t *>(p.ws.h);  // h rounded to bf16, [k*K][d_ff]
-    const uint32_t xs = sbase + kRing * slot;
+    const uint32_t xs = sbase + SH * slot;
     int cur = -1, m = 0, off = 0, it = 0;
     bool dead = s_abort != 0;
     for (int u = lo_g; u < hi_g; ++u) {
@@ -379,19 +392,21 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
         }
         bar_sync_n(kBarAll, kFC);
       }
-      float acc[NT][4];
+      float acc2[kMaxChunksP2][NT][4];  // one MMA chain per chunk slot: shorter dependency chains
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int j = 0; j < kMaxChunksP2; ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc2[j][nt][q] = 0.f;
       for (int sl = 0; sl < nsl; ++sl, ++it) {
-        const int s = it % kRing;
-        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        const int s = it % S;
+        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
         // A fragments go to registers first and the slot is released at once,
         // so the producer refills it while the MMAs run
         uint4 ag[kMaxChunksP2], au[kMaxChunksP2];
         if (!dead) {
-          const uint32_t st = sbase + s * slot;
+          const uint32_t st = slot_addr(s);
 #pragma unroll
           for (int j = 0; j < kMaxChunksP2; ++j) {
             if (c0 + j < c1) {
@@ -414,8 +429,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
                   const int row = nt * 8 + g;
                   uint4 b = make_uint4(0u, 0u, 0u, 0u);
                   if (row < m) b = lds128(xs + row * rsx + (xq ^ ((row & 1) ? p.swz_x : 0)) * 16);
-                  mma_bf16(acc[nt], ag[j].x, au[j].x, ag[j].y, au[j].y, b.x, b.y);
-                  mma_bf16(acc[nt], ag[j].z, au[j].z, ag[j].w, au[j].w, b.z, b.w);
+                  mma_bf16(acc2[j][nt], ag[j].x, au[j].x, ag[j].y, au[j].y, b.x, b.y);
+                  mma_bf16(acc2[j][nt], ag[j].z, au[j].z, ag[j].w, au[j].w, b.z, b.w);
                 }
               }
             }
@@ -425,7 +440,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         *reinterpret_cast<float4 *>(red + ((warp * NT + nt) * 32 + lane) * 4) =
-            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+            make_float4(acc2[0][nt][0] + acc2[1][nt][0], acc2[0][nt][1] + acc2[1][nt][1],
+                        acc2[0][nt][2] + acc2[1][nt][2], acc2[0][nt][3] + acc2[1][nt][3]);
       bar_sync_n(kBarAll, kFC);
       if (tid < NT * 64) {
         const int nt = tid >> 6, ln = (tid >> 1) & 31, q = tid & 1;
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
       const int r0 = tl * 16;
       for (int wi = 0; wi < nW; ++wi, ++jd, ++it) {
         if ((jd & 1) != grp) continue;
-        const int s = it % kRing;
+        const int s = it % S;
         const int eoff = s_off[wi], em = s_off[wi + 1] - eoff;
         // B fragments (h of this expert's tokens, bf16) straight from L2,
         // issued before the stage wait so the two latencies overlap
@@ -474,15 +490,17 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
               bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hbf + (size_t)(eoff + row) * I + ch * 32 + c * 8));
           }
         }
-        float acc[NT][4];
+        float acc2[2][NT][4];  // two MMA chains (chunks alternate)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / kRing) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc2[j][nt][q] = 0.f;
+        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
         uint4 a0[3], a1[3];
         if (!dead) {
-          const uint32_t st = sbase + s * slot;
+          const uint32_t st = slot_addr(s);
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             if (d0 + j < d1) {
@@ -501,8 +519,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 if (nt * 8 < em) {
-                  mma_bf16(acc[nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
-                  mma_bf16(acc[nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
+                  mma_bf16(acc2[j & 1][nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
+                  mma_bf16(acc2[j & 1][nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
                 }
               }
             }
@@ -511,7 +529,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
-              make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+              make_float4(acc2[0][nt][0] + acc2[1][nt][0], acc2[0][nt][1] + acc2[1][nt][1],
+                          acc2[0][nt][2] + acc2[1][nt][2], acc2[0][nt][3] + acc2[1][nt][3]);
         bar_sync_n(kBarGroup + grp, 256);
         const int gt = tid & 255;
         if (gt < NT * 128) {
@@ -560,8 +579,8 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   while (nsl <= C && (C % nsl) != 0) ++nsl;
   if (nsl > C) return false;
   const int ks = d / nsl;
-  auto pad = [](int b) { return (b % 128 == 0) ? b + 64 : b; };
-  const size_t gslot = (size_t)16 * pad(ks * 2);
+  if (ks / 32 > kFW * kMaxChunksP2) return false;
+  const size_t gslot = (size_t)16 * ks * 2;
   const size_t dslot = (size_t)16 * I * 2;
   size_t slot = gslot > dslot ? gslot : dslot;
   slot = (slot + 127) & ~(size_t)127;
@@ -571,13 +590,18 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   if (ysb > scratch) scratch = ysb;
   scratch = (scratch + 127) & ~(size_t)127;
   const size_t redb = (size_t)kFW * NT * 32 * 16;
-  const size_t smem = kRing * slot + scratch + redb + 16 * kRing;
-  if (smem > 220 * 1024) return false;
+  const size_t budget = 220 * 1024;
+  int ring = 0;
+  for (int r = kMaxRing - 1; r >= 4; --r) {
+    if (r * slot + scratch + redb + 16 * kMaxRing <= budget) { ring = r; break; }
+  }
+  if (ring < 4) return false;
   plan->ks = ks;
   plan->nsl = nsl;
   plan->slot = (int)slot;
   plan->scratch = (int)scratch;
-  plan->smem = smem;
+  plan->ring = ring;
+  plan->smem = ring * slot + scratch + redb + 16 * kMaxRing;
   return true;
 }
 
@@ -587,6 +611,7 @@ cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid,
   p.nsl = plan.nsl;
   p.slot = plan.slot;
   p.scratch = plan.scratch;
+  p.ring = plan.ring;
   auto kern = p.k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
