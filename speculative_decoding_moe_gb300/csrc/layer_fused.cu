@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, E = p.E, K = p.K, ks = p.ks, nsl = p.nsl;
   const int G = gridDim.x;
-  const int rsg = ks * 2;              // gate/up stage row stride (2-way conflicts are cheap)
+  const int rsg = fpad(ks * 2);        // gate/up stage row stride (64 mod 128: conflict-free)
   const int rsx = d * 2;               // staged x row stride (16B chunks XOR-swizzled)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t slot = p.slot;
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
       // they become one more ring stage
       int mmax = 0;
       for (int i = 0; i < s_nw; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
-      s_ring = (NT == 2 && mmax <= 8 && (uint32_t)(8 * rsx) >= slot && SH < kMaxRing) ? SH + 1 : SH;
+      s_ring = (NT == 2 && mmax <= 8 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing) ? SH + 1 : SH;
     }
     if (blockIdx.x == 0) {
       const int nW = s_nw;
@@ -319,13 +319,13 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
       const uint16_t *wg = reinterpret_cast<const uint16_t *>(p.wg);
       const uint16_t *wu = reinterpret_cast<const uint16_t *>(p.wu);
       const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
-      int it = 0;
+      int it = 0, ps = 0, pph = 0;  // fills issued; slot and phase of the next fill
       bool ok = true;
       for (int u = lo_g; u < hi_g && ok; ++u) {
         const int e = s_woken[u / tiles_g], i0 = (u % tiles_g) * kGateTile;
-        for (int sl = 0; sl < nsl; ++sl, ++it) {
-          const int s = it % S;
-          if (!mbar_wait_fast(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+        for (int sl = 0; sl < nsl; ++sl, ++it, ps = (ps + 1 == S) ? 0 : ps + 1, pph ^= (ps == 0)) {
+          const int s = ps;
+          if (!mbar_wait_fast(empty0 + 8 * s, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
             ok = false;
             break;
           }
@@ -339,9 +339,9 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
         }
       }
       for (int tl = blockIdx.x; tl < tiles_d && ok; tl += G) {
-        for (int wi = 0; wi < nW; ++wi, ++it) {
-          const int s = it % S;
-          if (!mbar_wait_fast(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+        for (int wi = 0; wi < nW; ++wi, ++it, ps = (ps + 1 == S) ? 0 : ps + 1, pph ^= (ps == 0)) {
+          const int s = ps;
+          if (!mbar_wait_fast(empty0 + 8 * s, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
             ok = false;
             break;
           }
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
     const int cpr = d / 8;
     uint16_t *hbf = reinterpret_cast<uint16_t *>(p.ws.h);  // h rounded to bf16, [k*K][d_ff]
     const uint32_t xs = sbase + SH * slot;
-    int cur = -1, m = 0, off = 0, it = 0;
+    int cur = -1, m = 0, off = 0, cs = 0, cph = 0;  // slot and phase of the next stage
     bool dead = s_abort != 0;
     for (int u = lo_g; u < hi_g; ++u) {
       const int wi = u / tiles_g, i0 = (u % tiles_g) * kGateTile;
@@ -392,16 +392,14 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
         }
         bar_sync_n(kBarAll, kFC);
       }
-      float acc2[kMaxChunksP2][NT][4];  // one MMA chain per chunk slot: shorter dependency chains
+      float acc[NT][4];
 #pragma unroll
-      for (int j = 0; j < kMaxChunksP2; ++j)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc2[j][nt][q] = 0.f;
-      for (int sl = 0; sl < nsl; ++sl, ++it) {
-        const int s = it % S;
-        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+      for (int sl = 0; sl < nsl; ++sl, cs = (cs + 1 == S) ? 0 : cs + 1, cph ^= (cs == 0)) {
+        const int s = cs;
+        if (!dead && !mbar_wait_fast(full0 + 8 * s, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
         // A fragments go to registers first and the slot is released at once,
         // so the producer refills it while the MMAs run
         uint4 ag[kMaxChunksP2], au[kMaxChunksP2];
@@ -429,8 +427,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
                   const int row = nt * 8 + g;
                   uint4 b = make_uint4(0u, 0u, 0u, 0u);
                   if (row < m) b = lds128(xs + row * rsx + (xq ^ ((row & 1) ? p.swz_x : 0)) * 16);
-                  mma_bf16(acc2[j][nt], ag[j].x, au[j].x, ag[j].y, au[j].y, b.x, b.y);
-                  mma_bf16(acc2[j][nt], ag[j].z, au[j].z, ag[j].w, au[j].w, b.z, b.w);
+                  mma_bf16(acc[nt], ag[j].x, au[j].x, ag[j].y, au[j].y, b.x, b.y);
+                  mma_bf16(acc[nt], ag[j].z, au[j].z, ag[j].w, au[j].w, b.z, b.w);
                 }
               }
             }
@@ -440,8 +438,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         *reinterpret_cast<float4 *>(red + ((warp * NT + nt) * 32 + lane) * 4) =
-            make_float4(acc2[0][nt][0] + acc2[1][nt][0], acc2[0][nt][1] + acc2[1][nt][1],
-                        acc2[0][nt][2] + acc2[1][nt][2], acc2[0][nt][3] + acc2[1][nt][3]);
+            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
       bar_sync_n(kBarAll, kFC);
       if (tid < NT * 64) {
         const int nt = tid >> 6, ln = (tid >> 1) & 31, q = tid & 1;
@@ -473,9 +470,9 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
     int jd = 0;
     for (int tl = blockIdx.x; tl < tiles_d; tl += G) {
       const int r0 = tl * 16;
-      for (int wi = 0; wi < nW; ++wi, ++jd, ++it) {
+      for (int wi = 0; wi < nW; ++wi, ++jd, cs = (cs + 1 == S) ? 0 : cs + 1, cph ^= (cs == 0)) {
         if ((jd & 1) != grp) continue;
-        const int s = it % S;
+        const int s = cs;
         const int eoff = s_off[wi], em = s_off[wi + 1] - eoff;
         // B fragments (h of this expert's tokens, bf16) straight from L2,
         // issued before the stage wait so the two latencies overlap
@@ -490,14 +487,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
               bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hbf + (size_t)(eoff + row) * I + ch * 32 + c * 8));
           }
         }
-        float acc2[2][NT][4];  // two MMA chains (chunks alternate)
+        float acc[NT][4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc2[j][nt][q] = 0.f;
-        if (!dead && !mbar_wait_fast(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+          for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+        if (!dead && !mbar_wait_fast(full0 + 8 * s, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
         uint4 a0[3], a1[3];
         if (!dead) {
           const uint32_t st = slot_addr(s);
@@ -519,8 +514,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 if (nt * 8 < em) {
-                  mma_bf16(acc2[j & 1][nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
-                  mma_bf16(acc2[j & 1][nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
+                  mma_bf16(acc[nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
+                  mma_bf16(acc[nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
                 }
               }
             }
@@ -529,8 +524,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
-              make_float4(acc2[0][nt][0] + acc2[1][nt][0], acc2[0][nt][1] + acc2[1][nt][1],
-                          acc2[0][nt][2] + acc2[1][nt][2], acc2[0][nt][3] + acc2[1][nt][3]);
+              make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
         bar_sync_n(kBarGroup + grp, 256);
         const int gt = tid & 255;
         if (gt < NT * 128) {
@@ -580,11 +574,15 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   if (nsl > C) return false;
   const int ks = d / nsl;
   if (ks / 32 > kFW * kMaxChunksP2) return false;
-  const size_t gslot = (size_t)16 * ks * 2;
+  auto pad = [](int b) { return (b % 128 == 0) ? b + 64 : b; };
+  const size_t gslot = (size_t)16 * pad(ks * 2);
   const size_t dslot = (size_t)16 * I * 2;
   size_t slot = gslot > dslot ? gslot : dslot;
   slot = (slot + 127) & ~(size_t)127;
   size_t scratch = (size_t)NT * 8 * d * 2;
+  // k > 8: staged-x rows 8..15 double as one more ring stage when no expert has
+  // more than 8 tokens; make that space one full slot
+  if (NT == 2 && (size_t)8 * d * 2 < slot + (size_t)8 * d * 2) scratch = (size_t)8 * d * 2 + slot;
   const size_t lgb = (size_t)k * E * 4, ysb = (size_t)k * 8 * 16 * 4;
   if (lgb > scratch) scratch = lgb;
   if (ysb > scratch) scratch = ysb;
