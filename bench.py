@@ -401,6 +401,8 @@ def run_gpu(args):
            "d2h_bytes_per_step": N_LAYERS * ho.numel() * ho.element_size(), "ms_per_step": e2e_ms,
            "api": "dfv_moe_block_forward_host per layer, pinned host buffers"}
 
+    mx = None if args.no_mxfp4 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         nthr = host_threads()
@@ -426,7 +428,7 @@ def run_gpu(args):
         "kernel_path": {"fused": fused_used, "why_not": dfv.fused_unavailable_reason()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
-        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen,
+        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "mxfp4": mx,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -434,6 +436,94 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
+    """mxfp4 experts: E=256, top-8, d=2048, d_ff=512, 40 layers, bf16 activations.
+    Bytes per woken expert count the packed codes and the scale bytes."""
+    shape = inputs.MXFP4
+    layers = [inputs.make_layer(shape, seed=5000 + 1000 * rank + l, device=dev) for l in range(N_LAYERS)]
+    Ls = [dfv.Layer(w) for w in layers]
+    exp_bytes = layers[0].expert_bytes()
+    router_bytes = layers[0].router_bytes()
+    ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], KBLOCK), device=dev)
+
+    def make_pass(k, mode="independent", seed=5):
+        x = inputs.make_hidden(k, shape.d, "bf16", seed=seed + 100 * rank, mode=mode, device=dev)
+        out = torch.empty_like(x)
+        nws = torch.zeros(N_LAYERS, dtype=torch.int32, device=dev)
+
+        def fn():
+            for l in range(N_LAYERS):
+                dfv.moe_block_forward(Ls[l], x, ws, out=out, n_woken=nws[l:l + 1])
+        return fn, nws, x
+
+    def pass_bytes(nws):
+        W = nws.to(torch.int64).cpu()
+        return float(W.sum().item() * exp_bytes + N_LAYERS * router_bytes), W
+
+    fn16, nw16, x16 = make_pass(KBLOCK, seed=15)
+    ms16 = graph_time(fn16, args.warmup, args.steps, barrier)
+    b16, W16 = pass_bytes(nw16)
+    fn1, nw1, _ = make_pass(1, seed=16)
+    ms1 = graph_time(fn1, args.warmup, args.steps, barrier)
+    b1, W1 = pass_bytes(nw1)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(N_LAYERS)]
+    out16 = torch.empty_like(x16)
+    tot = [0.0, 0.0, 0.0]
+    reps = 3
+    for r in range(reps + 1):
+        for l in range(N_LAYERS):
+            dfv.profile_set_events(evs[l])
+            dfv.moe_block_forward(Ls[l], x16, ws, out=out16)
+        dfv.profile_set_events(None)
+        torch.cuda.synchronize()
+        if r:
+            for l in range(N_LAYERS):
+                e = evs[l]
+                for i in range(3):
+                    tot[i] += e[i].elapsed_time(e[i + 1])
+    ph = [t / (reps * N_LAYERS) for t in tot]
+    Wm = float(W16.double().mean().item())
+    gate_bytes = Wm * 2 * (shape.d_ff * shape.d // 2 + shape.d_ff * shape.d // 32)
+    down_bytes = Wm * (shape.d * shape.d_ff // 2 + shape.d * shape.d_ff // 32)
+    layer_bytes = Wm * exp_bytes + router_bytes
+    res = {
+        "config": "E=256 top-8 d=2048 d_ff=512 mxfp4 experts (e2m1 + e8m0/32), bf16 router and activations, "
+                  "40 layers, k=16; inputs > L2 (%.1f GB of weights)" % (N_LAYERS * (exp_bytes * 256 + router_bytes) / 1e9),
+        "value_gbs": b16 / (ms16 * 1e-3) / 1e9, "frac_of_measured_hbm": b16 / (ms16 * 1e-3) / 1e9 / peak_bw,
+        "ms_per_pass": {"k16": ms16, "k1": ms1},
+        "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS},
+        "woken_mean": {"k16": Wm, "k1": float(W1.double().mean().item())},
+        "verify_decode": {"latency_ratio": ms16 / ms1, "woken_byte_ratio": b16 / b1, "quotient": (b16 / b1) / (ms16 / ms1)},
+        "per_launch_us": {"router": ph[0] * 1e3, "gate_up": ph[1] * 1e3, "down_combine": ph[2] * 1e3},
+        "gate_up_gbs": gate_bytes / (ph[1] * 1e-3) / 1e9, "down_combine_gbs": down_bytes / (ph[2] * 1e-3) / 1e9,
+        "layer_gbs_events": layer_bytes / (sum(ph) * 1e-3) / 1e9,
+        "device_error": dfv.read_device_error(ws),
+    }
+    if not args.no_stack:
+        V = 151936
+        xs0 = inputs.make_hidden(KBLOCK, shape.d, "bf16", seed=17 + 100 * rank, device=dev)
+        xs = xs0.clone()
+        logits, toks = inputs.spiked_logits(KBLOCK + 1, V, "bf16", 2.0, seed=18, device=dev)
+        nacc = 5
+        draft = toks[:KBLOCK].clone()
+        draft[nacc] = (draft[nacc] + 1) % V
+        aws = dfv.alloc_workspace(dfv.accept_workspace_size(KBLOCK, V), device=dev)
+        tau = torch.zeros(1, dtype=torch.int32, device=dev)
+        com = torch.zeros(KBLOCK + 1, dtype=torch.int32, device=dev)
+
+        def fn_stack():
+            xs.copy_(xs0)
+            dfv.moe_stack_forward(Ls, xs, ws)
+            dfv.accept_greedy(logits, draft, aws, tau=tau, committed=com)
+
+        ms_stack = graph_time(fn_stack, 2, max(3, args.steps // 4))
+        res["stack40_accept"] = {"ms": ms_stack, "layer_us": ms_stack * 1e3 / N_LAYERS, "tau": int(tau.item()),
+                                 "tau_expected": nacc + 1, "finite": bool(torch.isfinite(xs.float()).all().item())}
+    del layers, Ls
+    return res
 
 
 def main():
@@ -445,6 +535,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-mxfp4", action="store_true", help="skip the mxfp4-expert section")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=40, help="layers per step (profiling runs only)")
     args = ap.parse_args()

@@ -84,11 +84,18 @@ int check_layer(const dfv_moe_layer *L, int act) {
     return fail(DFV_ERR_UNSUPPORTED, "top_k %d outside 1..min(E, %d)", L->top_k, DFV_MAX_TOPK);
   if (L->d % 32 || L->d_ff % 32) return fail(DFV_ERR_UNSUPPORTED, "d and d_ff must be multiples of 32");
   const bool ok = (L->w_dtype == DFV_BF16 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
+                  (L->w_dtype == DFV_MXFP4 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
                   (L->w_dtype == DFV_F32 && L->r_dtype == DFV_F32 && act == DFV_F32);
   if (!ok)
     return fail(DFV_ERR_UNSUPPORTED, "unsupported dtype combination (experts %d, router %d, act %d)", L->w_dtype,
                 L->r_dtype, act);
   if (!L->w_router || !L->w_gate || !L->w_up || !L->w_down) return fail(DFV_ERR_INVALID_ARG, "NULL weight pointer");
+  if (L->w_dtype == DFV_MXFP4) {
+    if (L->d % 64 || L->d_ff % 64) return fail(DFV_ERR_UNSUPPORTED, "mxfp4 layers need d and d_ff multiples of 64");
+    if (!L->s_gate || !L->s_up || !L->s_down) return fail(DFV_ERR_INVALID_ARG, "mxfp4 layer without scale pointers");
+    if (!aligned(L->s_gate, 16) || !aligned(L->s_up, 16) || !aligned(L->s_down, 16))
+      return fail(DFV_ERR_INVALID_ARG, "scale pointers must be 16-byte aligned");
+  }
   if (!aligned(L->w_router, 16) || !aligned(L->w_gate, 16) || !aligned(L->w_up, 16) || !aligned(L->w_down, 16))
     return fail(DFV_ERR_INVALID_ARG, "weight pointers must be 16-byte aligned");
   return DFV_OK;
@@ -146,27 +153,31 @@ dfv::RouterParams router_params(const dfv_moe_layer *L, const void *x, int act, 
   return p;
 }
 
-// Single-launch fused layer (bf16 weights): grid = SM count, cooperative.
+// Single-launch fused layer (bf16 or mxfp4 experts): grid = SM count, cooperative.
 // Returns -1 when the shape or the device does not allow it (the caller then
 // uses the multi-kernel path), else a DFV status.
 int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void *out, const void *residual,
                     bool fuse_norm, float eps, int32_t *u_idx, int32_t *u_nw, const dfv::Workspace &w,
                     cudaStream_t s) {
-  if (L->w_dtype != DFV_BF16 || L->r_dtype != DFV_BF16 || act != DFV_BF16) return -1;
+  const bool mx = L->w_dtype == DFV_MXFP4;
+  if ((L->w_dtype != DFV_BF16 && !mx) || L->r_dtype != DFV_BF16 || act != DFV_BF16) return -1;
   dfv::FusedPlan plan;
-  if (!dfv::fused_plan(k, L->d, L->d_ff, L->n_experts, &plan)) return -1;
+  if (!(mx ? dfv::fused_mx_plan(k, L->d, L->d_ff, L->n_experts, &plan)
+           : dfv::fused_plan(k, L->d, L->d_ff, L->n_experts, &plan)))
+    return -1;
   static std::mutex mu;
-  static std::map<std::tuple<int, int, size_t>, int> cache;
+  static std::map<std::tuple<int, int, int, size_t>, int> cache;
   int dev = 0;
   cudaGetDevice(&dev);
   int grid;
   {
     std::lock_guard<std::mutex> lock(mu);
-    auto key = std::make_tuple(dev, k <= 8 ? 1 : 2, plan.smem);
+    auto key = std::make_tuple(dev, mx ? 1 : 0, k <= 8 ? 1 : 2, plan.smem);
     auto it = cache.find(key);
     if (it == cache.end()) {
       char why[256] = {0};
-      const int gmax = dfv::fused_max_grid(plan, k, why, sizeof why);
+      const int gmax = mx ? dfv::fused_mx_max_grid(plan, k, why, sizeof why)
+                          : dfv::fused_max_grid(plan, k, why, sizeof why);
       if (gmax <= 0 && g_fused_why.empty()) g_fused_why = why;
       it = cache.emplace(key, gmax).first;
     }
@@ -181,6 +192,11 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
   fp.wg = L->w_gate;
   fp.wu = L->w_up;
   fp.wd = L->w_down;
+  if (mx) {
+    fp.sg = L->s_gate;
+    fp.su = L->s_up;
+    fp.sd = L->s_down;
+  }
   fp.k = k;
   fp.d = L->d;
   fp.I = L->d_ff;
@@ -193,11 +209,14 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
   fp.ws = w;
   fp.u_idx = u_idx;
   fp.u_nw = u_nw;
+  auto go = [&](bool pdl) {
+    return mx ? dfv::launch_fused_mx(fp, plan, grid, s, pdl) : dfv::launch_fused(fp, plan, grid, s, pdl);
+  };
   mark(0, s);
-  cudaError_t e = dfv::launch_fused(fp, plan, grid, s, true);
+  cudaError_t e = go(true);
   if (e != cudaSuccess) {
     cudaGetLastError();  // clear, and retry without programmatic serialisation
-    e = dfv::launch_fused(fp, plan, grid, s, false);
+    e = go(false);
   }
   if (e != cudaSuccess) return cuda_fail(e, "fused layer launch");
   mark(1, s);
@@ -248,6 +267,27 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
   fp.swz_h = (L->d_ff % 64 == 0) ? 4 : 0;
   fp.ws = w;
   const int maxW = L->n_experts < k * L->top_k ? L->n_experts : k * L->top_k;
+  if (L->w_dtype == DFV_MXFP4) {
+    // codes widened in registers: gate/up units of (expert, 8 * 4/ks rows),
+    // ks the smallest split of d whose units still fill two CTAs per SM
+    const int sms = sm_count();
+    if (sms <= 0) return fail(DFV_ERR_CUDA, "cannot query the SM count");
+    int ks = 1;
+    while (ks < 4 && maxW * (L->d_ff / (8 * (4 / ks))) < 2 * sms) ks *= 2;
+    fp.ks = ks;
+    const int units_g = maxW * (L->d_ff / (8 * (4 / ks)));
+    const int units_d = maxW * (L->d / dfv::kDownTile);
+    const int lim_g = grid_limit(L->w_dtype, k, L->d, L->d_ff, 0);
+    const int lim_d = grid_limit(L->w_dtype, k, L->d, L->d_ff, 1);
+    if (lim_g <= 0 || lim_d <= 0) return fail(DFV_ERR_CUDA, "mxfp4 expert kernels cannot be resident (occupancy 0)");
+    e = dfv::launch_ffn_mxfp4(fp, 0, units_g < lim_g ? units_g : lim_g, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "mxfp4 expert gate/up launch");
+    mark(2, s);
+    e = dfv::launch_ffn_mxfp4(fp, 1, units_d < lim_d ? units_d : lim_d, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "mxfp4 expert down/combine launch");
+    mark(3, s);
+    return DFV_OK;
+  }
   dfv::TmaPlan plan;
   if (dfv::tma_plan(L->w_dtype, k, L->d, L->d_ff, &plan)) {
     // TMA-staged kernels: one persistent CTA per SM

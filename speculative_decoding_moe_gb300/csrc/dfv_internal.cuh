@@ -66,7 +66,8 @@ struct FfnParams {
   int swz_x;            // XOR swizzle mask for staged x rows (0 or 4)
   int swz_h;            // XOR swizzle mask for staged h rows (0 or 4)
   // TMA-staged kernels only
-  int ks;               // gate/up: k-columns per stage slice
+  int ks;               // TMA gate/up: k-columns per stage slice; mxfp4 gate/up:
+                        // parts of d per unit (1, 2 or 4 warps share a row group)
   int nslices;          // gate/up: slices per unit (d / ks)
   int stages;           // ring depth
   int rs;               // down: rows per unit
@@ -78,6 +79,7 @@ struct FusedParams {
   const void *residual;  // [k][d] bf16 or null: added in the combine
   void *out;             // [k][d] bf16
   const void *wr, *wg, *wu, *wd;
+  const uint8_t *sg, *su, *sd;  // mxfp4 experts: E8M0 scales (null for bf16)
   int k, d, I, E, K, norm_topk, fuse_norm, swz_x;
   float eps;
   int ks, nsl, slot, scratch, ring;  // filled from the plan
@@ -261,6 +263,9 @@ cudaError_t launch_router(const RouterParams &p, cudaStream_t s, bool pdl);
 // phase 0: gate/up, phase 1: down + combine
 cudaError_t launch_ffn_phase(const FfnParams &p, int w_dtype, int phase, int grid, cudaStream_t s, bool pdl);
 int ffn_grid_limit(int w_dtype, int k, int d, int I, int which);
+// mxfp4 experts (ffn_mxfp4.cu): phase 0 = gate/up, 1 = down + combine
+int mxfp4_grid_limit(int k, int d, int I, int which);
+cudaError_t launch_ffn_mxfp4(const FfnParams &p, int phase, int grid, cudaStream_t s, bool pdl);
 // TMA-staged expert FFN: geometry for a layer shape, 0 if it does not fit.
 struct TmaPlan {
   int ks, nslices, stages_g, rs, stages_d;
@@ -271,6 +276,10 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
 bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
 int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
 cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
+// single-launch layer with mxfp4 experts (layer_fused_mxfp4.cu)
+bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan);
+int fused_mx_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
+cudaError_t launch_fused_mx(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);

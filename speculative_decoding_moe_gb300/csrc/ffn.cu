@@ -27,54 +27,13 @@
 // thread.  The k index inside a 32-element chunk is permuted identically on the
 // A (weights) and B (tokens) side, so each thread's 16-byte load feeds two
 // MMAs without any shuffle.
-#include <map>
-#include <mutex>
-#include <utility>
-
-#include "dfv_internal.cuh"
+#include "ffn_common.cuh"
 
 namespace dfv {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kBatch = 8;  // 32-element k-chunks per load batch
-
-__device__ __forceinline__ void unit_range(int U, int &lo, int &hi) {
-  lo = (int)(((long long)blockIdx.x * U) / gridDim.x);
-  hi = (int)(((long long)(blockIdx.x + 1) * U) / gridDim.x);
-}
-
-// ----------------------------------------------------------------------------
-// combine: out[t][r] = residual[t][r] + sum_s ys[t*K+s][r], slot order, for the
-// rows of down tile dt.  Called by the last unit to finish that tile.
-__device__ void combine_tile(const FfnParams &p, int dt) {
-  const int r0 = dt * kDownTile;
-  const int rows = min(kDownTile, p.d - r0);
-  for (int idx = threadIdx.x; idx < p.k * kDownTile; idx += blockDim.x) {
-    const int t = idx / kDownTile, rr = idx % kDownTile;
-    if (rr >= rows) continue;
-    const int r = r0 + rr;
-    float s = 0.f;
-    for (int sl = 0; sl < p.K; ++sl) s += __ldcg(p.ws.ys + (size_t)(t * p.K + sl) * p.d + r);
-    if (p.residual) s = load_act(p.residual, (size_t)t * p.d + r, p.act) + s;
-    store_act(p.out, (size_t)t * p.d + r, p.act, s);
-  }
-}
-
-// Ticket for tile dt after this CTA wrote its ys rows; runs the combine if last.
-__device__ __forceinline__ void finish_down_unit(const FfnParams &p, int dt, int nW) {
-  __shared__ unsigned s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(p.ws.down_cnt + dt, 1u) == (unsigned)(nW - 1)) ? 1u : 0u;
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    combine_tile(p, dt);
-    __syncthreads();
-    if (threadIdx.x == 0) p.ws.down_cnt[dt] = 0u;
-  }
-}
 
 // ----------------------------------------------------------------------------
 // bf16 gate/up.  Dynamic smem: xs[NT*8][d] bf16 (16-byte chunks XOR-swizzled
@@ -355,50 +314,17 @@ __global__ void __launch_bounds__(kThreads) down_f32_kernel(FfnParams p) {
 // host side
 namespace {
 
-template <typename F>
-cudaError_t launch(F kern, int grid, size_t smem, const FfnParams &p, cudaStream_t s, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
 size_t gate_smem(int nt, int d) { return (size_t)nt * 8 * d * 2 + (size_t)kWarps * nt * 32 * 16; }
 size_t down_smem(int nt, int I) { return (size_t)nt * 8 * I * 4 + (size_t)8 * nt * 32 * 16; }
 
-// Raise a kernel's dynamic shared-memory limit once per (device, kernel); later
-// calls (including ones made while a stream is being captured) only look up.
 template <typename F>
-cudaError_t ensure_smem(F kern, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  static std::mutex mu;
-  static std::map<std::pair<int, const void *>, size_t> done;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> lock(mu);
-  auto key = std::make_pair(dev, (const void *)kern);
-  auto it = done.find(key);
-  if (it != done.end() && it->second >= bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) done[key] = bytes;
-  return e;
+cudaError_t launch(F kern, int grid, size_t smem, const FfnParams &p, cudaStream_t s, bool pdl) {
+  return launch_ffn_kernel(kern, grid, kThreads, smem, p, s, pdl);
 }
 
 template <typename F>
 int occupancy_grid(F kern, size_t smem) {
-  int dev = 0, sms = 0, per = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (ensure_smem(kern, smem) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, kThreads, smem) != cudaSuccess) return 0;
-  return sms * per;
+  return occupancy_grid(kern, kThreads, smem);
 }
 
 }  // namespace
@@ -415,6 +341,7 @@ int ffn_grid_limit(int w_dtype, int k, int d, int I, int which) {
   if (w_dtype == DFV_F32) {
     return which == 0 ? occupancy_grid(gateup_f32_kernel, 0) : occupancy_grid(down_f32_kernel, 0);
   }
+  if (w_dtype == DFV_MXFP4) return mxfp4_grid_limit(k, d, I, which);
   return 0;
 }
 

@@ -35,62 +35,9 @@
 // Every wait is bounded (2 s) and reports through the workspace error word.
 #include <cstdio>
 
-#include "dfv_internal.cuh"
+#include "fused_common.cuh"
 
 namespace dfv {
-
-constexpr int kFW = 16;           // consumer warps
-constexpr int kFC = kFW * 32;     // consumer threads
-constexpr int kFT = kFC + 32;     // + producer warp
-constexpr int kBarAll = 1;        // named barrier: all consumers
-constexpr int kBarGroup = 2;      // named barriers 2, 3: consumer groups of 8 warps
-constexpr int kMaxRing = 8;       // upper bound of ring stages (barrier arrays)
-constexpr int kMaxChunksP2 = 2;   // 32-column chunks per consumer warp per gate/up stage (ks <= 1024)
-
-__device__ __forceinline__ int fpad(int bytes) { return (bytes % 128 == 0) ? bytes + 64 : bytes; }
-
-__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(n) : "memory");
-}
-
-// Grid barrier, one thread per CTA.  ctr counts arrivals over the whole launch;
-// barrier number `nb` (1-based) completes when ctr reaches nb * G.  Gives up
-// when another CTA aborted or after kWaitNs.
-__device__ bool grid_sync(const FusedParams &p, unsigned nb) {
-  unsigned *ctr = p.ws.sync, *gabort = p.ws.sync + 2;
-  red_release_add(ctr, 1u);
-  const unsigned target = nb * gridDim.x;
-  const unsigned long long t0 = global_ns();
-  while (ld_acquire(ctr) < target) {
-    if (ld_relaxed(gabort)) return false;
-    if (global_ns() - t0 > kWaitNs) {
-      atomicOr(p.ws.err, DFV_DEVERR_GRID_WAIT);
-      atomicExch(gabort, 1u);
-      return false;
-    }
-  }
-  return true;
-}
-
-__device__ __forceinline__ void load8_bf16(const void *base, size_t elem, float (&f)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(base) + elem);
-  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
-}
-__device__ __forceinline__ float rnd_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
@@ -134,166 +81,16 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   __syncthreads();
 
   const bool consumer = warp < kFW;
-  // ------------------------------------------------------------------ P0: router GEMV
-  // Warp t computes token t's logits for this CTA's experts: lane-sequential
-  // products over its 16-byte chunks, then a fixed butterfly.  A token's logit
-  // therefore depends on nothing but its own row (the same in every block).
+  // ------------------------------------------------------------------ P0, P1: routing
   if (consumer) {
-    if (warp < k) {
-      const int t = warp;
-      const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
-      float inv = 1.f;
-      if (p.fuse_norm) {
-        float ss = 0.f;
-        for (int c = lane; c < d / 8; c += 32) {
-          float f[8];
-          load8_bf16(xr, (size_t)c * 8, f);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        inv = 1.0f / sqrtf(ss / (float)d + p.eps);
-        if (lane == 0) s_inv[t] = inv;
-      }
-      for (int e = blockIdx.x; e < E; e += G) {
-        const uint16_t *wr = reinterpret_cast<const uint16_t *>(p.wr) + (size_t)e * d;
-        float acc = 0.f;
-        for (int c = lane; c < d / 8; c += 32) {
-          float f[8], w8[8];
-          load8_bf16(xr, (size_t)c * 8, f);
-          load8_bf16(wr, (size_t)c * 8, w8);
-          if (p.fuse_norm) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) f[q] = rnd_bf16(f[q] * inv);
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc = fmaf(f[q], w8[q], acc);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) p.ws.logits[(size_t)t * E + e] = acc;
-      }
-    }
-    for (int i = tid; i < kMaxBlock * (kMaxExperts / 32); i += kFC) s_mask[i] = 0u;
-    bar_sync_n(kBarAll, kFC);
-    // ---- grid barrier 1: every CTA's logits are published
-    if (tid == 0 && !grid_sync(p, 1)) s_abort = 1;
-    bar_sync_n(kBarAll, kFC);
-
-    // ---------------------------------------------------------------- P1: routing
-    // Warp t: top-K of row t (lane holds experts lane + 32 q), then the routing
-    // weights in parallel over the K lanes.
-    if (warp < k) {
-      const int t = warp;
-      uint32_t key[8];
-      float val[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int e = lane + 32 * q;
-        val[q] = (e < E) ? __ldcg(p.ws.logits + (size_t)t * E + e) : 0.f;
-        key[q] = (e < E) ? max(float_key(val[q]), 1u) : 0u;
-      }
-      int sel_id = 0;
-      float sel_val = 0.f;
-      for (int s = 0; s < K; ++s) {
-        uint32_t bk = 0;
-        int bq = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (key[q] > bk) { bk = key[q]; bq = q; }
-        float bv = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q == bq) bv = val[q];
-        const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-        const uint32_t cand = (bk == m) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu;
-        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-        const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31));
-        if ((int)(win & 31) == lane) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (q == (int)(win >> 5)) key[q] = 0u;
-        }
-        if (lane == s) { sel_id = (int)win; sel_val = wv; }
-      }
-      const float m0 = __shfl_sync(0xffffffffu, sel_val, 0);
-      const float z = (lane < K) ? expf(sel_val - m0) : 0.f;
-      float den = 0.f;
-      if (p.norm_topk) {
-        den = z;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (lane + 32 * q < E) den += expf(val[q] - m0);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      if (lane < K) {
-        s_idx[t * K + lane] = sel_id;
-        s_w[t * K + lane] = z / den;
-        atomicOr(&s_mask[t * (kMaxExperts / 32) + (sel_id >> 5)], 1u << (sel_id & 31));
-      }
-    }
-    bar_sync_n(kBarAll, kFC);
-    // per-expert pair counts from the row masks
-    if (tid < E) {
-      int cnt = 0;
-      for (int t = 0; t < k; ++t) cnt += (s_mask[t * (kMaxExperts / 32) + (tid >> 5)] >> (tid & 31)) & 1u;
-      s_eoff[tid] = cnt;
-    }
-    bar_sync_n(kBarAll, kFC);
-    {
-      // exclusive scans over experts (E <= 256 <= 8 warps of threads)
-      int flag = 0, cnt = 0;
-      if (tid < E) { cnt = s_eoff[tid]; flag = cnt > 0; }
-      int fi = flag, ci = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, fi, o), b = __shfl_up_sync(0xffffffffu, ci, o);
-        if (lane >= o) { fi += a; ci += b; }
-      }
-      if (lane == 31) { s_wsum[warp] = fi; s_csum[warp] = ci; }
-      bar_sync_n(kBarAll, kFC);
-      int wb = 0, cb = 0, nW = 0;
-      for (int w = 0; w < kFW; ++w) {
-        if (w < warp) { wb += s_wsum[w]; cb += s_csum[w]; }
-        nW += s_wsum[w];
-      }
-      const int wpos = wb + fi - flag, off = cb + ci - cnt;
-      if (tid < E) s_eoff[tid] = off;
-      if (flag) { s_woken[wpos] = tid; s_off[wpos] = off; }
-      if (tid == 0) { s_off[nW] = k * K; s_nw = nW; }
-    }
-    bar_sync_n(kBarAll, kFC);
-    for (int q = tid; q < k * K; q += kFC) {
-      const int t = q / K, ex = s_idx[q];
-      int rank = 0;
-      for (int t2 = 0; t2 < t; ++t2) rank += (s_mask[t2 * (kMaxExperts / 32) + (ex >> 5)] >> (ex & 31)) & 1u;
-      s_gat[s_eoff[ex] + rank] = q;
-    }
-    bar_sync_n(kBarAll, kFC);
+    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort};
+    fused_route(p, rs);
     if (tid == 0) {
       // with at most 8 tokens per expert the staged-x rows 8..15 are unused:
       // they become one more ring stage
       int mmax = 0;
       for (int i = 0; i < s_nw; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
       s_ring = (NT == 2 && mmax <= 8 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing) ? SH + 1 : SH;
-    }
-    if (blockIdx.x == 0) {
-      const int nW = s_nw;
-      for (int q = tid; q < k * K; q += kFC) {
-        p.ws.topk_idx[q] = s_idx[q];
-        p.ws.topk_w[q] = s_w[q];
-        p.ws.gather[q] = s_gat[q];
-        if (p.u_idx) p.u_idx[q] = s_idx[q];
-      }
-      for (int i = tid; i < nW; i += kFC) { p.ws.woken[i] = s_woken[i]; p.ws.offsets[i] = s_off[i]; }
-      if (tid == 0) {
-        p.ws.offsets[nW] = s_off[nW];
-        *p.ws.n_woken = nW;
-        if (p.u_nw) *p.u_nw = nW;
-      }
     }
   }
   __syncthreads();  // routing tables visible to the producer

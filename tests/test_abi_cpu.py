@@ -46,8 +46,9 @@ def _layer(lib, **kw):
     c = dict(d=2048, n_experts=128, top_k=8, d_ff=768, norm_topk=1, w_dtype=1, r_dtype=1,
              w_router=0x10000, w_gate=0x20000, w_up=0x30000, w_down=0x40000)
     c.update(kw)
+    sc = c.get("scales", (None, None, None))
     return lib.CLayer(c["d"], c["n_experts"], c["top_k"], c["d_ff"], c["norm_topk"], c["w_dtype"], c["r_dtype"],
-                      c["w_router"], c["w_gate"], c["w_up"], c["w_down"], None, None, None)
+                      c["w_router"], c["w_gate"], c["w_up"], c["w_down"], *sc)
 
 
 def test_workspace_sizes(lib):
@@ -72,6 +73,10 @@ def test_workspace_sizes(lib):
     (dict(w_dtype=0), 4, 2),             # f32 experts with bf16 activations
     (dict(w_router=0x10001), 4, 1),      # misaligned weight
     (dict(w_gate=0), 4, 1),              # NULL weight
+    (dict(w_dtype=2), 4, 1),             # mxfp4 experts without scales
+    (dict(w_dtype=2, d=2080, scales=(0x81000, 0x82000, 0x83000)), 4, 2),   # mxfp4 needs d % 64
+    (dict(w_dtype=2, d_ff=736, scales=(0x81000, 0x82000, 0x83000)), 4, 2),  # and d_ff % 64
+    (dict(w_dtype=2, r_dtype=0, scales=(0x81000, 0x82000, 0x83000)), 4, 2),  # fp32 router with mxfp4
 ])
 def test_invalid_arguments_are_rejected_before_launch(lib, kw, k, status):
     L = lib.lib()
@@ -106,3 +111,11 @@ def test_product_path_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt and "orc_" not in txt, f
+
+
+def test_device_error_bits_match_the_header(lib):
+    src = open(os.path.join(ROOT, "include", "dfv.h")).read()
+    bits = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define DFV_DEVERR_([A-Z_]+) (0x[0-9a-fA-F]+)u", src)}
+    assert bits == {"STAGE_WAIT": 1, "SLOT_WAIT": 2, "DRAIN_WAIT": 4, "GRID_WAIT": 8, "SCALE_RANGE": 16}
+    for name, v in bits.items():
+        assert getattr(lib, "DEVERR_" + name) == v
