@@ -76,13 +76,14 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2 } dfv_dtype;
 #define DFV_DEVERR_SLOT_WAIT 0x2u    /* the producer gave up waiting for a free stage */
 #define DFV_DEVERR_DRAIN_WAIT 0x4u   /* copies still in flight at exit after a timeout */
 #define DFV_DEVERR_GRID_WAIT 0x8u    /* a CTA gave up waiting at a grid-wide barrier */
-/* An mxfp4 scale byte outside [104, 140] was met.  The codes are widened to
+/* An mxfp4 scale byte outside [113, 140] was met.  The codes are widened to
  * fp16 and multiplied by their block's scale 2^(s-127) there; inside that range
- * every product is exact, outside it the scale is clamped and the outputs are
- * approximate.  (With the OCP choice of a block's scale, 2^(floor(log2 amax)
- * - 2), that range holds every block whose largest magnitude amax lies in
- * [2^-21, 2^16).)  The kernels finish normally. */
+ * every product is exact, outside it the scaled codes are wrong.  (With the
+ * OCP choice of a block's scale, 2^(floor(log2 amax) - 2), that range holds
+ * every block whose largest magnitude amax lies in [2^-12, 2^16).)  The
+ * kernels finish normally; the outputs of that call are invalid. */
 #define DFV_DEVERR_SCALE_RANGE 0x10u
+#define DFV_DEVERR_REDUCE_WAIT 0x20u /* a warp gave up waiting for a free partial-sum buffer */
 
 /* Limits of this implementation. */
 #define DFV_MAX_BLOCK 16      /* k: positions in one verify block          */

@@ -196,6 +196,12 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
     fp.sg = L->s_gate;
     fp.su = L->s_up;
     fp.sd = L->s_down;
+    char why[256] = {0};
+    if (!dfv::fused_mx_tensor_maps(&fp, L, why, sizeof why)) {
+      std::lock_guard<std::mutex> lock(mu);
+      if (g_fused_why.empty()) g_fused_why = why;
+      return -1;
+    }
   }
   fp.k = k;
   fp.d = L->d;

@@ -2,6 +2,7 @@
 // workspace layout shared by the kernels of libdfv.so (sm_103a only).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -75,6 +76,9 @@ struct FfnParams {
 };
 
 struct FusedParams {
+  // mxfp4 experts: 2-D tensor maps over the gate/up codes ([E*d_ff][d/2] bytes,
+  // box 256 x 32) and their scales ([E*d_ff][d/32] bytes, box 16 x 32)
+  CUtensorMap tm_wg, tm_wu, tm_sg, tm_su;
   const void *x;         // [k][d] bf16 rows (the residual stream when fuse_norm)
   const void *residual;  // [k][d] bf16 or null: added in the combine
   void *out;             // [k][d] bf16
@@ -278,6 +282,8 @@ int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
 cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 // single-launch layer with mxfp4 experts (layer_fused_mxfp4.cu)
 bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan);
+// fills p->tm_* for an mxfp4 layer; false (with a reason) when the driver refuses
+bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, size_t why_len);
 int fused_mx_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
 cudaError_t launch_fused_mx(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,

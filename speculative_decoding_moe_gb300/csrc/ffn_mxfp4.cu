@@ -13,10 +13,10 @@
 // one scale block.  cvt.rn.f16x2.e2m1x2 widens a byte to two fp16 values
 // (low nibble -> low half), exactly: the E2M1 magnitudes are
 // {0, 0.5, 1, 1.5, 2, 3, 4, 6}.  One fp16x2 multiply by the block's scale
-// 2^(s-127) keeps them exact as long as every product is a normal fp16 number
-// or a subnormal on the 2^-24 grid, which holds for s in [104, 140].  A scale
-// outside that range sets DFV_DEVERR_SCALE_RANGE in the workspace error word
-// (the products are then rounded and the outputs approximate).
+// 2^(s-127) keeps them exact as long as the scale is a normal fp16 number and
+// every product a normal one or a subnormal on the 2^-24 grid, which holds for
+// s in [113, 140].  A scale outside that range sets DFV_DEVERR_SCALE_RANGE in
+// the workspace error word (the outputs are then wrong).
 //
 // Activations.  Each token row fed to the tensor cores (x for gate/up, h for
 // down) is staged in shared memory as fp16 after multiplying it by a power of
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kMxThreads) gateup_mxfp4_kernel(FfnParams p) {
   const size_t rowb = (size_t)d / 2;  // code bytes per row
   const int srow = d / 32;            // scale bytes per row
   const uint16_t *xg = reinterpret_cast<const uint16_t *>(p.x);
-  uint32_t bad = 0;
+  uint32_t range = 0;
 
   int cur = -1, m = 0, off = 0, e = 0;
   for (int u = lo; u < hi; ++u) {
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kMxThreads) gateup_mxfp4_kernel(FfnParams p) {
         const int ch = base + j;
         if (ch < c1) {
           const bool live = ch * 128 + c * 32 < d;
-          const uint32_t sgv = e8m0_half2(eg[j], bad), suv = e8m0_half2(eu[j], bad);
+          const uint32_t sgv = e8m0_half2(eg[j], range), suv = e8m0_half2(eu[j], range);
           const uint32_t wg4[4] = {ag[j].x, ag[j].y, ag[j].z, ag[j].w};
           const uint32_t wu4[4] = {au[j].x, au[j].y, au[j].z, au[j].w};
 #pragma unroll
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kMxThreads) gateup_mxfp4_kernel(FfnParams p) {
       __syncthreads();
     }
   }
-  if (bad) atomicOr(p.ws.err, DFV_DEVERR_SCALE_RANGE);
+  if (range > kScaleRangeMax) atomicOr(p.ws.err, DFV_DEVERR_SCALE_RANGE);
 }
 
 // ----------------------------------------------------------------------------
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kMxThreads) down_mxfp4_kernel(FfnParams p) {
   const int C = (I + 127) / 128;
   const size_t rowb = (size_t)I / 2;
   const int srow = I / 32;
-  uint32_t bad = 0;
+  uint32_t range = 0;
 
   int cur = -1, m = 0, off = 0, e = 0;
   for (int u = lo; u < hi; ++u) {
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kMxThreads) down_mxfp4_kernel(FfnParams p) {
         const int ch = base + j;
         if (ch < C) {
           const bool live = ch * 128 + c * 32 < I;
-          const uint32_t s0 = e8m0_half2(e0[j], bad), s1 = e8m0_half2(e1[j], bad);
+          const uint32_t s0 = e8m0_half2(e0[j], range), s1 = e8m0_half2(e1[j], range);
           const uint32_t w0[4] = {a0[j].x, a0[j].y, a0[j].z, a0[j].w};
           const uint32_t w1[4] = {a1[j].x, a1[j].y, a1[j].z, a1[j].w};
 #pragma unroll
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kMxThreads) down_mxfp4_kernel(FfnParams p) {
       }
     finish_down_unit(p, dt, nW);
   }
-  if (bad) atomicOr(p.ws.err, DFV_DEVERR_SCALE_RANGE);
+  if (range > kScaleRangeMax) atomicOr(p.ws.err, DFV_DEVERR_SCALE_RANGE);
 }
 
 size_t mx_gate_smem(int nt, int d) { return (size_t)nt * 8 * d * 2 + (size_t)kMxWarps * nt * 32 * 16; }

@@ -44,6 +44,7 @@ __device__ bool grid_sync(const FusedParams &p, unsigned nb) {
   const unsigned target = nb * gridDim.x;
   const unsigned long long t0 = global_ns();
   while (ld_acquire(ctr) < target) {
+    __nanosleep(64);  // leave the issue slots to the SM's other warps
     if (ld_relaxed(gabort)) return false;
     if (global_ns() - t0 > kWaitNs) {
       atomicOr(p.ws.err, DFV_DEVERR_GRID_WAIT);

@@ -11,31 +11,39 @@
 // and scales cross HBM exactly once and are widened to fp16 in registers.
 //
 // One CTA per SM: 16 consumer warps in 4 groups of 4, and one producer warp
-// that streams whole contiguous weight blocks through an 8-stage mbarrier ring
-// (4 bulk copies per gate/up stage, 2 per down stage).  Group q consumes the
-// stages q, q+4, q+8, ... of the ring sequence, so the groups run as four
-// independent pipelines that synchronise only among their own 128 threads.
+// that streams the weights through an 8-stage mbarrier ring (4 tensor copies
+// per gate/up stage, 2 bulk copies per down stage).  The producer feeds the
+// groups round-robin, so group q consumes stages q, q+4, q+8, ... (a group with
+// no unit left in a round gets an empty stage); no warp ever waits for another
+// warp's partial sums.
 //   P0, P1  routing, shared with the bf16 single-launch kernel (fused_route).
 //   P2  the k rows of x (after the optional RMSNorm, rounded to bf16) are
 //       staged once in shared memory as fp16, each multiplied by a power of
 //       two that puts its largest magnitude in [2^14, 2^15).  unit = (woken
-//       expert, 8 d_ff rows); its stage holds the 8 gate and 8 up rows of codes
-//       and their scales.  The group's 4 warps split d, widen their codes
-//       (cvt e2m1x2 -> fp16x2, times the block scale), run m16n8k16 fp16 MMAs
-//       (gate rows = M 0-7, up rows = M 8-15, the expert's tokens = N) and add
-//       the 4 partial sums in fixed order; h = silu(g) * u goes to global
-//       memory in fp32.
+//       expert, 32 d_ff rows), streamed as d/512 stages of 32 gate rows and
+//       32 up rows x 512 codes with their scales (2-D tensor copies).  Warp w
+//       of the group owns rows 8w..8w+7 over the whole of d: it widens its
+//       codes (cvt e2m1x2 -> fp16x2, times the block scale), runs m16n8k16 fp16
+//       MMAs (gate rows = M 0-7, up rows = M 8-15, the expert's tokens = N) and
+//       keeps the sums in its registers across the stages; h = silu(g) * u goes
+//       to global memory in fp32.
 //       -- grid barrier 2 (consumers only; the producer runs ahead into P3) --
 //   P3  unit = (woken expert, 64 d rows); its stage holds the 64 rows of down
 //       codes and scales.  Each warp owns 16 rows over the whole d_ff; the B
 //       operand is the expert's h rows, staged per expert in the group's
 //       shared buffer as fp16 with their own power-of-two scales.
-//       w[t,s] * y goes to ys[pair]; the last unit to finish a 64-row tile
-//       (atomic ticket, nothing waits) sums ys over the K slots in slot order,
-//       adds the residual and writes the output rows.  The sum order of every
-//       output depends only on its own token, never on the block.
+//       w[t,s] * y goes to ys[pair].
+//       -- grid barrier 3 --
+//   P4  every CTA sums ys over the K slots in slot order for its share of the
+//       output rows, adds the residual and writes them.  The sum order of
+//       every output depends only on its own token, never on the block.
 // Every wait is bounded (2 s) and reports through the workspace error word.
 #include <cstdio>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include <cudaTypedefs.h>
 
 #include "fused_common.cuh"
 #include "mxfp4_common.cuh"
@@ -43,20 +51,30 @@
 namespace dfv {
 namespace {
 
-constexpr int kMxRing = 8;               // ring stages (a power of two, a multiple of the groups)
 constexpr int kMxGroups = 4;             // consumer groups
 constexpr int kMxGW = kFW / kMxGroups;   // warps per group
+constexpr int kMxRing = 8;               // ring stages (two per group)
 constexpr int kMxBarGroup = 2;           // named barriers 2..5, one per group
-constexpr int kMxMaxCh = 4;              // 128-code chunks per warp and row: d <= 2048, d_ff <= 512
+constexpr int kMxCh = 4;                 // 128-code chunks per warp, row and stage
+constexpr int kMxRows = 32;              // d_ff rows per gate/up unit (8 per warp)
+constexpr int kMxCols = 512;             // codes per row and gate/up stage
+constexpr int kMxMaxD = 2048;            // staged x: at most 8 16-byte pieces per lane
 
-__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// 2-D tensor copy global -> shared (box given by the tensor map), completion
+// counted in bytes on `bar`.  x is the innermost (byte) coordinate.
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
+__global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_constant__ FusedParams p) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(128) unsigned char smem[];
@@ -64,10 +82,13 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
   const int G = gridDim.x;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t slot = p.slot;
-  unsigned char *scratch = smem + kMxRing * slot;                 // x rows (P2), h rows per group (P3)
-  float *red = reinterpret_cast<float *>(scratch + p.scratch);    // [groups][4 warps][NT][32][4]
-  const uint32_t full0 = smem_u32(red + kFW * NT * 32 * 4);
+  unsigned char *scratch = smem + kMxRing * slot;  // x rows (P2), h rows per group (P3)
+  const uint32_t full0 = sbase + kMxRing * slot + p.scratch;
   const uint32_t empty0 = full0 + 8 * kMxRing;
+  // plain C++ loads from shared memory (ordered by the compiler against the
+  // barrier waits, free to be scheduled early otherwise)
+  auto ld16 = [&](uint32_t a) { return *reinterpret_cast<const uint4 *>(smem + (a - sbase)); };
+  auto ld1 = [&](uint32_t a) { return (uint32_t)smem[a - sbase]; };
 
   __shared__ int s_idx[kMaxBlock * kMaxTopK];
   __shared__ float s_w[kMaxBlock * kMaxTopK];
@@ -81,7 +102,6 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
   __shared__ float s_hinv[kMxGroups][kMaxBlock];  // 2^-shift of each staged h row, per group
   __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_nw;
-  __shared__ unsigned s_last[kMxGroups];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -103,7 +123,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
   __syncthreads();  // routing tables visible to the producer
 
   const int nW = s_nw;
-  const int tiles_g = I / 8, tiles_d = d / 64;
+  const int tiles_g = I / kMxRows, tiles_d = d / 64, nq = d / kMxCols;
   int lo_g, hi_g, lo_d, hi_d;
   {
     const int U = nW * tiles_g, V = nW * tiles_d;
@@ -112,45 +132,76 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
     lo_d = (int)(((long long)blockIdx.x * V) / G);
     hi_d = (int)(((long long)(blockIdx.x + 1) * V) / G);
   }
-  // stage layouts: gate/up = [8][d/2] gate codes | [8][d/2] up codes |
-  // [8][d/32] gate scales | [8][d/32] up scales; down = [64][I/2] codes | [64][I/32] scales
-  const uint32_t rowb_g = d / 2, srow_g = d / 32, rowb_d = I / 2, srow_d = I / 32;
-  const uint32_t g_up = 8 * rowb_g, g_sc = 16 * rowb_g, g_scu = g_sc + 8 * srow_g, d_sc = 64 * rowb_d;
-  const uint32_t bytes_g = 16 * rowb_g + 16 * srow_g, bytes_d = 64 * rowb_d + 64 * srow_d;
+  const int R2 = (hi_g - lo_g + kMxGroups - 1) / kMxGroups, R3 = (hi_d - lo_d + kMxGroups - 1) / kMxGroups;
+  // stage layouts: gate/up = [32][256] gate codes | [32][256] up codes |
+  // [32][16] gate scales | [32][16] up scales; down = [64][I/2] codes | [64][I/32] scales
+  constexpr uint32_t g_up = kMxRows * kMxCols / 2, g_sc = 2 * g_up, g_scu = g_sc + kMxRows * kMxCols / 32;
+  constexpr uint32_t bytes_g = 2 * g_up + 2 * kMxRows * kMxCols / 32;
+  const uint32_t rowb_d = I / 2, srow_d = I / 32, d_sc = 64 * rowb_d;
+  const uint32_t bytes_d = 64 * rowb_d + 64 * srow_d;
 
   if (!consumer) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && !s_abort) {
-      const uint8_t *wg = reinterpret_cast<const uint8_t *>(p.wg);
-      const uint8_t *wu = reinterpret_cast<const uint8_t *>(p.wu);
       const uint8_t *wd = reinterpret_cast<const uint8_t *>(p.wd);
-      int it = 0, ps = 0, pph = 0;  // fills issued; slot and phase of the next fill
+      int it = 0, ps = 0, pph = 0;  // stages issued; slot and phase of the next one
       bool ok = true;
-      for (int u = lo_g; u < hi_g; ++u, ++it, ps = (ps + 1) & (kMxRing - 1), pph ^= (ps == 0)) {
-        if (!mbar_wait_fast(empty0 + 8 * ps, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
-          ok = false;
-          break;
+      auto take = [&]() -> bool {
+        if (!mbar_wait_fast(empty0 + 8 * ps, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) return false;
+        return true;
+      };
+      auto advance = [&]() {
+        ++it;
+        if (++ps == kMxRing) {
+          ps = 0;
+          pph ^= 1;
         }
-        const int wi = u / tiles_g;
-        const size_t row = (size_t)s_woken[wi] * I + (size_t)(u - wi * tiles_g) * 8;
-        const uint32_t fb = full0 + 8 * ps, dst = sbase + ps * slot;
-        mbar_expect_tx(fb, bytes_g);
-        bulk_g2s(dst, wg + row * rowb_g, 8 * rowb_g, fb);
-        bulk_g2s(dst + g_up, wu + row * rowb_g, 8 * rowb_g, fb);
-        bulk_g2s(dst + g_sc, p.sg + row * srow_g, 8 * srow_g, fb);
-        bulk_g2s(dst + g_scu, p.su + row * srow_g, 8 * srow_g, fb);
+      };
+      // gate/up: rounds of one unit per group, d/512 stages per unit
+      for (int r = 0; r < R2 && ok; ++r) {
+        for (int q = 0; q < nq && ok; ++q) {
+          for (int gq = 0; gq < kMxGroups; ++gq) {
+            if (!take()) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + 8 * ps, dst = sbase + ps * slot;
+            const int u = lo_g + r * kMxGroups + gq;
+            if (u < hi_g) {
+              const int wi = u / tiles_g;
+              const int row = s_woken[wi] * I + (u - wi * tiles_g) * kMxRows;
+              mbar_expect_tx(fb, bytes_g);
+              tma_2d(dst, &p.tm_wg, q * (kMxCols / 2), row, fb);
+              tma_2d(dst + g_up, &p.tm_wu, q * (kMxCols / 2), row, fb);
+              tma_2d(dst + g_sc, &p.tm_sg, q * (kMxCols / 32), row, fb);
+              tma_2d(dst + g_scu, &p.tm_su, q * (kMxCols / 32), row, fb);
+            } else {
+              mbar_arrive(fb);  // empty stage: this group has no unit in this round
+            }
+            advance();
+          }
+        }
       }
-      for (int u = lo_d; u < hi_d && ok; ++u, ++it, ps = (ps + 1) & (kMxRing - 1), pph ^= (ps == 0)) {
-        if (!mbar_wait_fast(empty0 + 8 * ps, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
-          ok = false;
-          break;
+      // down: rounds of one unit per group
+      for (int r = 0; r < R3 && ok; ++r) {
+        for (int gq = 0; gq < kMxGroups; ++gq) {
+          if (!take()) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * ps, dst = sbase + ps * slot;
+          const int u = lo_d + r * kMxGroups + gq;
+          if (u < hi_d) {
+            const int wi = u / tiles_d;
+            const size_t row = (size_t)s_woken[wi] * d + (size_t)(u - wi * tiles_d) * 64;
+            mbar_expect_tx(fb, bytes_d);
+            bulk_g2s(dst, wd + row * rowb_d, 64 * rowb_d, fb);
+            bulk_g2s(dst + d_sc, p.sd + row * srow_d, 64 * srow_d, fb);
+          } else {
+            mbar_arrive(fb);
+          }
+          advance();
         }
-        const int wi = u / tiles_d;
-        const size_t row = (size_t)s_woken[wi] * d + (size_t)(u - wi * tiles_d) * 64;
-        const uint32_t fb = full0 + 8 * ps, dst = sbase + ps * slot;
-        mbar_expect_tx(fb, bytes_d);
-        bulk_g2s(dst, wd + row * rowb_d, 64 * rowb_d, fb);
-        bulk_g2s(dst + d_sc, p.sd + row * srow_d, 64 * srow_d, fb);
       }
       // no copy may land after the CTA exits
       volatile int never = 0;
@@ -158,70 +209,70 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
         if (!mbar_wait(full0 + 8 * (j % kMxRing), (j / kMxRing) & 1, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never)) break;
     }
   } else {
-    const int grp = warp / kMxGW, wq = warp % kMxGW, gt = tid % (kMxGW * 32);
+    const int grp = warp / kMxGW, wq = warp % kMxGW;
     const int g = lane >> 2, c = lane & 3;
     const int bar_grp = kMxBarGroup + grp;
-    float *redg = red + grp * (kMxGW * NT * 32 * 4);
     float *hf = p.ws.h;  // [k*K][I] fp32, by sorted pair position
-    uint32_t bad = 0;
+    uint32_t range = 0;  // largest (scale - 113) met, unsigned
     bool dead = s_abort != 0;
 
     // ---- stage the k rows of x as fp16 (warp t: row t)
+    const int xrow = d * 2;  // bytes per staged x row
     const uint32_t xs = smem_u32(scratch);
-    const int cpr = d / 8;
     if (warp < k) {
-      const int t = warp;
+      const int t = warp, cpr = d / 8;
       const uint16_t *src = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
       const float inv = p.fuse_norm ? s_inv[t] : 1.f;
+      uint4 v[8];
       float amax = 0.f;
-      for (int q = lane; q < cpr; q += 32) {
-        float f[8];
-        load8_bf16(src, (size_t)q * 8, f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(p.fuse_norm ? rnd_bf16(f[i] * inv) : f[i]));
+      for (int i = 0; i < 8; ++i) {
+        const int q = lane + 32 * i;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (q < cpr) v[i] = *reinterpret_cast<const uint4 *>(src + (size_t)q * 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
+          if (p.fuse_norm) {
+            a = rnd_bf16(a * inv);
+            b = rnd_bf16(b * inv);
+          }
+          amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+        }
       }
       const int sh = row_shift(warp_max(amax));
       const float sc = exp2i(sh);
-      for (int q = lane; q < cpr; q += 32) {
-        float f[8];
-        load8_bf16(src, (size_t)q * 8, f);
-        if (p.fuse_norm) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = rnd_bf16(f[i] * inv);
+      for (int i = 0; i < 8; ++i) {
+        const int q = lane + 32 * i;
+        if (q < cpr) {
+          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
+            if (p.fuse_norm) {
+              a = rnd_bf16(a * inv);
+              b = rnd_bf16(b * inv);
+            }
+            o4[h] = pack_h2(a * sc, b * sc);
+          }
+          *reinterpret_cast<uint4 *>(scratch + (size_t)t * xrow + swz(q, t) * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
         }
-        *reinterpret_cast<uint4 *>(scratch + (size_t)t * d * 2 + swz(q, t) * 16) =
-            make_uint4(pack_h2(f[0] * sc, f[1] * sc), pack_h2(f[2] * sc, f[3] * sc), pack_h2(f[4] * sc, f[5] * sc),
-                       pack_h2(f[6] * sc, f[7] * sc));
       }
       if (lane == 0) s_xinv[t] = exp2i(-sh);
     }
     bar_sync_n(kBarAll, kFC);
 
-    // ---------------------------------------------------------------- P2: gate/up
-    const int C = (d + 127) / 128;
-    const int c0 = wq * C / kMxGW, c1 = (wq + 1) * C / kMxGW;
     int cs = grp, cph = 0;  // ring slot and phase of this group's next stage
-    for (int u = lo_g + grp; u < hi_g; u += kMxGroups) {
-      const int wi = u / tiles_g, i0 = (u - wi * tiles_g) * 8;
-      const int off = s_off[wi], m = s_off[wi + 1] - off;
+    auto stage_wait = [&]() {
       if (!dead && !mbar_wait_fast(full0 + 8 * cs, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
-      // codes and scales to registers, then the stage is released at once
-      uint4 ag[kMxMaxCh], au[kMxMaxCh];
-      uint32_t eg[kMxMaxCh], eu[kMxMaxCh];
-      const uint32_t st = sbase + cs * slot;
-#pragma unroll
-      for (int j = 0; j < kMxMaxCh; ++j) {
-        const int ch = c0 + j;
-        ag[j] = au[j] = make_uint4(0u, 0u, 0u, 0u);
-        eg[j] = eu[j] = 127u;
-        if (!dead && ch < c1 && ch * 128 + c * 32 < d) {
-          const uint32_t o = g * rowb_g + ch * 64 + c * 16;
-          ag[j] = lds128(st + o);
-          au[j] = lds128(st + g_up + o);
-          eg[j] = lds_u8(st + g_sc + g * srow_g + ch * 4 + c);
-          eu[j] = lds_u8(st + g_scu + g * srow_g + ch * 4 + c);
-        }
-      }
+    };
+    auto stage_release = [&]() {
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * cs);
       cs += kMxGroups;
@@ -229,64 +280,94 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
         cs -= kMxRing;
         cph ^= 1;
       }
-      int trow[NT];
+    };
+
+    // ---------------------------------------------------------------- P2: gate/up
+    const int rw = wq * 8 + g;  // this lane's row within the 32-row stage
+    for (int r = 0; r < R2; ++r) {
+      const int u = lo_g + r * kMxGroups + grp;
+      const bool live = u < hi_g;
+      int wi = 0, i0 = 0, off = 0, m = 0;
+      uint32_t bt[4] = {0u, 0u, 0u, 0u}, bb1 = 0, sw1 = 0;
+      if (live) {
+        wi = u / tiles_g;
+        i0 = (u - wi * tiles_g) * kMxRows + wq * 8;
+        off = s_off[wi];
+        m = s_off[wi + 1] - off;
+        // B rows: the expert's tokens (rows past m repeat the first token;
+        // their columns are discarded)
+        const int t = s_gat[off + (g < m ? g : 0)] / K;
+        const int sw = ((c >> 1) & 1) | ((t & 1) << 1);
+        const uint32_t b0 = xs + t * xrow + c * 64;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + g;
-        trow[nt] = n < m ? s_gat[off + n] / K : -1;
+        for (int tt = 0; tt < 4; ++tt) bt[tt] = b0 + ((tt ^ sw) << 4);
+        if (NT == 2 && m > 8) {
+          const int t1 = s_gat[off + (8 + g < m ? 8 + g : 0)] / K;
+          sw1 = ((c >> 1) & 1) | ((t1 & 1) << 1);
+          bb1 = xs + t1 * xrow + c * 64;
+        }
       }
-      float acc[NT][4];
+      float acc[NT][4];  // one accumulation order for every token column
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-      if (!dead) {
+      for (int q = 0; q < nq; ++q) {
+        stage_wait();
+        // codes and scales to registers, then the stage is released at once
+        uint4 ag[kMxCh], au[kMxCh];
+        uint32_t eg[kMxCh], eu[kMxCh];
+        {
+          const uint32_t st = sbase + cs * slot;
+          const uint32_t ar = st + rw * (kMxCols / 2) + c * 16;
+          const uint32_t sr = st + g_sc + rw * (kMxCols / 32) + c;
 #pragma unroll
-        for (int j = 0; j < kMxMaxCh; ++j) {
-          const int ch = c0 + j;
-          if (ch < c1) {
-            const bool live = ch * 128 + c * 32 < d;
-            const uint32_t sgv = e8m0_half2(eg[j], bad), suv = e8m0_half2(eu[j], bad);
-            const uint32_t wg4[4] = {ag[j].x, ag[j].y, ag[j].z, ag[j].w};
-            const uint32_t wu4[4] = {au[j].x, au[j].y, au[j].z, au[j].w};
+          for (int j = 0; j < kMxCh; ++j) {
+            ag[j] = au[j] = make_uint4(0u, 0u, 0u, 0u);
+            eg[j] = eu[j] = 127u;
+            if (live && !dead) {
+              ag[j] = ld16(ar + j * 64);
+              au[j] = ld16(ar + g_up + j * 64);
+              eg[j] = ld1(sr + j * 4);
+              eu[j] = ld1(sr + (g_scu - g_sc) + j * 4);
+            }
+          }
+        }
+        stage_release();
+        if (live && !dead) {
+#pragma unroll
+          for (int j = 0; j < kMxCh; ++j) {
+            const uint32_t sgv = e8m0_half2(eg[j], range), suv = e8m0_half2(eu[j], range);
+            const int xo = (q * kMxCh + j) * 256;  // this chunk's bytes in a staged x row
 #pragma unroll
             for (int tt = 0; tt < 4; ++tt) {
               uint32_t rg4[4], ru4[4];
-              mx_decode_word(wg4[tt], sgv, rg4);
-              mx_decode_word(wu4[tt], suv, ru4);
-              const int q = ch * 16 + c * 4 + tt;
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt * 8 < m) {
-                  uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                  if (trow[nt] >= 0 && live) b = lds128(xs + trow[nt] * (d * 2) + swz(q, trow[nt]) * 16);
-                  mma_f16x(acc[nt], rg4[0], ru4[0], rg4[1], ru4[1], b.x, b.y);
-                  mma_f16x(acc[nt], rg4[2], ru4[2], rg4[3], ru4[3], b.z, b.w);
-                }
+              mx_decode_word(word_of(ag[j], tt), sgv, rg4);
+              mx_decode_word(word_of(au[j], tt), suv, ru4);
+              const uint4 b = ld16(bt[tt] + xo);
+              mma_f16x(acc[0], rg4[0], ru4[0], rg4[1], ru4[1], b.x, b.y);
+              mma_f16x(acc[0], rg4[2], ru4[2], rg4[3], ru4[3], b.z, b.w);
+              if (NT == 2 && m > 8) {
+                const uint4 b1 = ld16(bb1 + ((tt ^ sw1) << 4) + xo);
+                mma_f16x(acc[NT - 1], rg4[0], ru4[0], rg4[1], ru4[1], b1.x, b1.y);
+                mma_f16x(acc[NT - 1], rg4[2], ru4[2], rg4[3], ru4[3], b1.z, b1.w);
               }
             }
           }
         }
       }
+      if (live && !dead) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        *reinterpret_cast<float4 *>(redg + ((wq * NT + nt) * 32 + lane) * 4) =
-            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-      bar_sync_n(bar_grp, kMxGW * 32);
-      if (gt < NT * 64 && !dead) {
-        const int nt = gt >> 6, ln = (gt >> 1) & 31, q = gt & 1;
-        const int tok = nt * 8 + 2 * (ln & 3) + q;
-        if (tok < m) {
-          float gs = 0.f, us = 0.f;
-          for (int w = 0; w < kMxGW; ++w) {
-            gs += redg[((w * NT + nt) * 32 + ln) * 4 + q];
-            us += redg[((w * NT + nt) * 32 + ln) * 4 + q + 2];
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int tok = nt * 8 + 2 * c + q;
+            if (tok < m) {
+              const float inv = s_xinv[s_gat[off + tok] / K];
+              hf[(size_t)(off + tok) * I + i0 + g] = silu(acc[nt][q] * inv) * (acc[nt][q + 2] * inv);
+            }
           }
-          const float inv = s_xinv[s_gat[off + tok] / K];
-          hf[(size_t)(off + tok) * I + i0 + (ln >> 2)] = silu(gs * inv) * (us * inv);
-        }
       }
-      bar_sync_n(bar_grp, kMxGW * 32);
     }
     // ---- grid barrier 2: every h row is written (and the staged x is dead)
     bar_sync_n(kBarAll, kFC);
@@ -294,134 +375,147 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
     bar_sync_n(kBarAll, kFC);
     dead = dead || s_abort != 0;
 
-    // ---------------------------------------------------------------- P3: down + combine
+    // ---------------------------------------------------------------- P3: down
     const int CI = (I + 127) / 128;
-    const int hcpr = I / 8;
-    unsigned char *hrows = scratch + (size_t)grp * (NT * 8) * I * 2;  // this group's staged h rows
+    const int hrow = CI * 256;  // bytes per staged h row
+    unsigned char *hrows = scratch + (size_t)grp * (NT * 8) * hrow;
     const uint32_t hb = smem_u32(hrows);
-    const int nP2 = hi_g - lo_g;
+    const bool tail_dead = (I & 127) != 0 && c >= 2;
     int cur = -1, m = 0, off = 0;
-    for (int u = lo_d + (((grp - nP2) % kMxGroups) + kMxGroups) % kMxGroups; u < hi_d; u += kMxGroups) {
-      const int wi = u / tiles_d, dt = u - wi * tiles_d;
-      if (wi != cur) {
+    for (int r = 0; r < R3; ++r) {
+      const int u = lo_d + r * kMxGroups + grp;
+      const bool live = u < hi_d;
+      const int wi = live ? u / tiles_d : cur, dt = live ? u - wi * tiles_d : 0;
+      if (live && wi != cur) {
         bar_sync_n(bar_grp, kMxGW * 32);  // the previous expert's h rows are no longer read
         cur = wi;
         off = s_off[wi];
         m = s_off[wi + 1] - off;
         for (int n = wq; n < m; n += kMxGW) {
           const float *src = hf + (size_t)(off + n) * I;
+          const int hcpr = I / 8;
+          float4 v[2][2];
           float amax = 0.f;
-          for (int q = lane; q < hcpr; q += 32) {
-            const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + q * 8));
-            const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + q * 8 + 4));
-            amax = fmaxf(amax, fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
-                                     fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w)))));
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int q = lane + 32 * i;
+            v[i][0] = v[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (q < hcpr) {
+              v[i][0] = __ldcg(reinterpret_cast<const float4 *>(src + q * 8));
+              v[i][1] = __ldcg(reinterpret_cast<const float4 *>(src + q * 8 + 4));
+            }
+            amax = fmaxf(amax, fmaxf(fmaxf(fmaxf(fabsf(v[i][0].x), fabsf(v[i][0].y)),
+                                           fmaxf(fabsf(v[i][0].z), fabsf(v[i][0].w))),
+                                     fmaxf(fmaxf(fabsf(v[i][1].x), fabsf(v[i][1].y)),
+                                           fmaxf(fabsf(v[i][1].z), fabsf(v[i][1].w)))));
           }
           const int sh = row_shift(warp_max(amax));
           const float sc = exp2i(sh);
-          for (int q = lane; q < hcpr; q += 32) {
-            const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + q * 8));
-            const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + q * 8 + 4));
-            *reinterpret_cast<uint4 *>(hrows + (size_t)n * I * 2 + swz(q, n) * 16) =
-                make_uint4(pack_h2(v0.x * sc, v0.y * sc), pack_h2(v0.z * sc, v0.w * sc),
-                           pack_h2(v1.x * sc, v1.y * sc), pack_h2(v1.z * sc, v1.w * sc));
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int q = lane + 32 * i;
+            if (q < CI * 16)
+              *reinterpret_cast<uint4 *>(hrows + (size_t)n * hrow + swz(q, n) * 16) =
+                  make_uint4(pack_h2(v[i][0].x * sc, v[i][0].y * sc), pack_h2(v[i][0].z * sc, v[i][0].w * sc),
+                             pack_h2(v[i][1].x * sc, v[i][1].y * sc), pack_h2(v[i][1].z * sc, v[i][1].w * sc));
           }
           if (lane == 0) s_hinv[grp][n] = exp2i(-sh);
         }
         bar_sync_n(bar_grp, kMxGW * 32);
       }
-      if (!dead && !mbar_wait_fast(full0 + 8 * cs, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
-      uint4 a0[kMxMaxCh], a1[kMxMaxCh];
-      uint32_t e0[kMxMaxCh], e1[kMxMaxCh];
-      const uint32_t st = sbase + cs * slot;
-      const int rr = wq * 16 + g;
+      stage_wait();
+      uint4 a0[kMxCh], a1[kMxCh];
+      uint32_t e0[kMxCh], e1[kMxCh];
+      {
+        const uint32_t st = sbase + cs * slot;
+        const int rr = wq * 16 + g;
+        const uint32_t ar = st + rr * rowb_d + c * 16;
+        const uint32_t sr = st + d_sc + rr * srow_d + c;
 #pragma unroll
-      for (int j = 0; j < kMxMaxCh; ++j) {
-        a0[j] = a1[j] = make_uint4(0u, 0u, 0u, 0u);
-        e0[j] = e1[j] = 127u;
-        if (!dead && j < CI && j * 128 + c * 32 < I) {
-          const uint32_t o = rr * rowb_d + j * 64 + c * 16;
-          a0[j] = lds128(st + o);
-          a1[j] = lds128(st + o + 8 * rowb_d);
-          e0[j] = lds_u8(st + d_sc + rr * srow_d + j * 4 + c);
-          e1[j] = lds_u8(st + d_sc + (rr + 8) * srow_d + j * 4 + c);
+        for (int j = 0; j < kMxCh; ++j) {
+          a0[j] = a1[j] = make_uint4(0u, 0u, 0u, 0u);
+          e0[j] = e1[j] = 127u;
+          if (live && !dead && j < CI && !(tail_dead && j == CI - 1)) {
+            a0[j] = ld16(ar + j * 64);
+            a1[j] = ld16(ar + 8 * rowb_d + j * 64);
+            e0[j] = ld1(sr + j * 4);
+            e1[j] = ld1(sr + 8 * srow_d + j * 4);
+          }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * cs);
-      cs += kMxGroups;
-      if (cs >= kMxRing) {
-        cs -= kMxRing;
-        cph ^= 1;
+      stage_release();
+      if (!live || dead) continue;
+      uint32_t bt[4], bb1 = 0, sw1 = 0;
+      {
+        const int nn = g < m ? g : 0;
+        const int sw = ((c >> 1) & 1) | ((nn & 1) << 1);
+        const uint32_t b0 = hb + nn * hrow + c * 64;
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) bt[tt] = b0 + ((tt ^ sw) << 4);
+        if (NT == 2 && m > 8) {
+          const int n1 = 8 + g < m ? 8 + g : 0;
+          sw1 = ((c >> 1) & 1) | ((n1 & 1) << 1);
+          bb1 = hb + n1 * hrow + c * 64;
+        }
       }
       float acc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-      if (!dead) {
 #pragma unroll
-        for (int j = 0; j < kMxMaxCh; ++j) {
-          if (j < CI) {
-            const bool live = j * 128 + c * 32 < I;
-            const uint32_t s0 = e8m0_half2(e0[j], bad), s1 = e8m0_half2(e1[j], bad);
-            const uint32_t w0[4] = {a0[j].x, a0[j].y, a0[j].z, a0[j].w};
-            const uint32_t w1[4] = {a1[j].x, a1[j].y, a1[j].z, a1[j].w};
+      for (int j = 0; j < kMxCh; ++j) {
+        if (j < CI) {
+          const uint32_t s0 = e8m0_half2(e0[j], range), s1 = e8m0_half2(e1[j], range);
 #pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-              uint32_t r0v[4], r1v[4];
-              mx_decode_word(w0[tt], s0, r0v);
-              mx_decode_word(w1[tt], s1, r1v);
-              const int q = j * 16 + c * 4 + tt;
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt * 8 < m) {
-                  const int n = nt * 8 + g;
-                  uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                  if (n < m && live) b = lds128(hb + n * (I * 2) + swz(q, n) * 16);
-                  mma_f16x(acc[nt], r0v[0], r1v[0], r0v[1], r1v[1], b.x, b.y);
-                  mma_f16x(acc[nt], r0v[2], r1v[2], r0v[3], r1v[3], b.z, b.w);
-                }
-              }
+          for (int tt = 0; tt < 4; ++tt) {
+            uint32_t r0v[4], r1v[4];
+            mx_decode_word(word_of(a0[j], tt), s0, r0v);
+            mx_decode_word(word_of(a1[j], tt), s1, r1v);
+            const uint4 b = ld16(bt[tt] + j * 256);
+            mma_f16x(acc[0], r0v[0], r1v[0], r0v[1], r1v[1], b.x, b.y);
+            mma_f16x(acc[0], r0v[2], r1v[2], r0v[3], r1v[3], b.z, b.w);
+            if (NT == 2 && m > 8) {
+              const uint4 b1 = ld16(bb1 + ((tt ^ sw1) << 4) + j * 256);
+              mma_f16x(acc[NT - 1], r0v[0], r1v[0], r0v[1], r1v[1], b1.x, b1.y);
+              mma_f16x(acc[NT - 1], r0v[2], r1v[2], r0v[3], r1v[3], b1.z, b1.w);
             }
           }
         }
       }
       const int r0 = dt * 64 + wq * 16;
-      if (!dead) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int tok = nt * 8 + 2 * c + q;
-            if (tok < m) {
-              const int pair = s_gat[off + tok];
-              const float w = s_w[pair] * s_hinv[grp][tok];
-              p.ws.ys[(size_t)pair * d + r0 + g] = w * acc[nt][q];
-              p.ws.ys[(size_t)pair * d + r0 + g + 8] = w * acc[nt][q + 2];
-            }
-          }
-      }
-      // tile ticket: the last of the nW experts to finish tile dt combines it
-      __threadfence();
-      bar_sync_n(bar_grp, kMxGW * 32);
-      if (gt == 0) s_last[grp] = (atomicAdd(p.ws.down_cnt + dt, 1u) == (unsigned)(nW - 1)) ? 1u : 0u;
-      bar_sync_n(bar_grp, kMxGW * 32);
-      if (s_last[grp]) {
-        __threadfence();
-        if (!dead) {
-          for (int idx = gt; idx < k * 64; idx += kMxGW * 32) {
-            const int t = idx >> 6, r = dt * 64 + (idx & 63);
-            float sum = 0.f;
-            for (int sl = 0; sl < K; ++sl) sum += __ldcg(p.ws.ys + (size_t)(t * K + sl) * d + r);
-            if (p.residual) sum = load_act(p.residual, (size_t)t * d + r, DFV_BF16) + sum;
-            store_act(p.out, (size_t)t * d + r, DFV_BF16, sum);
+        for (int q = 0; q < 2; ++q) {
+          const int tok = nt * 8 + 2 * c + q;
+          if (tok < m) {
+            const int pair = s_gat[off + tok];
+            const float w = s_w[pair] * s_hinv[grp][tok];
+            p.ws.ys[(size_t)pair * d + r0 + g] = w * acc[nt][q];
+            p.ws.ys[(size_t)pair * d + r0 + g + 8] = w * acc[nt][q + 2];
           }
         }
-        if (gt == 0) p.ws.down_cnt[dt] = 0u;
+    }
+    // ---- grid barrier 3: every ys row is written
+    bar_sync_n(kBarAll, kFC);
+    if (tid == 0 && !grid_sync(p, 3)) s_abort = 1;
+    bar_sync_n(kBarAll, kFC);
+    dead = dead || s_abort != 0;
+
+    // ---------------------------------------------------------------- P4: combine
+    if (!dead) {
+      const int n_out = k * d;
+      const int o0 = (int)(((long long)blockIdx.x * n_out) / G), o1 = (int)(((long long)(blockIdx.x + 1) * n_out) / G);
+      for (int o = o0 + tid; o < o1; o += kFC) {
+        const int t = o / d, rrow = o - t * d;
+        float sum = 0.f;
+        for (int sl = 0; sl < K; ++sl) sum += __ldcg(p.ws.ys + (size_t)(t * K + sl) * d + rrow);
+        if (p.residual) sum = load_act(p.residual, (size_t)t * d + rrow, DFV_BF16) + sum;
+        store_act(p.out, (size_t)t * d + rrow, DFV_BF16, sum);
       }
     }
-    if (bad) atomicOr(p.ws.err, DFV_DEVERR_SCALE_RANGE);
+    if (range > kScaleRangeMax) atomicOr(p.ws.err, DFV_DEVERR_SCALE_RANGE);
   }
 
   // exit ticket: the last CTA out resets the grid-barrier count for the next launch
@@ -436,15 +530,55 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(FusedParams p) {
 
 template <int NT>
 size_t mx_smem(int d, int I, size_t *slot_out, size_t *scratch_out) {
-  size_t gslot = (size_t)8 * d + d / 2, dslot = (size_t)34 * I;
+  size_t gslot = (size_t)kMxRows * kMxCols + (size_t)kMxRows * kMxCols / 16, dslot = (size_t)34 * I;
   size_t slot = gslot > dslot ? gslot : dslot;
   slot = (slot + 127) & ~(size_t)127;
-  size_t xsb = (size_t)NT * 8 * d * 2, hsb = (size_t)kMxGroups * NT * 8 * I * 2;
+  const size_t ipad = (size_t)(I + 127) / 128 * 128;
+  size_t xsb = (size_t)NT * 8 * d * 2, hsb = (size_t)kMxGroups * NT * 8 * ipad * 2;
   size_t scratch = xsb > hsb ? xsb : hsb;
   scratch = (scratch + 127) & ~(size_t)127;
   *slot_out = slot;
   *scratch_out = scratch;
-  return kMxRing * slot + scratch + (size_t)kFW * NT * 32 * 16 + 16 * kMxRing;
+  return (size_t)kMxRing * slot + scratch + 16 * kMxRing;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!tried) {
+    tried = true;
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  }
+  if (!fn) snprintf(why, why_len, "mxfp4: cuTensorMapEncodeTiled is not available");
+  return fn;
+}
+
+// 2-D uint8 tensor map over a [rows][cols] byte matrix with a box of bx x by.
+bool encode_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by, char *why,
+               size_t why_len) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(why, why_len);
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {bx, by};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(why, why_len, "mxfp4: tensor map encode failed (%d)", (int)r);
+    return false;
+  }
+  return true;
 }
 
 }  // namespace
@@ -453,7 +587,7 @@ size_t mx_smem(int d, int I, size_t *slot_out, size_t *scratch_out) {
 // host side
 bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan) {
   if (k < 1 || k > kMaxBlock || E < 1 || E > kMaxExperts) return false;
-  if (d % 64 || I % 64 || d > 128 * kMxMaxCh * kMxGW || I > 128 * kMxMaxCh) return false;
+  if (d % kMxCols || d > kMxMaxD || I % 64 || I > 128 * kMxCh) return false;
   size_t slot = 0, scratch = 0;
   const size_t smem = k <= 8 ? mx_smem<1>(d, I, &slot, &scratch) : mx_smem<2>(d, I, &slot, &scratch);
   if (smem > 220 * 1024) return false;
@@ -463,6 +597,43 @@ bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan) {
   plan->scratch = (int)scratch;
   plan->ring = kMxRing;
   plan->smem = smem;
+  return true;
+}
+
+bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, size_t why_len) {
+  // encoded maps are cached per (weights, shape): encoding is host work only
+  struct Maps {
+    CUtensorMap wg, wu, sg, su;
+  };
+  static std::mutex mu;
+  static std::map<std::tuple<const void *, const void *, const void *, const void *, int, int, int>, Maps> cache;
+  const auto key = std::make_tuple(L->w_gate, L->w_up, (const void *)L->s_gate, (const void *)L->s_up, L->d, L->d_ff,
+                                   L->n_experts);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      p->tm_wg = it->second.wg;
+      p->tm_wu = it->second.wu;
+      p->tm_sg = it->second.sg;
+      p->tm_su = it->second.su;
+      return true;
+    }
+  }
+  Maps m;
+  const uint64_t rows = (uint64_t)L->n_experts * L->d_ff;
+  if (!encode_2d(&m.wg, L->w_gate, L->d / 2, rows, kMxCols / 2, kMxRows, why, why_len) ||
+      !encode_2d(&m.wu, L->w_up, L->d / 2, rows, kMxCols / 2, kMxRows, why, why_len) ||
+      !encode_2d(&m.sg, L->s_gate, L->d / 32, rows, kMxCols / 32, kMxRows, why, why_len) ||
+      !encode_2d(&m.su, L->s_up, L->d / 32, rows, kMxCols / 32, kMxRows, why, why_len))
+    return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = m;
+  p->tm_wg = m.wg;
+  p->tm_wu = m.wu;
+  p->tm_sg = m.sg;
+  p->tm_su = m.su;
   return true;
 }
 

@@ -46,13 +46,17 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// E8M0 byte s -> fp16x2 {2^(s-127), 2^(s-127)}; bad |= 1 when s is outside the
-// range where the scaled codes stay exact in fp16 (the scale is then clamped).
-__device__ __forceinline__ uint32_t e8m0_half2(uint32_t s, uint32_t &bad) {
-  bad |= (s - 104u) > 36u ? 1u : 0u;
-  const int E = (int)min(max(s, 104u), 140u) - 127;  // [-23, 13]
-  const uint32_t h = E >= -14 ? (uint32_t)(E + 15) << 10 : 1u << (E + 24);
-  return h | (h << 16);
+// E8M0 byte s -> fp16x2 {2^(s-127), 2^(s-127)}: for s in [113, 140] the scale
+// is a normal fp16 number whose exponent field is s - 112, so one multiply-add
+// builds both halves ((s - 112) * 0x04000400, written modulo 2^32).  There the
+// product of any E2M1 value with the scale is exact in fp16 (at most 6 * 2^13,
+// at least 2^-15, a subnormal on the 2^-24 grid).  `range` keeps the largest
+// s - 113 seen (unsigned): above kScaleRangeMax a scale outside [113, 140] was
+// used and the kernel reports DFV_DEVERR_SCALE_RANGE.
+constexpr uint32_t kScaleRangeMax = 27;
+__device__ __forceinline__ uint32_t e8m0_half2(uint32_t s, uint32_t &range) {
+  range = max(range, s - 113u);
+  return s * 0x04000400u + 0x3FFE4000u;
 }
 
 __device__ __forceinline__ void mma_f16x(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

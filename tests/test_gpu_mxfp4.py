@@ -43,8 +43,14 @@ def path(request, dfv):
     dfv.set_path(True)
 
 
-def _check_path(dfv, path):
-    assert dfv.last_layer_path() == (1 if path == "fused" else 0), dfv.fused_unavailable_reason()
+def _fused_ok(d, I):
+    """Shapes the single-launch mxfp4 kernel takes (others use the multi-launch path)."""
+    return d % 512 == 0 and d <= 2048 and I % 64 == 0 and I <= 512
+
+
+def _check_path(dfv, path, d=2048, I=512):
+    want = 1 if (path == "fused" and _fused_ok(d, I)) else 0
+    assert dfv.last_layer_path() == want, dfv.fused_unavailable_reason()
 
 
 def _max_rel_err(got: np.ndarray, ref: np.ndarray) -> float:
@@ -87,8 +93,8 @@ def _one_hot_rows(k, d, seed):
     return x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("d,I", [(64, 64), (128, 192), (320, 128)])
-@pytest.mark.parametrize("scale_exp", [(119, 127), (104, 140)])
+@pytest.mark.parametrize("d,I", [(64, 64), (128, 192), (320, 128), (512, 64), (1024, 192), (2048, 448)])
+@pytest.mark.parametrize("scale_exp", [(119, 127), (113, 140)])
 def test_decode_every_code_and_scale_one_hot(dfv, path, d, I, scale_exp):
     """One expert, K = 1 (routing weight exactly 1): with one-hot rows the gate
     and up values are single weights, so a wrong nibble order, sign, code or
@@ -102,7 +108,7 @@ def test_decode_every_code_and_scale_one_hot(dfv, path, d, I, scale_exp):
     ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
     out = dfv.moe_block_forward(L, x.cuda(), ws)
     torch.cuda.synchronize()
-    _check_path(dfv, path)
+    _check_path(dfv, path, d, I)
     assert dfv.read_device_error(ws) == 0
     ref = oracle.moe_forward(ol, np_of(x))
     # compare per row (rows differ in magnitude by up to 2^36 with wide scales)
@@ -111,19 +117,20 @@ def test_decode_every_code_and_scale_one_hot(dfv, path, d, I, scale_exp):
         assert _max_rel_err(got[t:t + 1], ref[t:t + 1]) <= TOL_DECODE, t
 
 
-@pytest.mark.parametrize("bad_scale", [103, 141])
-def test_scale_outside_exact_range_sets_device_error(dfv, path, bad_scale):
-    s = _shape(128, 4, 2, 64)
+@pytest.mark.parametrize("bad_scale", [112, 141])
+@pytest.mark.parametrize("d", [128, 512])
+def test_scale_outside_exact_range_sets_device_error(dfv, path, bad_scale, d):
+    s = _shape(d, 4, 2, 64)
     lw = inputs.make_layer(s, seed=3)
     lw.s_gate[0, 0, 0] = bad_scale
     lw.s_gate[1:, 0, 0] = bad_scale
     lw.s_down[:, 5, 1] = bad_scale
     L = dfv.Layer(lw.to("cuda"))
     ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
-    x = inputs.make_hidden(16, 128, "bf16", seed=4, device="cuda")
+    x = inputs.make_hidden(16, d, "bf16", seed=4, device="cuda")
     dfv.moe_block_forward(L, x, ws)
     torch.cuda.synchronize()
-    _check_path(dfv, path)
+    _check_path(dfv, path, d, 64)
     assert dfv.read_device_error(ws) & dfv.DEVERR_SCALE_RANGE
 
 
@@ -132,6 +139,8 @@ SMALL = [
     (320, 24, 3, 192),
     (512, 40, 8, 128),
     (256, 8, 8, 64),  # K == E: every row wakes every expert
+    (512, 16, 4, 192),   # single-launch kernel: one gate/up stage per unit, ragged d_ff chunk
+    (2048, 24, 8, 64),   # single-launch kernel: four gate/up stages per unit
 ]
 
 
@@ -149,7 +158,7 @@ def test_mxfp4_layer_parity_small(dfv, path, shape, k):
     out = dfv.moe_block_forward(L, xg, ws)
     torch.cuda.synchronize()
     assert dfv.read_device_error(ws) == 0
-    _check_path(dfv, path)
+    _check_path(dfv, path, d, I)
     ref = oracle.moe_forward(ol, np_of(x), nthreads=8)
     assert _max_rel_err(_out_np(out), ref) <= TOL_MXFP4
 
