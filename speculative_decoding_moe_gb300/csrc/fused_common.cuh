@@ -87,7 +87,10 @@ struct RouteSmem {
 //       among equals), routing weights, woken union, per-expert pair offsets
 //       (block scan) and the (expert, token)-sorted pair list.  CTA 0 also
 //       publishes the decision to the workspace and the caller's copies.
-__device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSmem &r) {
+// `between` runs on the same threads after P0 and before grid barrier 1 (work
+// that needs neither the other CTAs' logits nor the routing decision).
+template <class Between>
+__device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSmem &r, Between &&between) {
   const int k = p.k, d = p.d, E = p.E, K = p.K;
   const int G = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -128,6 +131,7 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     }
   }
   for (int i = tid; i < kMaxBlock * (kMaxExperts / 32); i += kFC) r.mask[i] = 0u;
+  between();
   bar_sync_n(kBarAll, kFC);
   // ---- grid barrier 1: every CTA's logits are published
   if (tid == 0 && !grid_sync(p, 1)) *r.abort = 1;

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   // ------------------------------------------------------------------ P0, P1: routing
   if (consumer) {
     const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort};
-    fused_route(p, rs);
+    fused_route(p, rs, [] {});
     if (tid == 0) {
       // with at most 8 tokens per expert the staged-x rows 8..15 are unused:
       // they become one more ring stage

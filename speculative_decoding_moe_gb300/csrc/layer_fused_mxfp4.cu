@@ -73,6 +73,23 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
       : "memory");
 }
 
+// Bounded wait (one thread) until all `want` pieces of an expert's h are
+// published by the CTAs that wrote them.
+static __device__ __noinline__ bool h_ready(const unsigned *cnt, unsigned want, unsigned *err, volatile int *abort) {
+  if (ld_acquire(cnt) >= want) return true;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire(cnt) < want) {
+    __nanosleep(64);
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitNs) {
+      atomicOr(err, DFV_DEVERR_GRID_WAIT);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_constant__ FusedParams p) {
   pdl_trigger();
@@ -85,6 +102,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   unsigned char *scratch = smem + kMxRing * slot;  // x rows (P2), h rows per group (P3)
   const uint32_t full0 = sbase + kMxRing * slot + p.scratch;
   const uint32_t empty0 = full0 + 8 * kMxRing;
+  float *acc1s = reinterpret_cast<float *>(smem + kMxRing * slot + p.scratch + 16 * kMxRing);  // [16 warps][32][4]
   // plain C++ loads from shared memory (ordered by the compiler against the
   // barrier waits, free to be scheduled early otherwise)
   auto ld16 = [&](uint32_t a) { return *reinterpret_cast<const uint4 *>(smem + (a - sbase)); };
@@ -102,6 +120,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   __shared__ float s_hinv[kMxGroups][kMaxBlock];  // 2^-shift of each staged h row, per group
   __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_nw;
+  __shared__ unsigned s_last_cta;
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -118,7 +137,60 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   const bool consumer = warp < kFW;
   if (consumer) {
     const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort};
-    fused_route(p, rs);
+    // the k rows of x are staged in fp16 (warp t: row t) while the other CTAs
+    // finish their router logits
+    fused_route(p, rs, [&] {
+      const int xrow = d * 2;
+      if (warp < k) {
+        const int t = warp, cpr = d / 8;
+        const uint16_t *src = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
+        __syncwarp();  // s_inv[t] was written by this warp's lane 0
+        const float inv = p.fuse_norm ? s_inv[t] : 1.f;
+        uint4 v[8];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = lane + 32 * i;
+          v[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (q < cpr) v[i] = *reinterpret_cast<const uint4 *>(src + (size_t)q * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
+            if (p.fuse_norm) {
+              a = rnd_bf16(a * inv);
+              b = rnd_bf16(b * inv);
+            }
+            amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+          }
+        }
+        const int sh = row_shift(warp_max(amax));
+        const float sc = exp2i(sh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = lane + 32 * i;
+          if (q < cpr) {
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t o4[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
+              if (p.fuse_norm) {
+                a = rnd_bf16(a * inv);
+                b = rnd_bf16(b * inv);
+              }
+              o4[h] = pack_h2(a * sc, b * sc);
+            }
+            *reinterpret_cast<uint4 *>(scratch + (size_t)t * xrow + swz(q, t) * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+          }
+        }
+        if (lane == 0) s_xinv[t] = exp2i(-sh);
+      }
+
+    });
   }
   __syncthreads();  // routing tables visible to the producer
 
@@ -216,58 +288,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
     uint32_t range = 0;  // largest (scale - 113) met, unsigned
     bool dead = s_abort != 0;
 
-    // ---- stage the k rows of x as fp16 (warp t: row t)
     const int xrow = d * 2;  // bytes per staged x row
     const uint32_t xs = smem_u32(scratch);
-    if (warp < k) {
-      const int t = warp, cpr = d / 8;
-      const uint16_t *src = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
-      const float inv = p.fuse_norm ? s_inv[t] : 1.f;
-      uint4 v[8];
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int q = lane + 32 * i;
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (q < cpr) v[i] = *reinterpret_cast<const uint4 *>(src + (size_t)q * 8);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
-          if (p.fuse_norm) {
-            a = rnd_bf16(a * inv);
-            b = rnd_bf16(b * inv);
-          }
-          amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
-        }
-      }
-      const int sh = row_shift(warp_max(amax));
-      const float sc = exp2i(sh);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int q = lane + 32 * i;
-        if (q < cpr) {
-          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-          uint32_t o4[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
-            if (p.fuse_norm) {
-              a = rnd_bf16(a * inv);
-              b = rnd_bf16(b * inv);
-            }
-            o4[h] = pack_h2(a * sc, b * sc);
-          }
-          *reinterpret_cast<uint4 *>(scratch + (size_t)t * xrow + swz(q, t) * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-        }
-      }
-      if (lane == 0) s_xinv[t] = exp2i(-sh);
-    }
-    bar_sync_n(kBarAll, kFC);
-
     int cs = grp, cph = 0;  // ring slot and phase of this group's next stage
     auto stage_wait = [&]() {
       if (!dead && !mbar_wait_fast(full0 + 8 * cs, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
@@ -283,95 +305,116 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
     };
 
     // ---------------------------------------------------------------- P2: gate/up
+    // Token columns 0-7 accumulate in registers.  An expert with more than 8
+    // tokens (k > 8 only) gets a second pass over the same stage for columns
+    // 8-15: the codes are read again from the stage, which is released only
+    // after that, and the sums of those columns live in shared memory between
+    // stages.  Both passes add in the same order.
     const int rw = wq * 8 + g;  // this lane's row within the 32-row stage
+    // B-row addresses of token column `n0 + g` of the expert at `off`
+    auto x_rows = [&](int off, int m, int n0, uint32_t (&bt)[4]) {
+      const int n = n0 + g;
+      const int t = s_gat[off + (n < m ? n : 0)] / K;  // past m: any valid row, discarded
+      const int sw = ((c >> 1) & 1) | ((t & 1) << 1);
+      const uint32_t b0 = xs + t * xrow + c * 64;
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) bt[tt] = b0 + ((tt ^ sw) << 4);
+    };
+    auto g_load = [&](uint4 (&ag)[kMxCh], uint4 (&au)[kMxCh], uint32_t (&eg)[kMxCh], uint32_t (&eu)[kMxCh]) {
+      const uint32_t st = sbase + cs * slot;
+      const uint32_t ar = st + rw * (kMxCols / 2) + c * 16;
+      const uint32_t sr = st + g_sc + rw * (kMxCols / 32) + c;
+#pragma unroll
+      for (int j = 0; j < kMxCh; ++j) {
+        ag[j] = ld16(ar + j * 64);
+        au[j] = ld16(ar + g_up + j * 64);
+        eg[j] = ld1(sr + j * 4);
+        eu[j] = ld1(sr + (g_scu - g_sc) + j * 4);
+      }
+    };
+    auto g_mma = [&](float (&acc)[4], const uint4 (&ag)[kMxCh], const uint4 (&au)[kMxCh],
+                     const uint32_t (&eg)[kMxCh], const uint32_t (&eu)[kMxCh], const uint32_t (&bt)[4], int q) {
+#pragma unroll
+      for (int j = 0; j < kMxCh; ++j) {
+        const uint32_t sgv = e8m0_half2(eg[j], range), suv = e8m0_half2(eu[j], range);
+        const int xo = (q * kMxCh + j) * 256;  // this chunk's bytes in a staged x row
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          uint32_t rg4[4], ru4[4];
+          mx_decode_word(word_of(ag[j], tt), sgv, rg4);
+          mx_decode_word(word_of(au[j], tt), suv, ru4);
+          const uint4 b = ld16(bt[tt] + xo);
+          mma_f16x(acc, rg4[0], ru4[0], rg4[1], ru4[1], b.x, b.y);
+          mma_f16x(acc, rg4[2], ru4[2], rg4[3], ru4[3], b.z, b.w);
+        }
+      }
+    };
     for (int r = 0; r < R2; ++r) {
       const int u = lo_g + r * kMxGroups + grp;
-      const bool live = u < hi_g;
+      const bool live = u < hi_g && !dead;
       int wi = 0, i0 = 0, off = 0, m = 0;
-      uint32_t bt[4] = {0u, 0u, 0u, 0u}, bb1 = 0, sw1 = 0;
+      uint32_t bt[4] = {0u, 0u, 0u, 0u};
       if (live) {
         wi = u / tiles_g;
         i0 = (u - wi * tiles_g) * kMxRows + wq * 8;
         off = s_off[wi];
         m = s_off[wi + 1] - off;
-        // B rows: the expert's tokens (rows past m repeat the first token;
-        // their columns are discarded)
-        const int t = s_gat[off + (g < m ? g : 0)] / K;
-        const int sw = ((c >> 1) & 1) | ((t & 1) << 1);
-        const uint32_t b0 = xs + t * xrow + c * 64;
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) bt[tt] = b0 + ((tt ^ sw) << 4);
-        if (NT == 2 && m > 8) {
-          const int t1 = s_gat[off + (8 + g < m ? 8 + g : 0)] / K;
-          sw1 = ((c >> 1) & 1) | ((t1 & 1) << 1);
-          bb1 = xs + t1 * xrow + c * 64;
-        }
+        x_rows(off, m, 0, bt);
       }
-      float acc[NT][4];  // one accumulation order for every token column
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+      const bool two = NT == 2 && live && m > 8;
+      float *a1s = acc1s + (warp * 32 + lane) * 4;
+      if (two) *reinterpret_cast<float4 *>(a1s) = make_float4(0.f, 0.f, 0.f, 0.f);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int q = 0; q < nq; ++q) {
         stage_wait();
-        // codes and scales to registers, then the stage is released at once
+        if (!live || dead) {
+          stage_release();
+          continue;
+        }
         uint4 ag[kMxCh], au[kMxCh];
         uint32_t eg[kMxCh], eu[kMxCh];
-        {
-          const uint32_t st = sbase + cs * slot;
-          const uint32_t ar = st + rw * (kMxCols / 2) + c * 16;
-          const uint32_t sr = st + g_sc + rw * (kMxCols / 32) + c;
-#pragma unroll
-          for (int j = 0; j < kMxCh; ++j) {
-            ag[j] = au[j] = make_uint4(0u, 0u, 0u, 0u);
-            eg[j] = eu[j] = 127u;
-            if (live && !dead) {
-              ag[j] = ld16(ar + j * 64);
-              au[j] = ld16(ar + g_up + j * 64);
-              eg[j] = ld1(sr + j * 4);
-              eu[j] = ld1(sr + (g_scu - g_sc) + j * 4);
-            }
-          }
-        }
-        stage_release();
-        if (live && !dead) {
-#pragma unroll
-          for (int j = 0; j < kMxCh; ++j) {
-            const uint32_t sgv = e8m0_half2(eg[j], range), suv = e8m0_half2(eu[j], range);
-            const int xo = (q * kMxCh + j) * 256;  // this chunk's bytes in a staged x row
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-              uint32_t rg4[4], ru4[4];
-              mx_decode_word(word_of(ag[j], tt), sgv, rg4);
-              mx_decode_word(word_of(au[j], tt), suv, ru4);
-              const uint4 b = ld16(bt[tt] + xo);
-              mma_f16x(acc[0], rg4[0], ru4[0], rg4[1], ru4[1], b.x, b.y);
-              mma_f16x(acc[0], rg4[2], ru4[2], rg4[3], ru4[3], b.z, b.w);
-              if (NT == 2 && m > 8) {
-                const uint4 b1 = ld16(bb1 + ((tt ^ sw1) << 4) + xo);
-                mma_f16x(acc[NT - 1], rg4[0], ru4[0], rg4[1], ru4[1], b1.x, b1.y);
-                mma_f16x(acc[NT - 1], rg4[2], ru4[2], rg4[3], ru4[3], b1.z, b1.w);
-              }
-            }
-          }
+        g_load(ag, au, eg, eu);
+        if (!two) stage_release();  // the codes are in registers: refill at once
+        g_mma(acc, ag, au, eg, eu, bt, q);
+        if (NT == 2 && two) {
+          g_load(ag, au, eg, eu);
+          stage_release();
+          uint32_t bt1[4];
+          x_rows(off, m, 8, bt1);
+          const float4 v = *reinterpret_cast<const float4 *>(a1s);
+          float a1[4] = {v.x, v.y, v.z, v.w};
+          g_mma(a1, ag, au, eg, eu, bt1, q);
+          *reinterpret_cast<float4 *>(a1s) = make_float4(a1[0], a1[1], a1[2], a1[3]);
         }
       }
       if (live && !dead) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int q = 0; q < 2; ++q) {
+          const int tok = 2 * c + q;
+          if (tok < m) {
+            const float inv = s_xinv[s_gat[off + tok] / K];
+            hf[(size_t)(off + tok) * I + i0 + g] = silu(acc[q] * inv) * (acc[q + 2] * inv);
+          }
+        }
+        if (NT == 2 && two) {
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            const int tok = nt * 8 + 2 * c + q;
+            const int tok = 8 + 2 * c + q;
             if (tok < m) {
               const float inv = s_xinv[s_gat[off + tok] / K];
-              hf[(size_t)(off + tok) * I + i0 + g] = silu(acc[nt][q] * inv) * (acc[nt][q + 2] * inv);
+              hf[(size_t)(off + tok) * I + i0 + g] = silu(a1s[q] * inv) * (a1s[q + 2] * inv);
             }
           }
+        }
+      }
+      if (u < hi_g) {
+        // publish: 8 more d_ff rows of this expert's h are written
+        __syncwarp();
+        if (lane == 0) red_release_add(p.ws.hcnt + (u / tiles_g), 1u);
       }
     }
-    // ---- grid barrier 2: every h row is written (and the staged x is dead)
-    bar_sync_n(kBarAll, kFC);
-    if (tid == 0 && !grid_sync(p, 2)) s_abort = 1;
+    // the staged x rows are dead once the CTA's gate/up work is done; the
+    // down units wait only for the h rows of their own expert
     bar_sync_n(kBarAll, kFC);
     dead = dead || s_abort != 0;
 
@@ -387,7 +430,10 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
       const bool live = u < hi_d;
       const int wi = live ? u / tiles_d : cur, dt = live ? u - wi * tiles_d : 0;
       if (live && wi != cur) {
-        bar_sync_n(bar_grp, kMxGW * 32);  // the previous expert's h rows are no longer read
+        if (wq == 0 && lane == 0 && !dead && !h_ready(p.ws.hcnt + wi, (unsigned)(I / 8), p.ws.err, &s_abort))
+          dead = true;
+        bar_sync_n(bar_grp, kMxGW * 32);  // h of this expert complete; the previous one's rows are no longer read
+        dead = dead || s_abort != 0;
         cur = wi;
         off = s_off[wi];
         m = s_off[wi + 1] - off;
@@ -424,9 +470,15 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
         bar_sync_n(bar_grp, kMxGW * 32);
       }
       stage_wait();
+      if (!live || dead) {
+        stage_release();
+        continue;
+      }
+      const int r0 = dt * 64 + wq * 16;
+      const bool two = NT == 2 && m > 8;
       uint4 a0[kMxCh], a1[kMxCh];
       uint32_t e0[kMxCh], e1[kMxCh];
-      {
+      auto d_load = [&]() {
         const uint32_t st = sbase + cs * slot;
         const int rr = wq * 16 + g;
         const uint32_t ar = st + rr * rowb_d + c * 16;
@@ -435,71 +487,63 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
         for (int j = 0; j < kMxCh; ++j) {
           a0[j] = a1[j] = make_uint4(0u, 0u, 0u, 0u);
           e0[j] = e1[j] = 127u;
-          if (live && !dead && j < CI && !(tail_dead && j == CI - 1)) {
+          if (j < CI && !(tail_dead && j == CI - 1)) {
             a0[j] = ld16(ar + j * 64);
             a1[j] = ld16(ar + 8 * rowb_d + j * 64);
             e0[j] = ld1(sr + j * 4);
             e1[j] = ld1(sr + 8 * srow_d + j * 4);
           }
         }
-      }
-      stage_release();
-      if (!live || dead) continue;
-      uint32_t bt[4], bb1 = 0, sw1 = 0;
-      {
-        const int nn = g < m ? g : 0;
-        const int sw = ((c >> 1) & 1) | ((nn & 1) << 1);
-        const uint32_t b0 = hb + nn * hrow + c * 64;
+      };
+      // one pass = token columns n0..n0+7 of this expert over the stage's codes
+      auto d_pass = [&](int n0) {
+        uint32_t bt[4];
+        {
+          const int n = n0 + g, nn = n < m ? n : 0;
+          const int sw = ((c >> 1) & 1) | ((nn & 1) << 1);
+          const uint32_t b0 = hb + nn * hrow + c * 64;
 #pragma unroll
-        for (int tt = 0; tt < 4; ++tt) bt[tt] = b0 + ((tt ^ sw) << 4);
-        if (NT == 2 && m > 8) {
-          const int n1 = 8 + g < m ? 8 + g : 0;
-          sw1 = ((c >> 1) & 1) | ((n1 & 1) << 1);
-          bb1 = hb + n1 * hrow + c * 64;
+          for (int tt = 0; tt < 4; ++tt) bt[tt] = b0 + ((tt ^ sw) << 4);
         }
-      }
-      float acc[NT][4];
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int j = 0; j < kMxCh; ++j) {
+          if (j < CI) {
+            const uint32_t s0 = e8m0_half2(e0[j], range), s1 = e8m0_half2(e1[j], range);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMxCh; ++j) {
-        if (j < CI) {
-          const uint32_t s0 = e8m0_half2(e0[j], range), s1 = e8m0_half2(e1[j], range);
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            uint32_t r0v[4], r1v[4];
-            mx_decode_word(word_of(a0[j], tt), s0, r0v);
-            mx_decode_word(word_of(a1[j], tt), s1, r1v);
-            const uint4 b = ld16(bt[tt] + j * 256);
-            mma_f16x(acc[0], r0v[0], r1v[0], r0v[1], r1v[1], b.x, b.y);
-            mma_f16x(acc[0], r0v[2], r1v[2], r0v[3], r1v[3], b.z, b.w);
-            if (NT == 2 && m > 8) {
-              const uint4 b1 = ld16(bb1 + ((tt ^ sw1) << 4) + j * 256);
-              mma_f16x(acc[NT - 1], r0v[0], r1v[0], r0v[1], r1v[1], b1.x, b1.y);
-              mma_f16x(acc[NT - 1], r0v[2], r1v[2], r0v[3], r1v[3], b1.z, b1.w);
+            for (int tt = 0; tt < 4; ++tt) {
+              uint32_t r0v[4], r1v[4];
+              mx_decode_word(word_of(a0[j], tt), s0, r0v);
+              mx_decode_word(word_of(a1[j], tt), s1, r1v);
+              const uint4 b = ld16(bt[tt] + j * 256);
+              mma_f16x(acc, r0v[0], r1v[0], r0v[1], r1v[1], b.x, b.y);
+              mma_f16x(acc, r0v[2], r1v[2], r0v[3], r1v[3], b.z, b.w);
             }
           }
         }
-      }
-      const int r0 = dt * 64 + wq * 16;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const int tok = nt * 8 + 2 * c + q;
+          const int tok = n0 + 2 * c + q;
           if (tok < m) {
             const int pair = s_gat[off + tok];
             const float w = s_w[pair] * s_hinv[grp][tok];
-            p.ws.ys[(size_t)pair * d + r0 + g] = w * acc[nt][q];
-            p.ws.ys[(size_t)pair * d + r0 + g + 8] = w * acc[nt][q + 2];
+            p.ws.ys[(size_t)pair * d + r0 + g] = w * acc[q];
+            p.ws.ys[(size_t)pair * d + r0 + g + 8] = w * acc[q + 2];
           }
         }
+      };
+      d_load();
+      if (!two) stage_release();  // the codes are in registers: refill at once
+      d_pass(0);
+      if (NT == 2 && two) {  // an expert with more than 8 tokens: columns 8-15
+        d_load();
+        stage_release();
+        d_pass(8);
+      }
     }
-    // ---- grid barrier 3: every ys row is written
+    // ---- grid barrier 2: every ys row is written
     bar_sync_n(kBarAll, kFC);
-    if (tid == 0 && !grid_sync(p, 3)) s_abort = 1;
+    if (tid == 0 && !grid_sync(p, 2)) s_abort = 1;
     bar_sync_n(kBarAll, kFC);
     dead = dead || s_abort != 0;
 
@@ -520,8 +564,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
 
   // exit ticket: the last CTA out resets the grid-barrier count for the next launch
   __syncthreads();
-  if (tid == 0) {
-    if (atomicAdd(p.ws.sync + 1, 1u) == (unsigned)(G - 1)) {
+  if (tid == 0) s_last_cta = atomicAdd(p.ws.sync + 1, 1u) == (unsigned)(G - 1);
+  __syncthreads();
+  if (s_last_cta) {
+    __threadfence();
+    for (int i = tid; i < nW; i += blockDim.x) p.ws.hcnt[i] = 0u;  // indexed by woken position
+    if (tid == 0) {
       atomicExch(p.ws.sync, 0u);
       atomicExch(p.ws.sync + 1, 0u);
     }
@@ -539,7 +587,7 @@ size_t mx_smem(int d, int I, size_t *slot_out, size_t *scratch_out) {
   scratch = (scratch + 127) & ~(size_t)127;
   *slot_out = slot;
   *scratch_out = scratch;
-  return (size_t)kMxRing * slot + scratch + 16 * kMxRing;
+  return (size_t)kMxRing * slot + scratch + 16 * kMxRing + (NT == 2 ? (size_t)kFW * 32 * 16 : 0);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len) {
