@@ -38,6 +38,37 @@ N_LAYERS = 40   # layers per step (--layers overrides, for profiling runs only)
 KBLOCK = 16
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
+# DRAM bytes (read + write) per launch from one ncu capture of each single-launch
+# kernel at k=16 (the capture and its command are summarised under profiles/),
+# keyed by a hash of the kernel's sources: a kernel edited since the capture
+# reports traffic null.
+KERNEL_SOURCES = {
+    "moe_fused_kernel": ["layer_fused.cu", "fused_common.cuh", "dfv_internal.cuh"],
+    "moe_fused_mx_kernel": ["layer_fused_mxfp4.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
+}
+NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
+    "moe_fused_kernel": ("e6b5c0814dfea91e", 728468480 + 7187200, 77 * 9437184 + 524288),
+    "moe_fused_mx_kernel": ("ff79adaa8bd5838e", 171767808 + 6757376, 102 * 1671168 + 1048576),
+}
+
+
+def kernel_hash(name: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[name]:
+        with open(os.path.join(ROOT, "speculative_decoding_moe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name: str, algorithmic_bytes: float):
+    """Traffic of the captured launch scaled to a launch of `algorithmic_bytes`
+    (by the woken experts processed), or None when the kernel changed since."""
+    t = NCU_TRAFFIC.get(name)
+    if t is None or t[0] != kernel_hash(name):
+        return None
+    return t[1] * algorithmic_bytes / t[2]
+
 
 def load_peaks():
     try:
@@ -342,7 +373,9 @@ def run_gpu(args):
     down_bytes = float(W16.sum().item()) * (shape.d * shape.d_ff * 2) / N_LAYERS
     peak_bw = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
     roofline = {"bound": "hbm", "kernel": "moe_fused_kernel<2> (one launch per layer, k=16)", "achieved": fused_gbs,
-                "peak": peak_bw, "unit": "GB/s", "frac": fused_gbs / peak_bw, "traffic": None,
+                "peak": peak_bw, "unit": "GB/s", "frac": fused_gbs / peak_bw,
+                "traffic": ncu_traffic("moe_fused_kernel", layer_bytes),
+                "traffic_note": "ncu dram read+write of one k=16 launch, scaled to this average launch by woken experts",
                 "peak_kind": peak_kind + " (STREAM-style copy, burst)",
                 "per_launch_us": fused_ms * 1e3, "algorithmic_bytes_per_launch": layer_bytes,
                 "multi_kernel_per_launch_us": {"router": phm[0] * 1e3, "gate_up": phm[1] * 1e3,
@@ -485,6 +518,7 @@ def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
                 for i in range(3):
                     tot[i] += e[i].elapsed_time(e[i + 1])
     ph = [t / (reps * N_LAYERS) for t in tot]
+    fused = dfv.last_layer_path() == 1
     Wm = float(W16.double().mean().item())
     gate_bytes = Wm * 2 * (shape.d_ff * shape.d // 2 + shape.d_ff * shape.d // 32)
     down_bytes = Wm * (shape.d * shape.d_ff // 2 + shape.d * shape.d_ff // 32)
@@ -497,11 +531,19 @@ def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
         "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS},
         "woken_mean": {"k16": Wm, "k1": float(W1.double().mean().item())},
         "verify_decode": {"latency_ratio": ms16 / ms1, "woken_byte_ratio": b16 / b1, "quotient": (b16 / b1) / (ms16 / ms1)},
-        "per_launch_us": {"router": ph[0] * 1e3, "gate_up": ph[1] * 1e3, "down_combine": ph[2] * 1e3},
-        "gate_up_gbs": gate_bytes / (ph[1] * 1e-3) / 1e9, "down_combine_gbs": down_bytes / (ph[2] * 1e-3) / 1e9,
+        "kernel_path": "moe_fused_mx_kernel (one launch per layer)" if fused else "router + gate/up + down launches",
         "layer_gbs_events": layer_bytes / (sum(ph) * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "moe_fused_mx_kernel<2> (k=16)" if fused else "multi-launch",
+                     "achieved": layer_bytes / (sum(ph) * 1e-3) / 1e9, "peak": peak_bw, "unit": "GB/s",
+                     "frac": layer_bytes / (sum(ph) * 1e-3) / 1e9 / peak_bw,
+                     "traffic": ncu_traffic("moe_fused_mx_kernel", layer_bytes) if fused else None,
+                     "per_launch_us": sum(ph) * 1e3, "algorithmic_bytes_per_launch": layer_bytes},
         "device_error": dfv.read_device_error(ws),
     }
+    if not fused:
+        res["per_launch_us"] = {"router": ph[0] * 1e3, "gate_up": ph[1] * 1e3, "down_combine": ph[2] * 1e3}
+        res["gate_up_gbs"] = gate_bytes / (ph[1] * 1e-3) / 1e9
+        res["down_combine_gbs"] = down_bytes / (ph[2] * 1e-3) / 1e9
     if not args.no_stack:
         V = 151936
         xs0 = inputs.make_hidden(KBLOCK, shape.d, "bf16", seed=17 + 100 * rank, device=dev)

@@ -95,16 +95,32 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
   const int G = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (warp < k) {
-    const int t = warp;
+    // lane l takes the 16-byte pieces l, l+32, ... of the row, 8 at a time
+    // with all their loads in flight; the sums run in piece order
+    const int t = warp, cpr = d / 8;
     const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
     float inv = 1.f;
     if (p.fuse_norm) {
       float ss = 0.f;
-      for (int c = lane; c < d / 8; c += 32) {
-        float f[8];
-        load8_bf16(xr, (size_t)c * 8, f);
+      for (int c0 = 0; c0 < cpr; c0 += 256) {
+        uint4 xv[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + lane + 32 * i;
+          xv[i] = c < cpr ? *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + lane + 32 * i < cpr) {
+            const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
+              ss = fmaf(a, a, ss);
+              ss = fmaf(b, b, ss);
+            }
+          }
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -114,16 +130,34 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     for (int e = blockIdx.x; e < E; e += G) {
       const uint16_t *wr = reinterpret_cast<const uint16_t *>(p.wr) + (size_t)e * d;
       float acc = 0.f;
-      for (int c = lane; c < d / 8; c += 32) {
-        float f[8], w8[8];
-        load8_bf16(xr, (size_t)c * 8, f);
-        load8_bf16(wr, (size_t)c * 8, w8);
-        if (p.fuse_norm) {
+      for (int c0 = 0; c0 < cpr; c0 += 256) {
+        uint4 xv[8], wv[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) f[q] = rnd_bf16(f[q] * inv);
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + lane + 32 * i;
+          xv[i] = wv[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (c < cpr) {
+            xv[i] = *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8);
+            wv[i] = *reinterpret_cast<const uint4 *>(wr + (size_t)c * 8);
+          }
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc = fmaf(f[q], w8[q], acc);
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + lane + 32 * i < cpr) {
+            const uint32_t x4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+            const uint32_t w4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              float a = bf16_lo(x4[h]), b = bf16_hi(x4[h]);
+              if (p.fuse_norm) {
+                a = rnd_bf16(a * inv);
+                b = rnd_bf16(b * inv);
+              }
+              acc = fmaf(a, bf16_lo(w4[h]), acc);
+              acc = fmaf(b, bf16_hi(w4[h]), acc);
+            }
+          }
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
