@@ -52,14 +52,14 @@ dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
     return p;
   };
   // counters and the error word first, at offsets that depend on nothing but d
-  // (a fixed 5 KB for d <= 13312): calls of any k, and layers of any width in
+  // (a fixed 8 KB for d <= 13312): calls of any k, and layers of any width in
   // that range, can share a workspace
   w.router_cnt = (unsigned *)take(4);
   w.err = (unsigned *)take(4);
   w.sync = (unsigned *)take(16);
   const size_t tiles = (d + 15) / 16;
   w.down_cnt = (unsigned *)take(tiles * 4 > 3328 ? tiles * 4 : 3328);
-  w.hcnt = (unsigned *)take(DFV_MAX_EXPERTS * 4);
+  w.flags = (unsigned *)take(1024 * 4);
   w.logits = (float *)take(km * E * 4);
   w.topk_idx = (int32_t *)take(km * K * 4);
   w.topk_w = (float *)take(km * K * 4);

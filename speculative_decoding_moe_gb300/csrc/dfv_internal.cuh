@@ -33,7 +33,7 @@ struct Workspace {
   unsigned *err;         // [1] device error bits (DFV_DEVERR_*), sticky until cleared
   unsigned *sync;        // [4] fused kernel: grid-barrier count, exit ticket, abort flag
   unsigned *down_cnt;    // [ceil(d / 16)] one ticket per down tile
-  unsigned *hcnt;        // [E] mxfp4 single-launch kernel: h pieces written, by woken position
+  unsigned *flags;       // [1024] mxfp4 single-launch kernel: per-CTA "gate/up work done" flags
   void *xn;           // [k_max][d] activations staged for the expert FFN (act dtype)
   float *h;           // [k_max * K][d_ff]  SwiGLU activations, by sorted pair position
                       // (fused kernel: bf16 hi [kK][d_ff] then bf16 lo [kK][d_ff])

@@ -73,21 +73,26 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
       : "memory");
 }
 
-// Bounded wait (one thread) until all `want` pieces of an expert's h are
-// published by the CTAs that wrote them.
-static __device__ __noinline__ bool h_ready(const unsigned *cnt, unsigned want, unsigned *err, volatile int *abort) {
-  if (ld_acquire(cnt) >= want) return true;
+// Bounded wait, by one whole warp, until CTAs b0..b1 have published the end of
+// their gate/up work (every h row they own is written): lane l polls CTAs
+// b0 + l, b0 + l + 32, ... so the flags are read in parallel.
+static __device__ __noinline__ bool ctas_done(const unsigned *flags, int b0, int b1, unsigned *err,
+                                              volatile int *abort) {
+  const int lane = threadIdx.x & 31;
   const unsigned long long t0 = global_ns();
-  while (ld_acquire(cnt) < want) {
-    __nanosleep(64);
-    if (*abort) return false;
-    if (global_ns() - t0 > kWaitNs) {
-      atomicOr(err, DFV_DEVERR_GRID_WAIT);
-      *abort = 1;
-      return false;
+  bool ok = true;
+  for (int b = b0 + lane; b <= b1 && ok; b += 32) {
+    while (ld_acquire(flags + b) == 0u) {
+      __nanosleep(64);
+      if (*abort || global_ns() - t0 > kWaitNs) {
+        if (!*abort) atomicOr(err, DFV_DEVERR_GRID_WAIT);
+        *abort = 1;
+        ok = false;
+        break;
+      }
     }
   }
-  return true;
+  return __all_sync(0xffffffffu, ok);
 }
 
 template <int NT>
@@ -407,15 +412,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
           }
         }
       }
-      if (u < hi_g) {
-        // publish: 8 more d_ff rows of this expert's h are written
-        __syncwarp();
-        if (lane == 0) red_release_add(p.ws.hcnt + (u / tiles_g), 1u);
-      }
     }
-    // the staged x rows are dead once the CTA's gate/up work is done; the
-    // down units wait only for the h rows of their own expert
+    // the staged x rows are dead once the CTA's gate/up work is done; publish
+    // that (one release covers every h row this CTA wrote).  A down unit waits
+    // only for the CTAs that own its expert's gate/up units.
     bar_sync_n(kBarAll, kFC);
+    if (tid == 0) red_release_add(p.ws.flags + blockIdx.x, 1u);
     dead = dead || s_abort != 0;
 
     // ---------------------------------------------------------------- P3: down
@@ -430,8 +432,13 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
       const bool live = u < hi_d;
       const int wi = live ? u / tiles_d : cur, dt = live ? u - wi * tiles_d : 0;
       if (live && wi != cur) {
-        if (wq == 0 && lane == 0 && !dead && !h_ready(p.ws.hcnt + wi, (unsigned)(I / 8), p.ws.err, &s_abort))
-          dead = true;
+        if (wq == 0 && !dead) {
+          // gate/up unit u is CTA floor(((u + 1) G - 1) / U)'s
+          const long long U = (long long)nW * tiles_g;
+          const int b0 = (int)(((long long)(wi * tiles_g + 1) * G - 1) / U);
+          const int b1 = (int)(((long long)((wi + 1) * tiles_g) * G - 1) / U);
+          if (!ctas_done(p.ws.flags, b0, b1, p.ws.err, &s_abort)) dead = true;
+        }
         bar_sync_n(bar_grp, kMxGW * 32);  // h of this expert complete; the previous one's rows are no longer read
         dead = dead || s_abort != 0;
         cur = wi;
@@ -568,7 +575,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   __syncthreads();
   if (s_last_cta) {
     __threadfence();
-    for (int i = tid; i < nW; i += blockDim.x) p.ws.hcnt[i] = 0u;  // indexed by woken position
+    for (int i = tid; i < G; i += blockDim.x) p.ws.flags[i] = 0u;
     if (tid == 0) {
       atomicExch(p.ws.sync, 0u);
       atomicExch(p.ws.sync + 1, 0u);
@@ -714,6 +721,10 @@ int fused_mx_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
     snprintf(why, why_len, "SM count query: %s", cudaGetErrorString(e));
+    return 0;
+  }
+  if (sms > 1024) {  // the per-CTA flags in the workspace hold 1024 CTAs
+    snprintf(why, why_len, "mxfp4: %d SMs exceed the 1024 workspace flags", sms);
     return 0;
   }
   auto kern = k <= 8 ? moe_fused_mx_kernel<1> : moe_fused_mx_kernel<2>;
