@@ -216,6 +216,7 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
   fp.ws = w;
   fp.u_idx = u_idx;
   fp.u_nw = u_nw;
+  if (!mx) dfv::fused_tensor_maps(&fp, L, plan);
   auto go = [&](bool pdl) {
     return mx ? dfv::launch_fused_mx(fp, plan, grid, s, pdl) : dfv::launch_fused(fp, plan, grid, s, pdl);
   };

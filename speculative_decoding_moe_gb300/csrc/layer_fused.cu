@@ -34,13 +34,31 @@
 //       block and k single-token calls agree bit for bit.
 // Every wait is bounded (2 s) and reports through the workspace error word.
 #include <cstdio>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include <cudaTypedefs.h>
 
 #include "fused_common.cuh"
 
 namespace dfv {
 
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 template <int NT>
-__global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
+__global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant__ FusedParams p) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(128) unsigned char smem[];
@@ -48,6 +66,11 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
   const int G = gridDim.x;
   const int rsg = fpad(ks * 2);        // gate/up stage row stride (64 mod 128: conflict-free)
   const int rsx = d * 2;               // staged x row stride (16B chunks XOR-swizzled)
+  // gate/up stage layout: padded rows (mode 0) or [ks/256][8 rows][512 B] blocks
+  // from tensor copies (modes 1, 2); up rows follow the gate rows
+  const uint32_t row_b = p.tma_mode ? 512u : (uint32_t)rsg;
+  const uint32_t blk_b = p.tma_mode ? 4096u : 512u;
+  const uint32_t up_off = p.tma_mode ? 8u * ks * 2 : 8u * rsg;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t slot = p.slot;
   const int SH = p.ring;                                   // ring stages the launch reserved
@@ -128,10 +151,20 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
           }
           const uint32_t fb = full0 + 8 * s, dst = slot_addr(s);
           mbar_expect_tx(fb, 16u * ks * 2);
-          for (int r = 0; r < 8; ++r) {
-            const size_t row = ((size_t)e * I + i0 + r) * d + (size_t)sl * ks;
-            bulk_g2s(dst + r * rsg, wg + row, ks * 2, fb);
-            bulk_g2s(dst + (8 + r) * rsg, wu + row, ks * 2, fb);
+          if (p.tma_mode == 2) {  // [ks/256][8 rows][256]: one box per matrix
+            tma_3d(dst, &p.tm_wg, 0, e * I + i0, sl * (ks / 256), fb);
+            tma_3d(dst + up_off, &p.tm_wu, 0, e * I + i0, sl * (ks / 256), fb);
+          } else if (p.tma_mode == 1) {  // the same layout from 256-column boxes
+            for (int b = 0; b < ks / 256; ++b) {
+              tma_2d(dst + b * 4096, &p.tm_wg, sl * ks + b * 256, e * I + i0, fb);
+              tma_2d(dst + up_off + b * 4096, &p.tm_wu, sl * ks + b * 256, e * I + i0, fb);
+            }
+          } else {  // one padded row per copy
+            for (int r = 0; r < 8; ++r) {
+              const size_t row = ((size_t)e * I + i0 + r) * d + (size_t)sl * ks;
+              bulk_g2s(dst + r * rsg, wg + row, ks * 2, fb);
+              bulk_g2s(dst + (8 + r) * rsg, wu + row, ks * 2, fb);
+            }
           }
         }
       }
@@ -205,9 +238,10 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(FusedParams p) {
 #pragma unroll
           for (int j = 0; j < kMaxChunksP2; ++j) {
             if (c0 + j < c1) {
-              const uint32_t q16 = ((c0 + j) * 4 + c) * 16;
-              ag[j] = lds128(st + g * rsg + q16);
-              au[j] = lds128(st + (8 + g) * rsg + q16);
+              const int ch = c0 + j;  // 32-column chunk within the stage
+              const uint32_t o = g * row_b + (ch >> 3) * blk_b + (ch & 7) * 64 + c * 16;
+              ag[j] = lds128(st + o);
+              au[j] = lds128(st + up_off + o);
             }
           }
         }
@@ -398,6 +432,67 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   plan->ring = ring;
   plan->smem = ring * slot + scratch + redb + 16 * kMaxRing;
   return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len);
+
+void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan) {
+  // the gate/up stage of 8 rows x ks columns as one 3-D box ([ks/256][8][256]),
+  // else as ks/256 2-D boxes of 8 x 256; cached per (weights, shape)
+  struct Maps {
+    int mode;
+    CUtensorMap wg, wu;
+  };
+  static std::mutex mu;
+  static std::map<std::tuple<const void *, const void *, int, int, int, int>, Maps> cache;
+  p->tma_mode = 0;
+  const int d = L->d, I = L->d_ff, E = L->n_experts, ks = plan.ks;
+  if (d % 256 || ks % 256) return;
+  const auto key = std::make_tuple(L->w_gate, L->w_up, d, I, E, ks);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      p->tma_mode = it->second.mode;
+      p->tm_wg = it->second.wg;
+      p->tm_wu = it->second.wu;
+      return;
+    }
+  }
+  char why[128];
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(why, sizeof why);
+  Maps m = {};
+  if (fn) {
+    const cuuint64_t rows = (cuuint64_t)E * I;
+    auto enc3 = [&](CUtensorMap *map, const void *base) {
+      const cuuint64_t dims[3] = {256, rows, (cuuint64_t)d / 256};
+      const cuuint64_t strides[2] = {(cuuint64_t)d * 2, 512};
+      const cuuint32_t box[3] = {256, 8, (cuuint32_t)ks / 256};
+      const cuuint32_t es[3] = {1, 1, 1};
+      return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    auto enc2 = [&](CUtensorMap *map, const void *base) {
+      const cuuint64_t dims[2] = {(cuuint64_t)d, rows};
+      const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+      const cuuint32_t box[2] = {256, 8};
+      const cuuint32_t es[2] = {1, 1};
+      return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (enc3(&m.wg, L->w_gate) && enc3(&m.wu, L->w_up))
+      m.mode = 2;
+    else if (enc2(&m.wg, L->w_gate) && enc2(&m.wu, L->w_up))
+      m.mode = 1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = m;
+  p->tma_mode = m.mode;
+  p->tm_wg = m.wg;
+  p->tm_wu = m.wu;
 }
 
 cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {

@@ -597,25 +597,9 @@ size_t mx_smem(int d, int I, size_t *slot_out, size_t *scratch_out) {
   return (size_t)kMxRing * slot + scratch + 16 * kMxRing + (NT == 2 ? (size_t)kFW * 32 * 16 : 0);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len) {
-  static std::mutex mu;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!tried) {
-    tried = true;
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    else
-      cudaGetLastError();
-  }
-  if (!fn) snprintf(why, why_len, "mxfp4: cuTensorMapEncodeTiled is not available");
-  return fn;
-}
+}  // namespace
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len);
+namespace {
 
 // 2-D uint8 tensor map over a [rows][cols] byte matrix with a box of bx x by.
 bool encode_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by, char *why,
@@ -640,6 +624,26 @@ bool encode_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
 
 // ----------------------------------------------------------------------------
 // host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!tried) {
+    tried = true;
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  }
+  if (!fn) snprintf(why, why_len, "mxfp4: cuTensorMapEncodeTiled is not available");
+  return fn;
+}
+
 bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan) {
   if (k < 1 || k > kMaxBlock || E < 1 || E > kMaxExperts) return false;
   if (d % kMxCols || d > kMxMaxD || I % 64 || I > 128 * kMxCh) return false;
