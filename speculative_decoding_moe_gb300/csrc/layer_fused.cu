@@ -24,14 +24,16 @@
 //       reduce across warps in fixed order; h = silu(g) * u is written in
 //       bf16.  The producer then runs ahead into P3's weights.
 //       -- grid barrier 2 (consumers only) --
-//   P3  down: CTA b owns 16-row tiles b, b+G, ... of d; for each it streams
-//       the tile's rows of every woken expert (one contiguous copy each); two
-//       groups of 8 warps take alternate experts, reduce within the group,
-//       and scatter w[t,s] * y into a per-tile slot table in shared memory;
-//       the tile's outputs are summed over the K slots in slot order (+ the
-//       residual) and written once.  No cross-CTA reduction, no atomics on
-//       the output: the result of a token depends only on its own row, so a
-//       block and k single-token calls agree bit for bit.
+//   P3  down: unit = (woken expert, 16 d rows), expert-major and split into
+//       contiguous ranges over the CTAs (so every SM works and a warp reuses
+//       the h fragments of an expert across its tiles); each unit is one
+//       contiguous copy; two groups of 8 warps take alternate units, reduce
+//       within the group and write w[t,s] * y to ys[pair].
+//       -- grid barrier 3 --
+//   P4  every CTA sums ys over the K slots in slot order (+ the residual) for
+//       its share of the outputs.  No atomics on the output: the result of a
+//       token depends only on its own row, so a block and k single-token calls
+//       agree bit for bit.
 // Every wait is bounded (2 s) and reports through the workspace error word.
 #include <cstdio>
 #include <map>
@@ -132,6 +134,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
     hi_g = (int)(((long long)(blockIdx.x + 1) * U) / G);
   }
   const int tiles_d = d / 16;
+  int lo_d, hi_d;  // down units (woken expert, 16 d rows), expert-major, contiguous per CTA
+  {
+    const int U = nW * tiles_d;
+    lo_d = (int)(((long long)blockIdx.x * U) / G);
+    hi_d = (int)(((long long)(blockIdx.x + 1) * U) / G);
+  }
 
   if (!consumer) {
     // ---------------------------------------------------------------- producer
@@ -168,17 +176,16 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
           }
         }
       }
-      for (int tl = blockIdx.x; tl < tiles_d && ok; tl += G) {
-        for (int wi = 0; wi < nW; ++wi, ++it, ps = (ps + 1 == S) ? 0 : ps + 1, pph ^= (ps == 0)) {
-          const int s = ps;
-          if (!mbar_wait_fast(empty0 + 8 * s, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = full0 + 8 * s;
-          mbar_expect_tx(fb, 16u * I * 2);
-          bulk_g2s(slot_addr(s), wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb);
+      for (int u = lo_d; u < hi_d && ok; ++u, ++it, ps = (ps + 1 == S) ? 0 : ps + 1, pph ^= (ps == 0)) {
+        const int s = ps;
+        if (!mbar_wait_fast(empty0 + 8 * s, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+          ok = false;
+          break;
         }
+        const int wi = u / tiles_d, tl = u - wi * tiles_d;
+        const uint32_t fb = full0 + 8 * s;
+        mbar_expect_tx(fb, 16u * I * 2);
+        bulk_g2s(slot_addr(s), wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb);
       }
       // no copy may land after the CTA exits
       volatile int never = 0;
@@ -291,23 +298,23 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
     bar_sync_n(kBarAll, kFC);
     dead = dead || s_abort != 0;
 
-    // ---------------------------------------------------------------- P3: down + combine
+    // ---------------------------------------------------------------- P3: down
     const int grp = warp >> 3, wg = warp & 7;
     const int C = I / 32;
     const int d0 = wg * C / 8, d1 = (wg + 1) * C / 8;
     const int rsd = I * 2;
-    float *ysl = reinterpret_cast<float *>(scratch);  // [k*K][16]
-    float *redg = red + grp * 8 * NT * 32 * 4;         // this group's [8][NT][32][4]
-    int jd = 0;
-    for (int tl = blockIdx.x; tl < tiles_d; tl += G) {
-      const int r0 = tl * 16;
-      for (int wi = 0; wi < nW; ++wi, ++jd, cs = (cs + 1 == S) ? 0 : cs + 1, cph ^= (cs == 0)) {
-        if ((jd & 1) != grp) continue;
-        const int s = cs;
-        const int eoff = s_off[wi], em = s_off[wi + 1] - eoff;
-        // B fragments (h of this expert's tokens, bf16) straight from L2,
-        // issued before the stage wait so the two latencies overlap
-        uint4 bh[3][NT];
+    float *redg = red + grp * 8 * NT * 32 * 4;  // this group's [8][NT][32][4]
+    int jd = 0, cur_d = -1, eoff = 0, em = 0;
+    uint4 bh[3][NT];  // B fragments: h of the current expert's tokens (bf16), reused across its tiles
+    for (int u = lo_d; u < hi_d; ++u, ++jd, cs = (cs + 1 == S) ? 0 : cs + 1, cph ^= (cs == 0)) {
+      if ((jd & 1) != grp) continue;
+      const int s = cs;
+      const int wi = u / tiles_d, r0 = (u - wi * tiles_d) * 16;
+      if (wi != cur_d) {
+        // straight from L2, issued before the stage wait so the latencies overlap
+        cur_d = wi;
+        eoff = s_off[wi];
+        em = s_off[wi + 1] - eoff;
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
 #pragma unroll
@@ -318,69 +325,77 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
               bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hbf + (size_t)(eoff + row) * I + ch * 32 + c * 8));
           }
         }
-        float acc[NT][4];
+      }
+      float acc[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-        if (!dead && !mbar_wait_fast(full0 + 8 * s, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
-        uint4 a0[3], a1[3];
-        if (!dead) {
-          const uint32_t st = slot_addr(s);
+        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+      if (!dead && !mbar_wait_fast(full0 + 8 * s, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+      uint4 a0[3], a1[3];
+      if (!dead) {
+        const uint32_t st = slot_addr(s);
 #pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            if (d0 + j < d1) {
-              const uint32_t q16 = ((d0 + j) * 4 + c) * 16;
-              a0[j] = lds128(st + g * rsd + q16);
-              a1[j] = lds128(st + (g + 8) * rsd + q16);
-            }
+        for (int j = 0; j < 3; ++j) {
+          if (d0 + j < d1) {
+            const uint32_t q16 = ((d0 + j) * 4 + c) * 16;
+            a0[j] = lds128(st + g * rsd + q16);
+            a1[j] = lds128(st + (g + 8) * rsd + q16);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_n(empty0 + 8 * s, 2);  // released before the MMAs
-        if (!dead) {
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(empty0 + 8 * s, 2);  // released before the MMAs
+      if (!dead) {
 #pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            if (d0 + j < d1) {
+        for (int j = 0; j < 3; ++j) {
+          if (d0 + j < d1) {
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt * 8 < em) {
-                  mma_bf16(acc[nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
-                  mma_bf16(acc[nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+              if (nt * 8 < em) {
+                mma_bf16(acc[nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
+                mma_bf16(acc[nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
               }
             }
           }
         }
+      }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
-              make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-        bar_sync_n(kBarGroup + grp, 256);
-        const int gt = tid & 255;
-        if (gt < NT * 128) {
-          const int q4 = gt & 3, ln = (gt >> 2) & 31, nt = gt >> 7;
-          const int tok = nt * 8 + 2 * (ln & 3) + (q4 & 1);
-          if (tok < em) {
-            float y = 0.f;
-            for (int w = 0; w < 8; ++w) y += redg[((w * NT + nt) * 32 + ln) * 4 + q4];
-            const int pair = s_gat[eoff + tok];
-            ysl[pair * 16 + (ln >> 2) + ((q4 & 2) ? 8 : 0)] = s_w[pair] * y;
-          }
-        }
-        bar_sync_n(kBarGroup + grp, 256);
-      }
-      bar_sync_n(kBarAll, kFC);
-      if (!dead) {
-        for (int idx = tid; idx < k * 16; idx += kFC) {
-          const int t = idx >> 4, rr = idx & 15, r = r0 + rr;
-          float sum = 0.f;
-          for (int sl = 0; sl < K; ++sl) sum += ysl[(t * K + sl) * 16 + rr];
-          if (p.residual) sum = load_act(p.residual, (size_t)t * d + r, DFV_BF16) + sum;
-          store_act(p.out, (size_t)t * d + r, DFV_BF16, sum);
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
+            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+      bar_sync_n(kBarGroup + grp, 256);
+      const int gt = tid & 255;
+      if (gt < NT * 128 && !dead) {
+        const int q4 = gt & 3, ln = (gt >> 2) & 31, nt = gt >> 7;
+        const int tok = nt * 8 + 2 * (ln & 3) + (q4 & 1);
+        if (tok < em) {
+          float y = 0.f;
+          for (int w = 0; w < 8; ++w) y += redg[((w * NT + nt) * 32 + ln) * 4 + q4];
+          const int pair = s_gat[eoff + tok];
+          p.ws.ys[(size_t)pair * d + r0 + (ln >> 2) + ((q4 & 2) ? 8 : 0)] = s_w[pair] * y;
         }
       }
-      bar_sync_n(kBarAll, kFC);
+      bar_sync_n(kBarGroup + grp, 256);
+    }
+    // ---- grid barrier 3: every ys row is written
+    bar_sync_n(kBarAll, kFC);
+    if (tid == 0 && !grid_sync(p, 3)) s_abort = 1;
+    bar_sync_n(kBarAll, kFC);
+    dead = dead || s_abort != 0;
+
+    // ---------------------------------------------------------------- P4: combine
+    // out[t] = residual[t] + sum_s ys[t*K+s], slot order, for this CTA's share of the outputs
+    if (!dead) {
+      const int n_out = k * d;
+      const int o0 = (int)(((long long)blockIdx.x * n_out) / G), o1 = (int)(((long long)(blockIdx.x + 1) * n_out) / G);
+      for (int o = o0 + tid; o < o1; o += kFC) {
+        const int t = o / d, r = o - t * d;
+        float sum = 0.f;
+        for (int sl = 0; sl < K; ++sl) sum += __ldcg(p.ws.ys + (size_t)(t * K + sl) * d + r);
+        if (p.residual) sum = load_act(p.residual, (size_t)t * d + r, DFV_BF16) + sum;
+        store_act(p.out, (size_t)t * d + r, DFV_BF16, sum);
+      }
     }
   }
 
