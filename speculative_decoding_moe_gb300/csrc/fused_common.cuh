@@ -80,8 +80,9 @@ struct RouteSmem {
 // P0 + grid barrier 1 + P1, run by the kFW consumer warps of every CTA (named
 // barrier kBarAll over kFC threads).
 //   P0  router GEMV (optionally on RMSNorm(x) rounded to bf16): CTA b computes
-//       the logits of experts b, b+G, ...; warp t takes token t, so a token's
-//       logit depends on nothing but its own row.
+//       the logits of experts b, b+G, ...; each (token, expert) dot product is
+//       one warp's, in a fixed order, so a token's logit depends on nothing but
+//       its own row.
 //   P1  every CTA derives the whole routing decision itself from the logits:
 //       top-K per row (warp per row, redux max/min: largest logit, lowest id
 //       among equals), routing weights, woken union, per-expert pair offsets
@@ -94,13 +95,13 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
   const int k = p.k, d = p.d, E = p.E, K = p.K;
   const int G = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (warp < k) {
-    // lane l takes the 16-byte pieces l, l+32, ... of the row, 8 at a time
-    // with all their loads in flight; the sums run in piece order
-    const int t = warp, cpr = d / 8;
-    const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
-    float inv = 1.f;
-    if (p.fuse_norm) {
+  // lane l takes the 16-byte pieces l, l+32, ... of a row, 8 at a time with
+  // all their loads in flight; the sums run in piece order
+  const int cpr = d / 8;
+  if (p.fuse_norm) {
+    if (warp < k) {
+      const int t = warp;
+      const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
       float ss = 0.f;
       for (int c0 = 0; c0 < cpr; c0 += 256) {
         uint4 xv[8];
@@ -124,10 +125,19 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      inv = 1.0f / sqrtf(ss / (float)d + p.eps);
-      if (lane == 0) r.inv[t] = inv;
+      if (lane == 0) r.inv[t] = 1.0f / sqrtf(ss / (float)d + p.eps);
     }
-    for (int e = blockIdx.x; e < E; e += G) {
+    bar_sync_n(kBarAll, kFC);
+  }
+  // the (token, expert) dot products of this CTA's experts b, b+G, ... spread
+  // over all warps: pair q = slot * k + t on warp q mod 16 (each dot product is
+  // computed the same way whichever warp takes it)
+  {
+    const int n_e = blockIdx.x < E ? (E - 1 - blockIdx.x) / G + 1 : 0;
+    for (int q = warp; q < n_e * k; q += kFW) {
+      const int t = q % k, e = blockIdx.x + (q / k) * G;
+      const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
+      const float inv = p.fuse_norm ? r.inv[t] : 1.f;
       const uint16_t *wr = reinterpret_cast<const uint16_t *>(p.wr) + (size_t)e * d;
       float acc = 0.f;
       for (int c0 = 0; c0 < cpr; c0 += 256) {

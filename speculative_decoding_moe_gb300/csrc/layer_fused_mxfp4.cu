@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
       if (warp < k) {
         const int t = warp, cpr = d / 8;
         const uint16_t *src = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
-        __syncwarp();  // s_inv[t] was written by this warp's lane 0
+        __syncwarp();
         const float inv = p.fuse_norm ? s_inv[t] : 1.f;
         uint4 v[8];
         float amax = 0.f;
