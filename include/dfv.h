@@ -239,6 +239,21 @@ int dfv_set_path(int path);
  * multi-kernel, -1 none yet. */
 int dfv_last_layer_path(void);
 
+/*
+ * How the single-launch bf16 kernel fetches its gate/up stages, for later
+ * layer calls from this host thread (no counterpart on the method's pages):
+ * the highest mode allowed, 2 (default) one 3-D tensor-map copy per weight
+ * matrix and stage, 1 one 2-D tensor-map copy per 256 columns, 0 one 1-D bulk
+ * copy per weight row.  A mode the driver or the shape does not allow falls
+ * back to the next lower one.  All modes compute the same result bit for bit.
+ * Returns DFV_ERR_INVALID_ARG for a mode outside 0..2.
+ */
+int dfv_set_staging(int max_mode);
+
+/* Staging mode the last single-launch bf16 layer call from this host thread
+ * used (see dfv_set_staging), -1 none yet. */
+int dfv_last_staging(void);
+
 /* Why the fused path could not be set up on this device (empty if it could,
  * or if it was never tried). */
 const char *dfv_fused_unavailable_reason(void);

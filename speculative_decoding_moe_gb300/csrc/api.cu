@@ -17,6 +17,8 @@ thread_local cudaEvent_t g_events[4];
 thread_local bool g_profile = false;
 thread_local int g_last_path = -1;
 std::string g_fused_why;  // why the fused path is unavailable (first failure)
+thread_local int g_max_staging = 2;   // highest gate/up staging mode of the bf16 fused kernel
+thread_local int g_last_staging = -1;
 
 inline void mark(int i, cudaStream_t s) {
   if (g_profile) cudaEventRecord(g_events[i], s);
@@ -216,7 +218,10 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
   fp.ws = w;
   fp.u_idx = u_idx;
   fp.u_nw = u_nw;
-  if (!mx) dfv::fused_tensor_maps(&fp, L, plan);
+  if (!mx) {
+    dfv::fused_tensor_maps(&fp, L, plan, g_max_staging);
+    g_last_staging = fp.tma_mode;
+  }
   auto go = [&](bool pdl) {
     return mx ? dfv::launch_fused_mx(fp, plan, grid, s, pdl) : dfv::launch_fused(fp, plan, grid, s, pdl);
   };
@@ -443,6 +448,14 @@ int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, in
 int dfv_last_layer_path(void) { return g_last_path; }
 
 const char *dfv_fused_unavailable_reason(void) { return g_fused_why.c_str(); }
+
+int dfv_set_staging(int max_mode) {
+  if (max_mode < 0 || max_mode > 2) return fail(DFV_ERR_INVALID_ARG, "staging mode must be 0, 1 or 2");
+  g_max_staging = max_mode;
+  return DFV_OK;
+}
+
+int dfv_last_staging(void) { return g_last_staging; }
 
 int dfv_set_path(int path) {
   if (path != 0 && path != 1) return fail(DFV_ERR_INVALID_ARG, "path must be 0 (multi-kernel) or 1 (fused)");

@@ -282,8 +282,8 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
 bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
 int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
 cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
-// fills p->tm_wg / tm_wu and p->tma_mode for a bf16 layer (mode 0 when no tensor map fits)
-void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan);
+// fills p->tm_wg / tm_wu and p->tma_mode (<= max_mode) for a bf16 layer (mode 0 when no tensor map fits)
+void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode);
 // single-launch layer with mxfp4 experts (layer_fused_mxfp4.cu)
 bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan);
 // fills p->tm_* for an mxfp4 layer; false (with a reason) when the driver refuses

@@ -451,7 +451,7 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len);
 
-void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan) {
+void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode) {
   // the gate/up stage of 8 rows x ks columns as one 3-D box ([ks/256][8][256]),
   // else as ks/256 2-D boxes of 8 x 256; cached per (weights, shape)
   struct Maps {
@@ -459,11 +459,11 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
     CUtensorMap wg, wu;
   };
   static std::mutex mu;
-  static std::map<std::tuple<const void *, const void *, int, int, int, int>, Maps> cache;
+  static std::map<std::tuple<const void *, const void *, int, int, int, int, int>, Maps> cache;
   p->tma_mode = 0;
   const int d = L->d, I = L->d_ff, E = L->n_experts, ks = plan.ks;
-  if (d % 256 || ks % 256) return;
-  const auto key = std::make_tuple(L->w_gate, L->w_up, d, I, E, ks);
+  if (d % 256 || ks % 256 || max_mode <= 0) return;
+  const auto key = std::make_tuple(L->w_gate, L->w_up, d, I, E, ks, max_mode);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -497,7 +497,7 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    if (enc3(&m.wg, L->w_gate) && enc3(&m.wu, L->w_up))
+    if (max_mode >= 2 && enc3(&m.wg, L->w_gate) && enc3(&m.wu, L->w_up))
       m.mode = 2;
     else if (enc2(&m.wg, L->w_gate) && enc2(&m.wu, L->w_up))
       m.mode = 1;

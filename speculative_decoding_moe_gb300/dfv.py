@@ -21,7 +21,7 @@ DEVERR_SCALE_RANGE, DEVERR_REDUCE_WAIT = 0x10, 0x20
 _NAMES = {"f32": F32, "bf16": BF16, "mxfp4": MXFP4}
 EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_profile_set_events",
            "dfv_read_device_error", "dfv_set_path", "dfv_last_layer_path", "dfv_fused_unavailable_reason",
-           "dfv_accept_greedy_noalloc",
+           "dfv_accept_greedy_noalloc", "dfv_set_staging", "dfv_last_staging",
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
            "dfv_accept_workspace_size", "dfv_accept_greedy")
@@ -73,6 +73,10 @@ def _load():
         L.dfv_accept_greedy_noalloc.argtypes = [P, I, I, I, P, P, P, P]
         L.dfv_read_device_error.argtypes = [P, P, P]
         L.dfv_set_path.argtypes = [I]
+        L.dfv_set_staging.restype = I
+        L.dfv_set_staging.argtypes = [I]
+        L.dfv_last_staging.restype = I
+        L.dfv_last_staging.argtypes = []
         L.dfv_last_layer_path.restype = I
         L.dfv_fused_unavailable_reason.restype = ctypes.c_char_p
         _lib = L
@@ -219,6 +223,15 @@ def read_device_error(ws: torch.Tensor, stream=None) -> int:
     _check(_load().dfv_read_device_error(_p(ws), ctypes.byref(out), _stream(stream)), "dfv_read_device_error")
     (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return int(out.value)
+
+
+def set_staging(max_mode: int):
+    """Highest gate/up staging mode of the single-launch bf16 kernel (2, 1 or 0)."""
+    _check(_load().dfv_set_staging(int(max_mode)), "dfv_set_staging")
+
+
+def last_staging() -> int:
+    return int(_load().dfv_last_staging())
 
 
 def set_path(fused: bool):

@@ -120,3 +120,11 @@ def test_device_error_bits_match_the_header(lib):
                     "REDUCE_WAIT": 32}
     for name, v in bits.items():
         assert getattr(lib, "DEVERR_" + name) == v
+
+
+def test_staging_mode_is_validated(lib):
+    L = lib.lib()
+    assert L.dfv_set_staging(3) == 1
+    assert L.dfv_set_staging(-1) == 1
+    assert L.dfv_set_staging(2) == 0
+    assert L.dfv_last_staging() == -1
