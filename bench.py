@@ -47,8 +47,8 @@ KERNEL_SOURCES = {
     "moe_fused_mx_kernel": ["layer_fused_mxfp4.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
 }
 NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
-    "moe_fused_kernel": ("e6b5c0814dfea91e", 728468480 + 7187200, 77 * 9437184 + 524288),
-    "moe_fused_mx_kernel": ("ff79adaa8bd5838e", 171767808 + 6757376, 102 * 1671168 + 1048576),
+    "moe_fused_kernel": ("14732f832f4f389d", 728461312 + 7497984, 77 * 9437184 + 524288),
+    "moe_fused_mx_kernel": ("2f3341c20c1ad0f0", 171747328 + 6129664, 102 * 1671168 + 1048576),
 }
 
 

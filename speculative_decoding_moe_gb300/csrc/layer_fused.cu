@@ -18,8 +18,9 @@
 //       among equals), routing weights, woken union, per-expert pair offsets
 //       (block scan) and the (expert, token)-sorted pair list.
 //   P2  gate/up: unit = (woken expert, 8 d_ff rows).  The producer streams
-//       stages of 8 gate + 8 up rows x `ks` columns (1-D bulk copies into an
-//       mbarrier ring); the 16 consumer warps split the columns, run
+//       stages of 8 gate + 8 up rows x `ks` columns into an mbarrier ring (one
+//       3-D tensor-map box per matrix, else 2-D boxes of 256 columns, else one
+//       bulk copy per row); the 16 consumer warps split the columns, run
 //       m16n8k16 MMAs (gate rows = M 0-7, up rows = M 8-15, tokens = N) and
 //       reduce across warps in fixed order; h = silu(g) * u is written in
 //       bf16.  The producer then runs ahead into P3's weights.

@@ -26,14 +26,17 @@
 //       codes (cvt e2m1x2 -> fp16x2, times the block scale), runs m16n8k16 fp16
 //       MMAs (gate rows = M 0-7, up rows = M 8-15, the expert's tokens = N) and
 //       keeps the sums in its registers across the stages; h = silu(g) * u goes
-//       to global memory in fp32.
-//       -- grid barrier 2 (consumers only; the producer runs ahead into P3) --
+//       to global memory in fp32.  When all its gate/up units are done, the CTA
+//       sets its own flag in the workspace with one release.  No grid barrier
+//       follows: the producer runs straight on into P3's weights.
 //   P3  unit = (woken expert, 64 d rows); its stage holds the 64 rows of down
-//       codes and scales.  Each warp owns 16 rows over the whole d_ff; the B
-//       operand is the expert's h rows, staged per expert in the group's
-//       shared buffer as fp16 with their own power-of-two scales.
-//       w[t,s] * y goes to ys[pair].
-//       -- grid barrier 3 --
+//       codes and scales.  Before it first reads an expert's h, a group waits
+//       (acquire, bounded) for the flags of the CTAs that own that expert's
+//       gate/up units, polled by a whole warp at once.  Each warp owns 16 rows
+//       over the whole d_ff; the B operand is the expert's h rows, staged per
+//       expert in the group's shared buffer as fp16 with their own
+//       power-of-two scales.  w[t,s] * y goes to ys[pair].
+//       -- grid barrier 2 --
 //   P4  every CTA sums ys over the K slots in slot order for its share of the
 //       output rows, adds the residual and writes them.  The sum order of
 //       every output depends only on its own token, never on the block.
