@@ -219,6 +219,11 @@ def workload_config():
 # ---------------------------------------------------------------------------- GPU arm
 
 
+def progress(msg: str):
+    """One line on stderr per bench section (stdout carries only the JSON line)."""
+    print("[bench] %s" % msg, file=sys.stderr, flush=True)
+
+
 def graph_time(fn, warmup: int, steps: int, barrier=None, sampler=None):
     """Capture one step into a CUDA graph, replay `warmup` untimed then `steps`
     timed replays bracketed by CUDA events; returns ms per step."""
@@ -314,6 +319,7 @@ def run_gpu(args):
         return float(W.sum().item() * exp_bytes + N_LAYERS * router_bytes), W
 
     # ---- headline: k=16 verify pass over 40 layers (CUDA graph replay)
+    progress("headline k=16")
     fn16, nw16 = make_pass(KBLOCK)
     sampler = ClockSampler(local)
     ms16 = graph_time(fn16, args.warmup, args.steps, barrier, sampler)
@@ -328,11 +334,13 @@ def run_gpu(args):
     value = world * bytes16 / (ms_max * 1e-3) / 1e9
 
     # ---- decode: k=1 pass, same layers
+    progress("decode k=1")
     fn1, nw1 = make_pass(1, seed=6)
     ms1 = graph_time(fn1, args.warmup, args.steps, barrier)
     bytes1, W1 = pass_bytes(nw1)
 
     # ---- stream-launch numbers (no graph) for context
+    progress("stream launches")
     ms16_stream = stream_time(fn16, 2, max(3, args.steps // 4))
     ms1_stream = stream_time(fn1, 2, max(3, args.steps // 4))
 
@@ -389,6 +397,7 @@ def run_gpu(args):
         for mode in ("repeated", "independent"):
             rows = []
             for k in range(1, 17):
+                progress("sweep %s k=%d" % (mode, k))
                 fnk, nwk = make_pass(k, mode=mode, seed=50 + k)
                 msk = graph_time(fnk, 2, max(3, args.steps // 4))
                 bk, Wk = pass_bytes(nwk)
@@ -397,6 +406,7 @@ def run_gpu(args):
             sweep[mode] = rows
 
     # ---- 40-layer pre-norm residual stack + greedy acceptance (one verify cycle)
+    progress("stack")
     stack = None
     if not args.no_stack:
         V = 151936
@@ -420,6 +430,7 @@ def run_gpu(args):
                  "tau_expected": nacc + 1, "finite": bool(torch.isfinite(xs.float()).all().item())}
 
     # ---- end to end through the host-buffer entry point (plain stream launches)
+    progress("end to end")
     hx = x16.cpu().pin_memory()
     ho = torch.empty_like(hx).pin_memory()
 
@@ -474,6 +485,7 @@ def run_gpu(args):
 def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
     """mxfp4 experts: E=256, top-8, d=2048, d_ff=512, 40 layers, bf16 activations.
     Bytes per woken expert count the packed codes and the scale bytes."""
+    progress("mxfp4 section")
     shape = inputs.MXFP4
     layers = [inputs.make_layer(shape, seed=5000 + 1000 * rank + l, device=dev) for l in range(N_LAYERS)]
     Ls = [dfv.Layer(w) for w in layers]

@@ -84,6 +84,10 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2 } dfv_dtype;
  * kernels finish normally; the outputs of that call are invalid. */
 #define DFV_DEVERR_SCALE_RANGE 0x10u
 #define DFV_DEVERR_REDUCE_WAIT 0x20u /* a warp gave up waiting for a free partial-sum buffer */
+/* A single-launch kernel found its own routing tables inconsistent (an expert
+ * id, offset or pair index out of range, or a pair filed under the wrong
+ * expert) and skipped the layer's expert work rather than index with them. */
+#define DFV_DEVERR_ROUTING 0x40u
 
 /* Limits of this implementation. */
 #define DFV_MAX_BLOCK 16      /* k: positions in one verify block          */

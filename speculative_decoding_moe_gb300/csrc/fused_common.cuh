@@ -75,6 +75,7 @@ struct RouteSmem {
   int *wsum, *csum;  // [kFW] scan scratch
   int *nw;         // woken count
   volatile int *abort;
+  volatile int *bad;  // set when the tables fail their check (zeroed by the caller)
 };
 
 // P0 + grid barrier 1 + P1, run by the kFW consumer warps of every CTA (named
@@ -273,6 +274,33 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     r.gat[r.eoff[ex] + rank] = q;
   }
   bar_sync_n(kBarAll, kFC);
+  // every index the later phases take from these tables is checked once here:
+  // woken ids ascending and < E, offsets rising by 1..k and ending at k*K,
+  // and every sorted pair id < k*K, filed under the expert it chose
+  {
+    const int nW = *r.nw;
+    bool bad = tid == 0 && (nW < 1 || nW > E || nW > k * K || r.off[0] != 0 || r.off[nW] != k * K);
+    if (!bad && tid < nW && nW <= E) {
+      const int e = r.woken[tid], m = r.off[tid + 1] - r.off[tid];
+      bad = e < 0 || e >= E || (tid > 0 && e <= r.woken[tid - 1]) || m < 1 || m > k;
+    }
+    if (!bad && tid < k * K && nW >= 1 && nW <= E) {
+      const int q = r.gat[tid];
+      // the expert whose pair range holds position tid
+      int lo = 0, hi = nW - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (r.off[mid] <= tid) lo = mid; else hi = mid - 1;
+      }
+      bad = q < 0 || q >= k * K || r.idx[q] != r.woken[lo];
+    }
+    if (bad) *r.bad = 1;
+  }
+  bar_sync_n(kBarAll, kFC);
+  if (*r.bad) {
+    if (tid == 0) atomicOr(p.ws.err, DFV_DEVERR_ROUTING);
+    *r.abort = 1;
+  }
   if (blockIdx.x == 0) {
     const int nW = *r.nw;
     for (int q = tid; q < k * K; q += kFC) {

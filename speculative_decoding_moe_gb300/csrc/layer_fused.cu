@@ -62,8 +62,7 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int
 
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant__ FusedParams p) {
-  pdl_trigger();
-  pdl_wait();
+  pdl_wait();  // a no-op: cooperative launches are not chained programmatically
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, E = p.E, K = p.K, ks = p.ks, nsl = p.nsl;
   const int G = gridDim.x;
@@ -93,11 +92,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_tok[16];
   __shared__ int s_nw, s_ring;
-  __shared__ volatile int s_abort;
+  __shared__ volatile int s_abort, s_bad;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_abort = 0;
+    s_bad = 0;
     for (int s = 0; s <= SH; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kFW);
@@ -109,19 +109,19 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   const bool consumer = warp < kFW;
   // ------------------------------------------------------------------ P0, P1: routing
   if (consumer) {
-    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort};
+    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort, &s_bad};
     fused_route(p, rs, [] {});
     if (tid == 0) {
       // with at most 8 tokens per expert the staged-x rows 8..15 are unused:
       // they become one more ring stage
       int mmax = 0;
-      for (int i = 0; i < s_nw; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
+      for (int i = 0; !s_abort && i < s_nw; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
       s_ring = (NT == 2 && mmax <= 8 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing) ? SH + 1 : SH;
     }
   }
   __syncthreads();  // routing tables visible to the producer
 
-  const int nW = s_nw;
+  const int nW = s_abort ? 0 : s_nw;  // an aborted CTA takes no units
   const int S = s_ring;
   // stage s lives in the reserved ring, or (s == SH) in staged-x rows 8..15
   auto slot_addr = [&](int st) -> uint32_t {
@@ -148,16 +148,22 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       const uint16_t *wg = reinterpret_cast<const uint16_t *>(p.wg);
       const uint16_t *wu = reinterpret_cast<const uint16_t *>(p.wu);
       const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
-      int it = 0, ps = 0, pph = 0;  // fills issued; slot and phase of the next fill
+      // Stage phases are tracked per stage (bit s of pbits: parity of the next
+      // fill's phase on stage s), because gate/up fills go round the whole
+      // ring while down fills go round the stages of their consumer group.
+      int ps = 0;
+      uint32_t pbits = 0, used = 0;
       bool ok = true;
       for (int u = lo_g; u < hi_g && ok; ++u) {
         const int e = s_woken[u / tiles_g], i0 = (u % tiles_g) * kGateTile;
-        for (int sl = 0; sl < nsl; ++sl, ++it, ps = (ps + 1 == S) ? 0 : ps + 1, pph ^= (ps == 0)) {
+        for (int sl = 0; sl < nsl; ++sl, ps = (ps + 1 == S) ? 0 : ps + 1) {
           const int s = ps;
-          if (!mbar_wait_fast(empty0 + 8 * s, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+          if (!mbar_wait_fast(empty0 + 8 * s, ((pbits >> s) & 1u) ^ 1u, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
             ok = false;
             break;
           }
+          pbits ^= 1u << s;
+          used |= 1u << s;
           const uint32_t fb = full0 + 8 * s, dst = slot_addr(s);
           mbar_expect_tx(fb, 16u * ks * 2);
           if (p.tma_mode == 2) {  // [ks/256][8 rows][256]: one box per matrix
@@ -177,21 +183,31 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
           }
         }
       }
-      for (int u = lo_d; u < hi_d && ok; ++u, ++it, ps = (ps + 1 == S) ? 0 : ps + 1, pph ^= (ps == 0)) {
-        const int s = ps;
-        if (!mbar_wait_fast(empty0 + 8 * s, pph ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+      // down unit j (counted from lo_d) belongs to consumer group j & 1, which
+      // owns the stages of that parity: every wait on a stage then comes from
+      // warps that consumed the stage's previous fill, so a parity wait can
+      // never be mistaken for the phase before it
+      int pg[2] = {0, 1};
+      for (int u = lo_d, j = 0; u < hi_d && ok; ++u, ++j) {
+        const int gq = j & 1, s = pg[gq];
+        pg[gq] = (s + 2 < S) ? s + 2 : gq;
+        if (!mbar_wait_fast(empty0 + 8 * s, ((pbits >> s) & 1u) ^ 1u, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
           ok = false;
           break;
         }
+        pbits ^= 1u << s;
+        used |= 1u << s;
         const int wi = u / tiles_d, tl = u - wi * tiles_d;
         const uint32_t fb = full0 + 8 * s;
         mbar_expect_tx(fb, 16u * I * 2);
         bulk_g2s(slot_addr(s), wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb);
       }
-      // no copy may land after the CTA exits
+      // no copy may land after the CTA exits: wait for the last fill of every stage
       volatile int never = 0;
-      for (int j = it - S < 0 ? 0 : it - S; j < it; ++j)
-        if (!mbar_wait(full0 + 8 * (j % S), (j / S) & 1, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never)) break;
+      for (int s = 0; s < S; ++s)
+        if (((used >> s) & 1u) &&
+            !mbar_wait(full0 + 8 * s, ((pbits >> s) & 1u) ^ 1u, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never))
+          break;
     }
   } else {
     // ---------------------------------------------------------------- P2: gate/up
@@ -202,7 +218,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
     const int cpr = d / 8;
     uint16_t *hbf = reinterpret_cast<uint16_t *>(p.ws.h);  // h rounded to bf16, [k*K][d_ff]
     const uint32_t xs = sbase + SH * slot;
-    int cur = -1, m = 0, off = 0, cs = 0, cph = 0;  // slot and phase of the next stage
+    int cur = -1, m = 0, off = 0, cs = 0;  // cs: stage of the next gate/up fill
+    uint32_t cbits = 0;                     // bit s: parity of the next phase of stage s
     bool dead = s_abort != 0;
     for (int u = lo_g; u < hi_g; ++u) {
       const int wi = u / tiles_g, i0 = (u % tiles_g) * kGateTile;
@@ -235,9 +252,11 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-      for (int sl = 0; sl < nsl; ++sl, cs = (cs + 1 == S) ? 0 : cs + 1, cph ^= (cs == 0)) {
+      for (int sl = 0; sl < nsl; ++sl, cs = (cs + 1 == S) ? 0 : cs + 1) {
         const int s = cs;
-        if (!dead && !mbar_wait_fast(full0 + 8 * s, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+        if (!dead && !mbar_wait_fast(full0 + 8 * s, (cbits >> s) & 1u, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort))
+          dead = true;
+        cbits ^= 1u << s;
         // A fragments go to registers first and the slot is released at once,
         // so the producer refills it while the MMAs run
         uint4 ag[kMaxChunksP2], au[kMaxChunksP2];
@@ -306,10 +325,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
     const int rsd = I * 2;
     float *redg = red + grp * 8 * NT * 32 * 4;  // this group's [8][NT][32][4]
     int jd = 0, cur_d = -1, eoff = 0, em = 0;
+    int gs = grp;  // this group's next stage (the group owns the stages of its parity)
     uint4 bh[3][NT];  // B fragments: h of the current expert's tokens (bf16), reused across its tiles
-    for (int u = lo_d; u < hi_d; ++u, ++jd, cs = (cs + 1 == S) ? 0 : cs + 1, cph ^= (cs == 0)) {
+    for (int u = lo_d; u < hi_d; ++u, ++jd) {
       if ((jd & 1) != grp) continue;
-      const int s = cs;
+      const int s = gs;
+      gs = (gs + 2 < S) ? gs + 2 : grp;
       const int wi = u / tiles_d, r0 = (u - wi * tiles_d) * 16;
       if (wi != cur_d) {
         // straight from L2, issued before the stage wait so the latencies overlap
@@ -332,7 +353,9 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-      if (!dead && !mbar_wait_fast(full0 + 8 * s, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+      if (!dead && !mbar_wait_fast(full0 + 8 * s, (cbits >> s) & 1u, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort))
+        dead = true;
+      cbits ^= 1u << s;
       uint4 a0[3], a1[3];
       if (!dead) {
         const uint32_t st = slot_addr(s);
@@ -511,7 +534,9 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
   p->tm_wu = m.wu;
 }
 
-cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
+// A plain cooperative launch: no programmatic chaining with the kernels
+// around it, so the whole grid is resident on an otherwise idle device.
+cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s) {
   FusedParams p = p0;
   p.ks = plan.ks;
   p.nsl = plan.nsl;
@@ -526,13 +551,11 @@ cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid,
   cfg.blockDim = dim3(kFT);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

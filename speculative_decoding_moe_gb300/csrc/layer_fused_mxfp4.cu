@@ -100,8 +100,7 @@ static __device__ __noinline__ bool ctas_done(const unsigned *flags, int b0, int
 
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_constant__ FusedParams p) {
-  pdl_trigger();
-  pdl_wait();
+  pdl_wait();  // a no-op: cooperative launches are not chained programmatically
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, K = p.K;
   const int G = gridDim.x;
@@ -129,11 +128,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_nw;
   __shared__ unsigned s_last_cta;
-  __shared__ volatile int s_abort;
+  __shared__ volatile int s_abort, s_bad;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_abort = 0;
+    s_bad = 0;
     for (int s = 0; s < kMxRing; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kMxGW);
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
 
   const bool consumer = warp < kFW;
   if (consumer) {
-    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort};
+    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort, &s_bad};
     // the k rows of x are staged in fp16 (warp t: row t) while the other CTAs
     // finish their router logits
     fused_route(p, rs, [&] {
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   }
   __syncthreads();  // routing tables visible to the producer
 
-  const int nW = s_nw;
+  const int nW = s_abort ? 0 : s_nw;  // an aborted CTA takes no units
   const int tiles_g = I / kMxRows, tiles_d = d / 64, nq = d / kMxCols;
   int lo_g, hi_g, lo_d, hi_d;
   {
@@ -699,7 +699,9 @@ bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, siz
   return true;
 }
 
-cudaError_t launch_fused_mx(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
+// A plain cooperative launch: no programmatic chaining with the kernels
+// around it, so the whole grid is resident on an otherwise idle device.
+cudaError_t launch_fused_mx(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s) {
   FusedParams p = p0;
   p.slot = plan.slot;
   p.scratch = plan.scratch;
@@ -712,13 +714,11 @@ cudaError_t launch_fused_mx(const FusedParams &p0, const FusedPlan &plan, int gr
   cfg.blockDim = dim3(kFT);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -117,7 +117,7 @@ def test_device_error_bits_match_the_header(lib):
     src = open(os.path.join(ROOT, "include", "dfv.h")).read()
     bits = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define DFV_DEVERR_([A-Z_]+) (0x[0-9a-fA-F]+)u", src)}
     assert bits == {"STAGE_WAIT": 1, "SLOT_WAIT": 2, "DRAIN_WAIT": 4, "GRID_WAIT": 8, "SCALE_RANGE": 16,
-                    "REDUCE_WAIT": 32}
+                    "REDUCE_WAIT": 32, "ROUTING": 64}
     for name, v in bits.items():
         assert getattr(lib, "DEVERR_" + name) == v
 
