@@ -222,8 +222,15 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
     dfv::fused_tensor_maps(&fp, L, plan, g_max_staging);
     g_last_staging = fp.tma_mode;
   }
+  auto go = [&](bool pdl) {
+    return mx ? dfv::launch_fused_mx(fp, plan, grid, s, pdl) : dfv::launch_fused(fp, plan, grid, s, pdl);
+  };
   mark(0, s);
-  const cudaError_t e = mx ? dfv::launch_fused_mx(fp, plan, grid, s) : dfv::launch_fused(fp, plan, grid, s);
+  cudaError_t e = go(true);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear, and retry without programmatic serialisation
+    e = go(false);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "fused layer launch");
   mark(1, s);
   mark(2, s);

@@ -281,7 +281,7 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
 // Fused single-launch layer (bf16): plan, grid (0 = cannot run) and launch.
 bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
 int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
-cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s);
+cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 // fills p->tm_wg / tm_wu and p->tma_mode (<= max_mode) for a bf16 layer (mode 0 when no tensor map fits)
 void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode);
 // single-launch layer with mxfp4 experts (layer_fused_mxfp4.cu)
@@ -289,7 +289,7 @@ bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan);
 // fills p->tm_* for an mxfp4 layer; false (with a reason) when the driver refuses
 bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, size_t why_len);
 int fused_mx_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
-cudaError_t launch_fused_mx(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s);
+cudaError_t launch_fused_mx(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);

@@ -62,7 +62,8 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int
 
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant__ FusedParams p) {
-  pdl_wait();  // a no-op: cooperative launches are not chained programmatically
+  pdl_trigger();
+  pdl_wait();  // nothing before this reads or writes global memory
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, E = p.E, K = p.K, ks = p.ks, nsl = p.nsl;
   const int G = gridDim.x;
@@ -183,10 +184,10 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
           }
         }
       }
-      // down unit j (counted from lo_d) belongs to consumer group j & 1, which
-      // owns the stages of that parity: every wait on a stage then comes from
-      // warps that consumed the stage's previous fill, so a parity wait can
-      // never be mistaken for the phase before it
+      // down unit lo_d + j belongs to consumer group j & 1, which owns the
+      // stages of that parity: every wait on a stage then comes from warps
+      // that consumed the stage's previous fill, so a parity wait can never be
+      // taken for the phase before it
       int pg[2] = {0, 1};
       for (int u = lo_d, j = 0; u < hi_d && ok; ++u, ++j) {
         const int gq = j & 1, s = pg[gq];
@@ -534,9 +535,10 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
   p->tm_wu = m.wu;
 }
 
-// A plain cooperative launch: no programmatic chaining with the kernels
-// around it, so the whole grid is resident on an otherwise idle device.
-cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s) {
+// A cooperative launch (the grid barriers need every CTA resident), chained
+// to the previous kernel programmatically when `pdl`: CTAs may start while it
+// drains, and do nothing before griddepcontrol.wait.
+cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
   FusedParams p = p0;
   p.ks = plan.ks;
   p.nsl = plan.nsl;
@@ -551,11 +553,13 @@ cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid,
   cfg.blockDim = dim3(kFT);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

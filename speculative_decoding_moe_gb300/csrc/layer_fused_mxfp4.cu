@@ -100,7 +100,8 @@ static __device__ __noinline__ bool ctas_done(const unsigned *flags, int b0, int
 
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_constant__ FusedParams p) {
-  pdl_wait();  // a no-op: cooperative launches are not chained programmatically
+  pdl_trigger();
+  pdl_wait();  // nothing before this reads or writes global memory
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, K = p.K;
   const int G = gridDim.x;
@@ -699,9 +700,10 @@ bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, siz
   return true;
 }
 
-// A plain cooperative launch: no programmatic chaining with the kernels
-// around it, so the whole grid is resident on an otherwise idle device.
-cudaError_t launch_fused_mx(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s) {
+// A cooperative launch (the grid barriers need every CTA resident), chained
+// to the previous kernel programmatically when `pdl`: CTAs may start while it
+// drains, and do nothing before griddepcontrol.wait.
+cudaError_t launch_fused_mx(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
   FusedParams p = p0;
   p.slot = plan.slot;
   p.scratch = plan.scratch;
@@ -714,11 +716,13 @@ cudaError_t launch_fused_mx(const FusedParams &p0, const FusedPlan &plan, int gr
   cfg.blockDim = dim3(kFT);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
