@@ -47,8 +47,8 @@ KERNEL_SOURCES = {
     "moe_fused_mx_kernel": ["layer_fused_mxfp4.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
 }
 NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
-    "moe_fused_kernel": ("14732f832f4f389d", 728461312 + 7497984, 77 * 9437184 + 524288),
-    "moe_fused_mx_kernel": ("2f3341c20c1ad0f0", 171747328 + 6129664, 102 * 1671168 + 1048576),
+    "moe_fused_kernel": ("4da63dfb6994f569", 728447744 + 7643904, 77 * 9437184 + 524288),
+    "moe_fused_mx_kernel": ("21738ae36ae2f646", 172091648 + 6834688, 102 * 1671168 + 1048576),
 }
 
 
