@@ -317,3 +317,57 @@ def test_fused_staging_modes_agree(dfv, a3b, mode):
     assert dfv.read_device_error(ws) == 0
     ref = oracle.moe_forward(ol, np_of(x), nthreads=oracle.num_threads_available())
     assert _max_rel_err(_gpu_out_np(outs[mode]), ref) <= TOL_BF16
+
+
+@pytest.fixture(scope="module")
+def a3b_chain(dfv):
+    """Six A3B-shape layers with distinct weights (7 GB, far larger than L2)."""
+    lws = [inputs.make_layer(inputs.A3B, seed=900 + l, device="cuda") for l in range(6)]
+    return lws, [dfv.Layer(w) for w in lws]
+
+
+@pytest.mark.parametrize("k,mode", [(1, "independent"), (3, "repeated"), (8, "repeated"),
+                                    (12, "independent"), (13, "repeated"), (16, "independent")])
+def test_chained_launches_equal_isolated_launches(dfv, a3b_chain, k, mode):
+    """Layer launches chained back to back must give, bit for bit, what the same
+    launches give one at a time with a device synchronisation in between.
+    Every output depends only on its own row and each launch's layer.  So any
+    difference means a launch read data it should not have: a stage before its
+    copy landed, a stage that was being refilled, or another launch's workspace.
+    Covers eager chains and CUDA-graph replays, for ring sizes of both
+    parities (k <= 8 and k > 8)."""
+    _, Ls = a3b_chain
+    ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], 16))
+    x = inputs.make_hidden(k, 2048, "bf16", seed=4000 + k, mode=mode, device="cuda")
+    iso = []
+    for L in Ls:
+        o = dfv.moe_block_forward(L, x, ws)
+        torch.cuda.synchronize()
+        iso.append(o.clone())
+    assert dfv.last_layer_path() == 1, dfv.fused_unavailable_reason()
+    outs = [torch.empty_like(x) for _ in Ls]
+
+    def chain():
+        for L, o in zip(Ls, outs):
+            dfv.moe_block_forward(L, x, ws, out=o)
+
+    for _ in range(40):
+        chain()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(outs, iso))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for _ in range(40):
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(outs, iso))
+    assert dfv.read_device_error(ws) == 0
