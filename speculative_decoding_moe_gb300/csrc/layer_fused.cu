@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       // with at most 8 tokens per expert the staged-x rows 8..15 are unused:
       // they become one more ring stage
       int mmax = 0;
-      for (int i = 0; !s_abort && i < s_nw; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
+      const int nw0 = s_abort ? 0 : s_nw;  // one read of the volatile flag, not one per expert
+      for (int i = 0; i < nw0; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
       s_ring = (NT == 2 && mmax <= 8 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing) ? SH + 1 : SH;
     }
   }
