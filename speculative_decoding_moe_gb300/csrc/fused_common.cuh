@@ -55,6 +55,15 @@ __device__ bool grid_sync(const FusedParams &p, unsigned nb) {
   return true;
 }
 
+// The router rows of this CTA's experts b, b+G, ... start towards L2.  They are
+// weights no kernel writes, so this may run before griddepcontrol.wait, while
+// the previous launch drains; nothing else does.
+__device__ __forceinline__ void prefetch_router_rows(const FusedParams &p) {
+  const int e = blockIdx.x + (int)threadIdx.x * gridDim.x;
+  if (threadIdx.x < 8 && e < p.E)
+    prefetch_l2(reinterpret_cast<const char *>(p.wr) + (size_t)e * p.d * 2, (uint32_t)p.d * 2);
+}
+
 __device__ __forceinline__ void load8_bf16(const void *base, size_t elem, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(base) + elem);
   f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);

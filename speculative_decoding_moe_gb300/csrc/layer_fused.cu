@@ -63,7 +63,8 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant__ FusedParams p) {
   pdl_trigger();
-  pdl_wait();  // nothing before this reads or writes global memory
+  prefetch_router_rows(p);
+  pdl_wait();  // before this only the router-row prefetch touches global memory
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, E = p.E, K = p.K, ks = p.ks, nsl = p.nsl;
   const int G = gridDim.x;

@@ -101,7 +101,8 @@ static __device__ __noinline__ bool ctas_done(const unsigned *flags, int b0, int
 template <int NT>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_constant__ FusedParams p) {
   pdl_trigger();
-  pdl_wait();  // nothing before this reads or writes global memory
+  prefetch_router_rows(p);
+  pdl_wait();  // before this only the router-row prefetch touches global memory
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, K = p.K;
   const int G = gridDim.x;
