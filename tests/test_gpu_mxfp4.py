@@ -272,3 +272,52 @@ def test_mxfp4_fused_and_multikernel_paths_agree(dfv, mx_full):
     a, b = outs[0].double(), outs[1].double()
     assert (a - b).abs().max().item() <= TOL_MXFP4 * b.abs().max().item()
     assert dfv.read_device_error(ws) == 0
+
+
+@pytest.fixture(scope="module")
+def mx_chain(dfv):
+    """Six mxfp4 layers with distinct weights (E=256, d=2048, d_ff=512)."""
+    lws = [inputs.make_layer(inputs.MXFP4, seed=950 + l, device="cuda") for l in range(6)]
+    return lws, [dfv.Layer(w) for w in lws]
+
+
+@pytest.mark.parametrize("k,mode", [(1, "independent"), (5, "repeated"), (9, "repeated"), (16, "independent")])
+def test_mxfp4_chained_launches_equal_isolated_launches(dfv, mx_chain, k, mode):
+    """Back-to-back launches of the single-launch mxfp4 kernel (eager chains and
+    CUDA-graph replays) give, bit for bit, what isolated launches give: every
+    output depends only on its own row and its launch's layer."""
+    _, Ls = mx_chain
+    ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], 16))
+    x = inputs.make_hidden(k, 2048, "bf16", seed=4100 + k, mode=mode, device="cuda")
+    iso = []
+    for L in Ls:
+        o = dfv.moe_block_forward(L, x, ws)
+        torch.cuda.synchronize()
+        iso.append(o.clone())
+    assert dfv.last_layer_path() == 1, dfv.fused_unavailable_reason()
+    outs = [torch.empty_like(x) for _ in Ls]
+
+    def chain():
+        for L, o in zip(Ls, outs):
+            dfv.moe_block_forward(L, x, ws, out=o)
+
+    for _ in range(40):
+        chain()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(outs, iso))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for _ in range(40):
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(outs, iso))
+    assert dfv.read_device_error(ws) == 0
