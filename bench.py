@@ -79,6 +79,19 @@ def load_peaks():
         return PEAKS_FALLBACK, "fallback"
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over the ranks of the default process group (the
+    slowest replica's time), or `value` itself for a single process.  `device`
+    is where the collective's tensor lives: a CUDA device under NCCL, the CPU
+    under gloo."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -325,12 +338,7 @@ def run_gpu(args):
     ms16 = graph_time(fn16, args.warmup, args.steps, barrier, sampler)
     clocks = sampler.summary()
     bytes16, W16 = pass_bytes(nw16)
-    ms_max = ms16
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms16], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms16, dev)
     value = world * bytes16 / (ms_max * 1e-3) / 1e9
 
     # ---- decode: k=1 pass, same layers
