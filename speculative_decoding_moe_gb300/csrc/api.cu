@@ -17,7 +17,7 @@ thread_local cudaEvent_t g_events[4];
 thread_local bool g_profile = false;
 thread_local int g_last_path = -1;
 std::string g_fused_why;  // why the fused path is unavailable (first failure)
-thread_local int g_max_staging = 2;   // highest gate/up staging mode of the bf16 fused kernel
+thread_local int g_max_staging = 1;   // highest gate/up staging mode of the bf16 fused kernel
 thread_local int g_last_staging = -1;
 
 inline void mark(int i, cudaStream_t s) {
