@@ -156,16 +156,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------- reference arm (CPU oracle)
 
 
-def oracle_layer_sample(n_threads: int, budget_s: float, k: int = KBLOCK, min_calls: int = 1, max_calls: int = 8):
-    """Time the CPU oracle on config-2 layers at block k: returns (GB/s, calls, seconds, threads)."""
+def oracle_layer_sample(n_threads: int, budget_s: float, k: int = KBLOCK, n_layers: int = 2, max_calls: int = 2000):
+    """Time the CPU oracle on Qwen3-A3B-like layers at block k: `n_layers` layers
+    drawn once, then calls with fresh inputs, alternating layers, until
+    `budget_s` seconds of timed oracle work.  Returns (GB/s, calls, seconds)."""
     import oracle
     from speculative_decoding_moe_gb300 import inputs
     from tests._util import np_of, oracle_layer
     oracle.build()
+    lws = [inputs.make_layer(inputs.A3B, seed=9000 + i) for i in range(n_layers)]
+    ols = [oracle_layer(lw) for lw in lws]
     total_bytes, total_s, calls = 0.0, 0.0, 0
-    while calls < max_calls and (calls < min_calls or total_s < budget_s):
-        lw = inputs.make_layer(inputs.A3B, seed=9000 + calls)
-        ol = oracle_layer(lw)
+    while calls < max_calls and (calls == 0 or total_s < budget_s):
+        lw, ol = lws[calls % n_layers], ols[calls % n_layers]
         x = np_of(inputs.make_hidden(k, inputs.A3B.d, "bf16", seed=9100 + calls))
         _, idx, _ = oracle.route(ol, x)
         W = len(oracle.woken(idx, inputs.A3B.n_experts)[0])
@@ -460,7 +463,7 @@ def run_gpu(args):
         nthr = host_threads()
         gbs, calls, secs = oracle_layer_sample(nthr, budget_s=args.cpu_budget)
         cpu = {"value": gbs, "unit": "GB/s", "cores": nthr, "kind": "oracle",
-               "sample": "%d Qwen3-A3B-like layer call(s) at k=16 (oracle moe_forward, fp64, %d threads, %.1f s)"
+               "sample": "%d Qwen3-A3B-like layer call(s) at k=16 over 2 layers (oracle moe_forward, fp64, %d threads, %.1f s timed)"
                          % (calls, nthr, secs)}
 
     ratio = ms16 / ms1
