@@ -9,18 +9,21 @@
 // crosses HBM exactly once.
 //
 // One CTA per SM (grid = SM count, co-residency guaranteed by the cooperative
-// launch); 16 consumer warps and one producer warp.  Phases:
+// launch); 16 consumer warps and one producer warp.  Before griddepcontrol.wait
+// a CTA only starts its router rows towards L2.  Phases:
 //   P0  router GEMV (optionally on RMSNorm(x) rounded to bf16): CTA b computes
 //       the logits of experts b, b+G, ...; fixed-order reductions.
 //       -- grid barrier 1 --
 //   P1  every CTA derives the whole routing decision itself from the logits:
 //       top-K per row (warp per row, redux max/min: largest logit, lowest id
 //       among equals), routing weights, woken union, per-expert pair offsets
-//       (block scan) and the (expert, token)-sorted pair list.
+//       (block scan) and the (expert, token)-sorted pair list.  Each CTA
+//       checks these tables before any phase indexes with them.
 //   P2  gate/up: unit = (woken expert, 8 d_ff rows).  The producer streams
-//       stages of 8 gate + 8 up rows x `ks` columns into an mbarrier ring (one
-//       3-D tensor-map box per matrix, else 2-D boxes of 256 columns, else one
-//       bulk copy per row); the 16 consumer warps split the columns, run
+//       stages of 8 gate + 8 up rows x `ks` columns into an mbarrier ring
+//       (2-D tensor-map boxes of 256 columns by default; a 3-D box per matrix,
+//       or one bulk copy per row, on request); the 16 consumer warps split the
+//       columns, run
 //       m16n8k16 MMAs (gate rows = M 0-7, up rows = M 8-15, tokens = N) and
 //       reduce across warps in fixed order; h = silu(g) * u is written in
 //       bf16.  The producer then runs ahead into P3's weights.
@@ -29,7 +32,11 @@
 //       contiguous ranges over the CTAs (so every SM works and a warp reuses
 //       the h fragments of an expert across its tiles); each unit is one
 //       contiguous copy; two groups of 8 warps take alternate units, reduce
-//       within the group and write w[t,s] * y to ys[pair].
+//       within the group and write w[t,s] * y to ys[pair].  Each group owns
+//       the ring stages of its parity, and every warp tracks each stage's
+//       phase, so each parity wait is on a stage whose previous fill the
+//       waiting warps consumed (with one shared odd-sized ring, a group could
+//       pass a wait one phase early).
 //       -- grid barrier 3 --
 //   P4  every CTA sums ys over the K slots in slot order (+ the residual) for
 //       its share of the outputs.  No atomics on the output: the result of a
