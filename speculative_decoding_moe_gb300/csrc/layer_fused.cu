@@ -459,10 +459,10 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   const size_t dslot = (size_t)16 * I * 2;
   size_t slot = gslot > dslot ? gslot : dslot;
   slot = (slot + 127) & ~(size_t)127;
+  // staged x: NT * 8 rows.  k > 8: rows 8..15 double as one more ring stage
+  // when no expert has more than 8 tokens, so they span at least one full slot
   size_t scratch = (size_t)NT * 8 * d * 2;
-  // k > 8: staged-x rows 8..15 double as one more ring stage when no expert has
-  // more than 8 tokens; make that space one full slot
-  if (NT == 2 && (size_t)8 * d * 2 < slot + (size_t)8 * d * 2) scratch = (size_t)8 * d * 2 + slot;
+  if (NT == 2 && (size_t)8 * d * 2 + slot > scratch) scratch = (size_t)8 * d * 2 + slot;
   const size_t lgb = (size_t)k * E * 4, ysb = (size_t)k * 8 * 16 * 4;
   if (lgb > scratch) scratch = lgb;
   if (ysb > scratch) scratch = ysb;

@@ -88,6 +88,41 @@ def test_bf16_layer_parity_small(dfv, path, shape, k):
     assert _max_rel_err(_gpu_out_np(out), ref) <= TOL_BF16
 
 
+WIDE = [
+    # d, E, K, I: rows wider than 1024 (2-4 gate/up stages per unit, row copies
+    # when d is not a multiple of 256); a repeated-token block gives experts up
+    # to 16 tokens, so the staged x rows 8..15 are in use
+    (1056, 16, 4, 64),
+    (2304, 16, 4, 128),
+    (2560, 12, 2, 192),
+]
+
+
+@pytest.mark.parametrize("shape", WIDE)
+@pytest.mark.parametrize("k,mode", [(16, "repeated"), (12, "independent"), (1, "independent")])
+def test_bf16_wide_rows(dfv, path, shape, k, mode):
+    d, E, K, I = shape
+    lw = inputs.make_layer(inputs.LayerShape(d=d, n_experts=E, top_k=K, d_ff=I), seed=d + 7 * k, device="cuda")
+    ol = oracle_layer(lw.to("cpu"))
+    L = dfv.Layer(lw)
+    x = hidden_without_near_ties(ol, k, "bf16", seed=d + k, mode=mode)
+    xg = x.cuda()
+    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
+    _check_routing(dfv, L, ol, xg, ws)
+    out = dfv.moe_block_forward(L, xg, ws)
+    torch.cuda.synchronize()
+    assert dfv.last_layer_path() == (1 if path == "fused" else 0), dfv.fused_unavailable_reason()
+    assert dfv.read_device_error(ws) == 0
+    ref = oracle.moe_forward(ol, np_of(x), nthreads=oracle.num_threads_available())
+    assert _max_rel_err(_gpu_out_np(out), ref) <= TOL_BF16
+    if k > 1 and path == "fused":
+        # the block's rows equal single-token calls bit for bit
+        for t in (0, k - 1):
+            row = dfv.moe_block_forward(L, xg[t:t + 1].contiguous(), ws)
+            torch.cuda.synchronize()
+            assert torch.equal(row[0], out[t])
+
+
 @pytest.mark.parametrize("k", [1, 4])
 def test_tiny_fp32_config(dfv, k):
     lw = inputs.make_layer(inputs.TINY, seed=1)
