@@ -59,6 +59,8 @@ SMALL = [
     (352, 24, 3, 96),
     (512, 40, 8, 160),
     (256, 8, 8, 64),  # K == E: every row wakes every expert
+    (96, 8, 1, 64),   # top-1 routing, fewer experts than a warp has lanes
+    (64, 4, 2, 32),   # narrow rows: fewer 32-column chunks than consumer warps
 ]
 
 
