@@ -141,6 +141,8 @@ SMALL = [
     (256, 8, 8, 64),  # K == E: every row wakes every expert
     (512, 16, 4, 192),   # single-launch kernel: one gate/up stage per unit, ragged d_ff chunk
     (2048, 24, 8, 64),   # single-launch kernel: four gate/up stages per unit
+    (512, 8, 1, 64),     # top-1 routing, fewer experts than a warp has lanes
+    (1024, 4, 2, 448),   # four experts: up to 16 tokens each (second pass over held stages)
 ]
 
 
