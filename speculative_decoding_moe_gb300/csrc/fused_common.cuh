@@ -43,13 +43,16 @@ __device__ bool grid_sync(const FusedParams &p, unsigned nb) {
   red_release_add(ctr, 1u);
   const unsigned target = nb * gridDim.x;
   const unsigned long long t0 = global_ns();
-  while (ld_acquire(ctr) < target) {
-    __nanosleep(64);  // leave the issue slots to the SM's other warps
-    if (ld_relaxed(gabort)) return false;
-    if (global_ns() - t0 > kWaitNs) {
-      atomicOr(p.ws.err, DFV_DEVERR_GRID_WAIT);
-      atomicExch(gabort, 1u);
-      return false;
+  // one load per poll, so the count is seen within one L2 round trip of the
+  // last arrival; the abort flag and the clock are read every 16th poll
+  for (unsigned it = 1; ld_acquire(ctr) < target; ++it) {
+    if ((it & 15u) == 0) {
+      if (ld_relaxed(gabort)) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        atomicOr(p.ws.err, DFV_DEVERR_GRID_WAIT);
+        atomicExch(gabort, 1u);
+        return false;
+      }
     }
   }
   return true;
