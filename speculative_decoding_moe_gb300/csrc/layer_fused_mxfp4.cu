@@ -85,9 +85,9 @@ static __device__ __noinline__ bool ctas_done(const unsigned *flags, int b0, int
   const unsigned long long t0 = global_ns();
   bool ok = true;
   for (int b = b0 + lane; b <= b1 && ok; b += 32) {
-    while (ld_acquire(flags + b) == 0u) {
-      __nanosleep(64);
-      if (*abort || global_ns() - t0 > kWaitNs) {
+    // one load per poll; the abort flag and the clock every 16th poll
+    for (unsigned it = 1; ld_acquire(flags + b) == 0u; ++it) {
+      if ((it & 15u) == 0 && (*abort || global_ns() - t0 > kWaitNs)) {
         if (!*abort) atomicOr(err, DFV_DEVERR_GRID_WAIT);
         *abort = 1;
         ok = false;
