@@ -47,8 +47,8 @@ KERNEL_SOURCES = {
     "moe_fused_mx_kernel": ["layer_fused_mxfp4.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
 }
 NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
-    "moe_fused_kernel": ("8e62aac68f5e469f", 728453888 + 7190272, 77 * 9437184 + 524288),
-    "moe_fused_mx_kernel": ("8f3e74ebeb54dfe2", 172090112 + 6741760, 102 * 1671168 + 1048576),
+    "moe_fused_kernel": ("4edc31ec65b24f98", 728469504 + 7244288, 77 * 9437184 + 524288),
+    "moe_fused_mx_kernel": ("06fde88fbd60b9da", 172101632 + 7274240, 102 * 1671168 + 1048576),
 }
 
 
