@@ -1,0 +1,45 @@
+"""Host-side logic on the CPU: the binding refuses to run without its compiled
+library (no fallback path exists), and the bench's DRAM-traffic figure is
+reported only for the kernel sources it was measured on."""
+from __future__ import annotations
+
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    from speculative_decoding_moe_gb300 import dfv
+    monkeypatch.setattr(dfv, "LIB_PATH", str(tmp_path / "libdfv.so"))
+    monkeypatch.setattr(dfv, "_lib", None)
+    with pytest.raises(ImportError, match="not built"):
+        dfv._load()
+
+
+def test_ncu_traffic_is_keyed_by_the_kernel_sources(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    name = "moe_fused_kernel"
+    h = bench.kernel_hash(name)
+    assert len(h) == 16 and int(h, 16) >= 0
+    # the capture's bytes scale with the algorithmic bytes of the launch
+    monkeypatch.setitem(bench.NCU_TRAFFIC, name, (h, 1000.0, 500.0))
+    assert bench.ncu_traffic(name, 250.0) == 500.0
+    # an edited kernel (another hash) reports no traffic rather than a stale one
+    monkeypatch.setitem(bench.NCU_TRAFFIC, name, ("0" * 16, 1000.0, 500.0))
+    assert bench.ncu_traffic(name, 250.0) is None
+    assert bench.ncu_traffic("no_such_kernel", 250.0) is None
+
+
+def test_peaks_come_from_the_measured_file():
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks, kind = bench.load_peaks()
+    if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
+        assert kind == "measured"
+        assert peaks["hbm_gbs"] > 1000
+    else:
+        assert kind == "fallback"
