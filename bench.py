@@ -156,28 +156,55 @@ class ClockSampler:
 # ---------------------------------------------------------------------------- reference arm (CPU oracle)
 
 
-def oracle_layer_sample(n_threads: int, budget_s: float, k: int = KBLOCK, n_layers: int = 2, max_calls: int = 2000):
-    """Time the CPU oracle on Qwen3-A3B-like layers at block k: `n_layers` layers
-    drawn once, then calls with fresh inputs, alternating layers, until
-    `budget_s` seconds of timed oracle work.  Returns (GB/s, calls, seconds)."""
-    import oracle
-    from speculative_decoding_moe_gb300 import inputs
-    from tests._util import np_of, oracle_layer
-    oracle.build()
-    lws = [inputs.make_layer(inputs.A3B, seed=9000 + i) for i in range(n_layers)]
-    ols = [oracle_layer(lw) for lw in lws]
-    total_bytes, total_s, calls = 0.0, 0.0, 0
-    while calls < max_calls and (calls == 0 or total_s < budget_s):
-        lw, ol = lws[calls % n_layers], ols[calls % n_layers]
-        x = np_of(inputs.make_hidden(k, inputs.A3B.d, "bf16", seed=9100 + calls))
-        _, idx, _ = oracle.route(ol, x)
-        W = len(oracle.woken(idx, inputs.A3B.n_experts)[0])
-        t0 = time.perf_counter()
-        oracle.moe_forward(ol, x, nthreads=n_threads)
-        total_s += time.perf_counter() - t0
-        total_bytes += W * lw.expert_bytes() + lw.router_bytes()
-        calls += 1
-    return total_bytes / total_s / 1e9, calls, total_s
+class OracleSample:
+    """The CPU oracle on Qwen3-A3B-like layers: `n_layers` layers drawn once, then
+    timed calls with fresh hidden rows, alternating layers."""
+
+    def __init__(self, n_layers: int = 2):
+        import oracle
+        from speculative_decoding_moe_gb300 import inputs
+        from tests._util import np_of, oracle_layer
+        oracle.build()
+        self.oracle, self.inputs, self.np_of = oracle, inputs, np_of
+        self.lws = [inputs.make_layer(inputs.A3B, seed=9000 + i) for i in range(n_layers)]
+        self.ols = [oracle_layer(lw) for lw in self.lws]
+        self.seed = 9100
+
+    def run(self, n_threads: int, budget_s: float, k: int = KBLOCK, max_calls: int = 2000):
+        """Calls at block k on `n_threads` threads until `budget_s` seconds of timed
+        oracle work; returns (GB/s of woken-expert + router bytes, calls, seconds)."""
+        o, A3B = self.oracle, self.inputs.A3B
+        total_bytes, total_s, calls = 0.0, 0.0, 0
+        while calls < max_calls and (calls == 0 or total_s < budget_s):
+            lw, ol = self.lws[calls % len(self.lws)], self.ols[calls % len(self.ols)]
+            x = self.np_of(self.inputs.make_hidden(k, A3B.d, "bf16", seed=self.seed))
+            self.seed += 1
+            _, idx, _ = o.route(ol, x)
+            W = len(o.woken(idx, A3B.n_experts)[0])
+            t0 = time.perf_counter()
+            o.moe_forward(ol, x, nthreads=n_threads)
+            total_s += time.perf_counter() - t0
+            total_bytes += W * lw.expert_bytes() + lw.router_bytes()
+            calls += 1
+        return total_bytes / total_s / 1e9, calls, total_s
+
+
+def cpu_baseline_line(budget_s: float):
+    """`cpu_baseline`: the oracle at k=16 on every host thread (the headline, about
+    `budget_s` seconds), plus shorter samples single-threaded and at k=1."""
+    nthr = host_threads()
+    smp = OracleSample()
+    gbs, calls, secs = smp.run(nthr, budget_s)
+    side = {}
+    for name, nt, k in (("k16_1thread", 1, KBLOCK), ("k1_all_threads", nthr, 1), ("k1_1thread", 1, 1)):
+        g, c, t = smp.run(nt, budget_s / 4, k=k)
+        side[name] = {"value": g, "unit": "GB/s", "threads": nt, "k": k, "calls": c,
+                      "us_per_layer": t / c * 1e6}
+    return {"value": gbs, "unit": "GB/s", "cores": nthr, "kind": "oracle",
+            "us_per_layer": secs / calls * 1e6,
+            "sample": "%d Qwen3-A3B-like layer call(s) at k=16 over 2 layers (oracle moe_forward, fp64, "
+                      "%d threads, %.1f s timed)" % (calls, nthr, secs),
+            "also": side}
 
 
 def host_threads():
@@ -460,11 +487,8 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        nthr = host_threads()
-        gbs, calls, secs = oracle_layer_sample(nthr, budget_s=args.cpu_budget)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": nthr, "kind": "oracle",
-               "sample": "%d Qwen3-A3B-like layer call(s) at k=16 over 2 layers (oracle moe_forward, fp64, %d threads, %.1f s timed)"
-                         % (calls, nthr, secs)}
+        progress("cpu oracle sample")
+        cpu = cpu_baseline_line(args.cpu_budget)
 
     ratio = ms16 / ms1
     byte_ratio = bytes16 / bytes1

@@ -43,3 +43,16 @@ def test_peaks_come_from_the_measured_file():
         assert peaks["hbm_gbs"] > 1000
     else:
         assert kind == "fallback"
+
+
+def test_cpu_baseline_reports_all_threads_one_thread_and_k1():
+    sys.path.insert(0, ROOT)
+    import bench
+    line = bench.cpu_baseline_line(0.05)
+    assert line["kind"] == "oracle" and line["unit"] == "GB/s"
+    assert line["cores"] == bench.host_threads() and line["value"] > 0
+    side = line["also"]
+    assert side["k16_1thread"]["threads"] == 1 and side["k16_1thread"]["k"] == bench.KBLOCK
+    assert side["k1_all_threads"]["k"] == 1 and side["k1_all_threads"]["threads"] == line["cores"]
+    assert side["k1_1thread"]["threads"] == 1 and side["k1_1thread"]["k"] == 1
+    assert all(v["calls"] >= 1 and v["value"] > 0 for v in side.values())
