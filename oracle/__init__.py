@@ -12,8 +12,9 @@ with gcc and marshals numpy arrays across ctypes.
 Sources, by page title and section:
   * "Speculating on a Strix Halo", sections "Speculative decoding" (greedy
     acceptance, committed length), "What the pieces cost" (per-token routing,
-    woken-expert union), "The verify's own cost" (tokens sorted by expert),
-    reference 1 (256 experts, 8 routed).
+    woken-expert union, the always-on shared expert), "The verify's own cost"
+    (tokens sorted by expert), reference 1 (256 experts, 8 routed plus 1
+    shared activated).
   * "Speculating on a Strix Halo (part 2)", sections "The verification cog"
     and "Why drafter performance doesn't really matter" (prefix acceptance).
   * the MI355X / vLLM DFlash write-up (allbreaknews.com/?p=4397), sections
@@ -63,7 +64,7 @@ class _Layer(ctypes.Structure):
         ("w_dtype", ctypes.c_int), ("r_dtype", ctypes.c_int),
         ("w_router", ctypes.c_void_p), ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
         ("w_down", ctypes.c_void_p), ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p),
-        ("s_down", ctypes.c_void_p),
+        ("s_down", ctypes.c_void_p), ("n_shared", ctypes.c_int),
     ]
 
 
@@ -133,6 +134,7 @@ class Layer:
     s_up: Optional[np.ndarray] = None
     s_down: Optional[np.ndarray] = None
     norm_topk: int = 1
+    n_shared: int = 0   # 1: one always-on shared expert, stored as expert n_experts
 
     def c(self) -> _Layer:
         arrs = [self.w_router, self.w_gate, self.w_up, self.w_down, self.s_gate, self.s_up, self.s_down]
@@ -140,7 +142,8 @@ class Layer:
             if a is not None:
                 assert a.flags["C_CONTIGUOUS"]
         return _Layer(self.d, self.n_experts, self.top_k, self.d_ff, self.norm_topk,
-                      self.w_dtype, self.r_dtype, *[(_ptr(a).value if a is not None else None) for a in arrs])
+                      self.w_dtype, self.r_dtype, *[(_ptr(a).value if a is not None else None) for a in arrs],
+                      self.n_shared)
 
 
 # ---------------------------------------------------------------- scalars
@@ -212,7 +215,8 @@ def expert_ffn(layer: Layer, e: int, x_row: np.ndarray) -> np.ndarray:
 
 
 def moe_forward(layer: Layer, x: np.ndarray, nthreads: int = 1) -> np.ndarray:
-    """Routed MoE output of one layer, float64 [k, d]."""
+    """MoE output of one layer (routed experts + the shared expert when
+    layer.n_shared), float64 [k, d]."""
     k = x.shape[0]
     out = np.empty((k, layer.d), dtype=np.float64)
     lc = layer.c()

@@ -241,31 +241,41 @@ int orc_expert_ffn(const orc_layer *L, int e, const double *x, double *y) {
 }
 
 /*
- * Routed output of one MoE layer for a block of k rows:
+ * Output of one MoE layer for a block of k rows:
  *   out[t] = sum over slots s (in slot order) of w[t][s] * FFN_{idx[t][s]}(x[t])
- * The shared expert is not part of the routed output.
+ *            + FFN_E(x[t])                                   (when n_shared = 1)
+ * "What the pieces cost" names one always-on shared expert next to the routed
+ * ones, and the model card it cites counts "8 routed plus 1 shared" activated
+ * experts.  The pages give the shared expert no gate and no weight, so the
+ * reading taken is the plainest one: an expert of the same SwiGLU form and
+ * size as the routed ones, applied to every row and added with weight 1 after
+ * the routed sum.  Its weights are expert index E of the stacked matrices.
  */
 int orc_moe_forward(const orc_layer *L, const void *x, int x_dtype, int k,
                     double *out, int nthreads) {
   const int d = L->d, E = L->n_experts, K = L->top_k;
+  const int ns = L->n_shared ? 1 : 0;
+  if (L->n_shared < 0 || L->n_shared > 1) return -1;
   float *logits = malloc(sizeof(float) * (size_t)k * E);
   int32_t *idx = malloc(sizeof(int32_t) * (size_t)k * K);
   double *w = malloc(sizeof(double) * (size_t)k * K);
   double *xr = malloc(sizeof(double) * (size_t)k * d);
-  double *ys = malloc(sizeof(double) * (size_t)k * K * d);
+  double *ys = malloc(sizeof(double) * (size_t)k * (K + ns) * d);
   if (!logits || !idx || !w || !xr || !ys) return -2;
   int rc = orc_route(L, x, x_dtype, k, logits, idx, w);
   if (rc) return rc;
   orc_decode_rows(x_dtype, x, NULL, 0, k, d, xr);
 
-  int npairs = k * K;
+  /* pairs t*K+s of the routed experts, then k*K+t of the shared expert */
+  int npairs = k * K + k * ns;
 #ifdef _OPENMP
   if (nthreads < 1) nthreads = 1;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
 #endif
   for (int p = 0; p < npairs; ++p) {
-    int t = p / K;
-    orc_expert_ffn(L, idx[p], xr + (size_t)t * d, ys + (size_t)p * d);
+    int t = p < k * K ? p / K : p - k * K;
+    int e = p < k * K ? idx[p] : E;
+    orc_expert_ffn(L, e, xr + (size_t)t * d, ys + (size_t)p * d);
   }
   (void)nthreads;
 
@@ -274,6 +284,10 @@ int orc_moe_forward(const orc_layer *L, const void *x, int x_dtype, int k,
     for (int s = 0; s < K; ++s) {
       const double *y = ys + (size_t)(t * K + s) * d;
       for (int j = 0; j < d; ++j) out[(size_t)t * d + j] += w[t * K + s] * y[j];
+    }
+    if (ns) {
+      const double *y = ys + (size_t)(k * K + t) * d;
+      for (int j = 0; j < d; ++j) out[(size_t)t * d + j] += y[j];
     }
   }
   free(logits);

@@ -15,8 +15,9 @@
  *
  * Sources (page titles and sections of the method's write-ups):
  *   [P1] "Speculating on a Strix Halo", sections "Speculative decoding",
- *        "What the pieces cost", "The verify's own cost", reference 1 (model
- *        card: 256 experts, 8 routed).
+ *        "What the pieces cost" (including its always-on shared expert),
+ *        "The verify's own cost", reference 1 (model card: 256 experts, 8
+ *        routed plus 1 shared activated).
  *   [P2] "Speculating on a Strix Halo (part 2)", sections "The verification
  *        cog", "Why drafter performance doesn't really matter", "Two bugs
  *        upstream".
@@ -46,6 +47,9 @@ typedef struct {
   const void *w_gate, *w_up;      /* [E][d_ff][d]  (mxfp4: bytes [E][d_ff][d/2]) */
   const void *w_down;             /* [E][d][d_ff]  (mxfp4: bytes [E][d][d_ff/2]) */
   const uint8_t *s_gate, *s_up, *s_down; /* e8m0 scales (mxfp4 only) */
+  int n_shared;  /* 0 or 1: one always-on shared expert, stored as expert E of
+                    w_gate / w_up / w_down (and their scales); the router has
+                    E rows only */
 } orc_layer;
 
 /* scalar helpers */
@@ -71,7 +75,8 @@ int orc_woken(int k, int K, int E, const int32_t *topk_idx,
 /* one expert on one token row: y = W_down (silu(W_gate x) * (W_up x)) */
 int orc_expert_ffn(const orc_layer *L, int e, const double *x, double *y);
 
-/* routed MoE output of one layer, out[k][d] in double */
+/* MoE output of one layer (routed experts, plus the shared expert when
+ * n_shared = 1), out[k][d] in double */
 int orc_moe_forward(const orc_layer *L, const void *x, int x_dtype, int k,
                     double *out, int nthreads);
 

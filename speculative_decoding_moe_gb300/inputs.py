@@ -16,6 +16,9 @@ weights), scaled to one layer:
 * ``mxfp4``     d=2048, E=256, top-8, d_ff=512, e2m1 codes uniform over the 16
                 nibbles, e8m0 scales uniform in 2^{-8..0}, bf16 router
                 ~N(0, 0.02), bf16 activations.
+* ``e256+shared`` d=2048, E=256, top-8, d_ff=512, bf16, plus one always-on
+                shared expert of the same size ("What the pieces cost"; the
+                model card it cites: 8 routed plus 1 shared activated).
 * acceptance    logits[k+1, V] ~N(0, s) with drafts planted so the accepted
                 prefix length is Geometric(0.3) - 1, capped at k - 1.
 """
@@ -42,12 +45,15 @@ class LayerShape:
     r_std: float = 0.02
     scale_exp: tuple = (119, 127)   # e8m0 exponent range (inclusive), mxfp4 only
     norm_topk: int = 1
+    n_shared: int = 0               # 1: one always-on shared expert (expert index E)
 
 
 TINY = LayerShape(d=256, n_experts=16, top_k=2, d_ff=128, w_dtype="f32", r_dtype="f32", act="f32",
                   w_std=0.02, r_std=0.05)
 A3B = LayerShape(d=2048, n_experts=128, top_k=8, d_ff=768)
 MXFP4 = LayerShape(d=2048, n_experts=256, top_k=8, d_ff=512, w_dtype="mxfp4")
+# 256 routed experts (top-8) plus one always-on shared expert of the same size
+E256_SHARED = LayerShape(d=2048, n_experts=256, top_k=8, d_ff=512, n_shared=1)
 
 
 def _torch_dtype(name: str):
@@ -64,10 +70,12 @@ def _gen(seed: int, device) -> torch.Generator:
 class LayerWeights:
     """One layer's weights as torch tensors (any device).
 
-    f32/bf16: w_gate, w_up [E, d_ff, d]; w_down [E, d, d_ff].
-    mxfp4:    w_gate, w_up uint8 [E, d_ff, d/2]; w_down uint8 [E, d, d_ff/2]
+    f32/bf16: w_gate, w_up [E', d_ff, d]; w_down [E', d, d_ff].
+    mxfp4:    w_gate, w_up uint8 [E', d_ff, d/2]; w_down uint8 [E', d, d_ff/2]
               (low nibble = even column) and s_* uint8 e8m0 scales
-              [E, rows, cols/32].
+              [E', rows, cols/32].
+    E' = E + n_shared: the shared expert, if any, is the last one.  The
+    router is [E, d].
     """
     shape: LayerShape
     w_router: torch.Tensor
@@ -90,7 +98,7 @@ class LayerWeights:
         for t in (self.w_gate, self.w_up, self.w_down, self.s_gate, self.s_up, self.s_down):
             if t is not None:
                 per += t.numel() * t.element_size()
-        return per // s.n_experts
+        return per // (s.n_experts + s.n_shared)
 
     def router_bytes(self) -> int:
         return self.w_router.numel() * self.w_router.element_size()
@@ -100,6 +108,7 @@ def make_layer(shape: LayerShape, seed: int, device="cpu") -> LayerWeights:
     g = _gen(seed, device)
     E, d, I = shape.n_experts, shape.d, shape.d_ff
     wr = (torch.randn(E, d, generator=g, device=device) * shape.r_std).to(_torch_dtype(shape.r_dtype))
+    E = shape.n_experts + shape.n_shared  # expert matrices: routed experts, then the shared one
     if shape.w_dtype in ("f32", "bf16"):
         dt = _torch_dtype(shape.w_dtype)
         wg = (torch.randn(E, I, d, generator=g, device=device) * shape.w_std).to(dt)

@@ -28,7 +28,7 @@ def oracle_layer(lw: inputs.LayerWeights) -> oracle.Layer:
         s_gate=None if lw.s_gate is None else np_of(lw.s_gate),
         s_up=None if lw.s_up is None else np_of(lw.s_up),
         s_down=None if lw.s_down is None else np_of(lw.s_down),
-        norm_topk=s.norm_topk)
+        norm_topk=s.norm_topk, n_shared=s.n_shared)
 
 
 def topk_gap(logits: np.ndarray, K: int) -> np.ndarray:

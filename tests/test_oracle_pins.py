@@ -290,14 +290,86 @@ def test_identical_experts_make_routing_irrelevant():
         assert np.allclose(out[t], y, rtol=1e-12, atol=1e-15)
 
 
+# ---------------------------------------------------------------- shared expert
+# "What the pieces cost": one always-on shared expert next to the routed ones
+# (the cited model card: 8 routed plus 1 shared activated).  Reading: same
+# SwiGLU form and size, applied to every row, weight 1, stored as expert E.
+
+
+def test_shared_expert_closed_form_at_index_E():
+    # two routed experts with zero weights (routed sum exactly 0) and a shared
+    # expert (index 2) with one non-zero entry per matrix: a shared expert
+    # read from another index, or transposed, gives zeros
+    d, I, E = 3, 2, 2
+    wg = np.zeros((E + 1, I, d)); wg[2, 1, 2] = math.log(3.0)
+    wu = np.zeros((E + 1, I, d)); wu[2, 1, 2] = 2.0
+    wd = np.zeros((E + 1, d, I)); wd[2, 0, 1] = -4.0
+    L = _manual_layer(d, I, E, wg, wu, wd)
+    L.n_shared = 1
+    x = np.array([[0.0, 0.0, 1.0], [0.0, 0.0, -2.0]], dtype=np.float32)
+    out = oracle.moe_forward(L, x)
+    g = float(np.float32(math.log(3.0)))
+    for t, xt in enumerate((1.0, -2.0)):
+        z = g * xt
+        want = -4.0 * (z / (1.0 + math.exp(-z))) * (2.0 * xt)
+        assert out[t, 1] == 0.0 and out[t, 2] == 0.0
+        assert out[t, 0] == pytest.approx(want, rel=1e-15)
+    L.n_shared = 0
+    assert np.all(oracle.moe_forward(L, x) == 0.0)
+
+
+@pytest.mark.parametrize("j", [0, 7, 15])
+def test_shared_copy_of_the_chosen_expert_doubles_the_output(j):
+    # top-1 with renormalised weights gives the chosen expert weight exactly 1;
+    # a router that sends every row to expert j and a shared expert holding a
+    # copy of j's weights must give exactly twice the routed output
+    lw = _tiny_layer(12, n_shared=1, top_k=1)
+    wr = torch.zeros_like(lw.w_router)
+    wr[j] = 1.0
+    wg, wu, wd = lw.w_gate.clone(), lw.w_up.clone(), lw.w_down.clone()
+    wg[-1], wu[-1], wd[-1] = wg[j], wu[j], wd[j]
+    lw = inputs.LayerWeights(lw.shape, wr, wg, wu, wd)
+    x = np_of(inputs.make_hidden(4, 256, "f32", 12).abs())  # logit of j = sum |x| > 0 = the others
+    ol = oracle_layer(lw)
+    _, idx, w = oracle.route(ol, x)
+    assert np.all(idx == j) and np.all(w == 1.0)
+    both = oracle.moe_forward(ol, x)
+    ol.n_shared = 0
+    routed = oracle.moe_forward(ol, x)
+    assert np.array_equal(both, 2.0 * routed)
+    assert not np.array_equal(both, routed)
+
+
+def test_shared_expert_is_independent_of_routing():
+    # relabelling the routed experts (router rows and weights together) leaves
+    # the output unchanged; the shared expert stays last
+    lw = _tiny_layer(13, n_shared=1)
+    perm = torch.cat([torch.randperm(16, generator=torch.Generator().manual_seed(13)), torch.tensor([16])])
+    lp = inputs.LayerWeights(lw.shape, lw.w_router[perm[:16]].contiguous(), lw.w_gate[perm].contiguous(),
+                             lw.w_up[perm].contiguous(), lw.w_down[perm].contiguous())
+    x = np_of(inputs.make_hidden(4, 256, "f32", 13))
+    a = oracle.moe_forward(oracle_layer(lw), x)
+    b = oracle.moe_forward(oracle_layer(lp), x)
+    assert np.allclose(a, b, rtol=1e-13, atol=1e-16)
+    # and the shared term is the same whatever the router does
+    lz = inputs.LayerWeights(lw.shape, torch.zeros_like(lw.w_router), lw.w_gate, lw.w_up, lw.w_down)
+    lr = inputs.LayerWeights(lw.shape, lw.w_router, lw.w_gate, lw.w_up, lw.w_down)
+    dz = oracle.moe_forward(oracle_layer(lz), x)
+    dr = oracle.moe_forward(oracle_layer(lr), x)
+    olz, olr = oracle_layer(lz), oracle_layer(lr)
+    olz.n_shared = olr.n_shared = 0
+    assert np.allclose(dz - oracle.moe_forward(olz, x), dr - oracle.moe_forward(olr, x), rtol=1e-12, atol=1e-15)
+
+
 # ---------------------------------------------------------------- block invariants
 
 
+@pytest.mark.parametrize("n_shared", [0, 1])
 @pytest.mark.parametrize("w_dtype", ["f32", "bf16", "mxfp4"])
-def test_block_equals_row_by_row_decode(w_dtype):
+def test_block_equals_row_by_row_decode(w_dtype, n_shared):
     shape = inputs.LayerShape(d=128, n_experts=12, top_k=3, d_ff=64, w_dtype=w_dtype,
                               r_dtype="f32" if w_dtype == "f32" else "bf16",
-                              act="f32" if w_dtype == "f32" else "bf16")
+                              act="f32" if w_dtype == "f32" else "bf16", n_shared=n_shared)
     lw = inputs.make_layer(shape, 10)
     ol = oracle_layer(lw)
     x = np_of(inputs.make_hidden(6, 128, shape.act, 10))
