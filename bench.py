@@ -47,8 +47,8 @@ KERNEL_SOURCES = {
     "moe_fused_mx_kernel": ["layer_fused_mxfp4.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
 }
 NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
-    "moe_fused_kernel": ("4edc31ec65b24f98", 728469504 + 7244288, 77 * 9437184 + 524288),
-    "moe_fused_mx_kernel": ("06fde88fbd60b9da", 172101632 + 7274240, 102 * 1671168 + 1048576),
+    "moe_fused_kernel": ("45560a9ea2821278", 728468736 + 6998528, 77 * 9437184 + 524288),
+    "moe_fused_mx_kernel": ("de3c38d03fce886d", 171788032 + 6460416, 102 * 1671168 + 1048576),
 }
 
 
@@ -484,6 +484,7 @@ def run_gpu(args):
            "api": "dfv_moe_block_forward_host per layer, pinned host buffers"}
 
     mx = None if args.no_mxfp4 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
+    sh = None if args.no_shared else shared_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -507,7 +508,7 @@ def run_gpu(args):
         "kernel_path": {"fused": fused_used, "why_not": dfv.fused_unavailable_reason()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
-        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "mxfp4": mx,
+        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "mxfp4": mx, "shared_expert": sh,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -615,6 +616,78 @@ def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
     return res
 
 
+def shared_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
+    """256 routed experts (top-8) plus one always-on shared expert of the same
+    size, d=2048, d_ff=512, bf16, 40 layers.  The shared expert is read once
+    per block whatever k is, so a block's bytes are (W + 1) experts + router."""
+    progress("shared-expert section")
+    shape = inputs.E256_SHARED
+    layers = [inputs.make_layer(shape, seed=7000 + 1000 * rank + l, device=dev) for l in range(N_LAYERS)]
+    Ls = [dfv.Layer(w) for w in layers]
+    exp_bytes = layers[0].expert_bytes()
+    router_bytes = layers[0].router_bytes()
+    ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], KBLOCK), device=dev)
+
+    def make_pass(k, seed):
+        x = inputs.make_hidden(k, shape.d, "bf16", seed=seed + 100 * rank, device=dev)
+        out = torch.empty_like(x)
+        nws = torch.zeros(N_LAYERS, dtype=torch.int32, device=dev)  # routed experts woken per layer
+
+        def fn():
+            for l in range(N_LAYERS):
+                dfv.moe_block_forward(Ls[l], x, ws, out=out, n_woken=nws[l:l + 1])
+        return fn, nws, x
+
+    def pass_bytes(nws):
+        W = nws.to(torch.int64).cpu()
+        return float((W.sum().item() + N_LAYERS) * exp_bytes + N_LAYERS * router_bytes), W
+
+    fn16, nw16, x16 = make_pass(KBLOCK, seed=25)
+    ms16 = graph_time(fn16, args.warmup, args.steps, barrier)
+    b16, W16 = pass_bytes(nw16)
+    fn1, nw1, _ = make_pass(1, seed=26)
+    ms1 = graph_time(fn1, args.warmup, args.steps, barrier)
+    b1, W1 = pass_bytes(nw1)
+
+    # per-launch event timing of the single-launch kernel at k=16
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(N_LAYERS)]
+    out16 = torch.empty_like(x16)
+    tot = 0.0
+    reps = 3
+    for r in range(reps + 1):
+        for l in range(N_LAYERS):
+            dfv.profile_set_events(evs[l])
+            dfv.moe_block_forward(Ls[l], x16, ws, out=out16)
+        dfv.profile_set_events(None)
+        torch.cuda.synchronize()
+        if r:
+            tot += sum(evs[l][0].elapsed_time(evs[l][3]) for l in range(N_LAYERS))
+    per_launch_ms = tot / (reps * N_LAYERS)
+    fused = dfv.last_layer_path() == 1
+    Wm, Wm1 = float(W16.double().mean().item()), float(W1.double().mean().item())
+    layer_bytes = (Wm + 1) * exp_bytes + router_bytes
+    res = {
+        "config": "E=256 top-8 + 1 shared expert, d=2048, d_ff=512, bf16, 40 layers, k=16; inputs > L2 "
+                  "(%.1f GB of weights)" % (N_LAYERS * (exp_bytes * 257 + router_bytes) / 1e9),
+        "value_gbs": b16 / (ms16 * 1e-3) / 1e9, "frac_of_measured_hbm": b16 / (ms16 * 1e-3) / 1e9 / peak_bw,
+        "ms_per_pass": {"k16": ms16, "k1": ms1},
+        "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS},
+        "routed_woken_mean": {"k16": Wm, "k1": Wm1},
+        "verify_decode": {"latency_ratio": ms16 / ms1, "woken_byte_ratio": b16 / b1,
+                          "quotient": (b16 / b1) / (ms16 / ms1),
+                          "routed_only_byte_ratio": Wm / Wm1},
+        "kernel_path": "moe_fused_kernel (one launch per layer)" if fused else "router + gate/up + down launches",
+        "roofline": {"bound": "hbm", "kernel": "moe_fused_kernel<2> (k=16)" if fused else "multi-launch",
+                     "achieved": layer_bytes / (per_launch_ms * 1e-3) / 1e9, "peak": peak_bw, "unit": "GB/s",
+                     "frac": layer_bytes / (per_launch_ms * 1e-3) / 1e9 / peak_bw,
+                     "traffic": None, "per_launch_us": per_launch_ms * 1e3,
+                     "algorithmic_bytes_per_launch": layer_bytes},
+        "device_error": dfv.read_device_error(ws),
+    }
+    del layers, Ls
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -625,6 +698,7 @@ def main():
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-mxfp4", action="store_true", help="skip the mxfp4-expert section")
+    ap.add_argument("--no-shared", action="store_true", help="skip the shared-expert section")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=40, help="layers per step (profiling runs only)")
     args = ap.parse_args()

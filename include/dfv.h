@@ -21,6 +21,8 @@
  *       streaming is what makes verify cost more than decode.
  *   same page, section "Why drafter performance doesn't really matter": the
  *       n-th drafted token is accepted only if the n-1 before it were.
+ *   same page, section "What the pieces cost", and its reference 1: one
+ *       always-on shared expert besides the 8 routed ones.
  *   the MI355X / vLLM write-up (allbreaknews.com/?p=4397), sections "Why
  *       Quantize the Target Model on Top?" and "Results: Quantizing the Target
  *       Model": mxfp4 target weights, used natively, never re-materialised.
@@ -56,7 +58,7 @@
 extern "C" {
 #endif
 
-#define DFV_VERSION 1
+#define DFV_VERSION 2
 
 enum {
   DFV_OK = 0,
@@ -108,6 +110,13 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2 } dfv_dtype;
  * supported.  For F32/BF16 weights the scale pointers are ignored.
  * norm_topk: 1 renormalises the K selected routing weights to sum 1
  * (w_s = p_s / sum p), 0 keeps the softmax probabilities p_s.
+ * n_shared: 0, or 1 for one always-on shared expert ("What the pieces cost":
+ * the routed experts plus an always-on shared one).  It has the routed
+ * experts' form and size and is stored as expert index E of w_gate / w_up /
+ * w_down (and of s_gate / s_up / s_down), so those arrays then hold E + 1
+ * experts; w_router stays [E, d].  Every row of the block goes through it and
+ * its output is added with weight 1 after the routed sum.  (The pages give it
+ * no gate; none is applied.)
  * Supported combinations (w_dtype, r_dtype, activations):
  *   (BF16, BF16, BF16), (MXFP4, BF16, BF16), (F32, F32, F32).
  * Shapes: 1 <= K <= min(E, 8), E <= 256, d % 32 == 0, d_ff % 32 == 0
@@ -120,11 +129,12 @@ typedef struct dfv_moe_layer {
   const void *w_router;
   const void *w_gate, *w_up, *w_down;
   const uint8_t *s_gate, *s_up, *s_down;
+  int n_shared; /* 0 or 1 */
 } dfv_moe_layer;
 
 /* Bytes of workspace dfv_route_topk / dfv_moe_block_forward /
  * dfv_moe_stack_forward need for blocks of up to k_max positions
- * (0 on invalid arguments). */
+ * (0 on invalid arguments).  A layer with a shared expert needs more. */
 size_t dfv_moe_workspace_size(const dfv_moe_layer *layer, int k_max);
 
 /*
@@ -158,16 +168,18 @@ int dfv_route_topk(const dfv_moe_layer *layer, const void *hidden, int act, int 
 int dfv_read_device_error(const void *ws, uint32_t *err_host, void *stream);
 
 /*
- * Routed expert output of one MoE layer for a block of k positions: router,
+ * Expert output of one MoE layer for a block of k positions: router,
  * top-K, woken-expert union and per-expert token gather, SwiGLU expert FFN
  *   y = W_down (silu(W_gate x) * (W_up x)),  silu(z) = z / (1 + e^-z),
  * and the routing-weighted combine out[t] = sum_s w[t,s] y_{idx[t,s]}(x[t]),
- * summed in slot order ("What the pieces cost"; "The verify's own cost").
- * The residual and any shared expert are not included.
+ * summed in slot order, + y_E(x[t]) when n_shared = 1 ("What the pieces
+ * cost"; "The verify's own cost").  The residual is not included.  The
+ * shared expert runs as one more woken expert that every row selects.
  *   hidden  [k, d] act   input rows
- *   out     [k, d] act   routed output (bf16 or fp32, same dtype as hidden)
+ *   out     [k, d] act   output (bf16 or fp32, same dtype as hidden)
  *   opt_topk_idx [k, K] int32 and opt_n_woken [1] int32: optional copies of
- *           the routing decision (NULL to skip).
+ *           the routing decision (NULL to skip); n_woken counts the routed
+ *           experts only.
  * Accumulation is fp32.  Each weight byte of a woken expert is read from HBM
  * once per call; experts no row selected are not read.
  */

@@ -47,6 +47,7 @@ size_t act_size(int act) { return act == DFV_BF16 ? 2 : 4; }
 dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
   dfv::Workspace w = {};
   const size_t E = L->n_experts, K = L->top_k, d = L->d, I = L->d_ff, km = k_max;
+  const size_t ns = L->n_shared ? 1 : 0, KS = K + ns;  // pair slots per row: routed, then shared
   size_t off = 0;
   auto take = [&](size_t bytes) -> void * {
     void *p = base ? (void *)((char *)base + off) : nullptr;
@@ -64,14 +65,14 @@ dfv::Workspace layout(const dfv_moe_layer *L, int k_max, void *base) {
   w.flags = (unsigned *)take(1024 * 4);
   w.logits = (float *)take(km * E * 4);
   w.topk_idx = (int32_t *)take(km * K * 4);
-  w.topk_w = (float *)take(km * K * 4);
-  w.woken = (int32_t *)take(E * 4);
+  w.topk_w = (float *)take(km * KS * 4);
+  w.woken = (int32_t *)take((E + ns) * 4);
   w.n_woken = (int32_t *)take(4);
-  w.offsets = (int32_t *)take((E + 1) * 4);
-  w.gather = (int32_t *)take(km * K * 4);
+  w.offsets = (int32_t *)take((E + ns + 1) * 4);
+  w.gather = (int32_t *)take(km * KS * 4);
   w.xn = take(km * d * 4);
-  w.h = (float *)take(km * K * I * 4);
-  w.ys = (float *)take(km * K * d * 4);
+  w.h = (float *)take(km * KS * I * 4);
+  w.ys = (float *)take(km * KS * d * 4);
   w.xio = take(km * d * 4);
   w.oio = take(km * d * 4);
   w.bytes = off;
@@ -85,6 +86,8 @@ int check_layer(const dfv_moe_layer *L, int act) {
   if (L->n_experts > DFV_MAX_EXPERTS) return fail(DFV_ERR_UNSUPPORTED, "n_experts %d > %d", L->n_experts, DFV_MAX_EXPERTS);
   if (L->top_k > DFV_MAX_TOPK || L->top_k > L->n_experts)
     return fail(DFV_ERR_UNSUPPORTED, "top_k %d outside 1..min(E, %d)", L->top_k, DFV_MAX_TOPK);
+  if (L->n_shared < 0) return fail(DFV_ERR_INVALID_ARG, "n_shared %d < 0", L->n_shared);
+  if (L->n_shared > 1) return fail(DFV_ERR_UNSUPPORTED, "n_shared %d > 1", L->n_shared);
   if (L->d % 32 || L->d_ff % 32) return fail(DFV_ERR_UNSUPPORTED, "d and d_ff must be multiples of 32");
   const bool ok = (L->w_dtype == DFV_BF16 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
                   (L->w_dtype == DFV_MXFP4 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
@@ -150,6 +153,7 @@ dfv::RouterParams router_params(const dfv_moe_layer *L, const void *x, int act, 
   p.E = L->n_experts;
   p.K = L->top_k;
   p.norm_topk = L->norm_topk ? 1 : 0;
+  p.ns = L->n_shared ? 1 : 0;
   p.act = act;
   p.rdt = L->r_dtype;
   p.ws = w;
@@ -212,6 +216,7 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
   fp.E = L->n_experts;
   fp.K = L->top_k;
   fp.norm_topk = L->norm_topk ? 1 : 0;
+  fp.ns = L->n_shared ? 1 : 0;
   fp.fuse_norm = fuse_norm ? 1 : 0;
   fp.swz_x = (L->d % 64 == 0) ? 4 : 0;
   fp.eps = eps;
@@ -275,11 +280,12 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
   fp.I = L->d_ff;
   fp.E = L->n_experts;
   fp.K = L->top_k;
+  fp.ns = L->n_shared ? 1 : 0;
   fp.act = act;
   fp.swz_x = (L->d % 64 == 0) ? 4 : 0;
   fp.swz_h = (L->d_ff % 64 == 0) ? 4 : 0;
   fp.ws = w;
-  const int maxW = L->n_experts < k * L->top_k ? L->n_experts : k * L->top_k;
+  const int maxW = (L->n_experts < k * L->top_k ? L->n_experts : k * L->top_k) + fp.ns;  // + the shared expert
   if (L->w_dtype == DFV_MXFP4) {
     // codes widened in registers: gate/up units of (expert, 8 * 4/ks rows),
     // ks the smallest split of d whose units still fill two CTAs per SM
@@ -367,7 +373,7 @@ int dfv_profile_set_events(void *const *events, int n_events) {
 
 size_t dfv_moe_workspace_size(const dfv_moe_layer *layer, int k_max) {
   if (!layer || k_max < 1 || k_max > DFV_MAX_BLOCK || layer->n_experts <= 0 || layer->top_k <= 0 ||
-      layer->d <= 0 || layer->d_ff <= 0)
+      layer->d <= 0 || layer->d_ff <= 0 || layer->n_shared < 0 || layer->n_shared > 1)
     return 0;
   return layout(layer, k_max, nullptr).bytes;
 }

@@ -21,23 +21,27 @@ constexpr int kGateTile = 8;    // d_ff rows per gate/up unit (8 gate + 8 up = o
 // ---------------------------------------------------------------- workspace
 // Every section is 256-byte aligned.  Counters must start at zero; the kernel
 // that uses a counter returns it to zero.
+//
+// Pairs: pair t*K+s is row t's routed slot s; with a shared expert (ns = 1),
+// pair k*K+t is row t's shared slot.  The shared expert is the last woken
+// expert (id E) and every row selects it, with weight 1.  KS = K + ns.
 struct Workspace {
   float *logits;      // [k_max][E]
   int32_t *topk_idx;  // [k_max][K]
-  float *topk_w;      // [k_max][K]
-  int32_t *woken;     // [E]
-  int32_t *n_woken;   // [1]
-  int32_t *offsets;   // [E + 1]
-  int32_t *gather;    // [k_max * K]   pair ids t*K+s sorted by (expert, t)
+  float *topk_w;      // [k_max * KS]  weight of each pair
+  int32_t *woken;     // [E + ns]
+  int32_t *n_woken;   // [1]           woken experts, the shared one included
+  int32_t *offsets;   // [E + ns + 1]
+  int32_t *gather;    // [k_max * KS]  pair ids sorted by (expert, t)
   unsigned *router_cnt;  // [1]
   unsigned *err;         // [1] device error bits (DFV_DEVERR_*), sticky until cleared
   unsigned *sync;        // [4] fused kernel: grid-barrier count, exit ticket, abort flag
   unsigned *down_cnt;    // [ceil(d / 16)] one ticket per down tile
   unsigned *flags;       // [1024] mxfp4 single-launch kernel: per-CTA "gate/up work done" flags
   void *xn;           // [k_max][d] activations staged for the expert FFN (act dtype)
-  float *h;           // [k_max * K][d_ff]  SwiGLU activations, by sorted pair position
-                      // (fused kernel: bf16 hi [kK][d_ff] then bf16 lo [kK][d_ff])
-  float *ys;          // [k_max * K][d]     weighted expert outputs, by pair id
+  float *h;           // [k_max * KS][d_ff]  SwiGLU activations, by sorted pair position
+                      // (bf16 fused kernel: bf16 values, [k*KS][d_ff])
+  float *ys;          // [k_max * KS][d]     weighted expert outputs, by pair id
   void *xio;          // [k_max][d] host-variant input staging (4-byte elements)
   void *oio;          // [k_max][d] host-variant output staging
   size_t bytes;
@@ -48,6 +52,7 @@ struct RouterParams {
   const void *x;        // [k][d] act (input rows; when norm: residual stream)
   const void *wr;       // [E][d]
   int k, d, E, K, norm_topk, act, rdt;
+  int ns;               // 1: append the shared expert to the workspace tables
   int fuse_norm;        // 1: route RMSNorm(x) rounded to act, and stage it in ws.xn
   int stage_x;          // 1: copy x into ws.xn (block 0) for the FFN kernels
   float eps;
@@ -65,6 +70,7 @@ struct FfnParams {
   const void *residual; // [k][d] or null: added in the combine
   void *out;            // [k][d] act dtype
   int k, d, I, E, K, act;
+  int ns;               // 1: the tables end with the shared expert (pairs k*K + t)
   int swz_x;            // XOR swizzle mask for staged x rows (0 or 4)
   int swz_h;            // XOR swizzle mask for staged h rows (0 or 4)
   // TMA-staged kernels only
@@ -86,6 +92,7 @@ struct FusedParams {
   const void *wr, *wg, *wu, *wd;
   const uint8_t *sg, *su, *sd;  // mxfp4 experts: E8M0 scales (null for bf16)
   int k, d, I, E, K, norm_topk, fuse_norm, swz_x;
+  int ns;  // 1: one always-on shared expert, id E (pairs k*K + t, weight 1)
   float eps;
   int ks, nsl, slot, scratch, ring;  // filled from the plan
   int tma_mode;  // bf16 gate/up staging: 0 row bulk copies, 1 2-D tensor boxes, 2 one 3-D box per matrix
@@ -169,15 +176,20 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Row of pair q: routed pairs t*K+s, then the shared expert's pairs k*K+t.
+__device__ __forceinline__ int pair_token(int q, int k, int K) { return q < k * K ? q / K : q - k * K; }
+
 // ---------------------------------------------------------------- combine
-// out[t][r] = residual[t][r] + sum_s ys[t*K+s][r] (slot order) for rows
-// [r0, r0+rows) of every token, by threads tid = 0..nthr-1.
-__device__ __forceinline__ void combine_rows(const void *residual, void *out, const float *ys, int k, int K, int d,
-                                             int act, int r0, int rows, int tid, int nthr) {
+// out[t][r] = residual[t][r] + sum_s ys[t*K+s][r] (slot order) + ys[k*K+t][r]
+// (shared expert, when ns) for rows [r0, r0+rows) of every token, by threads
+// tid = 0..nthr-1.
+__device__ __forceinline__ void combine_rows(const void *residual, void *out, const float *ys, int k, int K, int ns,
+                                             int d, int act, int r0, int rows, int tid, int nthr) {
   for (int idx = tid; idx < k * rows; idx += nthr) {
     const int t = idx / rows, r = r0 + idx % rows;
     float s = 0.f;
     for (int sl = 0; sl < K; ++sl) s += __ldcg(ys + (size_t)(t * K + sl) * d + r);
+    if (ns) s += __ldcg(ys + (size_t)(k * K + t) * d + r);
     if (residual) s = load_act(residual, (size_t)t * d + r, act) + s;
     store_act(out, (size_t)t * d + r, act, s);
   }

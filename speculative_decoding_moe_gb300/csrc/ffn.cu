@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) gateup_bf16_kernel(FfnParams p) {
       e = p.ws.woken[wi];
       off = p.ws.offsets[wi];
       m = p.ws.offsets[wi + 1] - off;
-      if (tid < m) s_tok[tid] = p.ws.gather[off + tid] / K;
+      if (tid < m) s_tok[tid] = pair_token(p.ws.gather[off + tid], p.k, K);
       __syncthreads();
       for (int idx = tid; idx < m * cpr; idx += kThreads) {
         const int j = idx / cpr, q = idx % cpr;
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) down_bf16_kernel(FfnParams p) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem[];
-  const int d = p.d, I = p.I, K = p.K;
+  const int d = p.d, I = p.I;
   const int cpr = I / 8;
   uint4 *hh = reinterpret_cast<uint4 *>(smem);
   uint4 *hl = reinterpret_cast<uint4 *>(smem + (size_t)NT * 8 * I * 2);
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) gateup_f32_kernel(FfnParams p) {
     const int e = p.ws.woken[wi], off = p.ws.offsets[wi], m = p.ws.offsets[wi + 1] - off;
     const int rho = threadIdx.x >> 4, j = threadIdx.x & 15;  // 16 rows x 16 tokens
     if (rho < kGateTile && j < m) {
-      const int t = p.ws.gather[off + j] / K;
+      const int t = pair_token(p.ws.gather[off + j], p.k, K);
       const float *xr = x + (size_t)t * d;
       const float *gr = wg + ((size_t)e * I + i0 + rho) * d;
       const float *ur = wu + ((size_t)e * I + i0 + rho) * d;

@@ -19,8 +19,9 @@ __device__ __forceinline__ void unit_range(int U, int &lo, int &hi) {
   hi = (int)(((long long)(blockIdx.x + 1) * U) / gridDim.x);
 }
 
-// out[t][r] = residual[t][r] + sum_s ys[t*K+s][r], slot order, for the rows of
-// down tile dt (kDownTile rows).  Called by the last unit to finish that tile.
+// out[t][r] = residual[t][r] + sum_s ys[t*K+s][r], slot order, + ys[k*K+t][r]
+// (shared expert, when ns) for the rows of down tile dt (kDownTile rows).
+// Called by the last unit to finish that tile.
 __device__ __forceinline__ void combine_tile(const FfnParams &p, int dt) {
   const int r0 = dt * kDownTile;
   const int rows = min(kDownTile, p.d - r0);
@@ -30,13 +31,15 @@ __device__ __forceinline__ void combine_tile(const FfnParams &p, int dt) {
     const int r = r0 + rr;
     float s = 0.f;
     for (int sl = 0; sl < p.K; ++sl) s += __ldcg(p.ws.ys + (size_t)(t * p.K + sl) * p.d + r);
+    if (p.ns) s += __ldcg(p.ws.ys + (size_t)(p.k * p.K + t) * p.d + r);
     if (p.residual) s = load_act(p.residual, (size_t)t * p.d + r, p.act) + s;
     store_act(p.out, (size_t)t * p.d + r, p.act, s);
   }
 }
 
 // Ticket for tile dt after this CTA wrote its ys rows of that tile; the unit
-// that arrives last (of nW, one per woken expert) runs the combine and returns
+// that arrives last (of nW, one per woken expert, the shared one included)
+// runs the combine and returns
 // the ticket to zero.  Nothing waits.
 __device__ __forceinline__ void finish_down_unit(const FfnParams &p, int dt, int nW) {
   __shared__ unsigned s_last;

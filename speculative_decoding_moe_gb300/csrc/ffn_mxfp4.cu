@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kMxThreads) gateup_mxfp4_kernel(FfnParams p) {
       e = p.ws.woken[wi];
       off = p.ws.offsets[wi];
       m = p.ws.offsets[wi + 1] - off;
-      if (tid < m) s_tok[tid] = p.ws.gather[off + tid] / K;
+      if (tid < m) s_tok[tid] = pair_token(p.ws.gather[off + tid], p.k, K);
       __syncthreads();
       for (int j = warp; j < m; j += kMxWarps) {
         const uint16_t *src = xg + (size_t)s_tok[j] * d;

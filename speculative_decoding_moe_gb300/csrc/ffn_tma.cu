@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gateup_tma_kernel(FfnParams p)
       cur = wi;
       off = p.ws.offsets[wi];
       m = p.ws.offsets[wi + 1] - off;
-      if (tid < m) s_tok[tid] = p.ws.gather[off + tid] / K;
+      if (tid < m) s_tok[tid] = pair_token(p.ws.gather[off + tid], p.k, K);
       bar_sync_n(kBarConsumers, kConsumers);
       for (int idx = tid; idx < m * cpr; idx += kConsumers) {
         const int j = idx / cpr, q = idx % cpr;
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
     bar_sync_n(kBarConsumers, kConsumers);
     if (s_last) {
       __threadfence();
-      combine_rows(p.residual, p.out, p.ws.ys, p.k, K, d, p.act, r0, rows, tid, kConsumers);
+      combine_rows(p.residual, p.out, p.ws.ys, p.k, K, p.ns, d, p.act, r0, rows, tid, kConsumers);
       bar_sync_n(kBarConsumers, kConsumers);
       if (tid == 0) p.ws.down_cnt[dt] = 0u;
     }

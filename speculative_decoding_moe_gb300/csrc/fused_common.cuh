@@ -75,13 +75,16 @@ __device__ __forceinline__ void load8_bf16(const void *base, size_t elem, float 
 __device__ __forceinline__ float rnd_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 // Routing tables in the calling CTA's shared memory.
+// With a shared expert (p.ns = 1) the tables go on past the routed pairs: pair
+// k*K + t is row t's shared slot (expert E, weight 1), and E is the last woken
+// expert.
 struct RouteSmem {
-  int *idx;        // [k*K]    expert of pair t*K+s, by descending logit
-  float *w;        // [k*K]    routing weight of the pair
-  int *woken;      // [E]      ascending ids of the woken experts
-  int *off;        // [E+1]    per woken expert: first position in the sorted pair list
-  int *eoff;       // [E]      per expert id: first position in the sorted pair list
-  int *gat;        // [k*K]    pair ids sorted by (expert, token)
+  int *idx;        // [k*K + ns*k]  expert of pair t*K+s, by descending logit
+  float *w;        // [k*K + ns*k]  routing weight of the pair
+  int *woken;      // [E + ns]      ascending ids of the woken experts
+  int *off;        // [E + ns + 1]  per woken expert: first position in the sorted pair list
+  int *eoff;       // [E]           per routed expert id: first position in the sorted pair list
+  int *gat;        // [k*K + ns*k]  pair ids sorted by (expert, token)
   unsigned *mask;  // [kMaxBlock * E/32] experts chosen by each row
   float *inv;      // [kMaxBlock] 1/rms of each row (fuse_norm)
   int *wsum, *csum;  // [kFW] scan scratch
@@ -99,8 +102,9 @@ struct RouteSmem {
 //   P1  every CTA derives the whole routing decision itself from the logits:
 //       top-K per row (warp per row, redux max/min: largest logit, lowest id
 //       among equals), routing weights, woken union, per-expert pair offsets
-//       (block scan) and the (expert, token)-sorted pair list.  CTA 0 also
-//       publishes the decision to the workspace and the caller's copies.
+//       (block scan) and the (expert, token)-sorted pair list, then appends
+//       the shared expert (when p.ns).  CTA 0 also publishes the decision to
+//       the workspace and the routed part to the caller's copies.
 // `between` runs on the same threads after P0 and before grid barrier 1 (work
 // that needs neither the other CTAs' logits nor the routing decision).
 template <class Between>
@@ -285,18 +289,35 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     for (int t2 = 0; t2 < t; ++t2) rank += (r.mask[t2 * (kMaxExperts / 32) + (ex >> 5)] >> (ex & 31)) & 1u;
     r.gat[r.eoff[ex] + rank] = q;
   }
+  const int ns = p.ns ? 1 : 0, nP = k * K + ns * k, nE = E + ns;  // pairs, expert ids
+  if (ns) {
+    // the shared expert: the last woken expert (id E, above every routed id),
+    // selected by every row with weight 1
+    if (tid == 0) {
+      const int nW = *r.nw;
+      r.woken[nW] = E;
+      r.off[nW + 1] = nP;
+      *r.nw = nW + 1;
+    }
+    if (tid < k) {
+      r.idx[k * K + tid] = E;
+      r.w[k * K + tid] = 1.f;
+      r.gat[k * K + tid] = k * K + tid;
+    }
+  }
   bar_sync_n(kBarAll, kFC);
   // every index the later phases take from these tables is checked once here:
-  // woken ids ascending and < E, offsets rising by 1..k and ending at k*K,
-  // and every sorted pair id < k*K, filed under the expert it chose
+  // woken ids ascending and < E + ns, offsets rising by 1..k and ending at
+  // the pair count, and every sorted pair id below it, filed under the expert
+  // it chose
   {
     const int nW = *r.nw;
-    bool bad = tid == 0 && (nW < 1 || nW > E || nW > k * K || r.off[0] != 0 || r.off[nW] != k * K);
-    if (!bad && tid < nW && nW <= E) {
+    bool bad = tid == 0 && (nW < 1 || nW > nE || nW > k * K + ns || r.off[0] != 0 || r.off[nW] != nP);
+    if (!bad && tid < nW && nW <= nE) {
       const int e = r.woken[tid], m = r.off[tid + 1] - r.off[tid];
-      bad = e < 0 || e >= E || (tid > 0 && e <= r.woken[tid - 1]) || m < 1 || m > k;
+      bad = e < 0 || e >= nE || (tid > 0 && e <= r.woken[tid - 1]) || m < 1 || m > k;
     }
-    if (!bad && tid < k * K && nW >= 1 && nW <= E) {
+    if (!bad && tid < nP && nW >= 1 && nW <= nE) {
       const int q = r.gat[tid];
       // the expert whose pair range holds position tid
       int lo = 0, hi = nW - 1;
@@ -304,7 +325,7 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
         const int mid = (lo + hi + 1) >> 1;
         if (r.off[mid] <= tid) lo = mid; else hi = mid - 1;
       }
-      bad = q < 0 || q >= k * K || r.idx[q] != r.woken[lo];
+      bad = q < 0 || q >= nP || r.idx[q] != r.woken[lo];
     }
     if (bad) *r.bad = 1;
   }
@@ -317,15 +338,17 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     const int nW = *r.nw;
     for (int q = tid; q < k * K; q += kFC) {
       p.ws.topk_idx[q] = r.idx[q];
+      if (p.u_idx) p.u_idx[q] = r.idx[q];
+    }
+    for (int q = tid; q < nP; q += kFC) {
       p.ws.topk_w[q] = r.w[q];
       p.ws.gather[q] = r.gat[q];
-      if (p.u_idx) p.u_idx[q] = r.idx[q];
     }
     for (int i = tid; i < nW; i += kFC) { p.ws.woken[i] = r.woken[i]; p.ws.offsets[i] = r.off[i]; }
     if (tid == 0) {
       p.ws.offsets[nW] = r.off[nW];
       *p.ws.n_woken = nW;
-      if (p.u_nw) *p.u_nw = nW;
+      if (p.u_nw) *p.u_nw = nW - ns;  // the caller's count: routed experts only
     }
   }
 }

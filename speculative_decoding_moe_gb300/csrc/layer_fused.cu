@@ -18,7 +18,9 @@
 //       top-K per row (warp per row, redux max/min: largest logit, lowest id
 //       among equals), routing weights, woken union, per-expert pair offsets
 //       (block scan) and the (expert, token)-sorted pair list.  Each CTA
-//       checks these tables before any phase indexes with them.
+//       checks these tables before any phase indexes with them.  An
+//       always-on shared expert (same section) joins them as the last woken
+//       expert (id E), selected by every row with weight 1 (pairs k*K + t).
 //   P2  gate/up: unit = (woken expert, 8 d_ff rows).  The producer streams
 //       stages of 8 gate + 8 up rows x `ks` columns into an mbarrier ring
 //       (2-D tensor-map boxes of 256 columns by default; a 3-D box per matrix,
@@ -38,10 +40,10 @@
 //       waiting warps consumed (with one shared odd-sized ring, a group could
 //       pass a wait one phase early).
 //       -- grid barrier 3 --
-//   P4  every CTA sums ys over the K slots in slot order (+ the residual) for
-//       its share of the outputs.  No atomics on the output: the result of a
-//       token depends only on its own row, so a block and k single-token calls
-//       agree bit for bit.
+//   P4  every CTA sums ys over the K slots in slot order (then the shared
+//       slot, + the residual) for its share of the outputs.  No atomics on
+//       the output: the result of a token depends only on its own row, so a
+//       block and k single-token calls agree bit for bit.
 // Every wait is bounded (2 s) and reports through the workspace error word.
 #include <cstdio>
 #include <map>
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   prefetch_router_rows(p);
   pdl_wait();  // before this only the router-row prefetch touches global memory
   extern __shared__ __align__(128) unsigned char smem[];
-  const int k = p.k, d = p.d, I = p.I, E = p.E, K = p.K, ks = p.ks, nsl = p.nsl;
+  const int k = p.k, d = p.d, I = p.I, K = p.K, ks = p.ks, nsl = p.nsl;
   const int G = gridDim.x;
   const int rsg = fpad(ks * 2);        // gate/up stage row stride (64 mod 128: conflict-free)
   const int rsx = d * 2;               // staged x row stride (16B chunks XOR-swizzled)
@@ -90,12 +92,13 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   const uint32_t full0 = smem_u32(red + kFW * NT * 32 * 4);
   const uint32_t empty0 = full0 + 8 * kMaxRing;
 
-  __shared__ int s_idx[kMaxBlock * kMaxTopK];
-  __shared__ float s_w[kMaxBlock * kMaxTopK];
-  __shared__ int s_woken[kMaxExperts];
-  __shared__ int s_off[kMaxExperts + 1];
+  // routed pairs, then (with a shared expert) one shared pair per row
+  __shared__ int s_idx[kMaxBlock * (kMaxTopK + 1)];
+  __shared__ float s_w[kMaxBlock * (kMaxTopK + 1)];
+  __shared__ int s_woken[kMaxExperts + 1];
+  __shared__ int s_off[kMaxExperts + 2];
   __shared__ int s_eoff[kMaxExperts];
-  __shared__ int s_gat[kMaxBlock * kMaxTopK];
+  __shared__ int s_gat[kMaxBlock * (kMaxTopK + 1)];
   __shared__ unsigned s_mask[kMaxBlock * (kMaxExperts / 32)];
   __shared__ float s_inv[kMaxBlock];
   __shared__ int s_wsum[kFW], s_csum[kFW];
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
         cur = wi;
         off = s_off[wi];
         m = s_off[wi + 1] - off;
-        if (tid < m) s_tok[tid] = s_gat[off + tid] / K;
+        if (tid < m) s_tok[tid] = pair_token(s_gat[off + tid], p.k, p.K);
         bar_sync_n(kBarAll, kFC);
         for (int idx = tid; idx < m * cpr; idx += kFC) {
           const int j = idx / cpr, q = idx % cpr, t = s_tok[j];
@@ -419,7 +422,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
     dead = dead || s_abort != 0;
 
     // ---------------------------------------------------------------- P4: combine
-    // out[t] = residual[t] + sum_s ys[t*K+s], slot order, for this CTA's share of the outputs
+    // out[t] = residual[t] + sum_s ys[t*K+s], slot order, + ys[k*K+t] (shared
+    // expert), for this CTA's share of the outputs
     if (!dead) {
       const int n_out = k * d;
       const int o0 = (int)(((long long)blockIdx.x * n_out) / G), o1 = (int)(((long long)(blockIdx.x + 1) * n_out) / G);
@@ -427,6 +431,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
         const int t = o / d, r = o - t * d;
         float sum = 0.f;
         for (int sl = 0; sl < K; ++sl) sum += __ldcg(p.ws.ys + (size_t)(t * K + sl) * d + r);
+        if (p.ns) sum += __ldcg(p.ws.ys + (size_t)(k * K + t) * d + r);
         if (p.residual) sum = load_act(p.residual, (size_t)t * d + r, DFV_BF16) + sum;
         store_act(p.out, (size_t)t * d + r, DFV_BF16, sum);
       }
@@ -495,7 +500,7 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
   static std::mutex mu;
   static std::map<std::tuple<const void *, const void *, int, int, int, int, int>, Maps> cache;
   p->tma_mode = 0;
-  const int d = L->d, I = L->d_ff, E = L->n_experts, ks = plan.ks;
+  const int d = L->d, I = L->d_ff, E = L->n_experts + (L->n_shared ? 1 : 0), ks = plan.ks;  // the shared expert is the last
   if (d % 256 || ks % 256 || max_mode <= 0) return;
   const auto key = std::make_tuple(L->w_gate, L->w_up, d, I, E, ks, max_mode);
   {

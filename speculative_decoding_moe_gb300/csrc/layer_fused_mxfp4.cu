@@ -16,7 +16,9 @@
 // groups round-robin, so group q consumes stages q, q+4, q+8, ... (a group with
 // no unit left in a round gets an empty stage); no warp ever waits for another
 // warp's partial sums.
-//   P0, P1  routing, shared with the bf16 single-launch kernel (fused_route).
+//   P0, P1  routing, shared with the bf16 single-launch kernel (fused_route);
+//       an always-on shared expert ("What the pieces cost") joins the tables
+//       as the last woken expert, which every row selects with weight 1.
 //   P2  the k rows of x (after the optional RMSNorm, rounded to bf16) are
 //       staged once in shared memory as fp16, each multiplied by a power of
 //       two that puts its largest magnitude in [2^14, 2^15).  unit = (woken
@@ -37,8 +39,9 @@
 //       expert in the group's shared buffer as fp16 with their own
 //       power-of-two scales.  w[t,s] * y goes to ys[pair].
 //       -- grid barrier 2 --
-//   P4  every CTA sums ys over the K slots in slot order for its share of the
-//       output rows, adds the residual and writes them.  The sum order of
+//   P4  every CTA sums ys over the K slots in slot order (then the shared
+//       slot) for its share of the output rows, adds the residual and writes
+//       them.  The sum order of
 //       every output depends only on its own token, never on the block.
 // Every wait is bounded (2 s) and reports through the workspace error word.
 #include <cstdio>
@@ -117,12 +120,13 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   auto ld16 = [&](uint32_t a) { return *reinterpret_cast<const uint4 *>(smem + (a - sbase)); };
   auto ld1 = [&](uint32_t a) { return (uint32_t)smem[a - sbase]; };
 
-  __shared__ int s_idx[kMaxBlock * kMaxTopK];
-  __shared__ float s_w[kMaxBlock * kMaxTopK];
-  __shared__ int s_woken[kMaxExperts];
-  __shared__ int s_off[kMaxExperts + 1];
+  // routed pairs, then (with a shared expert) one shared pair per row
+  __shared__ int s_idx[kMaxBlock * (kMaxTopK + 1)];
+  __shared__ float s_w[kMaxBlock * (kMaxTopK + 1)];
+  __shared__ int s_woken[kMaxExperts + 1];
+  __shared__ int s_off[kMaxExperts + 2];
   __shared__ int s_eoff[kMaxExperts];
-  __shared__ int s_gat[kMaxBlock * kMaxTopK];
+  __shared__ int s_gat[kMaxBlock * (kMaxTopK + 1)];
   __shared__ unsigned s_mask[kMaxBlock * (kMaxExperts / 32)];
   __shared__ float s_inv[kMaxBlock];
   __shared__ float s_xinv[kMaxBlock];             // 2^-shift of each staged x row
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
     // B-row addresses of token column `n0 + g` of the expert at `off`
     auto x_rows = [&](int off, int m, int n0, uint32_t (&bt)[4]) {
       const int n = n0 + g;
-      const int t = s_gat[off + (n < m ? n : 0)] / K;  // past m: any valid row, discarded
+      const int t = pair_token(s_gat[off + (n < m ? n : 0)], p.k, p.K);  // past m: any valid row, discarded
       const int sw = ((c >> 1) & 1) | ((t & 1) << 1);
       const uint32_t b0 = xs + t * xrow + c * 64;
 #pragma unroll
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
         for (int q = 0; q < 2; ++q) {
           const int tok = 2 * c + q;
           if (tok < m) {
-            const float inv = s_xinv[s_gat[off + tok] / K];
+            const float inv = s_xinv[pair_token(s_gat[off + tok], p.k, p.K)];
             hf[(size_t)(off + tok) * I + i0 + g] = silu(acc[q] * inv) * (acc[q + 2] * inv);
           }
         }
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
           for (int q = 0; q < 2; ++q) {
             const int tok = 8 + 2 * c + q;
             if (tok < m) {
-              const float inv = s_xinv[s_gat[off + tok] / K];
+              const float inv = s_xinv[pair_token(s_gat[off + tok], p.k, p.K)];
               hf[(size_t)(off + tok) * I + i0 + g] = silu(a1s[q] * inv) * (a1s[q + 2] * inv);
             }
           }
@@ -567,6 +571,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
         const int t = o / d, rrow = o - t * d;
         float sum = 0.f;
         for (int sl = 0; sl < K; ++sl) sum += __ldcg(p.ws.ys + (size_t)(t * K + sl) * d + rrow);
+        if (p.ns) sum += __ldcg(p.ws.ys + (size_t)(k * K + t) * d + rrow);  // shared expert
         if (p.residual) sum = load_act(p.residual, (size_t)t * d + rrow, DFV_BF16) + sum;
         store_act(p.out, (size_t)t * d + rrow, DFV_BF16, sum);
       }
@@ -672,7 +677,7 @@ bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, siz
   static std::mutex mu;
   static std::map<std::tuple<const void *, const void *, const void *, const void *, int, int, int>, Maps> cache;
   const auto key = std::make_tuple(L->w_gate, L->w_up, (const void *)L->s_gate, (const void *)L->s_up, L->d, L->d_ff,
-                                   L->n_experts);
+                                   L->n_experts + (L->n_shared ? 1 : 0));
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -685,7 +690,7 @@ bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, siz
     }
   }
   Maps m;
-  const uint64_t rows = (uint64_t)L->n_experts * L->d_ff;
+  const uint64_t rows = (uint64_t)(L->n_experts + (L->n_shared ? 1 : 0)) * L->d_ff;  // the shared expert is the last
   if (!encode_2d(&m.wg, L->w_gate, L->d / 2, rows, kMxCols / 2, kMxRows, why, why_len) ||
       !encode_2d(&m.wu, L->w_up, L->d / 2, rows, kMxCols / 2, kMxRows, why, why_len) ||
       !encode_2d(&m.sg, L->s_gate, L->d / 32, rows, kMxCols / 32, kMxRows, why, why_len) ||

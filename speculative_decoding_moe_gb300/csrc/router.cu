@@ -13,7 +13,9 @@
 //      every row with a warp per row (redux.sync max on monotone float keys,
 //      ties to the lowest expert id), the routing weights, the woken-expert
 //      union (ascending), per-expert pair offsets (block-wide exclusive scan)
-//      and the pair gather list sorted by (expert, token).
+//      and the pair gather list sorted by (expert, token).  With an always-on
+//      shared expert (same section) it closes the workspace tables with that
+//      expert: id E, one pair k*K + t per row, weight 1.
 #include "dfv_internal.cuh"
 
 namespace dfv {
@@ -265,6 +267,20 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
     p.ws.topk_w[q] = s_sel[q];
     if (p.u_idx) p.u_idx[q] = ex;
     if (p.u_w) p.u_w[q] = s_sel[q];
+  }
+  if (p.ns) {
+    // the shared expert joins the workspace tables (not the caller's copies)
+    // as the last woken expert, id E: every row selects it, pair k*K + t,
+    // weight 1
+    if (tid == 0) {
+      p.ws.woken[nW] = E;
+      p.ws.offsets[nW + 1] = k * K + k;
+      *p.ws.n_woken = nW + 1;
+    }
+    for (int t = tid; t < k; t += kRouterThreads) {
+      p.ws.gather[k * K + t] = k * K + t;
+      p.ws.topk_w[k * K + t] = 1.f;
+    }
   }
   if (tid == 0) *p.ws.router_cnt = 0u;
 }

@@ -42,7 +42,7 @@ class CLayer(ctypes.Structure):
         ("w_dtype", ctypes.c_int), ("r_dtype", ctypes.c_int),
         ("w_router", ctypes.c_void_p), ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
         ("w_down", ctypes.c_void_p), ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p),
-        ("s_down", ctypes.c_void_p),
+        ("s_down", ctypes.c_void_p), ("n_shared", ctypes.c_int),
     ]
 
 
@@ -119,13 +119,16 @@ class Layer:
             if not t.is_cuda or not t.is_contiguous():
                 raise ValueError("layer weights must be contiguous CUDA tensors")
         s = w.shape
+        if w.w_gate.shape[0] != s.n_experts + s.n_shared:
+            raise ValueError("expert matrices hold %d experts, the shape needs %d routed + %d shared"
+                             % (w.w_gate.shape[0], s.n_experts, s.n_shared))
         self.w = w
         self.shape = s
         self.c = CLayer(s.d, s.n_experts, s.top_k, s.d_ff, s.norm_topk, _NAMES[s.w_dtype], _NAMES[s.r_dtype],
                         w.w_router.data_ptr(), w.w_gate.data_ptr(), w.w_up.data_ptr(), w.w_down.data_ptr(),
                         None if w.s_gate is None else w.s_gate.data_ptr(),
                         None if w.s_up is None else w.s_up.data_ptr(),
-                        None if w.s_down is None else w.s_down.data_ptr())
+                        None if w.s_down is None else w.s_down.data_ptr(), s.n_shared)
 
     @property
     def ref(self):

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     L = lib.lib()
-    assert L.dfv_version() == 1
+    assert L.dfv_version() == 2
     assert L.dfv_status_string(0) == b"DFV_OK"
     assert L.dfv_status_string(3) == b"DFV_ERR_WORKSPACE"
 
@@ -48,7 +48,7 @@ def _layer(lib, **kw):
     c.update(kw)
     sc = c.get("scales", (None, None, None))
     return lib.CLayer(c["d"], c["n_experts"], c["top_k"], c["d_ff"], c["norm_topk"], c["w_dtype"], c["r_dtype"],
-                      c["w_router"], c["w_gate"], c["w_up"], c["w_down"], *sc)
+                      c["w_router"], c["w_gate"], c["w_up"], c["w_down"], *sc, c.get("n_shared", 0))
 
 
 def test_workspace_sizes(lib):
@@ -61,6 +61,11 @@ def test_workspace_sizes(lib):
     assert L.dfv_moe_workspace_size(ctypes.byref(ly), 17) == 0
     assert L.dfv_accept_workspace_size(16, 151936) > 0
     assert L.dfv_accept_workspace_size(17, 151936) == 0
+    # a shared expert adds one pair slot per row: K+1 rows of h and ys per token
+    sh = L.dfv_moe_workspace_size(ctypes.byref(_layer(lib, n_shared=1)), 16)
+    assert sh - s16 >= 16 * (2048 + 768) * 4
+    assert L.dfv_moe_workspace_size(ctypes.byref(_layer(lib, n_shared=2)), 16) == 0
+    assert L.dfv_moe_workspace_size(ctypes.byref(_layer(lib, n_shared=-1)), 16) == 0
 
 
 @pytest.mark.parametrize("kw,k,status", [
@@ -77,6 +82,8 @@ def test_workspace_sizes(lib):
     (dict(w_dtype=2, d=2080, scales=(0x81000, 0x82000, 0x83000)), 4, 2),   # mxfp4 needs d % 64
     (dict(w_dtype=2, d_ff=736, scales=(0x81000, 0x82000, 0x83000)), 4, 2),  # and d_ff % 64
     (dict(w_dtype=2, r_dtype=0, scales=(0x81000, 0x82000, 0x83000)), 4, 2),  # fp32 router with mxfp4
+    (dict(n_shared=2), 4, 2),            # at most one shared expert
+    (dict(n_shared=-1), 4, 1),
 ])
 def test_invalid_arguments_are_rejected_before_launch(lib, kw, k, status):
     L = lib.lib()
