@@ -47,7 +47,7 @@ KERNEL_SOURCES = {
     "moe_fused_mx_kernel": ["layer_fused_mxfp4.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
 }
 NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
-    "moe_fused_kernel": ("45560a9ea2821278", 728468736 + 6998528, 77 * 9437184 + 524288),
+    "moe_fused_kernel": ("2f82a8ae8f35161b", 728471040 + 7303680, 77 * 9437184 + 524288),
     "moe_fused_mx_kernel": ("de3c38d03fce886d", 171788032 + 6460416, 102 * 1671168 + 1048576),
 }
 

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   __shared__ float s_inv[kMaxBlock];
   __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_tok[16];
-  __shared__ int s_nw, s_ring;
+  __shared__ int s_nw, s_ring, s_split;
   __shared__ volatile int s_abort, s_bad;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -124,12 +124,19 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
     const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort, &s_bad};
     fused_route(p, rs, [] {});
     if (tid == 0) {
-      // with at most 8 tokens per expert the staged-x rows 8..15 are unused:
-      // they become one more ring stage
+      // with at most 8 tokens per gate/up entry the staged-x rows 8..15 are
+      // unused: they become one more ring stage.  A shared expert with more
+      // than 8 tokens then enters gate/up as two entries (its rows 0-7 and
+      // 8-15), which reads its gate/up rows twice but keeps that stage.
       int mmax = 0;
       const int nw0 = s_abort ? 0 : s_nw;  // one read of the volatile flag, not one per expert
-      for (int i = 0; i < nw0; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
-      s_ring = (NT == 2 && mmax <= 8 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing) ? SH + 1 : SH;
+      const int nr = nw0 - ((p.ns && nw0 > 0) ? 1 : 0);  // routed experts
+      for (int i = 0; i < nr; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
+      const bool extra = NT == 2 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing;
+      const bool split = extra && p.ns && nw0 > 0 && k > 8 && mmax <= 8;
+      if (p.ns && nw0 > 0 && !split) mmax = max(mmax, k);
+      s_split = split ? 1 : 0;
+      s_ring = (extra && mmax <= 8) ? SH + 1 : SH;
     }
   }
   __syncthreads();  // routing tables visible to the producer
@@ -143,7 +150,9 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   const int tiles_g = I / kGateTile;
   int lo_g, hi_g;
   {
-    const int U = nW * tiles_g;
+    // gate/up entries: the woken experts, the shared one (last) possibly as
+    // two halves of 8 tokens
+    const int U = (nW + (nW > 0 ? s_split : 0)) * tiles_g;
     lo_g = (int)(((long long)blockIdx.x * U) / G);
     hi_g = (int)(((long long)(blockIdx.x + 1) * U) / G);
   }
@@ -168,7 +177,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       uint32_t pbits = 0, used = 0;
       bool ok = true;
       for (int u = lo_g; u < hi_g && ok; ++u) {
-        const int e = s_woken[u / tiles_g], i0 = (u % tiles_g) * kGateTile;
+        const int wi = u / tiles_g, i0 = (u % tiles_g) * kGateTile;
+        const int e = s_woken[wi < s_nw ? wi : s_nw - 1];  // the second half: the shared expert again
         for (int sl = 0; sl < nsl; ++sl, ps = (ps + 1 == S) ? 0 : ps + 1) {
           const int s = ps;
           if (!mbar_wait_fast(empty0 + 8 * s, ((pbits >> s) & 1u) ^ 1u, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
@@ -239,8 +249,14 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       if (wi != cur) {
         bar_sync_n(kBarAll, kFC);
         cur = wi;
-        off = s_off[wi];
-        m = s_off[wi + 1] - off;
+        const int nr = s_nw - p.ns;  // routed experts; the shared one follows them
+        if (wi < nr || !s_split) {
+          off = s_off[wi];
+          m = s_off[wi + 1] - off;
+        } else {  // half wi - nr of the shared expert's k tokens
+          off = s_off[nr] + 8 * (wi - nr);
+          m = wi > nr ? p.k - 8 : 8;
+        }
         if (tid < m) s_tok[tid] = pair_token(s_gat[off + tid], p.k, p.K);
         bar_sync_n(kBarAll, kFC);
         for (int idx = tid; idx < m * cpr; idx += kFC) {
