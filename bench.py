@@ -189,9 +189,32 @@ class OracleSample:
         return total_bytes / total_s / 1e9, calls, total_s
 
 
+def oracle_stack_sample(ols, d: int, n_threads: int, n_total: int = 40, V: int = 151936):
+    """The oracle's pre-norm stack over the given layers at k=16 plus greedy
+    acceptance on [k+1, V] logits, timed once; the stack time is scaled to
+    `n_total` layers (every layer costs the same work at a fixed woken count)."""
+    import oracle
+    from speculative_decoding_moe_gb300 import inputs
+    from tests._util import np_of
+    x = np_of(inputs.make_hidden(KBLOCK, d, "bf16", seed=9400))
+    t0 = time.perf_counter()
+    oracle.stack_forward(ols, x, nthreads=n_threads)
+    t_stack = time.perf_counter() - t0
+    lg, toks = inputs.spiked_logits(KBLOCK + 1, V, "bf16", 2.0, seed=9401)
+    draft = toks[:KBLOCK].contiguous().numpy()
+    t0 = time.perf_counter()
+    tau, _ = oracle.accept_greedy(np_of(lg), draft)
+    t_acc = time.perf_counter() - t0
+    return {"layers_timed": len(ols), "stack_ms": t_stack * 1e3, "accept_ms": t_acc * 1e3, "tau": tau,
+            "threads": n_threads, "stack%d_accept_ms_extrapolated" % n_total:
+                t_stack * 1e3 * n_total / len(ols) + t_acc * 1e3}
+
+
 def cpu_baseline_line(budget_s: float):
     """`cpu_baseline`: the oracle at k=16 on every host thread (the headline, about
-    `budget_s` seconds), plus shorter samples single-threaded and at k=1."""
+    `budget_s` seconds), plus shorter samples single-threaded and at k=1, and the
+    40-layer stack + acceptance of the bf16 and mxfp4 layers, timed on two
+    layers and scaled."""
     nthr = host_threads()
     smp = OracleSample()
     gbs, calls, secs = smp.run(nthr, budget_s)
@@ -200,6 +223,11 @@ def cpu_baseline_line(budget_s: float):
         g, c, t = smp.run(nt, budget_s / 4, k=k)
         side[name] = {"value": g, "unit": "GB/s", "threads": nt, "k": k, "calls": c,
                       "us_per_layer": t / c * 1e6}
+    from speculative_decoding_moe_gb300 import inputs
+    from tests._util import oracle_layer
+    side["stack_bf16"] = oracle_stack_sample(smp.ols, inputs.A3B.d, nthr)
+    mx = [oracle_layer(inputs.make_layer(inputs.MXFP4, seed=9500 + i)) for i in range(2)]
+    side["stack_mxfp4"] = oracle_stack_sample(mx, inputs.MXFP4.d, nthr)
     return {"value": gbs, "unit": "GB/s", "cores": nthr, "kind": "oracle",
             "us_per_layer": secs / calls * 1e6,
             "sample": "%d Qwen3-A3B-like layer call(s) at k=16 over 2 layers (oracle moe_forward, fp64, "

@@ -55,4 +55,8 @@ def test_cpu_baseline_reports_all_threads_one_thread_and_k1():
     assert side["k16_1thread"]["threads"] == 1 and side["k16_1thread"]["k"] == bench.KBLOCK
     assert side["k1_all_threads"]["k"] == 1 and side["k1_all_threads"]["threads"] == line["cores"]
     assert side["k1_1thread"]["threads"] == 1 and side["k1_1thread"]["k"] == 1
-    assert all(v["calls"] >= 1 and v["value"] > 0 for v in side.values())
+    assert all(side[n]["calls"] >= 1 and side[n]["value"] > 0 for n in ("k16_1thread", "k1_all_threads", "k1_1thread"))
+    for n in ("stack_bf16", "stack_mxfp4"):
+        st = side[n]
+        assert st["layers_timed"] == 2 and st["tau"] == bench.KBLOCK + 1  # every planted draft token matches
+        assert st["stack40_accept_ms_extrapolated"] == pytest.approx(20 * st["stack_ms"] + st["accept_ms"])
