@@ -296,6 +296,21 @@ const char *dfv_fused_unavailable_reason(void);
 int dfv_accept_greedy_noalloc(const void *logits, int dtype, int k, int V, const int32_t *draft,
                               int32_t *tau, int32_t *committed, void *stream);
 
+/*
+ * Self-test of the device-side bounded waits (no counterpart on the method's
+ * pages).  One launch of one thread waits on an mbarrier phase that nothing
+ * completes, then on a grid barrier that its single CTA can never fill.  Both
+ * are the waits the single-launch kernels use, with their limit (2 s): each
+ * gives up, sets its bit in the workspace error word (DFV_DEVERR_STAGE_WAIT,
+ * DFV_DEVERR_GRID_WAIT) and returns.  The call takes about 4 s of GPU time;
+ * no copy is in flight when a wait gives up, and the context stays usable.
+ * Read the word with dfv_read_device_error, then zero-fill the workspace
+ * before other calls use it.
+ *   ws  a zero-filled workspace of any dfv_moe_workspace_size() (the
+ *       counters sit in its first 8 KB).
+ */
+int dfv_selftest_bounded_waits(void *ws, size_t ws_bytes, void *stream);
+
 const char *dfv_status_string(int status);
 const char *dfv_last_error_detail(void);
 int dfv_version(void);

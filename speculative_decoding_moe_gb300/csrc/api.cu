@@ -10,6 +10,10 @@
 
 #include "dfv_internal.cuh"
 
+namespace dfv {
+cudaError_t launch_wait_selftest(const Workspace &w, cudaStream_t s);  // selftest.cu
+}
+
 namespace {
 
 thread_local std::string g_detail;
@@ -466,6 +470,22 @@ int dfv_last_staging(void) { return g_last_staging; }
 int dfv_set_path(int path) {
   if (path != 0 && path != 1) return fail(DFV_ERR_INVALID_ARG, "path must be 0 (multi-kernel) or 1 (fused)");
   g_fused_enabled = path == 1;
+  return DFV_OK;
+}
+
+int dfv_selftest_bounded_waits(void *ws, size_t ws_bytes, void *stream) {
+  if (!ws) return fail(DFV_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(DFV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  // the counters sit at fixed offsets, the same for every layer up to d = 13312
+  dfv_moe_layer probe = {};
+  probe.d = 32;
+  probe.n_experts = 1;
+  probe.top_k = 1;
+  probe.d_ff = 32;
+  const size_t need = layout(&probe, 1, nullptr).bytes;
+  if (ws_bytes < need) return fail(DFV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  cudaError_t e = dfv::launch_wait_selftest(layout(&probe, 1, ws), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test launch");
   return DFV_OK;
 }
 

@@ -24,7 +24,7 @@ EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_pro
            "dfv_accept_greedy_noalloc", "dfv_set_staging", "dfv_last_staging",
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
-           "dfv_accept_workspace_size", "dfv_accept_greedy")
+           "dfv_accept_workspace_size", "dfv_accept_greedy", "dfv_selftest_bounded_waits")
 
 
 class DfvError(RuntimeError):
@@ -72,6 +72,7 @@ def _load():
         L.dfv_profile_set_events.argtypes = [P, I]
         L.dfv_accept_greedy_noalloc.argtypes = [P, I, I, I, P, P, P, P]
         L.dfv_read_device_error.argtypes = [P, P, P]
+        L.dfv_selftest_bounded_waits.argtypes = [P, S, P]
         L.dfv_set_path.argtypes = [I]
         L.dfv_set_staging.restype = I
         L.dfv_set_staging.argtypes = [I]
@@ -226,6 +227,13 @@ def read_device_error(ws: torch.Tensor, stream=None) -> int:
     _check(_load().dfv_read_device_error(_p(ws), ctypes.byref(out), _stream(stream)), "dfv_read_device_error")
     (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return int(out.value)
+
+
+def selftest_bounded_waits(ws: torch.Tensor, stream=None):
+    """Run the bounded-wait self-test on `ws` (about 4 s on the GPU; read the
+    error word with read_device_error, then zero-fill ws)."""
+    _check(_load().dfv_selftest_bounded_waits(_p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "dfv_selftest_bounded_waits")
 
 
 def set_staging(max_mode: int):
