@@ -295,9 +295,11 @@ def progress(msg: str):
     print("[bench] %s" % msg, file=sys.stderr, flush=True)
 
 
-def graph_time(fn, warmup: int, steps: int, barrier=None, sampler=None):
+def graph_time(fn, warmup: int, steps: int, barrier=None, sampler=None, per_step=None):
     """Capture one step into a CUDA graph, replay `warmup` untimed then `steps`
-    timed replays bracketed by CUDA events; returns ms per step."""
+    timed replays bracketed by CUDA events; returns ms per step.  With a list
+    `per_step`, an event between consecutive replays also gives each step's
+    own time (appended to the list, in ms)."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -313,17 +315,30 @@ def graph_time(fn, warmup: int, steps: int, barrier=None, sampler=None):
     if barrier:
         barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps - 1)] if per_step is not None else []
     ctx = sampler if sampler is not None else _Null()
     with ctx:
         a.record()
-        for _ in range(steps):
+        for i in range(steps):
             g.replay()
+            if mids and i < steps - 1:
+                mids[i].record()
         b.record()
         b.synchronize()
     torch.cuda.synchronize()
     if barrier:
         barrier()
+    if per_step is not None:
+        marks = [a] + mids + [b]
+        per_step.extend(marks[i].elapsed_time(marks[i + 1]) for i in range(steps))
     return a.elapsed_time(b) / steps
+
+
+def spread_us(per_step_ms, per: int):
+    """Median, p10 and p90 of per-step times, in µs per `per` (e.g. per layer)."""
+    v = sorted(x * 1e3 / per for x in per_step_ms)
+    q = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]
+    return {"median": statistics.median(v), "p10": q(0.1), "p90": q(0.9), "steps": len(v)}
 
 
 class _Null:
@@ -393,7 +408,8 @@ def run_gpu(args):
     progress("headline k=16")
     fn16, nw16 = make_pass(KBLOCK)
     sampler = ClockSampler(local)
-    ms16 = graph_time(fn16, args.warmup, args.steps, barrier, sampler)
+    steps16 = []
+    ms16 = graph_time(fn16, args.warmup, args.steps, barrier, sampler, per_step=steps16)
     clocks = sampler.summary()
     bytes16, W16 = pass_bytes(nw16)
     ms_max = max_over_ranks(ms16, dev)
@@ -526,6 +542,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and hidden rows)",
         "config": dict(workload_config(), weights_gb=round(N_LAYERS * (exp_bytes * 128 + router_bytes) / 1e9, 2)),
+        "layer_us_spread_k16": spread_us(steps16, N_LAYERS),
         "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS,
                      "k16_multi_kernel": ms16_multi * 1e3 / N_LAYERS,
                      "k16_stream": ms16_stream * 1e3 / N_LAYERS, "k1_stream": ms1_stream * 1e3 / N_LAYERS},

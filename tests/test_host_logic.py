@@ -60,3 +60,14 @@ def test_cpu_baseline_reports_all_threads_one_thread_and_k1():
         st = side[n]
         assert st["layers_timed"] == 2 and st["tau"] == bench.KBLOCK + 1  # every planted draft token matches
         assert st["stack40_accept_ms_extrapolated"] == pytest.approx(20 * st["stack_ms"] + st["accept_ms"])
+
+
+def test_spread_is_per_layer_percentiles():
+    sys.path.insert(0, ROOT)
+    import bench
+    per_step_ms = [4.0, 5.0, 6.0, 5.5, 5.2, 4.8, 5.1, 5.0, 4.9, 7.0]  # 40-layer steps
+    s = bench.spread_us(per_step_ms, 40)
+    assert s["steps"] == 10
+    assert s["median"] == pytest.approx(126.25)       # (5.0 + 5.1) / 2 ms over 40 layers, in µs
+    assert s["p10"] == pytest.approx(120.0) and s["p90"] == pytest.approx(150.0)
+    assert s["p10"] <= s["median"] <= s["p90"]
