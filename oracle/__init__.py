@@ -35,7 +35,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-F32, BF16, MXFP4 = 0, 1, 2
+F32, BF16, MXFP4, Q8 = 0, 1, 2, 3
 _lib = None
 
 
@@ -81,6 +81,8 @@ def lib():
         L.orc_e2m1_value.argtypes = [I]
         L.orc_e8m0_value.restype = D
         L.orc_e8m0_value.argtypes = [I]
+        L.orc_fp16_to_double.restype = D
+        L.orc_fp16_to_double.argtypes = [ctypes.c_uint16]
         L.orc_silu.restype = D
         L.orc_silu.argtypes = [D]
         L.orc_decode_rows.argtypes = [I, P, P, I, I, I, P]
@@ -118,7 +120,8 @@ class Layer:
 
     bf16 arrays hold raw uint16 bit patterns; mxfp4 matrices hold packed
     nibbles (uint8, low nibble = even column) plus e8m0 scales (uint8, one per
-    32 consecutive elements of a row).
+    32 consecutive elements of a row); q8 matrices hold int8 codes plus one
+    float16 scale per 32 consecutive elements of a row.
     """
     d: int
     n_experts: int
@@ -161,6 +164,10 @@ def e2m1_value(code: int) -> float:
 
 def e8m0_value(e: int) -> float:
     return lib().orc_e8m0_value(int(e))
+
+
+def fp16_to_double(bits: int) -> float:
+    return lib().orc_fp16_to_double(int(bits))
 
 
 def silu(z: float) -> float:

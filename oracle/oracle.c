@@ -65,6 +65,18 @@ double orc_e8m0_value(int e) {
   return ldexp(1.0, e - 127);
 }
 
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits; exponent 0 holds zero and the subnormals (fraction * 2^-24), exponent
+ * 31 infinity and NaN.  Every value widens exactly to double. */
+double orc_fp16_to_double(uint16_t bits) {
+  int sign = bits >> 15, e = (bits >> 10) & 31, f = bits & 1023;
+  double m;
+  if (e == 0) m = ldexp((double)f, -24);
+  else if (e == 31) m = f ? NAN : INFINITY;
+  else m = ldexp((double)(1024 + f), e - 25);
+  return sign ? -m : m;
+}
+
 double orc_silu(double z) { return z / (1.0 + exp(-z)); }
 
 int orc_decode_rows(int dtype, const void *data, const uint8_t *scales,
@@ -84,6 +96,14 @@ int orc_decode_rows(int dtype, const void *data, const uint8_t *scales,
         int code = (c & 1) ? (byte >> 4) : (byte & 15);
         int s = scales[row * (cols / 32) + c / 32];
         v = orc_e2m1_value(code) * orc_e8m0_value(s);
+      } else if (dtype == ORC_Q8) {
+        /* 8-bit weights, read as llama.cpp's Q8_0 block: 32 int8 codes of a
+         * row share one binary16 scale (codes and scales kept in two arrays,
+         * like the mxfp4 ones) */
+        if (!scales || cols % 32) return -1;
+        int code = ((const int8_t *)data)[row * cols + c];
+        uint16_t s = ((const uint16_t *)scales)[row * (cols / 32) + c / 32];
+        v = (double)code * orc_fp16_to_double(s);
       } else {
         return -1;
       }

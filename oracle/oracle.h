@@ -28,7 +28,10 @@
  * Array conventions: row-major, contiguous.  dtype codes below.  bf16 arrays
  * are passed as their raw 16-bit patterns.  mxfp4 matrices are passed as
  * packed nibbles [rows][cols/2] (low nibble = even column) plus one e8m0 scale
- * byte per 32 consecutive elements of a row, [rows][cols/32].
+ * byte per 32 consecutive elements of a row, [rows][cols/32].  q8 matrices are
+ * passed as int8 codes [rows][cols] plus one IEEE binary16 scale per 32
+ * consecutive elements of a row, [rows][cols/32] (through the `scales`
+ * pointer); element value = code * scale.
  */
 #ifndef DFV_ORACLE_H
 #define DFV_ORACLE_H
@@ -38,7 +41,7 @@
 extern "C" {
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_MXFP4 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_MXFP4 = 2, ORC_Q8 = 3 };
 
 typedef struct {
   int d, n_experts, top_k, d_ff, norm_topk;
@@ -57,6 +60,7 @@ double   orc_bf16_to_double(uint16_t bits);
 uint16_t orc_double_to_bf16(double v);          /* round to nearest, ties to even */
 double   orc_e2m1_value(int code);              /* 4-bit code -> value */
 double   orc_e8m0_value(int e);                 /* 2^(e-127) */
+double   orc_fp16_to_double(uint16_t bits);     /* IEEE binary16, exact */
 double   orc_silu(double z);
 
 /* decode rows [r0, r0+nrows) of a (possibly mxfp4) matrix with `cols` columns */

@@ -29,7 +29,7 @@ from typing import Optional
 
 import torch
 
-DTYPES = ("f32", "bf16", "mxfp4")
+DTYPES = ("f32", "bf16", "mxfp4", "q8")
 
 
 @dataclass(frozen=True)
@@ -38,7 +38,7 @@ class LayerShape:
     n_experts: int
     top_k: int
     d_ff: int
-    w_dtype: str = "bf16"      # expert weights: f32 | bf16 | mxfp4
+    w_dtype: str = "bf16"      # expert weights: f32 | bf16 | mxfp4 | q8
     r_dtype: str = "bf16"      # router weights: f32 | bf16
     act: str = "bf16"          # activations:    f32 | bf16
     w_std: float = 0.02
@@ -74,6 +74,8 @@ class LayerWeights:
     mxfp4:    w_gate, w_up uint8 [E', d_ff, d/2]; w_down uint8 [E', d, d_ff/2]
               (low nibble = even column) and s_* uint8 e8m0 scales
               [E', rows, cols/32].
+    q8:       w_gate, w_up int8 [E', d_ff, d]; w_down int8 [E', d, d_ff] and
+              s_* float16 scales [E', rows, cols/32].
     E' = E + n_shared: the shared expert, if any, is the last one.  The
     router is [E, d].
     """
@@ -130,6 +132,22 @@ def make_layer(shape: LayerShape, seed: int, device="cpu") -> LayerWeights:
         wg, sg = codes(I, d), scales(I, d)
         wu, su = codes(I, d), scales(I, d)
         wd, sd = codes(d, I), scales(d, I)
+        return LayerWeights(shape, wr, wg, wu, wd, sg, su, sd)
+    if shape.w_dtype == "q8":
+        assert d % 32 == 0 and I % 32 == 0
+
+        def q8_codes(rows, cols):
+            return torch.randint(-127, 128, (E, rows, cols), generator=g, device=device, dtype=torch.int32).to(torch.int8)
+
+        def q8_scales(rows, cols):
+            # codes uniform over [-127, 127] spread about 73.3; scales around
+            # w_std / 73.3 give weights of about the other layers' spread
+            u = torch.rand(E, rows, cols // 32, generator=g, device=device)
+            return (shape.w_std / 73.3 * (0.5 + u)).to(torch.float16)
+
+        wg, sg = q8_codes(I, d), q8_scales(I, d)
+        wu, su = q8_codes(I, d), q8_scales(I, d)
+        wd, sd = q8_codes(d, I), q8_scales(d, I)
         return LayerWeights(shape, wr, wg, wu, wd, sg, su, sd)
     raise ValueError(shape.w_dtype)
 

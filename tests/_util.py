@@ -8,7 +8,7 @@ import torch
 import oracle
 from speculative_decoding_moe_gb300 import inputs
 
-_CODE = {"f32": oracle.F32, "bf16": oracle.BF16, "mxfp4": oracle.MXFP4}
+_CODE = {"f32": oracle.F32, "bf16": oracle.BF16, "mxfp4": oracle.MXFP4, "q8": oracle.Q8}
 
 
 def np_of(t: torch.Tensor) -> np.ndarray:

@@ -83,6 +83,56 @@ def test_mxfp4_decode_packing_and_scales_exhaustive():
     assert got[0] == -12.0 and got[1] == 2.0
 
 
+def test_fp16_widening_matches_numpy_for_every_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.fp16_to_double(int(b)) for b in bits])
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+    assert math.copysign(1.0, oracle.fp16_to_double(0x8000)) == -1.0
+
+
+def test_q8_decode_codes_and_scales_exhaustive():
+    # 8-bit weights read as llama.cpp's Q8_0 block: 32 int8 codes of a row share
+    # one binary16 scale.  Row r holds all 256 codes in 8 blocks, each with its
+    # own scale (subnormal, negative, large), so a wrong block index or a code
+    # read unsigned shows
+    scale_bits = np.array([0x3C00, 0x0001, 0x03FF, 0xB800, 0x7BFF, 0x1A3D, 0x2E66, 0x0400], dtype=np.uint16)
+    codes = np.arange(-128, 128, dtype=np.int16).astype(np.int8).reshape(1, 256)
+    for shift in range(8):  # rotate the scales over the blocks
+        sc = np.roll(scale_bits, shift).reshape(1, 8).view(np.float16)
+        got = oracle.decode_rows(oracle.Q8, codes, sc, 0, 1, 256)[0]
+        want = codes[0].astype(np.float64) * np.repeat(sc[0].astype(np.float64), 32)
+        assert np.array_equal(got, want)
+
+
+def test_q8_layer_equals_the_bf16_layer_of_the_same_values():
+    # codes times a per-block power of two (2^-7 .. 2^-9) are exact in bf16, so
+    # the q8 layer and the bf16 layer holding the decoded values must agree
+    # exactly: this ties the q8 layout (rows, blocks along a row, the down
+    # matrix's transposed shape) to the already-pinned bf16 path
+    d, E, K, I = 128, 6, 2, 64
+    g = torch.Generator().manual_seed(21)
+
+    def pair(rows, cols):
+        q = torch.randint(-127, 128, (E, rows, cols), generator=g, dtype=torch.int32).to(torch.int8)
+        ex = torch.randint(7, 10, (E, rows, cols // 32), generator=g)
+        sc = torch.pow(2.0, -ex.double()).to(torch.float16)
+        val = q.double() * sc.double().repeat_interleave(32, dim=2)
+        return q, sc, val.to(torch.bfloat16)
+
+    (qg, sg, vg), (qu, su, vu), (qd, sd, vd) = pair(I, d), pair(I, d), pair(d, I)
+    assert torch.equal(vg.double(), qg.double() * sg.double().repeat_interleave(32, dim=2))
+    wr = (torch.randn(E, d, generator=g) * 0.05).to(torch.bfloat16)
+    s8 = inputs.LayerShape(d=d, n_experts=E, top_k=K, d_ff=I, w_dtype="q8")
+    s16 = inputs.LayerShape(d=d, n_experts=E, top_k=K, d_ff=I, w_dtype="bf16")
+    l8 = oracle_layer(inputs.LayerWeights(s8, wr, qg, qu, qd, sg, su, sd))
+    l16 = oracle_layer(inputs.LayerWeights(s16, wr, vg, vu, vd))
+    x = np_of(inputs.make_hidden(5, d, "bf16", seed=22))
+    a, b = oracle.moe_forward(l8, x), oracle.moe_forward(l16, x)
+    assert np.array_equal(a, b) and np.abs(a).max() > 0
+
+
 def test_silu_closed_forms():
     # logistic(ln 3) = 3/4, logistic(-ln 3) = 1/4
     assert oracle.silu(0.0) == 0.0
@@ -365,7 +415,7 @@ def test_shared_expert_is_independent_of_routing():
 
 
 @pytest.mark.parametrize("n_shared", [0, 1])
-@pytest.mark.parametrize("w_dtype", ["f32", "bf16", "mxfp4"])
+@pytest.mark.parametrize("w_dtype", ["f32", "bf16", "mxfp4", "q8"])
 def test_block_equals_row_by_row_decode(w_dtype, n_shared):
     shape = inputs.LayerShape(d=128, n_experts=12, top_k=3, d_ff=64, w_dtype=w_dtype,
                               r_dtype="f32" if w_dtype == "f32" else "bf16",
