@@ -235,6 +235,11 @@ def cpu_baseline_line(budget_s: float):
             "also": side}
 
 
+def achieved_gbs(nbytes: float, ms: float) -> float:
+    """Bytes moved over a time in ms, as GB/s (1e9 bytes per second)."""
+    return nbytes / (ms * 1e-3) / 1e9
+
+
 def host_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -413,7 +418,7 @@ def run_gpu(args):
     clocks = sampler.summary()
     bytes16, W16 = pass_bytes(nw16)
     ms_max = max_over_ranks(ms16, dev)
-    value = world * bytes16 / (ms_max * 1e-3) / 1e9
+    value = achieved_gbs(world * bytes16, ms_max)
 
     # ---- decode: k=1 pass, same layers
     progress("decode k=1")
