@@ -135,3 +135,11 @@ def test_staging_mode_is_validated(lib):
     assert L.dfv_set_staging(-1) == 1
     assert L.dfv_set_staging(2) == 0
     assert L.dfv_last_staging() == -1
+
+
+def test_selftest_entry_point_validates_its_workspace(lib):
+    L = lib.lib()
+    assert L.dfv_selftest_bounded_waits(None, 1 << 20, None) == 3
+    assert L.dfv_selftest_bounded_waits(ctypes.c_void_p(0x70010), 1 << 20, None) == 3  # not 256-aligned
+    assert L.dfv_selftest_bounded_waits(ctypes.c_void_p(0x70000), 4096, None) == 3      # under the 8 KB of counters
+    assert L.dfv_last_error_detail()
