@@ -129,3 +129,32 @@ def test_mxfp4_ring_groups_own_their_stages():
         for units_d in range(0, 40, 5):
             for nq in (1, 2, 4):
                 assert _check(*mx_ring(units_g, units_d, nq)) == 0
+
+
+def test_mxfp4_down_units_wait_for_exactly_the_owner_ctas():
+    """layer_fused_mxfp4.cu: CTA b takes gate/up units [floor(bU/G),
+    floor((b+1)U/G)).  Before a down group reads expert wi's h it waits for
+    the flags of CTAs b0..b1, from the closed form owner(u) =
+    floor(((u+1)G - 1)/U).  Every CTA holding one of the expert's units must be
+    in that range (a missing one is a race on h), and both ends must hold one.
+    A CTA strictly inside the range may hold no unit at all (more CTAs than
+    units); it sets its flag as soon as its empty gate/up phase ends, so the
+    wait for it is short and harmless."""
+    for G in (1, 2, 7, 152, 160):
+        for tiles_g in (1, 2, 16, 64, 96):
+            for nW in (1, 2, 3, 9, 47, 103, 257):
+                U = nW * tiles_g
+                owner = [None] * U
+                for b in range(G):
+                    for u in range(b * U // G, (b + 1) * U // G):
+                        assert owner[u] is None
+                        owner[u] = b
+                assert None not in owner
+                assert all(owner[u] == ((u + 1) * G - 1) // U for u in range(0, U, max(1, U // 97)))
+                for wi in {0, nW // 2, nW - 1}:
+                    b0 = ((wi * tiles_g + 1) * G - 1) // U
+                    b1 = (((wi + 1) * tiles_g) * G - 1) // U
+                    owners = set(owner[wi * tiles_g:(wi + 1) * tiles_g])
+                    assert owners <= set(range(b0, b1 + 1)) and b0 in owners and b1 in owners
+                    for b in set(range(b0, b1 + 1)) - owners:
+                        assert b * U // G == (b + 1) * U // G  # an idle CTA
