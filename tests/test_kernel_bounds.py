@@ -1,11 +1,13 @@
-"""CPU model of the bf16 single-launch kernel's index arithmetic (compute-
-sanitizer is not available): the shared-memory plan, the routing tables with
+"""CPU models of the single-launch kernels' index arithmetic (compute-
+sanitizer is not available).  bf16: the shared-memory plan, the routing tables with
 the shared expert and its split gate/up entries, and the extreme index of
 every shared-memory, TMA, global-weight, h and ys access a unit makes, checked
 against the size of its buffer.  The formulas are the kernel's (layer_fused.cu:
 fused_plan, slot_addr, the producer's copies, the consumers' fragment loads and
-stores); routing comes from seeded draws of the sweep's kinds (repeated-token
-and independent blocks)."""
+stores).  mxfp4 (layer_fused_mxfp4.cu): the plan, the gate/up and down stage
+layouts, the tensor-map coordinates, the swizzled x and h staging and the hf /
+ys stores.  Routing comes from seeded draws of the sweep's kinds
+(repeated-token and independent blocks)."""
 from __future__ import annotations
 
 import random
@@ -165,3 +167,96 @@ def test_fused_bf16_indices_stay_in_their_buffers(d, I):
     # at k > 8 with independent rows the staged-x stage is in use, with and without
     # the shared expert (the split keeps it)
     assert (True, 0, True) in extra_stage and (True, 1, True) in extra_stage
+
+
+# ---------------------------------------------------------------- mxfp4 single-launch kernel
+MX_GROUPS, MX_RING, MX_CH, MX_ROWS, MX_COLS, MX_MAX_D = 4, 8, 4, 32, 512, 2048
+
+
+def mx_plan(k, d, I):
+    """fused_mx_plan / mx_smem of layer_fused_mxfp4.cu."""
+    if d % MX_COLS or d > MX_MAX_D or I % 64 or I > 128 * MX_CH:
+        return None
+    NT = 1 if k <= 8 else 2
+    slot = max(MX_ROWS * MX_COLS + MX_ROWS * MX_COLS // 16, 34 * I)
+    slot = (slot + 127) & ~127
+    ipad = (I + 127) // 128 * 128
+    scratch = max(NT * 8 * d * 2, MX_GROUPS * NT * 8 * ipad * 2)
+    scratch = (scratch + 127) & ~127
+    smem = MX_RING * slot + scratch + 16 * MX_RING + (FW * 32 * 16 if NT == 2 else 0)
+    return None if smem > SMEM_BUDGET else dict(NT=NT, slot=slot, scratch=scratch, smem=smem)
+
+
+def swz(q, j):
+    return q ^ (((q >> 3) & 1) | ((j & 1) << 1))
+
+
+def check_mx_layer(k, d, I, E, K, idx, ns):
+    P = mx_plan(k, d, I)
+    if P is None:
+        return None
+    NT, slot, scratch = P["NT"], P["slot"], P["scratch"]
+    woken, off, gat = tables(idx, k, K, E, ns)
+    nW, nP = len(woken), k * K + ns * k
+    # gate/up stage: [32][256] gate codes | [32][256] up codes | [32][16] gate scales | [32][16] up scales
+    g_up = MX_ROWS * MX_COLS // 2
+    g_sc, g_scu = 2 * g_up, 2 * g_up + MX_ROWS * MX_COLS // 32
+    bytes_g = 2 * g_up + 2 * MX_ROWS * MX_COLS // 32
+    assert bytes_g <= slot
+    rw, c, j = 31, 3, MX_CH - 1  # the largest row, lane column and chunk
+    assert g_up + rw * (MX_COLS // 2) + c * 16 + j * 64 + 16 <= g_sc       # up codes
+    assert g_scu + rw * (MX_COLS // 32) + c + j * 4 + 1 <= bytes_g         # up scales
+    # down stage: [64][I/2] codes | [64][I/32] scales
+    rowb_d, srow_d = I // 2, I // 32
+    d_sc, bytes_d = 64 * rowb_d, 64 * rowb_d + 64 * srow_d
+    assert bytes_d <= slot
+    CI = (I + 127) // 128
+    for c in (0, 3):
+        # with a ragged last 128-code chunk, lanes c >= 2 skip it (no codes there)
+        jl = CI - 1 if (I % 128 == 0 or c < 2) else CI - 2
+        if jl >= 0:
+            assert 63 * rowb_d + c * 16 + jl * 64 + 16 <= d_sc  # codes of row 63
+            assert d_sc + 63 * srow_d + c + jl * 4 + 1 <= bytes_d  # its scales
+    # TMA coordinates: x bytes 16-aligned, boxes inside the matrices
+    nq = d // MX_COLS
+    for q in (0, nq - 1):
+        assert (q * (MX_COLS // 2)) % 16 == 0 and (q * (MX_COLS // 32)) % 16 == 0
+        assert q * (MX_COLS // 2) + 256 <= d // 2 and q * (MX_COLS // 32) + 16 <= d // 32
+    # staged x rows (P2): k rows of d fp16, 16-byte pieces swizzled within groups of 4
+    xrow = d * 2
+    cpr = d // 8
+    assert all(swz(q, t) < cpr for q in range(cpr) for t in (0, 1))
+    assert k * xrow <= scratch
+    # B reads of token t: bt = t*xrow + c*64 + ((tt ^ sw) << 4), plus chunk (q*4 + j)*256
+    assert 3 * 64 + (3 << 4) + ((nq - 1) * MX_CH + MX_CH - 1) * 256 + 16 <= xrow
+    # staged h rows (P3): per group NT*8 rows of CI*256 bytes
+    hrow = CI * 256
+    assert MX_GROUPS * NT * 8 * hrow <= scratch
+    assert all(swz(q, n) < CI * 16 for q in range(CI * 16) for n in (0, 1))
+    assert 3 * 64 + (3 << 4) + (CI - 1) * 256 + 16 <= hrow
+    tiles_g, tiles_d = I // MX_ROWS, d // 64
+    for wi in range(nW):
+        e, eo, m = woken[wi], off[wi], off[wi + 1] - off[wi]
+        assert m <= NT * 8
+        assert e * I + (tiles_g - 1) * MX_ROWS + MX_ROWS <= (E + ns) * I  # gate/up box rows
+        row = e * d + (tiles_d - 1) * 64
+        assert (row + 64) * rowb_d <= (E + ns) * d * rowb_d and (row * srow_d) % 16 == 0 and (64 * srow_d) % 16 == 0
+        for tok in range(m):
+            pair = gat[eo + tok]
+            assert 0 <= pair < nP
+            assert (eo + tok) * I + (tiles_g - 1) * MX_ROWS + 3 * 8 + 7 < MAX_BLOCK * (K + ns) * I  # hf (fp32)
+            assert pair * d + (tiles_d - 1) * 64 + 3 * 16 + 7 + 8 < MAX_BLOCK * (K + ns) * d       # ys
+    return True
+
+
+@pytest.mark.parametrize("d", [512, 1024, 2048])
+@pytest.mark.parametrize("I", [64, 192, 448, 512])
+def test_fused_mxfp4_indices_stay_in_their_buffers(d, I):
+    rnd = random.Random(d * 7919 + I)
+    checked = 0
+    for E, K in ((4, 2), (16, 4), (256, 8)):
+        for k in (1, 8, 9, 16):
+            for idx in _draws(k, E, K, rnd):
+                for ns in (0, 1):
+                    checked += check_mx_layer(k, d, I, E, K, idx, ns) is not None
+    assert checked > 0
