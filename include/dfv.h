@@ -68,7 +68,8 @@ enum {
   DFV_ERR_CUDA = 4          /* a CUDA launch or copy failed               */
 };
 
-typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2 } dfv_dtype;
+/* DFV_F16 (IEEE binary16) appears only in dfv_selftest_mma. */
+typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_F16 = 4 } dfv_dtype;
 
 /* Device-side error bits a kernel may set in the workspace (see
  * dfv_read_device_error).  Every wait inside a kernel is bounded; a wait that
@@ -285,8 +286,10 @@ const char *dfv_fused_unavailable_reason(void);
  * buffers.
  * Its scratch is a fixed device array inside libdfv.so (about 41 KB, enough
  * for every k <= 16 and any V) that each GPU holds until the process exits.
- * The first call on a device looks the array's device address up
- * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * The first call in a CUDA context (per device, and again after
+ * cudaDeviceReset) looks the array's device address up (cudaGetSymbolAddress)
+ * and keeps it for that context, so make that first call before any stream
+ * capture.
  * Each call clears the array's ticket with cudaMemsetAsync on `stream` and
  * allocates nothing.  All calls share the array: calls whose kernels overlap
  * on the GPU race; order them (one stream, or synchronise).
@@ -310,6 +313,20 @@ int dfv_accept_greedy_noalloc(const void *logits, int dtype, int k, int V, const
  *       counters sit in its first 8 KB).
  */
 int dfv_selftest_bounded_waits(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Self-test of the tensor-core fragment path the expert kernels use (its
+ * instance comes from "Speculating on a Strix Halo (part 2)", section "Two
+ * bugs upstream": a multiply-add with an exact result must return it whatever
+ * the sign of its zero operands).  One warp computes
+ *   D[i][j] = sum_l A[i][l] * B[l][j]      (16 x 16 x 16, fp32 accumulate)
+ * with the MMA helper and operand mapping of the bf16 kernels (dtype
+ * DFV_BF16) or of the mxfp4 kernels (DFV_F16: binary16 operands).
+ *   A, B  [16][16] 16-bit elements (device), row-major
+ *   D     [16][16] fp32 (device)
+ * Returns DFV_ERR_UNSUPPORTED for another dtype.
+ */
+int dfv_selftest_mma(int dtype, const void *A, const void *B, float *D, void *stream);
 
 const char *dfv_status_string(int status);
 const char *dfv_last_error_detail(void);

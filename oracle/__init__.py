@@ -35,7 +35,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-F32, BF16, MXFP4, Q8 = 0, 1, 2, 3
+F32, BF16, MXFP4, Q8, F16 = 0, 1, 2, 3, 4
 _lib = None
 
 
@@ -87,6 +87,7 @@ def lib():
         L.orc_silu.argtypes = [D]
         L.orc_decode_rows.argtypes = [I, P, P, I, I, I, P]
         L.orc_route.argtypes = [P, P, I, I, P, P, P]
+        L.orc_matmul.argtypes = [I, P, P, I, I, I, P]
         L.orc_woken.argtypes = [I, I, I, P, P, P, P, P]
         L.orc_expert_ffn.argtypes = [P, I, P, P]
         L.orc_moe_forward.argtypes = [P, P, I, I, P, I]
@@ -179,6 +180,19 @@ def decode_rows(dtype: int, data: np.ndarray, scales: Optional[np.ndarray], r0: 
     rc = lib().orc_decode_rows(dtype, _ptr(data), _ptr(scales), r0, nrows, cols, _ptr(out))
     if rc:
         raise ValueError("orc_decode_rows failed (%d)" % rc)
+    return out
+
+
+def matmul(dtype: int, a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """D = A . B in double from operands of one element format (F32 as
+    float32, BF16 / F16 as their uint16 bit patterns)."""
+    M, L = a.shape
+    L2, N = b.shape
+    assert L == L2
+    out = np.empty((M, N), dtype=np.float64)
+    rc = lib().orc_matmul(int(dtype), _ptr(np.ascontiguousarray(a)), _ptr(np.ascontiguousarray(b)), M, L, N, _ptr(out))
+    if rc:
+        raise ValueError("orc_matmul failed (%d)" % rc)
     return out
 
 

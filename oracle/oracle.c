@@ -104,6 +104,8 @@ int orc_decode_rows(int dtype, const void *data, const uint8_t *scales,
         int code = ((const int8_t *)data)[row * cols + c];
         uint16_t s = ((const uint16_t *)scales)[row * (cols / 32) + c / 32];
         v = (double)code * orc_fp16_to_double(s);
+      } else if (dtype == ORC_F16) {
+        v = orc_fp16_to_double(((const uint16_t *)data)[row * cols + c]);
       } else {
         return -1;
       }
@@ -114,6 +116,35 @@ int orc_decode_rows(int dtype, const void *data, const uint8_t *scales,
 }
 
 static int act_ok(int dt) { return dt == ORC_F32 || dt == ORC_BF16; }
+
+/*
+ * Plain matrix product of decoded operands, the contraction inside every
+ * expert projection:  D[i][j] = sum over l of A[i][l] * B[l][j]  for A [M][L]
+ * and B [L][N] of one element format (F32, BF16 or F16), summed in double in
+ * the order l = 0, 1, ... .  "Speculating on a Strix Halo (part 2)", section
+ * "Two bugs upstream", prints a 16x16 instance whose exact result a correct
+ * multiply-add must return whatever the sign of its zero operands.
+ */
+int orc_matmul(int dtype, const void *A, const void *B, int M, int L, int N,
+               double *D) {
+  if (M < 1 || L < 1 || N < 1 ||
+      !(dtype == ORC_F32 || dtype == ORC_BF16 || dtype == ORC_F16))
+    return -1;
+  double *a = malloc(sizeof(double) * (size_t)M * L);
+  double *b = malloc(sizeof(double) * (size_t)L * N);
+  if (!a || !b) return -2;
+  orc_decode_rows(dtype, A, NULL, 0, M, L, a);
+  orc_decode_rows(dtype, B, NULL, 0, L, N, b);
+  for (int i = 0; i < M; ++i)
+    for (int j = 0; j < N; ++j) {
+      double acc = 0.0;
+      for (int l = 0; l < L; ++l) acc += a[(size_t)i * L + l] * b[(size_t)l * N + j];
+      D[(size_t)i * N + j] = acc;
+    }
+  free(a);
+  free(b);
+  return 0;
+}
 
 /* ------------------------------------------------------------------ */
 /* router                                                              */

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_MXFP4 = 2, ORC_Q8 = 3 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_MXFP4 = 2, ORC_Q8 = 3, ORC_F16 = 4 /* IEEE binary16 */ };
 
 typedef struct {
   int d, n_experts, top_k, d_ff, norm_topk;
@@ -68,6 +68,10 @@ int orc_decode_rows(int dtype, const void *data, const uint8_t *scales,
                     int r0, int nrows, int cols, double *out);
 
 /* router: logits (rounded to fp32), top-K indices, routing weights */
+/* D[M][N] = A[M][L] . B[L][N] in double (operands F32, BF16 or F16). */
+int orc_matmul(int dtype, const void *A, const void *B, int M, int L, int N,
+               double *D);
+
 int orc_route(const orc_layer *L, const void *x, int x_dtype, int k,
               float *logits, int32_t *topk_idx, double *topk_w);
 

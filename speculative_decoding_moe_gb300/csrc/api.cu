@@ -12,6 +12,7 @@
 
 namespace dfv {
 cudaError_t launch_wait_selftest(const Workspace &w, cudaStream_t s);  // selftest.cu
+cudaError_t launch_mma_selftest(const void *A, const void *B, float *D, int bf16, cudaStream_t s);
 }
 
 namespace {
@@ -486,6 +487,15 @@ int dfv_selftest_bounded_waits(void *ws, size_t ws_bytes, void *stream) {
   if (ws_bytes < need) return fail(DFV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
   cudaError_t e = dfv::launch_wait_selftest(layout(&probe, 1, ws), (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test launch");
+  return DFV_OK;
+}
+
+int dfv_selftest_mma(int dtype, const void *A, const void *B, float *D, void *stream) {
+  if (dtype != DFV_BF16 && dtype != DFV_F16) return fail(DFV_ERR_UNSUPPORTED, "MMA self-test dtype %d", dtype);
+  if (!A || !B || !D || !aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
+    return fail(DFV_ERR_INVALID_ARG, "A, B and D must be non-NULL and 16-byte aligned");
+  cudaError_t e = dfv::launch_mma_selftest(A, B, D, dtype == DFV_BF16 ? 1 : 0, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "MMA self-test launch");
   return DFV_OK;
 }
 

@@ -14,7 +14,7 @@ from .inputs import LayerWeights
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdfv.so")
 
-F32, BF16, MXFP4 = 0, 1, 2
+F32, BF16, MXFP4, F16 = 0, 1, 2, 4
 # device error bits (DFV_DEVERR_* in include/dfv.h)
 DEVERR_STAGE_WAIT, DEVERR_SLOT_WAIT, DEVERR_DRAIN_WAIT, DEVERR_GRID_WAIT = 0x1, 0x2, 0x4, 0x8
 DEVERR_SCALE_RANGE, DEVERR_REDUCE_WAIT, DEVERR_ROUTING = 0x10, 0x20, 0x40
@@ -24,7 +24,7 @@ EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_pro
            "dfv_accept_greedy_noalloc", "dfv_set_staging", "dfv_last_staging",
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
-           "dfv_accept_workspace_size", "dfv_accept_greedy", "dfv_selftest_bounded_waits")
+           "dfv_accept_workspace_size", "dfv_accept_greedy", "dfv_selftest_bounded_waits", "dfv_selftest_mma")
 
 
 class DfvError(RuntimeError):
@@ -73,6 +73,7 @@ def _load():
         L.dfv_accept_greedy_noalloc.argtypes = [P, I, I, I, P, P, P, P]
         L.dfv_read_device_error.argtypes = [P, P, P]
         L.dfv_selftest_bounded_waits.argtypes = [P, S, P]
+        L.dfv_selftest_mma.argtypes = [I, P, P, P, P]
         L.dfv_set_path.argtypes = [I]
         L.dfv_set_staging.restype = I
         L.dfv_set_staging.argtypes = [I]
@@ -234,6 +235,20 @@ def selftest_bounded_waits(ws: torch.Tensor, stream=None):
     error word with read_device_error, then zero-fill ws)."""
     _check(_load().dfv_selftest_bounded_waits(_p(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "dfv_selftest_bounded_waits")
+
+
+def selftest_mma(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
+    """D = A . B (16 x 16 x 16) through the expert kernels' MMA fragment path;
+    a and b are bf16 or fp16 CUDA tensors [16, 16]."""
+    if a.shape != (16, 16) or b.shape != (16, 16) or a.dtype != b.dtype:
+        raise ValueError("A and B must be [16, 16] tensors of one dtype")
+    code = {torch.bfloat16: BF16, torch.float16: F16}.get(a.dtype)
+    if code is None:
+        raise TypeError("A and B must be bf16 or fp16, got %s" % a.dtype)
+    a, b = a.contiguous(), b.contiguous()
+    out = torch.empty(16, 16, dtype=torch.float32, device=a.device)
+    _check(_load().dfv_selftest_mma(code, _p(a), _p(b), _p(out), _stream(stream)), "dfv_selftest_mma")
+    return out
 
 
 def set_staging(max_mode: int):

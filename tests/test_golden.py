@@ -24,7 +24,8 @@ def _rows(name):
         for line in f:
             line = line.strip()
             if line and not line.startswith("#"):
-                out.append([None if v == "-" else float(v) for v in line.split()])
+                out.append([None if v == "-" else (float(int(v, 16)) if v.startswith("0x") else float(v))
+                            for v in line.split()])
     return out
 
 
@@ -67,3 +68,52 @@ def test_effective_bandwidth_arithmetic(gb, ms, gbs):
     sys.path.insert(0, ROOT)
     import bench
     assert bench.achieved_gbs(gb * 1e9, ms) == pytest.approx(gbs, rel=0.02)
+
+
+# ---------------------------------------------------------------- signed-zero multiply-add
+# "Speculating on a Strix Halo (part 2)", section "Two bugs upstream".
+SIGNED_ZERO = _rows("signed_zero_mma.txt")
+
+
+def signed_zero_operands(neg_zero_row=None, fmt="f16"):
+    """A and B of the page's 16x16 case as 16-bit patterns: column 12 of A is
+    -1, row 12 of B is (j+1)/16, every other entry +0.0; with neg_zero_row set,
+    that row of B holds -0.0 instead."""
+    import torch
+    dt = torch.float16 if fmt == "f16" else torch.bfloat16
+    a = torch.zeros(16, 16, dtype=dt)
+    a[:, 12] = -1.0
+    b = torch.zeros(16, 16, dtype=dt)
+    b[12, :] = torch.arange(1, 17, dtype=torch.float32) / 16
+    if neg_zero_row is not None:
+        assert neg_zero_row != 12
+        b[neg_zero_row, :] = -0.0
+    return a, b
+
+
+def _bits(t):
+    import torch
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+@pytest.mark.parametrize("neg_zero_row", [None, 0, 7, 15])
+def test_signed_zero_mma_exact_in_the_oracle(fmt, neg_zero_row):
+    a, b = signed_zero_operands(neg_zero_row, fmt)
+    if neg_zero_row is not None:  # the -0 run differs from the +0 run in 16 elements of B
+        b0 = _bits(signed_zero_operands(None, fmt)[1])
+        assert int((_bits(b) != b0).sum()) == 16
+        assert np.all(_bits(a)[:, neg_zero_row] == 0)  # A is +0 in the column those entries meet
+    code = oracle.F16 if fmt == "f16" else oracle.BF16
+    d = oracle.matmul(code, _bits(a), _bits(b)).astype(np.float32)
+    want = np.tile(-(np.arange(1, 17, dtype=np.float32)) / 16, (16, 1))
+    assert np.array_equal(d.view(np.uint32), want.view(np.uint32))
+    for i, j, value, bits in SIGNED_ZERO:
+        assert d[int(i), int(j)] == value
+        assert int(d[int(i), int(j):int(j) + 1].view(np.uint32)[0]) == int(bits)
+
+
+def test_signed_zero_fixture_bits_are_the_printed_values():
+    for i, j, value, bits in SIGNED_ZERO:
+        assert np.float32(value).view(np.uint32) == int(bits)
+        assert value == -(j + 1) / 16
