@@ -11,6 +11,7 @@
 // the largest logit with the lowest column among equals.  The last CTA to
 // finish (atomic ticket, no waiting) reduces the slices of every row, matches
 // the draft prefix and writes tau and the committed tokens.
+#include <map>
 #include <mutex>
 
 #include "dfv_internal.cuh"
@@ -148,24 +149,49 @@ constexpr size_t kNoAllocPartials = (size_t)(kMaxBlock + 1) * kNoAllocMaxChunks;
 static __device__ __align__(256) unsigned long long g_accept_scratch[32 + kNoAllocPartials];
 
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[256];  // per device ordinal, set up once
+// device address of the array, per CUDA context: the address belongs to the
+// context that loaded the module, so a new context (another device, or the
+// primary context again after cudaDeviceReset) gets its own lookup
+std::map<CUcontext, void *> g_scratch_ptr;
+
+CUresult current_context(CUcontext *ctx) {
+  using Fn = CUresult (*)(CUcontext *);
+  static Fn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {  // called with g_scratch_mu held
+    tried = true;
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(f);
+    else
+      cudaGetLastError();
+  }
+  return fn ? fn(ctx) : CUDA_ERROR_NOT_FOUND;
+}
 }  // namespace
 
 cudaError_t accept_noalloc_scratch(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *ptr = nullptr;
-    // The array's name is only a host-side stand-in: the device address of
-    // this device's copy has to be looked up with the device current.
-    e = cudaGetSymbolAddress(&ptr, g_accept_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = ptr;
+  CUcontext ctx = nullptr;
+  if (current_context(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx) {
+    auto it = g_scratch_ptr.find(ctx);
+    if (it != g_scratch_ptr.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
   }
-  *out = g_scratch_ptr[dev];
+  // The array's name is only a host-side stand-in: the device address of the
+  // current context's copy has to be looked up with that context current.  The
+  // lookup also creates the device's primary context when none is current yet.
+  void *ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_accept_scratch);
+  if (e != cudaSuccess) return e;
+  if (!ctx && (current_context(&ctx) != CUDA_SUCCESS || !ctx)) return cudaErrorDeviceUninitialized;
+  g_scratch_ptr[ctx] = ptr;
+  *out = ptr;
   return cudaSuccess;
 }
 

@@ -4,8 +4,8 @@ dfv_accept_greedy_noalloc serves callers that cannot allocate device memory:
 its scratch is a fixed device array inside the library rather than a
 caller-provided workspace.  It must compute exactly what dfv_accept_greedy
 computes; this test calls both through the C ABI on the same inputs, twice in a
-row with different inputs (the shared array keeps the previous call's
-contents, so the second call also checks that the ticket is cleared)."""
+row with different inputs (the second call runs on the array as the first call
+left it, so it shows that a call does not depend on what the array held)."""
 from __future__ import annotations
 
 import ctypes
