@@ -13,6 +13,7 @@ constexpr int kFC = kFW * 32;     // consumer threads
 constexpr int kFT = kFC + 32;     // + producer warp
 constexpr int kBarAll = 1;        // named barrier: all consumers
 constexpr int kBarGroup = 2;      // named barriers 2, 3: consumer groups of 8 warps
+constexpr int kBarProducer = 7;   // named barrier: warp 0 releases the producer (64 threads)
 constexpr int kMaxRing = 8;       // upper bound of ring stages (barrier arrays)
 constexpr int kMaxChunksP2 = 2;   // 32-column chunks per consumer warp per gate/up stage (ks <= 1024)
 
@@ -67,6 +68,17 @@ __device__ __forceinline__ void prefetch_router_rows(const FusedParams &p) {
     prefetch_l2(reinterpret_cast<const char *>(p.wr) + (size_t)e * p.d * 2, (uint32_t)p.d * 2);
 }
 
+// Arrive on named barrier `id` (n threads in all) without waiting.
+__device__ __forceinline__ void bar_arrive_n(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Start fetching a tensor map (kernel parameter, generic address) into the
+// descriptor cache before its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
 __device__ __forceinline__ void load8_bf16(const void *base, size_t elem, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(base) + elem);
   f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
@@ -85,98 +97,187 @@ struct RouteSmem {
   int *off;        // [E + ns + 1]  per woken expert: first position in the sorted pair list
   int *eoff;       // [E]           per routed expert id: first position in the sorted pair list
   int *gat;        // [k*K + ns*k]  pair ids sorted by (expert, token)
-  unsigned *mask;  // [kMaxBlock * E/32] experts chosen by each row
+  unsigned *tmask; // [E]           bit t set when row t selected the expert
   float *inv;      // [kMaxBlock] 1/rms of each row (fuse_norm)
-  int *wsum, *csum;  // [kFW] scan scratch
   int *nw;         // woken count
   volatile int *abort;
   volatile int *bad;  // set when the tables fail their check (zeroed by the caller)
 };
 
-// P0 + grid barrier 1 + P1, run by the kFW consumer warps of every CTA (named
-// barrier kBarAll over kFC threads).
-//   P0  router GEMV (optionally on RMSNorm(x) rounded to bf16): CTA b computes
-//       the logits of experts b, b+G, ...; each (token, expert) dot product is
-//       one warp's, in a fixed order, so a token's logit depends on nothing but
-//       its own row.
-//   P1  every CTA derives the whole routing decision itself from the logits:
-//       top-K per row (warp per row, redux max/min: largest logit, lowest id
-//       among equals), routing weights, woken union, per-expert pair offsets
-//       (block scan) and the (expert, token)-sorted pair list, then appends
-//       the shared expert (when p.ns).  CTA 0 also publishes the decision to
-//       the workspace and the routed part to the caller's copies.
-// `between` runs on the same threads after P0 and before grid barrier 1 (work
-// that needs neither the other CTAs' logits nor the routing decision).
-template <class Between>
-__device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSmem &r, Between &&between) {
-  const int k = p.k, d = p.d, E = p.E, K = p.K;
+// What the routing prologue needs, copied out of the kernel parameters and
+// passed by value to the non-inlined prologue functions, so that they keep
+// every field in registers (through a reference the compiler would reload
+// them after each store it cannot prove distinct).
+struct RouteArgs {
+  int k, d, E, K, fuse_norm, norm_topk, ns;
+  float eps;
+  const uint16_t *wr;       // router [E][d] bf16
+  const uint16_t *xs;       // x rows [k][d] bf16 (shared memory, or p.x)
+  uint32_t xbar;            // mbarrier of the x copy (0: xs is p.x)
+  float *logits;            // workspace logits [k][E]
+  unsigned *err, *sync;     // workspace error word, grid-barrier words
+  int32_t *topk_idx, *woken, *offsets, *gather, *n_woken;  // workspace copies (CTA 0)
+  float *topk_w;
+  int32_t *u_idx, *u_nw;    // the caller's copies (CTA 0)
+  // shared-memory tables
+  int *idx;        // [k*K + ns*k]  expert of pair t*K+s, by descending logit
+  float *w;        // [k*K + ns*k]  routing weight of the pair
+  int *s_woken;    // [E + ns]      ascending ids of the woken experts
+  int *off;        // [E + ns + 1]  per woken expert: first position in the sorted pair list
+  int *eoff;       // [E]           per routed expert id: first position in the sorted pair list
+  int *gat;        // [k*K + ns*k]  pair ids sorted by (expert, token)
+  unsigned *tmask; // [E]           bit t set when row t selected the expert
+  float *inv;      // [kMaxBlock]   1/rms of each row (fuse_norm)
+  int *nw;         // woken count
+  volatile int *abort;
+  volatile int *bad;  // set when the tables fail their check (zeroed by the caller)
+};
+
+__device__ __forceinline__ RouteArgs route_args(const FusedParams &p, const RouteSmem &r, const uint16_t *xs,
+                                                uint32_t xbar) {
+  RouteArgs a;
+  a.k = p.k; a.d = p.d; a.E = p.E; a.K = p.K;
+  a.fuse_norm = p.fuse_norm; a.norm_topk = p.norm_topk; a.ns = p.ns ? 1 : 0;
+  a.eps = p.eps;
+  a.wr = reinterpret_cast<const uint16_t *>(p.wr);
+  a.xs = xs;
+  a.xbar = xbar;
+  a.logits = p.ws.logits;
+  a.err = p.ws.err;
+  a.sync = p.ws.sync;
+  a.topk_idx = p.ws.topk_idx; a.woken = p.ws.woken; a.offsets = p.ws.offsets; a.gather = p.ws.gather;
+  a.n_woken = p.ws.n_woken; a.topk_w = p.ws.topk_w;
+  a.u_idx = p.u_idx; a.u_nw = p.u_nw;
+  a.idx = r.idx; a.w = r.w; a.s_woken = r.woken; a.off = r.off; a.eoff = r.eoff; a.gat = r.gat;
+  a.tmask = r.tmask; a.inv = r.inv; a.nw = r.nw; a.abort = r.abort; a.bad = r.bad;
+  return a;
+}
+
+// grid_sync on the raw workspace words (for the non-inlined prologue).
+__device__ __forceinline__ bool grid_sync_raw(unsigned *sync, unsigned *err, unsigned nb) {
+  unsigned *ctr = sync, *gabort = sync + 2;
+  red_release_add(ctr, 1u);
+  const unsigned target = nb * gridDim.x;
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 1; ld_acquire(ctr) < target; ++it) {
+    if ((it & 15u) == 0) {
+      if (ld_relaxed(gabort)) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        atomicOr(err, DFV_DEVERR_GRID_WAIT);
+        atomicExch(gabort, 1u);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// The k rows of x start towards shared memory (one bulk copy per row, all on
+// mbarrier `xbar`), issued by one thread after griddepcontrol.wait: x is the
+// previous launch's output in a stack.  `dst` must hold k * d bf16 and be
+// 16-byte aligned; d * 2 is a multiple of 16.
+__device__ __forceinline__ void stage_x_rows(const FusedParams &p, uint32_t dst, uint32_t xbar) {
+  const uint32_t rb = (uint32_t)p.d * 2;
+  mbar_expect_tx(xbar, rb * (uint32_t)p.k);
+  for (int t = 0; t < p.k; ++t)
+    bulk_g2s(dst + (uint32_t)t * rb, reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * p.d, rb, xbar);
+}
+
+// P0, run by the kFW consumer warps of every CTA (named barrier kBarAll over
+// kFC threads).  Router GEMV, optionally on RMSNorm(x) rounded to bf16: CTA b
+// computes the logits of experts b, b+G, ....  r.xs holds the k rows of x
+// (bf16, row stride d), in shared memory once r.xbar completes (xbar == 0:
+// xs is p.x in global memory).  The CTA's n_e experts share its warps: kFW /
+// n_e warps per expert, each loading its expert's router row once (issued
+// before the wait for x, so the two transfers overlap) and taking every
+// (kFW / n_e)-th token.  Each (token, expert) dot product is one warp's,
+// computed in one fixed order whichever warp takes it, so a token's logit
+// depends on nothing but its own row.
+__device__ __forceinline__ void route_p0(const RouteArgs &r) {
+  const int k = r.k, d = r.d, E = r.E;
   const int G = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // lane l takes the 16-byte pieces l, l+32, ... of a row, 8 at a time with
-  // all their loads in flight; the sums run in piece order
-  const int cpr = d / 8;
-  if (p.fuse_norm) {
+  const uint16_t *xs = r.xs;
+  for (int i = tid; i < kMaxExperts; i += kFC) r.tmask[i] = 0u;
+  const int cpr = d / 8;  // 16-byte pieces per row; lane l takes pieces l, l+32, ...
+  const int n_e = blockIdx.x < E ? (E - 1 - blockIdx.x) / G + 1 : 0;
+  const int wpe = n_e >= kFW ? 1 : (n_e > 0 ? kFW / n_e : kFW);  // warps per expert
+  const int jstep = kFW / wpe;
+  const int j0 = warp / wpe;
+  const bool active = n_e > 0 && j0 < n_e && warp < wpe * jstep;
+  // the first 256 pieces of this warp's first router row, in flight while x arrives
+  uint4 wv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int c = lane + 32 * i;
+    wv[i] = (active && c < cpr)
+                ? __ldg(reinterpret_cast<const uint4 *>(r.wr + (size_t)(blockIdx.x + j0 * G) * d + (size_t)c * 8))
+                : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (r.xbar) {
+    // one thread waits (bounded) for the x copy; the named barrier then
+    // orders the copied rows before every consumer's reads, and all consumers
+    // see the same abort flag after it
+    if (tid == 0 && !mbar_wait(r.xbar, 0u, r.err, DFV_DEVERR_STAGE_WAIT, r.abort)) *r.abort = 1;
+    bar_sync_n(kBarAll, kFC);
+    if (*r.abort) return;
+  }
+  if (r.fuse_norm) {
     if (warp < k) {
-      const int t = warp;
-      const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
+      const uint16_t *xr = xs + (size_t)warp * d;
       float ss = 0.f;
-      for (int c0 = 0; c0 < cpr; c0 += 256) {
-        uint4 xv[8];
+      for (int c = lane; c < cpr; c += 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c0 + lane + 32 * i;
-          xv[i] = c < cpr ? *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (c0 + lane + 32 * i < cpr) {
-            const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
-              ss = fmaf(a, a, ss);
-              ss = fmaf(b, b, ss);
-            }
-          }
+        for (int h = 0; h < 4; ++h) {
+          const float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
+          ss = fmaf(a, a, ss);
+          ss = fmaf(b, b, ss);
         }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) r.inv[t] = 1.0f / sqrtf(ss / (float)d + p.eps);
+      if (lane == 0) r.inv[warp] = 1.0f / sqrtf(ss / (float)d + r.eps);
     }
     bar_sync_n(kBarAll, kFC);
   }
-  // the (token, expert) dot products of this CTA's experts b, b+G, ... spread
-  // over all warps: pair q = slot * k + t on warp q mod 16 (each dot product is
-  // computed the same way whichever warp takes it)
-  {
-    const int n_e = blockIdx.x < E ? (E - 1 - blockIdx.x) / G + 1 : 0;
-    for (int q = warp; q < n_e * k; q += kFW) {
-      const int t = q % k, e = blockIdx.x + (q / k) * G;
-      const uint16_t *xr = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
-      const float inv = p.fuse_norm ? r.inv[t] : 1.f;
-      const uint16_t *wr = reinterpret_cast<const uint16_t *>(p.wr) + (size_t)e * d;
+  if (!active) return;
+  // rolled loops over experts, tokens and 256-piece chunks of a row: this code
+  // runs once per launch, so its size (cold instruction fetch) counts more
+  // than its loop overhead
+  int cur_j = j0, cur_c0 = 0;  // the router-row chunk wv holds
+#pragma unroll 1
+  for (int j = j0; j < n_e; j += jstep) {
+    const int e = blockIdx.x + j * G;
+    const uint16_t *wr = r.wr + (size_t)e * d;
+#pragma unroll 1
+    for (int t = warp % wpe; t < k; t += wpe) {
+      const uint16_t *xr = xs + (size_t)t * d;
+      const float inv = r.fuse_norm ? r.inv[t] : 1.f;
       float acc = 0.f;
+#pragma unroll 1
       for (int c0 = 0; c0 < cpr; c0 += 256) {
-        uint4 xv[8], wv[8];
+        if (cur_j != j || cur_c0 != c0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c0 + lane + 32 * i;
-          xv[i] = wv[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (c < cpr) {
-            xv[i] = *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8);
-            wv[i] = *reinterpret_cast<const uint4 *>(wr + (size_t)c * 8);
+          for (int i = 0; i < 8; ++i) {
+            const int c = c0 + lane + 32 * i;
+            wv[i] = c < cpr ? __ldg(reinterpret_cast<const uint4 *>(wr + (size_t)c * 8)) : make_uint4(0u, 0u, 0u, 0u);
           }
+          cur_j = j;
+          cur_c0 = c0;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (c0 + lane + 32 * i < cpr) {
-            const uint32_t x4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+          const int c = c0 + lane + 32 * i;
+          if (c < cpr) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8);
+            const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
             const uint32_t w4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               float a = bf16_lo(x4[h]), b = bf16_hi(x4[h]);
-              if (p.fuse_norm) {
+              if (r.fuse_norm) {
                 a = rnd_bf16(a * inv);
                 b = rnd_bf16(b * inv);
               }
@@ -188,17 +289,30 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) p.ws.logits[(size_t)t * E + e] = acc;
+      if (lane == 0) r.logits[(size_t)t * E + e] = acc;
     }
   }
-  for (int i = tid; i < kMaxBlock * (kMaxExperts / 32); i += kFC) r.mask[i] = 0u;
-  between();
-  bar_sync_n(kBarAll, kFC);
+}
+
+// grid barrier 1 + P1, run by the kFW consumer warps of every CTA.  Every CTA
+// derives the whole routing decision itself from the published logits:
+// top-K per row (warp per row, redux max/min: largest logit, lowest id among
+// equals), routing weights, per-expert token masks, woken union and pair
+// offsets (one warp's scan over the experts), the (expert, token)-sorted pair
+// list (a pair's position is its expert's offset plus the number of earlier
+// rows that chose the expert), then the shared expert (when p.ns).  The tables
+// are checked before anything indexes with them.  CTA 0 also publishes the
+// decision to the workspace and the routed part to the caller's copies.  Not
+// inlined, like route_p0.
+template <class AfterScan>
+__device__ __forceinline__ void route_p1(const RouteArgs &r, AfterScan &&after_scan) {
+  const int k = r.k, E = r.E, K = r.K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // ---- grid barrier 1: every CTA's logits are published
-  if (tid == 0 && !grid_sync(p, 1)) *r.abort = 1;
+  bar_sync_n(kBarAll, kFC);
+  if (tid == 0 && !grid_sync_raw(r.sync, r.err, 1)) *r.abort = 1;
   bar_sync_n(kBarAll, kFC);
 
-  // ---------------------------------------------------------------- P1: routing
   // Warp t: top-K of row t (lane holds experts lane + 32 q), then the routing
   // weights in parallel over the K lanes.
   if (warp < k) {
@@ -208,7 +322,7 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int e = lane + 32 * q;
-      val[q] = (e < E) ? __ldcg(p.ws.logits + (size_t)t * E + e) : 0.f;
+      val[q] = (e < E) ? __ldcg(r.logits + (size_t)t * E + e) : 0.f;
       key[q] = (e < E) ? max(float_key(val[q]), 1u) : 0u;
     }
     int sel_id = 0;
@@ -237,7 +351,7 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     const float m0 = __shfl_sync(0xffffffffu, sel_val, 0);
     const float z = (lane < K) ? expf(sel_val - m0) : 0.f;
     float den = 0.f;
-    if (p.norm_topk) {
+    if (r.norm_topk) {
       den = z;
     } else {
 #pragma unroll
@@ -249,56 +363,63 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     if (lane < K) {
       r.idx[t * K + lane] = sel_id;
       r.w[t * K + lane] = z / den;
-      atomicOr(&r.mask[t * (kMaxExperts / 32) + (sel_id >> 5)], 1u << (sel_id & 31));
+      atomicOr(&r.tmask[sel_id], 1u << t);
     }
   }
   bar_sync_n(kBarAll, kFC);
-  // per-expert pair counts from the row masks
-  if (tid < E) {
-    int cnt = 0;
-    for (int t = 0; t < k; ++t) cnt += (r.mask[t * (kMaxExperts / 32) + (tid >> 5)] >> (tid & 31)) & 1u;
-    r.eoff[tid] = cnt;
-  }
-  bar_sync_n(kBarAll, kFC);
-  {
-    // exclusive scans over experts (E <= 256 <= 8 warps of threads)
-    int flag = 0, cnt = 0;
-    if (tid < E) { cnt = r.eoff[tid]; flag = cnt > 0; }
-    int fi = flag, ci = cnt;
+  // woken union and pair offsets: warp 0, lane l holding experts 8l .. 8l+7
+  // (E <= 256); exclusive scans of the woken flags and the pair counts
+  if (warp == 0) {
+    int cnt[8], nf = 0, nc = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      cnt[i] = e < E ? __popc(r.tmask[e]) : 0;
+      nf += cnt[i] > 0;
+      nc += cnt[i];
+    }
+    int fi = nf, ci = nc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int a = __shfl_up_sync(0xffffffffu, fi, o), b = __shfl_up_sync(0xffffffffu, ci, o);
       if (lane >= o) { fi += a; ci += b; }
     }
-    if (lane == 31) { r.wsum[warp] = fi; r.csum[warp] = ci; }
-    bar_sync_n(kBarAll, kFC);
-    int wb = 0, cb = 0, nW = 0;
-    for (int w = 0; w < kFW; ++w) {
-      if (w < warp) { wb += r.wsum[w]; cb += r.csum[w]; }
-      nW += r.wsum[w];
+    int wpos = fi - nf, off = ci - nc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) {
+        r.eoff[e] = off;
+        if (cnt[i] > 0) { r.s_woken[wpos] = e; r.off[wpos] = off; ++wpos; }
+        off += cnt[i];
+      }
     }
-    const int wpos = wb + fi - flag, off = cb + ci - cnt;
-    if (tid < E) r.eoff[tid] = off;
-    if (flag) { r.woken[wpos] = tid; r.off[wpos] = off; }
-    if (tid == 0) { r.off[nW] = k * K; *r.nw = nW; }
+    if (lane == 31) {
+      r.off[fi] = k * K;
+      int nW = fi;
+      if (r.ns) {
+        // the shared expert: the last woken expert (id E, above every routed
+        // id), selected by every row with weight 1
+        r.s_woken[nW] = E;
+        r.off[nW + 1] = k * K + k;
+        ++nW;
+      }
+      *r.nw = *r.abort ? 0 : nW;  // a CTA that gave up at the grid barrier takes no units
+    }
+    __syncwarp();
+    if (lane == 0) after_scan();
+    __syncwarp();
+    // the woken list and the offsets are all the producer needs: release it
+    bar_arrive_n(kBarProducer, 64);
   }
   bar_sync_n(kBarAll, kFC);
   for (int q = tid; q < k * K; q += kFC) {
     const int t = q / K, ex = r.idx[q];
-    int rank = 0;
-    for (int t2 = 0; t2 < t; ++t2) rank += (r.mask[t2 * (kMaxExperts / 32) + (ex >> 5)] >> (ex & 31)) & 1u;
-    r.gat[r.eoff[ex] + rank] = q;
+    r.gat[r.eoff[ex] + __popc(r.tmask[ex] & ((1u << t) - 1u))] = q;
   }
-  const int ns = p.ns ? 1 : 0, nP = k * K + ns * k, nE = E + ns;  // pairs, expert ids
+  const int ns = r.ns, nP = k * K + ns * k, nE = E + ns;  // pairs, expert ids
   if (ns) {
-    // the shared expert: the last woken expert (id E, above every routed id),
-    // selected by every row with weight 1
-    if (tid == 0) {
-      const int nW = *r.nw;
-      r.woken[nW] = E;
-      r.off[nW + 1] = nP;
-      *r.nw = nW + 1;
-    }
+    // the shared expert's pairs k*K + t, weight 1, in token order
     if (tid < k) {
       r.idx[k * K + tid] = E;
       r.w[k * K + tid] = 1.f;
@@ -314,8 +435,8 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
     const int nW = *r.nw;
     bool bad = tid == 0 && (nW < 1 || nW > nE || nW > k * K + ns || r.off[0] != 0 || r.off[nW] != nP);
     if (!bad && tid < nW && nW <= nE) {
-      const int e = r.woken[tid], m = r.off[tid + 1] - r.off[tid];
-      bad = e < 0 || e >= nE || (tid > 0 && e <= r.woken[tid - 1]) || m < 1 || m > k;
+      const int e = r.s_woken[tid], m = r.off[tid + 1] - r.off[tid];
+      bad = e < 0 || e >= nE || (tid > 0 && e <= r.s_woken[tid - 1]) || m < 1 || m > k;
     }
     if (!bad && tid < nP && nW >= 1 && nW <= nE) {
       const int q = r.gat[tid];
@@ -325,30 +446,30 @@ __device__ __forceinline__ void fused_route(const FusedParams &p, const RouteSme
         const int mid = (lo + hi + 1) >> 1;
         if (r.off[mid] <= tid) lo = mid; else hi = mid - 1;
       }
-      bad = q < 0 || q >= nP || r.idx[q] != r.woken[lo];
+      bad = q < 0 || q >= nP || r.idx[q] != r.s_woken[lo];
     }
     if (bad) *r.bad = 1;
   }
   bar_sync_n(kBarAll, kFC);
   if (*r.bad) {
-    if (tid == 0) atomicOr(p.ws.err, DFV_DEVERR_ROUTING);
+    if (tid == 0) atomicOr(r.err, DFV_DEVERR_ROUTING);
     *r.abort = 1;
   }
   if (blockIdx.x == 0) {
     const int nW = *r.nw;
     for (int q = tid; q < k * K; q += kFC) {
-      p.ws.topk_idx[q] = r.idx[q];
-      if (p.u_idx) p.u_idx[q] = r.idx[q];
+      r.topk_idx[q] = r.idx[q];
+      if (r.u_idx) r.u_idx[q] = r.idx[q];
     }
     for (int q = tid; q < nP; q += kFC) {
-      p.ws.topk_w[q] = r.w[q];
-      p.ws.gather[q] = r.gat[q];
+      r.topk_w[q] = r.w[q];
+      r.gather[q] = r.gat[q];
     }
-    for (int i = tid; i < nW; i += kFC) { p.ws.woken[i] = r.woken[i]; p.ws.offsets[i] = r.off[i]; }
+    for (int i = tid; i < nW; i += kFC) { r.woken[i] = r.s_woken[i]; r.offsets[i] = r.off[i]; }
     if (tid == 0) {
-      p.ws.offsets[nW] = r.off[nW];
-      *p.ws.n_woken = nW;
-      if (p.u_nw) *p.u_nw = nW - ns;  // the caller's count: routed experts only
+      r.offsets[nW] = r.off[nW];
+      *r.n_woken = nW;
+      if (r.u_nw) *r.u_nw = nW - ns;  // the caller's count: routed experts only
     }
   }
 }

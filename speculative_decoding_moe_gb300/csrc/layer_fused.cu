@@ -12,7 +12,9 @@
 // launch); 16 consumer warps and one producer warp.  Before griddepcontrol.wait
 // a CTA only starts its router rows towards L2.  Phases:
 //   P0  router GEMV (optionally on RMSNorm(x) rounded to bf16): CTA b computes
-//       the logits of experts b, b+G, ...; fixed-order reductions.
+//       the logits of experts b, b+G, ...; fixed-order reductions.  The idle
+//       producer first copies the k rows of x into the staged-x rows, while
+//       each warp's router row is in flight.
 //       -- grid barrier 1 --
 //   P1  every CTA derives the whole routing decision itself from the logits:
 //       top-K per row (warp per row, redux max/min: largest logit, lowest id
@@ -99,14 +101,17 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   __shared__ int s_off[kMaxExperts + 2];
   __shared__ int s_eoff[kMaxExperts];
   __shared__ int s_gat[kMaxBlock * (kMaxTopK + 1)];
-  __shared__ unsigned s_mask[kMaxBlock * (kMaxExperts / 32)];
+  __shared__ unsigned s_tmask[kMaxExperts];
   __shared__ float s_inv[kMaxBlock];
-  __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_tok[16];
   __shared__ int s_nw, s_ring, s_split;
   __shared__ volatile int s_abort, s_bad;
+  __shared__ __align__(8) unsigned long long s_xbar;  // the copy of the k rows of x
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the k rows of x are copied into the staged-x rows (idle until gate/up),
+  // which always hold at least k rows
+  const uint32_t xbar = smem_u32(&s_xbar);
   if (tid == 0) {
     s_abort = 0;
     s_bad = 0;
@@ -114,22 +119,33 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kFW);
     }
+    mbar_init(xbar, 1);
     mbar_init_fence();
   }
   __syncthreads();
 
   const bool consumer = warp < kFW;
+  if (!consumer && lane == 0) {
+    stage_x_rows(p, sbase + SH * slot, xbar);
+    if (p.tma_mode) {
+      prefetch_tensormap(&p.tm_wg);
+      prefetch_tensormap(&p.tm_wu);
+    }
+  }
   // ------------------------------------------------------------------ P0, P1: routing
   if (consumer) {
-    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort, &s_bad};
-    fused_route(p, rs, [] {});
-    if (tid == 0) {
-      // with at most 8 tokens per gate/up entry the staged-x rows 8..15 are
-      // unused: they become one more ring stage.  A shared expert with more
-      // than 8 tokens then enters gate/up as two entries (its rows 0-7 and
-      // 8-15), which reads its gate/up rows twice but keeps that stage.
+    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_tmask, s_inv, &s_nw, &s_abort, &s_bad};
+    const RouteArgs ra = route_args(p, rs, reinterpret_cast<const uint16_t *>(scratch), xbar);
+    route_p0(ra);
+    route_p1(ra, [&] {
+      // (warp 0, lane 0, right after the woken list is known; the producer
+      // reads both words) with at most 8 tokens per gate/up entry the
+      // staged-x rows 8..15 are unused: they become one more ring stage.  A
+      // shared expert with more than 8 tokens then enters gate/up as two
+      // entries (its rows 0-7 and 8-15), which reads its gate/up rows twice
+      // but keeps that stage.
       int mmax = 0;
-      const int nw0 = s_abort ? 0 : s_nw;  // one read of the volatile flag, not one per expert
+      const int nw0 = s_nw;
       const int nr = nw0 - ((p.ns && nw0 > 0) ? 1 : 0);  // routed experts
       for (int i = 0; i < nr; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
       const bool extra = NT == 2 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing;
@@ -137,11 +153,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       if (p.ns && nw0 > 0 && !split) mmax = max(mmax, k);
       s_split = split ? 1 : 0;
       s_ring = (extra && mmax <= 8) ? SH + 1 : SH;
-    }
+    });
+  } else {
+    bar_sync_n(kBarProducer, 64);  // released as soon as the woken list is known
   }
-  __syncthreads();  // routing tables visible to the producer
 
-  const int nW = s_abort ? 0 : s_nw;  // an aborted CTA takes no units
+  const int nW = s_nw;  // 0 when the CTA aborted before its routing
   const int S = s_ring;
   // stage s lives in the reserved ring, or (s == SH) in staged-x rows 8..15
   auto slot_addr = [&](int st) -> uint32_t {
@@ -153,20 +170,25 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
     // gate/up entries: the woken experts, the shared one (last) possibly as
     // two halves of 8 tokens
     const int U = (nW + (nW > 0 ? s_split : 0)) * tiles_g;
-    lo_g = (int)(((long long)blockIdx.x * U) / G);
-    hi_g = (int)(((long long)(blockIdx.x + 1) * U) / G);
+    lo_g = (int)((unsigned)blockIdx.x * (unsigned)U / (unsigned)G);
+    hi_g = (int)((unsigned)(blockIdx.x + 1) * (unsigned)U / (unsigned)G);
   }
   const int tiles_d = d / 16;
   int lo_d, hi_d;  // down units (woken expert, 16 d rows), expert-major, contiguous per CTA
   {
     const int U = nW * tiles_d;
-    lo_d = (int)(((long long)blockIdx.x * U) / G);
-    hi_d = (int)(((long long)(blockIdx.x + 1) * U) / G);
+    lo_d = (int)((unsigned)blockIdx.x * (unsigned)U / (unsigned)G);
+    hi_d = (int)((unsigned)(blockIdx.x + 1) * (unsigned)U / (unsigned)G);
   }
 
   if (!consumer) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && !s_abort) {
+      // the consumers read the x copy in the staged-x rows with generic loads,
+      // and rows 8..15 may become a ring stage: order those reads before the
+      // ring's async-proxy writes
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const uint64_t pol = l2_evict_first();  // expert weights are read once per launch
       const uint16_t *wg = reinterpret_cast<const uint16_t *>(p.wg);
       const uint16_t *wu = reinterpret_cast<const uint16_t *>(p.wu);
       const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
@@ -190,18 +212,18 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
           const uint32_t fb = full0 + 8 * s, dst = slot_addr(s);
           mbar_expect_tx(fb, 16u * ks * 2);
           if (p.tma_mode == 2) {  // [ks/256][8 rows][256]: one box per matrix
-            tma_3d(dst, &p.tm_wg, 0, e * I + i0, sl * (ks / 256), fb);
-            tma_3d(dst + up_off, &p.tm_wu, 0, e * I + i0, sl * (ks / 256), fb);
+            tma_3d_hint(dst, &p.tm_wg, 0, e * I + i0, sl * (ks / 256), fb, pol);
+            tma_3d_hint(dst + up_off, &p.tm_wu, 0, e * I + i0, sl * (ks / 256), fb, pol);
           } else if (p.tma_mode == 1) {  // the same layout from 256-column boxes
             for (int b = 0; b < ks / 256; ++b) {
-              tma_2d(dst + b * 4096, &p.tm_wg, sl * ks + b * 256, e * I + i0, fb);
-              tma_2d(dst + up_off + b * 4096, &p.tm_wu, sl * ks + b * 256, e * I + i0, fb);
+              tma_2d_hint(dst + b * 4096, &p.tm_wg, sl * ks + b * 256, e * I + i0, fb, pol);
+              tma_2d_hint(dst + up_off + b * 4096, &p.tm_wu, sl * ks + b * 256, e * I + i0, fb, pol);
             }
           } else {  // one padded row per copy
             for (int r = 0; r < 8; ++r) {
               const size_t row = ((size_t)e * I + i0 + r) * d + (size_t)sl * ks;
-              bulk_g2s(dst + r * rsg, wg + row, ks * 2, fb);
-              bulk_g2s(dst + (8 + r) * rsg, wu + row, ks * 2, fb);
+              bulk_g2s_hint(dst + r * rsg, wg + row, ks * 2, fb, pol);
+              bulk_g2s_hint(dst + (8 + r) * rsg, wu + row, ks * 2, fb, pol);
             }
           }
         }
@@ -223,7 +245,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
         const int wi = u / tiles_d, tl = u - wi * tiles_d;
         const uint32_t fb = full0 + 8 * s;
         mbar_expect_tx(fb, 16u * I * 2);
-        bulk_g2s(slot_addr(s), wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb);
+        bulk_g2s_hint(slot_addr(s), wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb, pol);
       }
       // no copy may land after the CTA exits: wait for the last fill of every stage
       volatile int never = 0;
@@ -231,6 +253,10 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
         if (((used >> s) & 1u) &&
             !mbar_wait(full0 + 8 * s, ((pbits >> s) & 1u) ^ 1u, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never))
           break;
+    }
+    if (lane == 0) {  // the x copy too (complete already unless a wait gave up)
+      volatile int never = 0;
+      mbar_wait(xbar, 0u, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never);
     }
   } else {
     // ---------------------------------------------------------------- P2: gate/up

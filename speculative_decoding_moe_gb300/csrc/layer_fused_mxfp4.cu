@@ -16,12 +16,16 @@
 // groups round-robin, so group q consumes stages q, q+4, q+8, ... (a group with
 // no unit left in a round gets an empty stage); no warp ever waits for another
 // warp's partial sums.
-//   P0, P1  routing, shared with the bf16 single-launch kernel (fused_route);
+//   P0, P1  routing, shared with the bf16 single-launch kernel (route_p0,
+//       route_p1, on the k rows of x the producer copies into the staged-x
+//       rows at the start; the producer starts streaming as soon as the woken
+//       list is known);
 //       an always-on shared expert ("What the pieces cost") joins the tables
 //       as the last woken expert, which every row selects with weight 1.
-//   P2  the k rows of x (after the optional RMSNorm, rounded to bf16) are
-//       staged once in shared memory as fp16, each multiplied by a power of
-//       two that puts its largest magnitude in [2^14, 2^15).  unit = (woken
+//   P2  the k rows of x (after the optional RMSNorm, rounded to bf16) become
+//       fp16 in place in shared memory, each multiplied by a power of two that
+//       puts its largest magnitude in [2^14, 2^15), while the first stages
+//       are in flight.  unit = (woken
 //       expert, 32 d_ff rows), streamed as d/512 stages of 32 gate rows and
 //       32 up rows x 512 codes with their scales (2-D tensor copies).  Warp w
 //       of the group owns rows 8w..8w+7 over the whole of d: it widens its
@@ -127,16 +131,17 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   __shared__ int s_off[kMaxExperts + 2];
   __shared__ int s_eoff[kMaxExperts];
   __shared__ int s_gat[kMaxBlock * (kMaxTopK + 1)];
-  __shared__ unsigned s_mask[kMaxBlock * (kMaxExperts / 32)];
+  __shared__ unsigned s_tmask[kMaxExperts];
   __shared__ float s_inv[kMaxBlock];
   __shared__ float s_xinv[kMaxBlock];             // 2^-shift of each staged x row
   __shared__ float s_hinv[kMxGroups][kMaxBlock];  // 2^-shift of each staged h row, per group
-  __shared__ int s_wsum[kFW], s_csum[kFW];
   __shared__ int s_nw;
   __shared__ unsigned s_last_cta;
   __shared__ volatile int s_abort, s_bad;
+  __shared__ __align__(8) unsigned long long s_xbar;  // the copy of the k rows of x
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t xbar = smem_u32(&s_xbar);
   if (tid == 0) {
     s_abort = 0;
     s_bad = 0;
@@ -144,79 +149,39 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kMxGW);
     }
+    mbar_init(xbar, 1);
     mbar_init_fence();
   }
   __syncthreads();
 
   const bool consumer = warp < kFW;
-  if (consumer) {
-    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_mask, s_inv, s_wsum, s_csum, &s_nw, &s_abort, &s_bad};
-    // the k rows of x are staged in fp16 (warp t: row t) while the other CTAs
-    // finish their router logits
-    fused_route(p, rs, [&] {
-      const int xrow = d * 2;
-      if (warp < k) {
-        const int t = warp, cpr = d / 8;
-        const uint16_t *src = reinterpret_cast<const uint16_t *>(p.x) + (size_t)t * d;
-        __syncwarp();
-        const float inv = p.fuse_norm ? s_inv[t] : 1.f;
-        uint4 v[8];
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int q = lane + 32 * i;
-          v[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (q < cpr) v[i] = *reinterpret_cast<const uint4 *>(src + (size_t)q * 8);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
-            if (p.fuse_norm) {
-              a = rnd_bf16(a * inv);
-              b = rnd_bf16(b * inv);
-            }
-            amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
-          }
-        }
-        const int sh = row_shift(warp_max(amax));
-        const float sc = exp2i(sh);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int q = lane + 32 * i;
-          if (q < cpr) {
-            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            uint32_t o4[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
-              if (p.fuse_norm) {
-                a = rnd_bf16(a * inv);
-                b = rnd_bf16(b * inv);
-              }
-              o4[h] = pack_h2(a * sc, b * sc);
-            }
-            *reinterpret_cast<uint4 *>(scratch + (size_t)t * xrow + swz(q, t) * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-          }
-        }
-        if (lane == 0) s_xinv[t] = exp2i(-sh);
-      }
-
-    });
+  if (!consumer && lane == 0) {
+    // the producer is idle until the routing is known: it copies the k rows
+    // of x into the staged-x rows and warms the tensor maps
+    stage_x_rows(p, smem_u32(scratch), xbar);
+    prefetch_tensormap(&p.tm_wg);
+    prefetch_tensormap(&p.tm_wu);
+    prefetch_tensormap(&p.tm_sg);
+    prefetch_tensormap(&p.tm_su);
   }
-  __syncthreads();  // routing tables visible to the producer
+  if (consumer) {
+    const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_tmask, s_inv, &s_nw, &s_abort, &s_bad};
+    const RouteArgs ra = route_args(p, rs, reinterpret_cast<const uint16_t *>(scratch), xbar);
+    route_p0(ra);
+    route_p1(ra, [] {});
+  } else {
+    bar_sync_n(kBarProducer, 64);  // released as soon as the woken list is known
+  }
 
-  const int nW = s_abort ? 0 : s_nw;  // an aborted CTA takes no units
+  const int nW = s_nw;  // 0 when the CTA aborted before its routing
   const int tiles_g = I / kMxRows, tiles_d = d / 64, nq = d / kMxCols;
   int lo_g, hi_g, lo_d, hi_d;
   {
     const int U = nW * tiles_g, V = nW * tiles_d;
-    lo_g = (int)(((long long)blockIdx.x * U) / G);
-    hi_g = (int)(((long long)(blockIdx.x + 1) * U) / G);
-    lo_d = (int)(((long long)blockIdx.x * V) / G);
-    hi_d = (int)(((long long)(blockIdx.x + 1) * V) / G);
+    lo_g = (int)((unsigned)blockIdx.x * (unsigned)U / (unsigned)G);
+    hi_g = (int)((unsigned)(blockIdx.x + 1) * (unsigned)U / (unsigned)G);
+    lo_d = (int)((unsigned)blockIdx.x * (unsigned)V / (unsigned)G);
+    hi_d = (int)((unsigned)(blockIdx.x + 1) * (unsigned)V / (unsigned)G);
   }
   const int R2 = (hi_g - lo_g + kMxGroups - 1) / kMxGroups, R3 = (hi_d - lo_d + kMxGroups - 1) / kMxGroups;
   // stage layouts: gate/up = [32][256] gate codes | [32][256] up codes |
@@ -229,6 +194,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
   if (!consumer) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && !s_abort) {
+      const uint64_t pol = l2_evict_first();  // expert weights are read once per launch
       const uint8_t *wd = reinterpret_cast<const uint8_t *>(p.wd);
       int it = 0, ps = 0, pph = 0;  // stages issued; slot and phase of the next one
       bool ok = true;
@@ -257,10 +223,10 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
               const int wi = u / tiles_g;
               const int row = s_woken[wi] * I + (u - wi * tiles_g) * kMxRows;
               mbar_expect_tx(fb, bytes_g);
-              tma_2d(dst, &p.tm_wg, q * (kMxCols / 2), row, fb);
-              tma_2d(dst + g_up, &p.tm_wu, q * (kMxCols / 2), row, fb);
-              tma_2d(dst + g_sc, &p.tm_sg, q * (kMxCols / 32), row, fb);
-              tma_2d(dst + g_scu, &p.tm_su, q * (kMxCols / 32), row, fb);
+              tma_2d_hint(dst, &p.tm_wg, q * (kMxCols / 2), row, fb, pol);
+              tma_2d_hint(dst + g_up, &p.tm_wu, q * (kMxCols / 2), row, fb, pol);
+              tma_2d_hint(dst + g_sc, &p.tm_sg, q * (kMxCols / 32), row, fb, pol);
+              tma_2d_hint(dst + g_scu, &p.tm_su, q * (kMxCols / 32), row, fb, pol);
             } else {
               mbar_arrive(fb);  // empty stage: this group has no unit in this round
             }
@@ -281,8 +247,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
             const int wi = u / tiles_d;
             const size_t row = (size_t)s_woken[wi] * d + (size_t)(u - wi * tiles_d) * 64;
             mbar_expect_tx(fb, bytes_d);
-            bulk_g2s(dst, wd + row * rowb_d, 64 * rowb_d, fb);
-            bulk_g2s(dst + d_sc, p.sd + row * srow_d, 64 * srow_d, fb);
+            bulk_g2s_hint(dst, wd + row * rowb_d, 64 * rowb_d, fb, pol);
+            bulk_g2s_hint(dst + d_sc, p.sd + row * srow_d, 64 * srow_d, fb, pol);
           } else {
             mbar_arrive(fb);
           }
@@ -294,6 +260,10 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
       for (int j = it - kMxRing < 0 ? 0 : it - kMxRing; j < it; ++j)
         if (!mbar_wait(full0 + 8 * (j % kMxRing), (j / kMxRing) & 1, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never)) break;
     }
+    if (lane == 0) {  // the x copy too (complete already unless a wait gave up)
+      volatile int never = 0;
+      mbar_wait(xbar, 0u, p.ws.err, DFV_DEVERR_DRAIN_WAIT, &never);
+    }
   } else {
     const int grp = warp / kMxGW, wq = warp % kMxGW;
     const int g = lane >> 2, c = lane & 3;
@@ -304,6 +274,50 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_mx_kernel(const __grid_const
 
     const int xrow = d * 2;  // bytes per staged x row
     const uint32_t xs = smem_u32(scratch);
+    // the k rows of x (bf16, copied in at the start) become fp16 in place,
+    // each times the power of two that puts its largest magnitude in
+    // [2^14, 2^15) (warp t: row t).  The loops stay rolled: this code runs
+    // once per launch, so its size (cold instruction fetch), not its
+    // instruction count, sets its time.
+    if (warp < k) {
+      const int t = warp, cpr = d / 8;
+      unsigned char *row = scratch + (size_t)t * xrow;
+      const float inv = p.fuse_norm ? s_inv[t] : 1.f;
+      // largest magnitude: bf16 patterns without the sign compare as integers
+      uint32_t mb = 0;
+#pragma unroll 1
+      for (int q = lane; q < cpr; q += 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + q * 16);
+        mb = __vmaxu2(mb, __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                   __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
+      }
+      mb = __reduce_max_sync(0xffffffffu, max(mb & 0xffffu, mb >> 16));
+      float amax = __uint_as_float(mb << 16);
+      if (p.fuse_norm) amax = rnd_bf16(amax * inv);  // rounding is monotone: the max of the rounded rows
+      const int sh = row_shift(amax);
+      const float sc = exp2i(sh);
+#pragma unroll 1
+      for (int q0 = 0; q0 < cpr; q0 += 32) {
+        const int q = q0 + lane;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (q < cpr) v = *reinterpret_cast<const uint4 *>(row + q * 16);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float a = bf16_lo(w4[h]), b = bf16_hi(w4[h]);
+          if (p.fuse_norm) {
+            a = rnd_bf16(a * inv);
+            b = rnd_bf16(b * inv);
+          }
+          o4[h] = pack_h2(a * sc, b * sc);
+        }
+        __syncwarp();  // the 32 chunks of this pass are read before any is rewritten
+        if (q < cpr) *reinterpret_cast<uint4 *>(row + swz(q, t) * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+      if (lane == 0) s_xinv[t] = exp2i(-sh);
+    }
+    bar_sync_n(kBarAll, kFC);  // every staged x row is fp16 before any group reads it
     int cs = grp, cph = 0;  // ring slot and phase of this group's next stage
     auto stage_wait = [&]() {
       if (!dead && !mbar_wait_fast(full0 + 8 * cs, cph, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
