@@ -44,11 +44,11 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # reports traffic null.
 KERNEL_SOURCES = {
     "moe_fused_kernel": ["layer_fused.cu", "fused_common.cuh", "dfv_internal.cuh"],
-    "moe_fused_mx_kernel": ["layer_fused_mxfp4.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
+    "moe_fused_bs_kernel": ["layer_fused_bs.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
 }
 NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
     "moe_fused_kernel": ("2f82a8ae8f35161b", 728471040 + 7303680, 77 * 9437184 + 524288),
-    "moe_fused_mx_kernel": ("de3c38d03fce886d", 171788032 + 6460416, 102 * 1671168 + 1048576),
+
 }
 
 
@@ -637,12 +637,12 @@ def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
         "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS},
         "woken_mean": {"k16": Wm, "k1": float(W1.double().mean().item())},
         "verify_decode": {"latency_ratio": ms16 / ms1, "woken_byte_ratio": b16 / b1, "quotient": (b16 / b1) / (ms16 / ms1)},
-        "kernel_path": "moe_fused_mx_kernel (one launch per layer)" if fused else "router + gate/up + down launches",
+        "kernel_path": "moe_fused_bs_kernel<mxfp4> (one launch per layer)" if fused else "router + gate/up + down launches",
         "layer_gbs_events": layer_bytes / (sum(ph) * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "moe_fused_mx_kernel<2> (k=16)" if fused else "multi-launch",
+        "roofline": {"bound": "hbm", "kernel": "moe_fused_bs_kernel<mxfp4, 2> (k=16)" if fused else "multi-launch",
                      "achieved": layer_bytes / (sum(ph) * 1e-3) / 1e9, "peak": peak_bw, "unit": "GB/s",
                      "frac": layer_bytes / (sum(ph) * 1e-3) / 1e9 / peak_bw,
-                     "traffic": ncu_traffic("moe_fused_mx_kernel", layer_bytes) if fused else None,
+                     "traffic": ncu_traffic("moe_fused_bs_kernel", layer_bytes) if fused else None,
                      "per_launch_us": sum(ph) * 1e3, "algorithmic_bytes_per_launch": layer_bytes},
         "device_error": dfv.read_device_error(ws),
     }

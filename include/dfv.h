@@ -68,8 +68,9 @@ enum {
   DFV_ERR_CUDA = 4          /* a CUDA launch or copy failed               */
 };
 
-/* DFV_F16 (IEEE binary16) appears only in dfv_selftest_mma. */
-typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_F16 = 4 } dfv_dtype;
+/* DFV_Q8: 8-bit expert weights (see dfv_moe_layer).  DFV_F16 (IEEE binary16)
+ * appears only in dfv_selftest_mma. */
+typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_Q8 = 3, DFV_F16 = 4 } dfv_dtype;
 
 /* Device-side error bits a kernel may set in the workspace (see
  * dfv_read_device_error).  Every wait inside a kernel is bounded; a wait that
@@ -79,12 +80,14 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_F16 = 4 } dfv_dtype
 #define DFV_DEVERR_SLOT_WAIT 0x2u    /* the producer gave up waiting for a free stage */
 #define DFV_DEVERR_DRAIN_WAIT 0x4u   /* copies still in flight at exit after a timeout */
 #define DFV_DEVERR_GRID_WAIT 0x8u    /* a CTA gave up waiting at a grid-wide barrier */
-/* An mxfp4 scale byte outside [113, 140] was met.  The codes are widened to
- * fp16 and multiplied by their block's scale 2^(s-127) there; inside that range
- * every product is exact, outside it the scaled codes are wrong.  (With the
- * OCP choice of a block's scale, 2^(floor(log2 amax) - 2), that range holds
- * every block whose largest magnitude amax lies in [2^-12, 2^16).)  The
- * kernels finish normally; the outputs of that call are invalid. */
+/* An mxfp4 scale byte outside [113, 140] was met on the multi-kernel path
+ * (layers whose shape the single-launch kernel does not take: see
+ * dfv_moe_layer).  That path widens each code to fp16 and multiplies it by its
+ * block's scale 2^(s-127) in fp16, exact only inside that range (with the OCP
+ * choice of a block's scale, 2^(floor(log2 amax) - 2), blocks whose largest
+ * magnitude lies in [2^-12, 2^16)); outside it the call's outputs are invalid
+ * and this bit says so.  The single-launch kernel applies every scale to fp32
+ * partial sums and is exact for every scale 0..254; it never sets the bit. */
 #define DFV_DEVERR_SCALE_RANGE 0x10u
 #define DFV_DEVERR_REDUCE_WAIT 0x20u /* a warp gave up waiting for a free partial-sum buffer */
 /* A single-launch kernel found its own routing tables inconsistent (an expert
@@ -108,7 +111,14 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_F16 = 4 } dfv_dtype
  * bytes), and s_gate/s_up/s_down hold one E8M0 scale byte per 32 consecutive
  * elements of a row ([E, d_ff, d/32], [E, d_ff, d/32], [E, d, d_ff/32]);
  * element value = e2m1(code) * 2^(scale - 127).  Scale 255 (NaN) is not
- * supported.  For F32/BF16 weights the scale pointers are ignored.
+ * supported.
+ * For w_dtype = DFV_Q8 (8-bit weights; the pages run the target "at Q8" and
+ * fix no format, read here as llama.cpp's Q8_0 block: 32 int8 codes of a row
+ * share one IEEE binary16 scale) the expert matrices hold int8 codes ([E,
+ * d_ff, d], [E, d, d_ff]) and s_gate/s_up/s_down one binary16 scale per 32
+ * consecutive elements of a row, as uint16 patterns ([E, d_ff, d/32], ...);
+ * element value = code * scale.  Scales must be finite.
+ * For F32/BF16 weights the scale pointers are ignored.
  * norm_topk: 1 renormalises the K selected routing weights to sum 1
  * (w_s = p_s / sum p), 0 keeps the softmax probabilities p_s.
  * n_shared: 0, or 1 for one always-on shared expert ("What the pieces cost":
@@ -119,9 +129,13 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_F16 = 4 } dfv_dtype
  * its output is added with weight 1 after the routed sum.  (The pages give it
  * no gate; none is applied.)
  * Supported combinations (w_dtype, r_dtype, activations):
- *   (BF16, BF16, BF16), (MXFP4, BF16, BF16), (F32, F32, F32).
+ *   (BF16, BF16, BF16), (MXFP4, BF16, BF16), (Q8, BF16, BF16), (F32, F32, F32).
  * Shapes: 1 <= K <= min(E, 8), E <= 256, d % 32 == 0, d_ff % 32 == 0
- * (MXFP4: d % 64 == 0 and d_ff % 64 == 0).
+ * (MXFP4: d % 64 == 0 and d_ff % 64 == 0).  Block-scaled layers run in one
+ * launch when d % 512 == 0 (Q8: d % 256 == 0), d <= 2048, 64 <= d_ff <= 512
+ * and d_ff % 128 == 0 (Q8: d_ff % 64 == 0, and d_ff % 256 == 0 above 256);
+ * other MXFP4 shapes take the multi-kernel path, other Q8 shapes are
+ * DFV_ERR_UNSUPPORTED.
  */
 typedef struct dfv_moe_layer {
   int d, n_experts, top_k, d_ff, norm_topk;
@@ -202,7 +216,7 @@ int dfv_moe_block_forward_host(const dfv_moe_layer *layer, const void *hidden_ho
  * Pre-norm residual stack of MoE layers over a bf16 residual stream, in place:
  *   n_l     = bf16(x_l / sqrt(mean(x_l^2) + eps))      (RMSNorm, unit gain)
  *   x_{l+1} = bf16(x_l + MoE_l(n_l))                    (one rounding)
- *   layers  host array of n_layers layer descriptors (BF16 or MXFP4 experts,
+ *   layers  host array of n_layers layer descriptors (BF16, MXFP4 or Q8 experts,
  *           BF16 router), all with the same d
  *   x       [k, d] bf16 device buffer, input and output
  */

@@ -96,14 +96,23 @@ int check_layer(const dfv_moe_layer *L, int act) {
   if (L->d % 32 || L->d_ff % 32) return fail(DFV_ERR_UNSUPPORTED, "d and d_ff must be multiples of 32");
   const bool ok = (L->w_dtype == DFV_BF16 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
                   (L->w_dtype == DFV_MXFP4 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
+                  (L->w_dtype == DFV_Q8 && L->r_dtype == DFV_BF16 && act == DFV_BF16) ||
                   (L->w_dtype == DFV_F32 && L->r_dtype == DFV_F32 && act == DFV_F32);
   if (!ok)
     return fail(DFV_ERR_UNSUPPORTED, "unsupported dtype combination (experts %d, router %d, act %d)", L->w_dtype,
                 L->r_dtype, act);
   if (!L->w_router || !L->w_gate || !L->w_up || !L->w_down) return fail(DFV_ERR_INVALID_ARG, "NULL weight pointer");
-  if (L->w_dtype == DFV_MXFP4) {
-    if (L->d % 64 || L->d_ff % 64) return fail(DFV_ERR_UNSUPPORTED, "mxfp4 layers need d and d_ff multiples of 64");
-    if (!L->s_gate || !L->s_up || !L->s_down) return fail(DFV_ERR_INVALID_ARG, "mxfp4 layer without scale pointers");
+  if (L->w_dtype == DFV_MXFP4 || L->w_dtype == DFV_Q8) {
+    if (L->w_dtype == DFV_MXFP4 && (L->d % 64 || L->d_ff % 64))
+      return fail(DFV_ERR_UNSUPPORTED, "mxfp4 layers need d and d_ff multiples of 64");
+    if (L->w_dtype == DFV_Q8) {
+      dfv::FusedPlan qp;
+      if (!dfv::fused_bs_plan(DFV_Q8, 1, L->d, L->d_ff, L->n_experts, &qp))
+        return fail(DFV_ERR_UNSUPPORTED, "8-bit layers need d %% 256 == 0, d <= 2048, d_ff %% 64 == 0, "
+                                         "64 <= d_ff <= 512 and d_ff %% 256 == 0 above 256 (d=%d, d_ff=%d)",
+                    L->d, L->d_ff);
+    }
+    if (!L->s_gate || !L->s_up || !L->s_down) return fail(DFV_ERR_INVALID_ARG, "block-scaled layer without scale pointers");
     if (!aligned(L->s_gate, 16) || !aligned(L->s_up, 16) || !aligned(L->s_down, 16))
       return fail(DFV_ERR_INVALID_ARG, "scale pointers must be 16-byte aligned");
   }
@@ -171,10 +180,10 @@ dfv::RouterParams router_params(const dfv_moe_layer *L, const void *x, int act, 
 int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void *out, const void *residual,
                     bool fuse_norm, float eps, int32_t *u_idx, int32_t *u_nw, const dfv::Workspace &w,
                     cudaStream_t s) {
-  const bool mx = L->w_dtype == DFV_MXFP4;
+  const bool mx = L->w_dtype == DFV_MXFP4 || L->w_dtype == DFV_Q8;  // block-scaled experts
   if ((L->w_dtype != DFV_BF16 && !mx) || L->r_dtype != DFV_BF16 || act != DFV_BF16) return -1;
   dfv::FusedPlan plan;
-  if (!(mx ? dfv::fused_mx_plan(k, L->d, L->d_ff, L->n_experts, &plan)
+  if (!(mx ? dfv::fused_bs_plan(L->w_dtype, k, L->d, L->d_ff, L->n_experts, &plan)
            : dfv::fused_plan(k, L->d, L->d_ff, L->n_experts, &plan)))
     return -1;
   static std::mutex mu;
@@ -184,11 +193,11 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
   int grid;
   {
     std::lock_guard<std::mutex> lock(mu);
-    auto key = std::make_tuple(dev, mx ? 1 : 0, k <= 8 ? 1 : 2, plan.smem);
+    auto key = std::make_tuple(dev, mx ? L->w_dtype : 0, k <= 8 ? 1 : 2, plan.smem);
     auto it = cache.find(key);
     if (it == cache.end()) {
       char why[256] = {0};
-      const int gmax = mx ? dfv::fused_mx_max_grid(plan, k, why, sizeof why)
+      const int gmax = mx ? dfv::fused_bs_max_grid(plan, L->w_dtype, k, why, sizeof why)
                           : dfv::fused_max_grid(plan, k, why, sizeof why);
       if (gmax <= 0 && g_fused_why.empty()) g_fused_why = why;
       it = cache.emplace(key, gmax).first;
@@ -209,7 +218,7 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
     fp.su = L->s_up;
     fp.sd = L->s_down;
     char why[256] = {0};
-    if (!dfv::fused_mx_tensor_maps(&fp, L, why, sizeof why)) {
+    if (!dfv::fused_bs_tensor_maps(&fp, L, why, sizeof why)) {
       std::lock_guard<std::mutex> lock(mu);
       if (g_fused_why.empty()) g_fused_why = why;
       return -1;
@@ -233,7 +242,7 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
     g_last_staging = fp.tma_mode;
   }
   auto go = [&](bool pdl) {
-    return mx ? dfv::launch_fused_mx(fp, plan, grid, s, pdl) : dfv::launch_fused(fp, plan, grid, s, pdl);
+    return mx ? dfv::launch_fused_bs(fp, L->w_dtype, plan, grid, s, pdl) : dfv::launch_fused(fp, plan, grid, s, pdl);
   };
   mark(0, s);
   cudaError_t e = go(true);
@@ -259,6 +268,9 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
       return st;
     }
   }
+  if (L->w_dtype == DFV_Q8)  // 8-bit weights run only in the single-launch kernel
+    return fail(DFV_ERR_UNSUPPORTED, "8-bit layer: the single-launch kernel is unavailable (%s)",
+                g_fused_enabled ? g_fused_why.c_str() : "multi-kernel path selected");
   g_last_path = 0;
   dfv::RouterParams rp = router_params(L, x, act, k, w);
   rp.fuse_norm = fuse_norm ? 1 : 0;

@@ -83,9 +83,12 @@ struct FfnParams {
 };
 
 struct FusedParams {
-  // mxfp4 experts: 2-D tensor maps over the gate/up codes ([E*d_ff][d/2] bytes,
-  // box 256 x 32) and their scales ([E*d_ff][d/32] bytes, box 16 x 32)
-  CUtensorMap tm_wg, tm_wu, tm_sg, tm_su;
+  // block-scaled experts (mxfp4, 8-bit): 2-D tensor maps over the gate / up /
+  // down codes (boxes of 64 bytes x 32 or 64 rows, 64-byte swizzle) and the
+  // gate / up scales (boxes of 16 bytes x 32 rows); tm_sd over the down scales
+  // when a down row takes more than one stage.  The bf16 kernel uses tm_wg and
+  // tm_wu for its gate/up boxes.
+  CUtensorMap tm_wg, tm_wu, tm_sg, tm_su, tm_wd, tm_sd;
   const void *x;         // [k][d] bf16 rows (the residual stream when fuse_norm)
   const void *residual;  // [k][d] bf16 or null: added in the combine
   void *out;             // [k][d] bf16
@@ -331,12 +334,13 @@ int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
 cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 // fills p->tm_wg / tm_wu and p->tma_mode (<= max_mode) for a bf16 layer (mode 0 when no tensor map fits)
 void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode);
-// single-launch layer with mxfp4 experts (layer_fused_mxfp4.cu)
-bool fused_mx_plan(int k, int d, int I, int E, FusedPlan *plan);
-// fills p->tm_* for an mxfp4 layer; false (with a reason) when the driver refuses
-bool fused_mx_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, size_t why_len);
-int fused_mx_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
-cudaError_t launch_fused_mx(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
+// single-launch layer with block-scaled experts, fmt = DFV_MXFP4 or DFV_Q8
+// (layer_fused_bs.cu)
+bool fused_bs_plan(int fmt, int k, int d, int I, int E, FusedPlan *plan);
+// fills p->tm_* for a block-scaled layer; false (with a reason) when the driver refuses
+bool fused_bs_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, size_t why_len);
+int fused_bs_max_grid(const FusedPlan &plan, int fmt, int k, char *why, size_t why_len);
+cudaError_t launch_fused_bs(const FusedParams &p, int fmt, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);

@@ -14,11 +14,11 @@ from .inputs import LayerWeights
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdfv.so")
 
-F32, BF16, MXFP4, F16 = 0, 1, 2, 4
+F32, BF16, MXFP4, Q8, F16 = 0, 1, 2, 3, 4
 # device error bits (DFV_DEVERR_* in include/dfv.h)
 DEVERR_STAGE_WAIT, DEVERR_SLOT_WAIT, DEVERR_DRAIN_WAIT, DEVERR_GRID_WAIT = 0x1, 0x2, 0x4, 0x8
 DEVERR_SCALE_RANGE, DEVERR_REDUCE_WAIT, DEVERR_ROUTING = 0x10, 0x20, 0x40
-_NAMES = {"f32": F32, "bf16": BF16, "mxfp4": MXFP4}
+_NAMES = {"f32": F32, "bf16": BF16, "mxfp4": MXFP4, "q8": Q8}
 EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_profile_set_events",
            "dfv_read_device_error", "dfv_set_path", "dfv_last_layer_path", "dfv_fused_unavailable_reason",
            "dfv_accept_greedy_noalloc", "dfv_set_staging", "dfv_last_staging",

@@ -16,6 +16,9 @@ weights), scaled to one layer:
 * ``mxfp4``     d=2048, E=256, top-8, d_ff=512, e2m1 codes uniform over the 16
                 nibbles, e8m0 scales uniform in 2^{-8..0}, bf16 router
                 ~N(0, 0.02), bf16 activations.
+* ``q8``        the mxfp4 layer's shape with 8-bit weights: int8 codes uniform
+                over [-127, 127], one binary16 scale per 32 elements uniform in
+                w_std/73.3 * [0.5, 1.5) (weights of the other layers' spread).
 * ``e256+shared`` d=2048, E=256, top-8, d_ff=512, bf16, plus one always-on
                 shared expert of the same size ("What the pieces cost"; the
                 model card it cites: 8 routed plus 1 shared activated).
@@ -52,6 +55,8 @@ TINY = LayerShape(d=256, n_experts=16, top_k=2, d_ff=128, w_dtype="f32", r_dtype
                   w_std=0.02, r_std=0.05)
 A3B = LayerShape(d=2048, n_experts=128, top_k=8, d_ff=768)
 MXFP4 = LayerShape(d=2048, n_experts=256, top_k=8, d_ff=512, w_dtype="mxfp4")
+# the same layer with 8-bit weights (int8 codes, one binary16 scale per 32 elements)
+Q8 = LayerShape(d=2048, n_experts=256, top_k=8, d_ff=512, w_dtype="q8")
 # 256 routed experts (top-8) plus one always-on shared expert of the same size
 E256_SHARED = LayerShape(d=2048, n_experts=256, top_k=8, d_ff=512, n_shared=1)
 

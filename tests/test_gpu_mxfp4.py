@@ -45,7 +45,7 @@ def path(request, dfv):
 
 def _fused_ok(d, I):
     """Shapes the single-launch mxfp4 kernel takes (others use the multi-launch path)."""
-    return d % 512 == 0 and d <= 2048 and I % 64 == 0 and I <= 512
+    return d % 512 == 0 and d <= 2048 and I % 128 == 0 and 128 <= I <= 512
 
 
 def _check_path(dfv, path, d=2048, I=512):
@@ -93,7 +93,8 @@ def _one_hot_rows(k, d, seed):
     return x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("d,I", [(64, 64), (128, 192), (320, 128), (512, 64), (1024, 192), (2048, 448)])
+@pytest.mark.parametrize("d,I", [(64, 64), (128, 192), (320, 128), (512, 64), (512, 128), (1024, 192), (2048, 384),
+                                 (2048, 448)])
 @pytest.mark.parametrize("scale_exp", [(119, 127), (113, 140)])
 def test_decode_every_code_and_scale_one_hot(dfv, path, d, I, scale_exp):
     """One expert, K = 1 (routing weight exactly 1): with one-hot rows the gate
@@ -117,9 +118,51 @@ def test_decode_every_code_and_scale_one_hot(dfv, path, d, I, scale_exp):
         assert _max_rel_err(got[t:t + 1], ref[t:t + 1]) <= TOL_DECODE, t
 
 
+@pytest.mark.parametrize("d,I", [(512, 256), (2048, 512), (1024, 128)])
+def test_fused_decode_exact_for_every_scale(dfv, d, I):
+    """The single-launch kernel applies each block's scale to fp32 partial
+    sums, so every E8M0 exponent is exact as long as the values stay inside
+    the fp32 range (above 251 the largest E2M1 codes, 6 * 2^125, would leave
+    it at any input).  Gate scales are drawn over 0..251 and each up scale is
+    251 minus its gate scale (g * u stays near 1, so h is finite and normal);
+    each down row r has one scale s_r spread over 20..219.  With one-hot rows every output is a short sum; each output is
+    divided by 2^(s_r - 127) before the comparison, so rows of every
+    magnitude are held to the same bar."""
+    s = _shape(d, 1, 1, I)
+    lw = inputs.make_layer(s, seed=d + 3 * I)
+    g = torch.Generator().manual_seed(d + I)
+    lw.s_gate = torch.randint(0, 252, lw.s_gate.shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    lw.s_up = (251 - lw.s_gate.to(torch.int32)).to(torch.uint8)
+    srow = (20 + (torch.arange(d) * 37) % 200).to(torch.uint8)
+    lw.s_down = srow.view(1, d, 1).expand(lw.s_down.shape).contiguous()
+    assert int(lw.s_gate.min()) == 0 and int(lw.s_gate.max()) == 251
+    ol = oracle_layer(lw)
+    k = 16
+    x = _one_hot_rows(k, d, seed=d + 1)
+    dfv.set_path(True)
+    L = dfv.Layer(lw.to("cuda"))
+    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
+    out = dfv.moe_block_forward(L, x.cuda(), ws)
+    torch.cuda.synchronize()
+    _check_path(dfv, "fused", d, I)
+    assert dfv.read_device_error(ws) == 0
+    ref = oracle.moe_forward(ol, np_of(x))
+    norm = np.exp2(srow.double().numpy() - 127.0)
+    got = _out_np(out) / norm
+    refn = ref / norm
+    assert np.all(np.isfinite(got))
+    for t in range(k):
+        assert _max_rel_err(got[t:t + 1], refn[t:t + 1]) <= TOL_DECODE, t
+
+
 @pytest.mark.parametrize("bad_scale", [112, 141])
 @pytest.mark.parametrize("d", [128, 512])
-def test_scale_outside_exact_range_sets_device_error(dfv, path, bad_scale, d):
+def test_scale_outside_exact_range_sets_device_error_on_the_multi_launch_path(dfv, bad_scale, d):
+    """The multi-launch mxfp4 kernels scale codes in fp16, exact for scales in
+    [113, 140]; outside it they report DFV_DEVERR_SCALE_RANGE (d_ff = 64 is a
+    shape only they take)."""
+    path = "multi"
+    dfv.set_path(False)
     s = _shape(d, 4, 2, 64)
     lw = inputs.make_layer(s, seed=3)
     lw.s_gate[0, 0, 0] = bad_scale
@@ -131,6 +174,7 @@ def test_scale_outside_exact_range_sets_device_error(dfv, path, bad_scale, d):
     dfv.moe_block_forward(L, x, ws)
     torch.cuda.synchronize()
     _check_path(dfv, path, d, 64)
+    dfv.set_path(True)
     assert dfv.read_device_error(ws) & dfv.DEVERR_SCALE_RANGE
 
 
@@ -139,10 +183,12 @@ SMALL = [
     (320, 24, 3, 192),
     (512, 40, 8, 128),
     (256, 8, 8, 64),  # K == E: every row wakes every expert
-    (512, 16, 4, 192),   # single-launch kernel: one gate/up stage per unit, ragged d_ff chunk
-    (2048, 24, 8, 64),   # single-launch kernel: four gate/up stages per unit
-    (512, 8, 1, 64),     # top-1 routing, fewer experts than a warp has lanes
-    (1024, 4, 2, 448),   # four experts: up to 16 tokens each (second pass over held stages)
+    (512, 16, 4, 192),   # multi-launch path: ragged d_ff chunk
+    (512, 16, 4, 256),   # single-launch kernel: one gate/up stage per unit, two 64-byte boxes per down row
+    (2048, 24, 8, 128),  # single-launch kernel: four gate/up stages per unit
+    (512, 8, 1, 128),    # top-1 routing, fewer experts than a warp has lanes
+    (1024, 4, 2, 384),   # four experts: up to 16 tokens each (both token tiles), three boxes per down row
+    (1024, 4, 2, 448),   # multi-launch path: up to 16 tokens per expert
 ]
 
 

@@ -4,9 +4,10 @@ the shared expert and its split gate/up entries, and the extreme index of
 every shared-memory, TMA, global-weight, h and ys access a unit makes, checked
 against the size of its buffer.  The formulas are the kernel's (layer_fused.cu:
 fused_plan, slot_addr, the producer's copies, the consumers' fragment loads and
-stores).  mxfp4 (layer_fused_mxfp4.cu): the plan, the gate/up and down stage
-layouts, the tensor-map coordinates, the swizzled x and h staging and the hf /
-ys stores.  Routing comes from seeded draws of the sweep's kinds
+stores).  Block-scaled weights, mxfp4 and 8-bit (layer_fused_bs.cu): the plan,
+the gate/up and down stage layouts, the ldmatrix addresses in the 64-byte
+swizzled boxes, the tensor-map coordinates, the swizzled x and h staging and
+the hf / ys stores.  Routing comes from seeded draws of the sweep's kinds
 (repeated-token and independent blocks)."""
 from __future__ import annotations
 
@@ -169,94 +170,143 @@ def test_fused_bf16_indices_stay_in_their_buffers(d, I):
     assert (True, 0, True) in extra_stage and (True, 1, True) in extra_stage
 
 
-# ---------------------------------------------------------------- mxfp4 single-launch kernel
-MX_GROUPS, MX_RING, MX_CH, MX_ROWS, MX_COLS, MX_MAX_D = 4, 8, 4, 32, 512, 2048
+# ---------------------------------------------------------------- block-scaled single-launch kernel
+BS_GROUPS, BS_RING, BS_ROWS_G, BS_ROWS_D, BS_ROW_BYTES, BS_BOX, BS_MAX_D = 4, 8, 32, 64, 256, 64, 2048
+BS_CODES, BS_STAGE, BS_SLOT = 16384, 17408, 18432
+FMT = {"mxfp4": dict(CPS=512, BPI=4, SB=1, num=1, den=2), "q8": dict(CPS=256, BPI=2, SB=2, num=1, den=1)}
 
 
-def mx_plan(k, d, I):
-    """fused_mx_plan / mx_smem of layer_fused_mxfp4.cu."""
-    if d % MX_COLS or d > MX_MAX_D or I % 64 or I > 128 * MX_CH:
+def bs_plan(fmt, k, d, I):
+    """fused_bs_plan / bs_smem of layer_fused_bs.cu."""
+    if d > BS_MAX_D or I > 512 or I < 64:
+        return None
+    if fmt == "mxfp4" and (d % 512 or I % 128):
+        return None
+    if fmt == "q8" and (d % 256 or I % 64 or (I > 256 and I % 256)):
         return None
     NT = 1 if k <= 8 else 2
-    slot = max(MX_ROWS * MX_COLS + MX_ROWS * MX_COLS // 16, 34 * I)
-    slot = (slot + 127) & ~127
-    ipad = (I + 127) // 128 * 128
-    scratch = max(NT * 8 * d * 2, MX_GROUPS * NT * 8 * ipad * 2)
+    scratch = max(NT * 8 * d * 2, BS_GROUPS * NT * 8 * I * 2)
     scratch = (scratch + 127) & ~127
-    smem = MX_RING * slot + scratch + 16 * MX_RING + (FW * 32 * 16 if NT == 2 else 0)
-    return None if smem > SMEM_BUDGET else dict(NT=NT, slot=slot, scratch=scratch, smem=smem)
+    smem = 1024 + BS_RING * BS_SLOT + scratch + 16 * BS_RING
+    return None if smem + 8 * 1024 > SMEM_MAX else dict(NT=NT, scratch=scratch, smem=smem)
 
 
-def swz(q, j):
-    return q ^ (((q >> 3) & 1) | ((j & 1) << 1))
+def sw64(box, row, j):
+    """the kernel's sw64: chunk j of row `row` of a 64-byte-swizzled box."""
+    return box + row * BS_BOX + ((j ^ ((row >> 1) & 3)) << 4)
 
 
-def check_mx_layer(k, d, I, E, K, idx, ns):
-    P = mx_plan(k, d, I)
+def swz2(q, r):
+    return q ^ ((r & 1) << 2)
+
+
+def check_bs_layer(fmt, k, d, I, E, K, idx, ns):
+    P = bs_plan(fmt, k, d, I)
     if P is None:
         return None
-    NT, slot, scratch = P["NT"], P["slot"], P["scratch"]
+    F = FMT[fmt]
+    NT, scratch = P["NT"], P["scratch"]
+    assert P["smem"] + 7168 <= SMEM_MAX  # + the kernel's static shared memory
     woken, off, gat = tables(idx, k, K, E, ns)
     nW, nP = len(woken), k * K + ns * k
-    # gate/up stage: [32][256] gate codes | [32][256] up codes | [32][16] gate scales | [32][16] up scales
-    g_up = MX_ROWS * MX_COLS // 2
-    g_sc, g_scu = 2 * g_up, 2 * g_up + MX_ROWS * MX_COLS // 32
-    bytes_g = 2 * g_up + 2 * MX_ROWS * MX_COLS // 32
-    assert bytes_g <= slot
-    rw, c, j = 31, 3, MX_CH - 1  # the largest row, lane column and chunk
-    assert g_up + rw * (MX_COLS // 2) + c * 16 + j * 64 + 16 <= g_sc       # up codes
-    assert g_scu + rw * (MX_COLS // 32) + c + j * 4 + 1 <= bytes_g         # up scales
-    # down stage: [64][I/2] codes | [64][I/32] scales
-    rowb_d, srow_d = I // 2, I // 32
-    d_sc, bytes_d = 64 * rowb_d, 64 * rowb_d + 64 * srow_d
-    assert bytes_d <= slot
-    CI = (I + 127) // 128
-    for c in (0, 3):
-        # with a ragged last 128-code chunk, lanes c >= 2 skip it (no codes there)
-        jl = CI - 1 if (I % 128 == 0 or c < 2) else CI - 2
-        if jl >= 0:
-            assert 63 * rowb_d + c * 16 + jl * 64 + 16 <= d_sc  # codes of row 63
-            assert d_sc + 63 * srow_d + c + jl * 4 + 1 <= bytes_d  # its scales
-    # TMA coordinates: x bytes 16-aligned, boxes inside the matrices
-    nq = d // MX_COLS
+    Et = E + ns
+    cb = lambda n: n * F["num"] // F["den"]  # code bytes of n elements
+    # ---- gate/up stage: [4 boxes][32][64] gate | same for up | [32][16] gate scales | [32][16] up scales
+    up_off, sc_off, scu_off = BS_CODES // 2, BS_CODES, BS_CODES + 512
+    assert scu_off + 32 * 16 == BS_STAGE <= BS_SLOT and BS_SLOT % 1024 == 0
+    for itb in range(4):
+        for wq in range(4):
+            for lane in range(32):
+                a = sw64(up_off + itb * BS_ROWS_G * BS_BOX, wq * 8 + (lane & 7), lane >> 3)
+                assert up_off <= a and a + 16 <= sc_off  # ldmatrix rows of the up codes
+                assert (up_off + itb * BS_ROWS_G * BS_BOX) % 512 == 0  # swizzle atom alignment
+    assert scu_off + 31 * 16 + 16 <= BS_STAGE  # lds128 of the last up-scale row
+    nq = d // F["CPS"]
+    assert cb(d) == nq * BS_ROW_BYTES
+    for q in (0, nq - 1):  # TMA x coordinates: 16-byte aligned, boxes inside the row
+        for b in range(4):
+            x = q * BS_ROW_BYTES + b * BS_BOX
+            assert x % 16 == 0 and x + BS_BOX <= cb(d)
+        assert (q * 16) % 16 == 0 and q * 16 + 16 <= d // 32 * F["SB"]
+    # ---- down stage: [nb boxes][64][64] codes | [64][srs] scales
+    rowb = cb(I)
+    nqd = (rowb + BS_ROW_BYTES - 1) // BS_ROW_BYTES
+    srow = I // 32 * F["SB"]
+    srs = srow if nqd == 1 else 16
+    assert (srow * 64) % 16 == 0 and (nqd == 1 or srow % 16 == 0)  # bulk size / tensor-map stride
+    for q in range(nqd):
+        nb = min(4, (rowb - q * BS_ROW_BYTES) // BS_BOX)
+        assert 1 <= nb <= 4 and (rowb - q * BS_ROW_BYTES) % BS_BOX == 0
+        assert nb * BS_ROWS_D * BS_BOX <= BS_CODES and BS_CODES + BS_ROWS_D * srs <= BS_STAGE
+        for b in range(nb):
+            x = q * BS_ROW_BYTES + b * BS_BOX
+            assert x % 16 == 0 and x + BS_BOX <= rowb
+        for itb in range(nb):
+            for wq in range(4):
+                for lane in (0, 7, 31):
+                    for half in (0, 8):
+                        a = sw64(itb * BS_ROWS_D * BS_BOX, wq * 16 + half + (lane & 7), lane >> 3)
+                        assert 0 <= a and a + 16 <= nb * BS_ROWS_D * BS_BOX
+            # scale words: rows up to 63, word itb
+            assert BS_CODES + 63 * srs + itb * 4 + 4 <= BS_CODES + BS_ROWS_D * srs
+            assert (63 * srs + itb * 4) % 4 == 0
+            # blocks of this box: the B chunk index stays inside the staged h row
+            for mb in range(F["BPI"]):
+                hq = q * (F["CPS"] // 8) + (itb * F["BPI"] + mb) * 4 + 3
+                assert swz2(hq, 1) < I // 8 and swz2(hq, 0) < I // 8
+    # ---- staged x (P2) and h (P3) rows
+    xrow, cpr = d * 2, d // 8
+    assert k * xrow <= scratch and cpr % 64 == 0
+    assert all(swz2(q, t) < cpr for q in range(cpr) for t in (0, 1))
     for q in (0, nq - 1):
-        assert (q * (MX_COLS // 2)) % 16 == 0 and (q * (MX_COLS // 32)) % 16 == 0
-        assert q * (MX_COLS // 2) + 256 <= d // 2 and q * (MX_COLS // 32) + 16 <= d // 32
-    # staged x rows (P2): k rows of d fp16, 16-byte pieces swizzled within groups of 4
-    xrow = d * 2
-    cpr = d // 8
-    assert all(swz(q, t) < cpr for q in range(cpr) for t in (0, 1))
-    assert k * xrow <= scratch
-    # B reads of token t: bt = t*xrow + c*64 + ((tt ^ sw) << 4), plus chunk (q*4 + j)*256
-    assert 3 * 64 + (3 << 4) + ((nq - 1) * MX_CH + MX_CH - 1) * 256 + 16 <= xrow
-    # staged h rows (P3): per group NT*8 rows of CI*256 bytes
-    hrow = CI * 256
-    assert MX_GROUPS * NT * 8 * hrow <= scratch
-    assert all(swz(q, n) < CI * 16 for q in range(CI * 16) for n in (0, 1))
-    assert 3 * 64 + (3 << 4) + (CI - 1) * 256 + 16 <= hrow
-    tiles_g, tiles_d = I // MX_ROWS, d // 64
+        for blk in range(F["CPS"] // 32):
+            xq = q * (F["CPS"] // 8) + blk * 4 + 3
+            assert swz2(xq, 1) < cpr
+    hrow, hcpr = I * 2, I // 8
+    assert BS_GROUPS * NT * 8 * hrow <= scratch and hcpr % 8 == 0
+    assert (BS_GROUPS - 1) * NT * 8 * hrow + (NT * 8 - 1) * hrow + hcpr * 16 <= scratch
+    # ---- weights, h and ys
+    tiles_g, tiles_d = I // BS_ROWS_G, d // BS_ROWS_D
     for wi in range(nW):
         e, eo, m = woken[wi], off[wi], off[wi + 1] - off[wi]
         assert m <= NT * 8
-        assert e * I + (tiles_g - 1) * MX_ROWS + MX_ROWS <= (E + ns) * I  # gate/up box rows
-        row = e * d + (tiles_d - 1) * 64
-        assert (row + 64) * rowb_d <= (E + ns) * d * rowb_d and (row * srow_d) % 16 == 0 and (64 * srow_d) % 16 == 0
+        assert e * I + (tiles_g - 1) * BS_ROWS_G + BS_ROWS_G <= Et * I  # gate/up box rows
+        row = e * d + (tiles_d - 1) * BS_ROWS_D
+        assert row + BS_ROWS_D <= Et * d and (row * srow) % 16 == 0
         for tok in range(m):
             pair = gat[eo + tok]
             assert 0 <= pair < nP
-            assert (eo + tok) * I + (tiles_g - 1) * MX_ROWS + 3 * 8 + 7 < MAX_BLOCK * (K + ns) * I  # hf (fp32)
-            assert pair * d + (tiles_d - 1) * 64 + 3 * 16 + 7 + 8 < MAX_BLOCK * (K + ns) * d       # ys
+            assert (eo + tok) * I + (tiles_g - 1) * BS_ROWS_G + 3 * 8 + 7 < MAX_BLOCK * (K + ns) * I  # hf (fp32)
+            assert pair * d + (tiles_d - 1) * BS_ROWS_D + 3 * 16 + 7 + 8 < MAX_BLOCK * (K + ns) * d  # ys
     return True
 
 
+@pytest.mark.parametrize("fmt", ["mxfp4", "q8"])
 @pytest.mark.parametrize("d", [512, 1024, 2048])
-@pytest.mark.parametrize("I", [64, 192, 448, 512])
-def test_fused_mxfp4_indices_stay_in_their_buffers(d, I):
-    rnd = random.Random(d * 7919 + I)
+@pytest.mark.parametrize("I", [64, 128, 256, 384, 512])
+def test_fused_block_scaled_indices_stay_in_their_buffers(fmt, d, I):
+    rnd = random.Random(d * 7919 + I + (1 if fmt == "q8" else 0))
     checked = 0
     for E, K in ((4, 2), (16, 4), (256, 8)):
         for k in (1, 8, 9, 16):
             for idx in _draws(k, E, K, rnd):
                 for ns in (0, 1):
-                    checked += check_mx_layer(k, d, I, E, K, idx, ns) is not None
-    assert checked > 0
+                    checked += check_bs_layer(fmt, k, d, I, E, K, idx, ns) is not None
+    ok = bs_plan(fmt, 16, d, I) is not None
+    assert (checked > 0) == ok
+
+
+def test_q8_block_order_matches_the_mma_k_slots():
+    """The 8-bit kernel stores each 32-element block of a token row so that
+    lane c's 16-byte chunk holds elements 4c..4c+3 and 16+4c..16+4c+3 (the k
+    slots its two MMAs take from code chunks 2m and 2m+1); the shuffle
+    permutation (q8_permute) reaches exactly that."""
+    for lane in range(32):
+        cc, base = lane & 3, lane & ~3
+        s1, s2 = base + (cc >> 1), base + 2 + (cc >> 1)
+        h = cc & 1
+        # input chunk of lane L holds elements 8 (L & 3) .. +8 of its block, as 4 words of 2
+        words = [(8 * (s1 & 3) + 2 * (2 * h + i), 8 * (s1 & 3) + 2 * (2 * h + i) + 1) for i in range(2)]
+        words += [(8 * (s2 & 3) + 2 * (2 * h + i), 8 * (s2 & 3) + 2 * (2 * h + i) + 1) for i in range(2)]
+        got = [e for w in words for e in w]
+        assert got == [4 * cc, 4 * cc + 1, 4 * cc + 2, 4 * cc + 3, 16 + 4 * cc, 17 + 4 * cc, 18 + 4 * cc, 19 + 4 * cc]

@@ -99,7 +99,7 @@ def test_old_shared_odd_ring_is_caught():
 
 
 def mx_ring(units_g, units_d, nq, ring=8, groups=4):
-    """layer_fused_mxfp4.cu: rounds of one stage per group, round robin over
+    """layer_fused_bs.cu: rounds of one stage per group, round robin over
     the ring (a group without a unit in a round still gets a stage, filled
     empty); group q's stages are q, q + groups, ..."""
     R2 = -(-units_g // groups)
@@ -132,7 +132,7 @@ def test_mxfp4_ring_groups_own_their_stages():
 
 
 def test_mxfp4_down_units_wait_for_exactly_the_owner_ctas():
-    """layer_fused_mxfp4.cu: CTA b takes gate/up units [floor(bU/G),
+    """layer_fused_bs.cu: CTA b takes gate/up units [floor(bU/G),
     floor((b+1)U/G)).  Before a down group reads expert wi's h it waits for
     the flags of CTAs b0..b1, from the closed form owner(u) =
     floor(((u+1)G - 1)/U).  Every CTA holding one of the expert's units must be
