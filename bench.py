@@ -44,7 +44,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # reports traffic null.
 KERNEL_SOURCES = {
     "moe_fused_kernel": ["layer_fused.cu", "fused_common.cuh", "dfv_internal.cuh"],
-    "moe_fused_bs_kernel": ["layer_fused_bs.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
+    "moe_fused_bs_kernel_mxfp4": ["layer_fused_bs.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
+    "moe_fused_bs_kernel_q8": ["layer_fused_bs.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
 }
 NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
     "moe_fused_kernel": ("2f82a8ae8f35161b", 728471040 + 7303680, 77 * 9437184 + 524288),
@@ -541,6 +542,7 @@ def run_gpu(args):
            "api": "dfv_moe_block_forward_host per layer, pinned host buffers"}
 
     mx = None if args.no_mxfp4 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
+    q8 = None if args.no_q8 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw, fmt="q8")
     sh = None if args.no_shared else shared_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
 
     cpu = None
@@ -566,7 +568,7 @@ def run_gpu(args):
         "kernel_path": {"fused": fused_used, "why_not": dfv.fused_unavailable_reason()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
-        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "mxfp4": mx, "shared_expert": sh,
+        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "mxfp4": mx, "q8": q8, "shared_expert": sh,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -576,11 +578,13 @@ def run_gpu(args):
     return 0
 
 
-def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
-    """mxfp4 experts: E=256, top-8, d=2048, d_ff=512, 40 layers, bf16 activations.
-    Bytes per woken expert count the packed codes and the scale bytes."""
-    progress("mxfp4 section")
-    shape = inputs.MXFP4
+def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw, fmt="mxfp4"):
+    """Block-scaled experts, E=256, top-8, d=2048, d_ff=512, 40 layers, bf16
+    activations: mxfp4 (e2m1 codes + e8m0 per 32) or, with fmt="q8", 8-bit
+    codes + a binary16 scale per 32 (the pages' "Q8" target).  Bytes per woken
+    expert count the codes and the scale bytes."""
+    progress("%s section" % fmt)
+    shape = inputs.MXFP4 if fmt == "mxfp4" else inputs.Q8
     layers = [inputs.make_layer(shape, seed=5000 + 1000 * rank + l, device=dev) for l in range(N_LAYERS)]
     Ls = [dfv.Layer(w) for w in layers]
     exp_bytes = layers[0].expert_bytes()
@@ -629,20 +633,21 @@ def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
     gate_bytes = Wm * 2 * (shape.d_ff * shape.d // 2 + shape.d_ff * shape.d // 32)
     down_bytes = Wm * (shape.d * shape.d_ff // 2 + shape.d * shape.d_ff // 32)
     layer_bytes = Wm * exp_bytes + router_bytes
+    desc = "mxfp4 experts (e2m1 + e8m0/32)" if fmt == "mxfp4" else "8-bit experts (int8 + binary16/32)"
     res = {
-        "config": "E=256 top-8 d=2048 d_ff=512 mxfp4 experts (e2m1 + e8m0/32), bf16 router and activations, "
-                  "40 layers, k=16; inputs > L2 (%.1f GB of weights)" % (N_LAYERS * (exp_bytes * 256 + router_bytes) / 1e9),
+        "config": "E=256 top-8 d=2048 d_ff=512 %s, bf16 router and activations, "
+                  "40 layers, k=16; inputs > L2 (%.1f GB of weights)" % (desc, N_LAYERS * (exp_bytes * 256 + router_bytes) / 1e9),
         "value_gbs": b16 / (ms16 * 1e-3) / 1e9, "frac_of_measured_hbm": b16 / (ms16 * 1e-3) / 1e9 / peak_bw,
         "ms_per_pass": {"k16": ms16, "k1": ms1},
         "layer_us": {"k16": ms16 * 1e3 / N_LAYERS, "k1": ms1 * 1e3 / N_LAYERS},
         "woken_mean": {"k16": Wm, "k1": float(W1.double().mean().item())},
         "verify_decode": {"latency_ratio": ms16 / ms1, "woken_byte_ratio": b16 / b1, "quotient": (b16 / b1) / (ms16 / ms1)},
-        "kernel_path": "moe_fused_bs_kernel<mxfp4> (one launch per layer)" if fused else "router + gate/up + down launches",
+        "kernel_path": "moe_fused_bs_kernel<%s> (one launch per layer)" % fmt if fused else "router + gate/up + down launches",
         "layer_gbs_events": layer_bytes / (sum(ph) * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "moe_fused_bs_kernel<mxfp4, 2> (k=16)" if fused else "multi-launch",
+        "roofline": {"bound": "hbm", "kernel": "moe_fused_bs_kernel<%s, 2> (k=16)" % fmt if fused else "multi-launch",
                      "achieved": layer_bytes / (sum(ph) * 1e-3) / 1e9, "peak": peak_bw, "unit": "GB/s",
                      "frac": layer_bytes / (sum(ph) * 1e-3) / 1e9 / peak_bw,
-                     "traffic": ncu_traffic("moe_fused_bs_kernel", layer_bytes) if fused else None,
+                     "traffic": ncu_traffic("moe_fused_bs_kernel_" + fmt, layer_bytes) if fused else None,
                      "per_launch_us": sum(ph) * 1e3, "algorithmic_bytes_per_launch": layer_bytes},
         "device_error": dfv.read_device_error(ws),
     }
@@ -757,6 +762,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-mxfp4", action="store_true", help="skip the mxfp4-expert section")
     ap.add_argument("--no-shared", action="store_true", help="skip the shared-expert section")
+    ap.add_argument("--no-q8", action="store_true", help="skip the 8-bit-expert section")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=40, help="layers per step (profiling runs only)")
     args = ap.parse_args()

@@ -31,10 +31,10 @@
 // exponent 0..254 and every binary16 scale the products are exact, and only
 // the fp32 sums round.  The token rows (x for gate/up, h for down) sit in
 // shared memory as fp16, each multiplied by the power of two 2^sh that puts
-// its largest magnitude in [2^14, 2^15) (exact); every block scale carries a
-// factor 2^-14, so the accumulators hold 2^(sh-14) times the true sums
-// (about their true size: no overflow short of the fp32 range itself), and
-// the per-token factor 2^(14-sh) brings them back; for 8-bit weights the 32 elements of each block are stored in the
+// its largest magnitude in [1, 2), so the accumulators hold about the true
+// sums (no overflow short of the fp32 range itself) and 2^-sh brings them
+// back; bf16 elements down to 2^-17 of their row's largest stay exact, and
+// smaller ones round at 2^-25 of it; for 8-bit weights the 32 elements of each block are stored in the
 // order the MMA's k slots take them, so one 16-byte load feeds two MMAs in
 // both formats.
 //
@@ -96,11 +96,12 @@ struct Fmt<kFmtMx> {
   static constexpr int CPS = 512, BPI = 4, SB = 1;
   // A fragments of block m of the four chunks ch[]: pairs of codes 8c..8c+7
   __device__ static __forceinline__ void frag(const uint32_t (&ch)[4], int m, uint32_t (&a)[4]) { e2m1_word(ch[m], a); }
-  // the scale of block m of this iteration, from word `w` of the row's
-  // scales, times 2^-14: 2^(s-141), exact (below 2^-126 as an fp32 subnormal)
+  // the scale 2^(s-127) of block m of this iteration, from word `w` of the
+  // row's scales: byte m moved into the fp32 exponent field (s = 0 gives
+  // the fp32 subnormal 2^-127)
   __device__ static __forceinline__ float scale(uint32_t w, int m) {
-    const uint32_t s = (w >> (8 * m)) & 0xffu;
-    return __uint_as_float(s >= 15u ? (s - 14u) << 23 : 1u << (s + 8u));
+    const uint32_t e = (m < 3 ? (w << (23 - 8 * m)) : (w >> 1)) & 0x7f800000u;
+    return __uint_as_float(max(e, 0x00400000u));
   }
 };
 // int8 code bytes b0..b3 -> fp16x2 (b0, b1), (b2, b3), exactly: 0x64XX is
@@ -120,11 +121,19 @@ struct Fmt<kFmtQ8> {
     q8_word(ch[2 * m], a[0], a[1]);
     q8_word(ch[2 * m + 1], a[2], a[3]);
   }
-  // block m's binary16 scale times 2^-14 (exact)
+  // block m's binary16 scale (exact in fp32)
   __device__ static __forceinline__ float scale(uint32_t w, int m) {
-    return __half2float(__ushort_as_half((unsigned short)(m ? (w >> 16) : (w & 0xffffu)))) * 0x1p-14f;
+    return __half2float(__ushort_as_half((unsigned short)(m ? (w >> 16) : (w & 0xffffu))));
   }
 };
+
+// Power-of-two exponent that brings a row's largest magnitude amax into [1, 2).
+__device__ __forceinline__ int row_shift1(float amax) {
+  if (!(amax > 0.f) || !(amax < INFINITY)) return 0;
+  int ex;
+  frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+  return min(max(1 - ex, -126), 126);
+}
 
 // 16-byte chunk q of staged token row r sits at chunk q ^ ((r & 1) << 2):
 // the quarter-warp reading chunks Q..Q+3 of rows 2i and 2i+1 then spans all
@@ -223,8 +232,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
   __shared__ int s_gat[kMaxBlock * (kMaxTopK + 1)];
   __shared__ unsigned s_tmask[kMaxExperts];
   __shared__ float s_inv[kMaxBlock];
-  __shared__ float s_xinv[kMaxBlock];             // 2^(14-shift) of each staged x row
-  __shared__ float s_hinv[kBsGroups][kMaxBlock];  // 2^(14-shift) of each staged h row, per group
+  __shared__ float s_xinv[kMaxBlock];             // 2^-shift of each staged x row
+  __shared__ float s_hinv[kBsGroups][kMaxBlock];  // 2^-shift of each staged h row, per group
   __shared__ int s_nw;
   __shared__ unsigned s_last_cta;
   __shared__ volatile int s_abort, s_bad;
@@ -376,8 +385,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
     const uint32_t xs = smem_u32(scratch);
 
     // the k rows of x (bf16, copied in at the start) become fp16 in place,
-    // each times the power of two that puts its largest magnitude in
-    // [2^14, 2^15) (warp t: row t), chunks swizzled (and, for 8-bit weights,
+    // each times the power of two that puts its largest magnitude in [1, 2)
+    // (warp t: row t), chunks swizzled (and, for 8-bit weights,
     // each block's elements in k-slot order).  The loops stay rolled: this
     // code runs once per launch, so its size (cold instruction fetch), not
     // its instruction count, sets its time.
@@ -395,7 +404,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
       mb = __reduce_max_sync(0xffffffffu, max(mb & 0xffffu, mb >> 16));
       float amax = __uint_as_float(mb << 16);
       if (p.fuse_norm) amax = rnd_bf16(amax * inv);  // rounding is monotone: the max of the rounded row
-      const int sh = row_shift(amax);
+      const int sh = row_shift1(amax);
       const float sc = exp2i(sh);
 #pragma unroll 1
       for (int q0 = 0; q0 < cpr; q0 += 32) {  // cpr is a multiple of 64
@@ -416,7 +425,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
         __syncwarp();  // the 32 chunks of this pass are read before any is rewritten
         *reinterpret_cast<uint4 *>(row + swz2(q, t) * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
-      if (lane == 0) s_xinv[t] = exp2i(14 - sh);  // the block scales carry the other 2^-14
+      if (lane == 0) s_xinv[t] = exp2i(-sh);
     }
     bar_sync_n(kBarAll, kFC);  // every staged x row is fp16 before any group reads it
 
@@ -468,6 +477,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
         const uint32_t st = sbase + cs * kBsSlot;
         const int rw = wq * 8 + g;  // this lane's gate / up row in the stage
         const uint4 sgv = lds128(st + kScOff + rw * 16), suv = lds128(st + kScUpOff + rw * 16);
+        // B chunks: lane c's chunk of block blk of this stage in token row t
+        // sits at 4 * (blk ^ (t & 1)) + c (swizzle): per parity, one base for
+        // even and one for odd blocks, plus an immediate per block
+        const uint32_t xq0 = (uint32_t)(q * (F::CPS / 8) + c) * 16;
+        const uint32_t x0e = xb0 + xq0 + ((t0 & 1) ? 64u : 0u), x0o = xb0 + xq0 - ((t0 & 1) ? 64u : 0u);
+        const uint32_t x1e = xb1 + xq0 + ((t1 & 1) ? 64u : 0u), x1o = xb1 + xq0 - ((t1 & 1) ? 64u : 0u);
 #pragma unroll 1
         for (int itb = 0; itb < 4; ++itb) {  // one box = four 16-byte chunks per row
           uint32_t cg[4], cu[4];
@@ -475,32 +490,33 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
           ldsm_x4(sw64(st + kUpOff + itb * (kBsRowsG * kBsBox), wq * 8 + lrow, lchunk), cu);
           const uint32_t swg = itb == 0 ? sgv.x : itb == 1 ? sgv.y : itb == 2 ? sgv.z : sgv.w;
           const uint32_t swu = itb == 0 ? suv.x : itb == 1 ? suv.y : itb == 2 ? suv.z : suv.w;
+          const uint32_t ib = (uint32_t)itb * F::BPI * 64;
 #pragma unroll
           for (int mb = 0; mb < F::BPI; ++mb) {
             uint32_t ag[4], au[4];
             F::frag(cg, mb, ag);
             F::frag(cu, mb, au);
             const float fg = F::scale(swg, mb), fu = F::scale(swu, mb);
-            // x elements of this block for k slots of lane c: chunk q*CPS/8 + block*4 + c
-            const int xq = q * (F::CPS / 8) + (itb * F::BPI + mb) * 4 + c;
             float tmp[4];
             {
-              const uint4 b = lds128(xb0 + swz2(xq, t0) * 16);
+              const uint4 b = lds128(((mb & 1) ? x0o : x0e) + ib + mb * 64);
+              float tmp2[4];  // the block's two MMAs are independent: no MMA-to-MMA latency
               mma_f16_z(tmp, ag[0], au[0], ag[1], au[1], b.x, b.y);
-              mma_f16x(tmp, ag[2], au[2], ag[3], au[3], b.z, b.w);
-              acc0[0] = fmaf(fg, tmp[0], acc0[0]);
-              acc0[1] = fmaf(fg, tmp[1], acc0[1]);
-              acc0[2] = fmaf(fu, tmp[2], acc0[2]);
-              acc0[3] = fmaf(fu, tmp[3], acc0[3]);
+              mma_f16_z(tmp2, ag[2], au[2], ag[3], au[3], b.z, b.w);
+              acc0[0] = fmaf(fg, tmp[0] + tmp2[0], acc0[0]);
+              acc0[1] = fmaf(fg, tmp[1] + tmp2[1], acc0[1]);
+              acc0[2] = fmaf(fu, tmp[2] + tmp2[2], acc0[2]);
+              acc0[3] = fmaf(fu, tmp[3] + tmp2[3], acc0[3]);
             }
             if (NT == 2 && two) {
-              const uint4 b = lds128(xb1 + swz2(xq, t1) * 16);
+              const uint4 b = lds128(((mb & 1) ? x1o : x1e) + ib + mb * 64);
+              float tmp2[4];  // the block's two MMAs are independent: no MMA-to-MMA latency
               mma_f16_z(tmp, ag[0], au[0], ag[1], au[1], b.x, b.y);
-              mma_f16x(tmp, ag[2], au[2], ag[3], au[3], b.z, b.w);
-              acc1[0] = fmaf(fg, tmp[0], acc1[0]);
-              acc1[1] = fmaf(fg, tmp[1], acc1[1]);
-              acc1[2] = fmaf(fu, tmp[2], acc1[2]);
-              acc1[3] = fmaf(fu, tmp[3], acc1[3]);
+              mma_f16_z(tmp2, ag[2], au[2], ag[3], au[3], b.z, b.w);
+              acc1[0] = fmaf(fg, tmp[0] + tmp2[0], acc1[0]);
+              acc1[1] = fmaf(fg, tmp[1] + tmp2[1], acc1[1]);
+              acc1[2] = fmaf(fu, tmp[2] + tmp2[2], acc1[2]);
+              acc1[3] = fmaf(fu, tmp[3] + tmp2[3], acc1[3]);
             }
           }
         }
@@ -581,7 +597,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
               for (int i = 0; i < 4; ++i)
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j][i].x), fabsf(v[j][i].y)),
                                          fmaxf(fabsf(v[j][i].z), fabsf(v[j][i].w))));
-              const int sh = row_shift(warp_max(amax));
+              const int sh = row_shift1(warp_max(amax));
               const float sc = exp2i(sh);
 #pragma unroll
               for (int cq = 0; cq < 2; ++cq) {
@@ -594,7 +610,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
                   *reinterpret_cast<uint4 *>(hrows + (size_t)n * hrow + swz2(q, n) * 16) =
                       make_uint4(o4[0], o4[1], o4[2], o4[3]);
               }
-              if (lane == 0) s_hinv[grp][n] = exp2i(14 - sh);  // the block scales carry the other 2^-14
+              if (lane == 0) s_hinv[grp][n] = exp2i(-sh);
             }
           }
         }
@@ -616,40 +632,44 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
         const uint32_t st = sbase + cs * kBsSlot;
         const int nb = min(4, (rowb_d - q * kBsRowBytes) / kBsBox);
         const int rlo = wq * 16 + g, rhi = rlo + 8;  // this lane's two rows in the stage
+        const uint32_t hq0 = (uint32_t)(q * (F::CPS / 8) + c) * 16;
+        const uint32_t h0e = hb0 + hq0 + ((n0s & 1) ? 64u : 0u), h0o = hb0 + hq0 - ((n0s & 1) ? 64u : 0u);
+        const uint32_t h1e = hb1 + hq0 + ((n1s & 1) ? 64u : 0u), h1o = hb1 + hq0 - ((n1s & 1) ? 64u : 0u);
 #pragma unroll 1
         for (int itb = 0; itb < nb; ++itb) {
-          uint32_t c0r[4], c1r[4];
+          uint32_t c0r[4], c1r[4], wlo, whi;
           const uint32_t box = st + itb * (kBsRowsD * kBsBox);
           ldsm_x4(sw64(box, wq * 16 + lrow, lchunk), c0r);
           ldsm_x4(sw64(box, wq * 16 + 8 + lrow, lchunk), c1r);
-          uint32_t wlo, whi;
           asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wlo) : "r"(st + kScOff + rlo * srs_d + itb * 4));
           asm volatile("ld.shared.u32 %0, [%1];" : "=r"(whi) : "r"(st + kScOff + rhi * srs_d + itb * 4));
+          const uint32_t ib = (uint32_t)itb * F::BPI * 64;
 #pragma unroll
           for (int mb = 0; mb < F::BPI; ++mb) {
             uint32_t a0[4], a1[4];
             F::frag(c0r, mb, a0);
             F::frag(c1r, mb, a1);
             const float f0 = F::scale(wlo, mb), f1 = F::scale(whi, mb);
-            const int hq = q * (F::CPS / 8) + (itb * F::BPI + mb) * 4 + c;
             float tmp[4];
             {
-              const uint4 b = lds128(hb0 + swz2(hq, n0s) * 16);
+              const uint4 b = lds128(((mb & 1) ? h0o : h0e) + ib + mb * 64);
+              float tmp2[4];  // the block's two MMAs are independent: no MMA-to-MMA latency
               mma_f16_z(tmp, a0[0], a1[0], a0[1], a1[1], b.x, b.y);
-              mma_f16x(tmp, a0[2], a1[2], a0[3], a1[3], b.z, b.w);
-              acc0[0] = fmaf(f0, tmp[0], acc0[0]);
-              acc0[1] = fmaf(f0, tmp[1], acc0[1]);
-              acc0[2] = fmaf(f1, tmp[2], acc0[2]);
-              acc0[3] = fmaf(f1, tmp[3], acc0[3]);
+              mma_f16_z(tmp2, a0[2], a1[2], a0[3], a1[3], b.z, b.w);
+              acc0[0] = fmaf(f0, tmp[0] + tmp2[0], acc0[0]);
+              acc0[1] = fmaf(f0, tmp[1] + tmp2[1], acc0[1]);
+              acc0[2] = fmaf(f1, tmp[2] + tmp2[2], acc0[2]);
+              acc0[3] = fmaf(f1, tmp[3] + tmp2[3], acc0[3]);
             }
             if (NT == 2 && two) {
-              const uint4 b = lds128(hb1 + swz2(hq, n1s) * 16);
+              const uint4 b = lds128(((mb & 1) ? h1o : h1e) + ib + mb * 64);
+              float tmp2[4];  // the block's two MMAs are independent: no MMA-to-MMA latency
               mma_f16_z(tmp, a0[0], a1[0], a0[1], a1[1], b.x, b.y);
-              mma_f16x(tmp, a0[2], a1[2], a0[3], a1[3], b.z, b.w);
-              acc1[0] = fmaf(f0, tmp[0], acc1[0]);
-              acc1[1] = fmaf(f0, tmp[1], acc1[1]);
-              acc1[2] = fmaf(f1, tmp[2], acc1[2]);
-              acc1[3] = fmaf(f1, tmp[3], acc1[3]);
+              mma_f16_z(tmp2, a0[2], a1[2], a0[3], a1[3], b.z, b.w);
+              acc1[0] = fmaf(f0, tmp[0] + tmp2[0], acc1[0]);
+              acc1[1] = fmaf(f0, tmp[1] + tmp2[1], acc1[1]);
+              acc1[2] = fmaf(f1, tmp[2] + tmp2[2], acc1[2]);
+              acc1[3] = fmaf(f1, tmp[3] + tmp2[3], acc1[3]);
             }
           }
         }
