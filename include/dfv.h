@@ -342,6 +342,19 @@ int dfv_selftest_bounded_waits(void *ws, size_t ws_bytes, void *stream);
  */
 int dfv_selftest_mma(int dtype, const void *A, const void *B, float *D, void *stream);
 
+/*
+ * Self-test of the fifth-generation tensor-core path the batched kernels use
+ * (no counterpart on the method's pages): one CTA computes
+ *   D[i][j] = sum_l A[i][l] * B[j][l]     (128 x N x K, bf16 in, fp32 out)
+ * with the operands in shared memory (128-byte swizzled, K-major), tcgen05
+ * MMAs into tensor memory and tcgen05 loads back.
+ *   A [128][K], B [N][K] bf16 (device), D [128][N] fp32 (device)
+ *   N = 16..256, a multiple of 16; K = 64 or 128
+ *   status [1] int32 (device, zeroed by the caller): 1 if the bounded wait
+ *   for the MMAs gave up (D is then not written).
+ */
+int dfv_selftest_tcgen05(const void *A, const void *B, int N, int K, float *D, int32_t *status, void *stream);
+
 const char *dfv_status_string(int status);
 const char *dfv_last_error_detail(void);
 int dfv_version(void);

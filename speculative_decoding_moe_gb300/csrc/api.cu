@@ -13,6 +13,7 @@
 namespace dfv {
 cudaError_t launch_wait_selftest(const Workspace &w, cudaStream_t s);  // selftest.cu
 cudaError_t launch_mma_selftest(const void *A, const void *B, float *D, int bf16, cudaStream_t s);
+cudaError_t launch_tc05_selftest(const void *A, const void *B, int N, int K, float *D, int *status, cudaStream_t s);
 }
 
 namespace {
@@ -508,6 +509,16 @@ int dfv_selftest_mma(int dtype, const void *A, const void *B, float *D, void *st
     return fail(DFV_ERR_INVALID_ARG, "A, B and D must be non-NULL and 16-byte aligned");
   cudaError_t e = dfv::launch_mma_selftest(A, B, D, dtype == DFV_BF16 ? 1 : 0, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "MMA self-test launch");
+  return DFV_OK;
+}
+
+int dfv_selftest_tcgen05(const void *A, const void *B, int N, int K, float *D, int32_t *status, void *stream) {
+  if (N < 16 || N > 256 || N % 16 || (K != 64 && K != 128))
+    return fail(DFV_ERR_UNSUPPORTED, "tcgen05 self-test takes N = 16..256 (multiple of 16) and K = 64 or 128");
+  if (!A || !B || !D || !status || !aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
+    return fail(DFV_ERR_INVALID_ARG, "A, B, D and status must be non-NULL, A, B and D 16-byte aligned");
+  cudaError_t e = dfv::launch_tc05_selftest(A, B, N, K, D, status, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 self-test launch");
   return DFV_OK;
 }
 

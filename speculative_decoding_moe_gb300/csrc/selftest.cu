@@ -88,3 +88,92 @@ cudaError_t launch_mma_selftest(const void *A, const void *B, float *D, int bf16
 }
 
 }  // namespace dfv
+
+// ----------------------------------------------------------------------------
+// The tcgen05 path on one tile (no counterpart in the method: it lets a test
+// check the shared-memory and instruction descriptors, the TMEM allocation and
+// the epilogue loads against a plain matrix product before the batched expert
+// kernels rely on them).  One CTA of four warps: the operands go to shared
+// memory in the 128-byte-swizzled K-major layout, one thread issues K/16 MMAs
+// into TMEM (M = 128 rows of A, N rows of B), commits them to an mbarrier, and
+// each warp reads its 32 TMEM lanes back.  The wait is bounded (2 s); a
+// timeout leaves status = 1.
+#include "tc05.cuh"
+
+namespace dfv {
+
+__global__ void __launch_bounds__(128) tc05_selftest_kernel(const uint16_t *A, const uint16_t *B, int N, int K,
+                                                            float *D, int *status) {
+  extern __shared__ __align__(1024) unsigned char tsm_raw[];
+  unsigned char *tsm = tsm_raw + ((1024u - (smem_u32(tsm_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) unsigned long long s_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int natoms = K / 64;
+  const uint32_t a_base = smem_u32(tsm), b_base = a_base + (uint32_t)natoms * 128u * 128u;
+  // operands into the swizzled layout: atom a holds K columns [64a, 64a + 64)
+  for (int i = tid; i < 128 * K; i += 128) {
+    const int r = i / K, kk = i % K;
+    *reinterpret_cast<uint16_t *>(tsm + (kk / 64) * 128 * 128 + sw128_off(r, kk % 64)) = A[i];
+  }
+  for (int i = tid; i < N * K; i += 128) {
+    const int r = i / K, kk = i % K;
+    *reinterpret_cast<uint16_t *>(tsm + natoms * 128 * 128 + (kk / 64) * N * 128 + sw128_off(r, kk % 64)) = B[i];
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> async-proxy reads
+  const uint32_t bar = smem_u32(&s_bar);
+  uint32_t ncols = 32;
+  while ((int)ncols < N) ncols <<= 1;
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(bar, 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&s_tmem), ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16(128, N);
+    for (int ks = 0; ks < K / 16; ++ks) {
+      const int at = ks / 4, kk = ks % 4;
+      const uint64_t ad = sdesc_k128(a_base + (uint32_t)at * 128u * 128u) + (uint64_t)(2 * kk);
+      const uint64_t bd = sdesc_k128(b_base + (uint32_t)at * (uint32_t)N * 128u) + (uint64_t)(2 * kk);
+      tc_mma(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+    }
+    tc_commit(bar);
+  }
+  __syncwarp();
+  bool ok = true;
+  if (lane == 0) ok = mbar_wait(bar, 0u, (unsigned *)status, 1u, &s_abort);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  tc_fence_after();
+  if (ok) {
+    const int row = warp * 32 + lane;
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) D[row * N + c0 + j] = v[j];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
+cudaError_t launch_tc05_selftest(const void *A, const void *B, int N, int K, float *D, int *status, cudaStream_t s) {
+  const size_t smem = 1024 + (size_t)(128 + N) * K * 2;
+  cudaError_t e = cudaFuncSetAttribute(tc05_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  tc05_selftest_kernel<<<1, 128, smem, s>>>(static_cast<const uint16_t *>(A), static_cast<const uint16_t *>(B), N, K,
+                                           D, status);
+  return cudaGetLastError();
+}
+
+}  // namespace dfv

@@ -24,7 +24,8 @@ EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_pro
            "dfv_accept_greedy_noalloc", "dfv_set_staging", "dfv_last_staging",
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
-           "dfv_accept_workspace_size", "dfv_accept_greedy", "dfv_selftest_bounded_waits", "dfv_selftest_mma")
+           "dfv_accept_workspace_size", "dfv_accept_greedy", "dfv_selftest_bounded_waits", "dfv_selftest_mma",
+           "dfv_selftest_tcgen05")
 
 
 class DfvError(RuntimeError):
@@ -74,6 +75,7 @@ def _load():
         L.dfv_read_device_error.argtypes = [P, P, P]
         L.dfv_selftest_bounded_waits.argtypes = [P, S, P]
         L.dfv_selftest_mma.argtypes = [I, P, P, P, P]
+        L.dfv_selftest_tcgen05.argtypes = [P, P, I, I, P, P, P]
         L.dfv_set_path.argtypes = [I]
         L.dfv_set_staging.restype = I
         L.dfv_set_staging.argtypes = [I]
@@ -249,6 +251,19 @@ def selftest_mma(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
     out = torch.empty(16, 16, dtype=torch.float32, device=a.device)
     _check(_load().dfv_selftest_mma(code, _p(a), _p(b), _p(out), _stream(stream)), "dfv_selftest_mma")
     return out
+
+
+def selftest_tcgen05(a: torch.Tensor, b: torch.Tensor, stream=None):
+    """D = A . B^T (A [128, K], B [N, K], bf16) through the tcgen05 / TMEM path;
+    returns (D [128, N] fp32, status)."""
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16 or a.shape[0] != 128 or a.shape[1] != b.shape[1]:
+        raise ValueError("A must be [128, K] and B [N, K], both bf16")
+    a, b = a.contiguous(), b.contiguous()
+    d = torch.full((128, b.shape[0]), float("nan"), dtype=torch.float32, device=a.device)
+    st = torch.zeros(1, dtype=torch.int32, device=a.device)
+    _check(_load().dfv_selftest_tcgen05(_p(a), _p(b), b.shape[0], a.shape[1], _p(d), _p(st), _stream(stream)),
+           "dfv_selftest_tcgen05")
+    return d, st
 
 
 def set_staging(max_mode: int):
