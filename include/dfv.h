@@ -99,6 +99,7 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_Q8 = 3, DFV_F16 = 4
 #define DFV_MAX_BLOCK 16      /* k: positions in one verify block          */
 #define DFV_MAX_EXPERTS 256   /* E                                          */
 #define DFV_MAX_TOPK 8        /* K                                          */
+#define DFV_MAX_BATCH_ROWS 512 /* n_blocks * k in one batched verify call     */
 
 /*
  * One MoE layer.  All weights are caller-owned device memory.
@@ -222,6 +223,32 @@ int dfv_moe_block_forward_host(const dfv_moe_layer *layer, const void *hidden_ho
  */
 int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, int k, float eps,
                           void *ws, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace dfv_moe_batch_forward needs for up to n_rows_max rows
+ * (n_blocks * k) of a layer (0 on invalid arguments). */
+size_t dfv_moe_batch_workspace_size(const dfv_moe_layer *layer, int n_rows_max);
+
+/*
+ * Batched verify: n_blocks verify blocks of k positions each (T = n_blocks * k
+ * <= 512 rows, e.g. 32 concurrent requests with 16-token blocks; the MI355X /
+ * vLLM write-up, section "Results: Throughput and Speedup", serves up to 32)
+ * through one MoE layer, every row routed on its own exactly as in
+ * dfv_moe_block_forward:
+ *   out[t] = sum_s w[t,s] y_{idx[t,s]}(x[t])  (+ y_E(x[t]) with a shared expert)
+ * Rows of different blocks share nothing but the weights: each woken expert's
+ * weights are streamed once for all rows of all blocks that route to it.
+ *   hidden [T, d] bf16 rows, block b in rows [b k, (b+1) k)
+ *   out    [T, d] bf16
+ *   opt_topk_idx [T, K] int32, opt_n_woken [1] int32 (routed experts woken
+ *          by the whole batch): optional copies of the routing (NULL to skip)
+ * Supported: bf16 experts and router, d % 128 == 0, d_ff % 128 == 0,
+ * d <= 8192.  Row t's routing equals dfv_moe_block_forward's on the block
+ * holding t (the same fp32 logits); the expert contractions run on the
+ * fifth-generation tensor cores, fp32 accumulation, h rounded to bf16.
+ * The workspace needs no zero-filling: every call rewrites what it reads.
+ */
+int dfv_moe_batch_forward(const dfv_moe_layer *layer, const void *hidden, int n_blocks, int k, void *out,
+                          int32_t *opt_topk_idx, int32_t *opt_n_woken, void *ws, size_t ws_bytes, void *stream);
 
 /* Bytes of workspace dfv_accept_greedy needs for up to k_max drafted tokens
  * over a vocabulary of V (0 on invalid arguments). */

@@ -258,6 +258,43 @@ int run_layer_fused(const dfv_moe_layer *L, const void *x, int act, int k, void 
   return DFV_OK;
 }
 
+// Batched-verify workspace: counters (first 256 bytes), the error word at byte
+// 256 (as in the single-block workspace), then the tables and buffers.
+struct BatchWs {
+  dfv::BatchParams p;
+  size_t bytes;
+};
+BatchWs batch_layout(const dfv_moe_layer *L, int tmax, void *base) {
+  BatchWs b = {};
+  const size_t E = L->n_experts, K = L->top_k, d = L->d, I = L->d_ff, ns = L->n_shared ? 1 : 0;
+  const size_t T = ((size_t)tmax + 31) / 32 * 32, P = T * K + ns * T;
+  const size_t units = (E + 1) * ((I > d ? I : d) / 128) * 2;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void * {
+    void *q = base ? (void *)((char *)base + off) : nullptr;
+    off += align256(bytes);
+    return q;
+  };
+  b.p.n_units = (int *)take(16);
+  b.p.err = (unsigned *)take(4);
+  b.p.n_woken = (int32_t *)take(4);
+  b.p.logits = (float *)take(T * E * 4);
+  b.p.tmask = (unsigned *)take((E + 1) * (T / 32) * 4);
+  b.p.topk_idx = (int32_t *)take(T * K * 4);
+  b.p.topk_w = (float *)take(P * 4);
+  b.p.woken = (int32_t *)take((E + 1) * 4);
+  b.p.off = (int32_t *)take((E + 2) * 4);
+  b.p.gather = (int32_t *)take(P * 4);
+  b.p.units_g = (int4 *)take(units * 16);
+  b.p.units_d = (int4 *)take(units * 16);
+  b.p.xg = take(P * d * 2);
+  b.p.h = (uint16_t *)take(P * I * 2);
+  b.p.ys = (float *)take(P * d * 4);
+  b.p.Tmax = (int)T;
+  b.bytes = off;
+  return b;
+}
+
 thread_local bool g_fused_enabled = true;
 
 int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, const void *residual,
@@ -465,6 +502,53 @@ int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, in
     const dfv::Workspace w = layout(&layers[l], k, ws);
     int st = run_layer(&layers[l], x, DFV_BF16, k, x, x, true, eps, nullptr, nullptr, w, (cudaStream_t)stream);
     if (st) return st;
+  }
+  return DFV_OK;
+}
+
+size_t dfv_moe_batch_workspace_size(const dfv_moe_layer *layer, int n_rows_max) {
+  if (!layer || n_rows_max < 1 || n_rows_max > DFV_MAX_BATCH_ROWS || layer->n_experts <= 0 || layer->top_k <= 0 ||
+      layer->d <= 0 || layer->d_ff <= 0 || layer->n_shared < 0 || layer->n_shared > 1)
+    return 0;
+  return batch_layout(layer, n_rows_max, nullptr).bytes;
+}
+
+int dfv_moe_batch_forward(const dfv_moe_layer *layer, const void *hidden, int n_blocks, int k, void *out,
+                          int32_t *opt_topk_idx, int32_t *opt_n_woken, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_layer(layer, DFV_BF16);
+  if (st) return st;
+  if (layer->w_dtype != DFV_BF16) return fail(DFV_ERR_UNSUPPORTED, "batched verify takes bf16 expert weights");
+  if (layer->d % 128 || layer->d_ff % 128 || layer->d > 8192)
+    return fail(DFV_ERR_UNSUPPORTED, "batched verify needs d and d_ff multiples of 128 and d <= 8192 (d=%d, d_ff=%d)",
+                layer->d, layer->d_ff);
+  if (k < 1 || k > DFV_MAX_BLOCK || n_blocks < 1 || n_blocks * k > DFV_MAX_BATCH_ROWS)
+    return fail(DFV_ERR_INVALID_ARG, "n_blocks=%d, k=%d: need 1 <= k <= %d and n_blocks * k <= %d", n_blocks, k,
+                DFV_MAX_BLOCK, DFV_MAX_BATCH_ROWS);
+  if (!hidden || !out || !aligned(hidden, 16) || !aligned(out, 16))
+    return fail(DFV_ERR_INVALID_ARG, "hidden/out NULL or not 16-byte aligned");
+  if (!ws || !aligned(ws, 256)) return fail(DFV_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  const int T = n_blocks * k;
+  const size_t need = batch_layout(layer, T, nullptr).bytes;
+  if (ws_bytes < need) return fail(DFV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  BatchWs b = batch_layout(layer, T, ws);
+  dfv::BatchParams &p = b.p;
+  p.x = hidden;
+  p.wr = layer->w_router;
+  p.out = out;
+  p.T = T;
+  p.d = layer->d;
+  p.E = layer->n_experts;
+  p.K = layer->top_k;
+  p.I = layer->d_ff;
+  p.ns = layer->n_shared ? 1 : 0;
+  p.norm_topk = layer->norm_topk ? 1 : 0;
+  p.u_idx = opt_topk_idx;
+  p.u_nw = opt_n_woken;
+  char why[256] = {0};
+  cudaError_t e = dfv::launch_batch(p, layer, (cudaStream_t)stream, why, sizeof why);
+  if (e != cudaSuccess) {
+    if (why[0]) return fail(DFV_ERR_CUDA, "batched verify: %s", why);
+    return cuda_fail(e, "batched verify launch");
   }
   return DFV_OK;
 }

@@ -108,6 +108,27 @@ struct FusedPlan {
   size_t smem;
 };
 
+// Batched verify (batch.cu): T = n_blocks * k rows through one bf16 layer.
+struct BatchParams {
+  const void *x;        // [T][d] bf16 rows
+  const void *wr;       // [E][d] bf16 router
+  void *out;            // [T][d] bf16
+  int T, Tmax, d, E, K, I, ns, norm_topk;
+  float *logits;        // [Tmax][E]
+  unsigned *tmask;      // [E + 1][Tmax / 32] bit t: row t chose the expert
+  int32_t *topk_idx;    // [Tmax][K]
+  float *topk_w;        // [Tmax * K + ns * Tmax] pair weights
+  int32_t *woken, *off, *n_woken;  // [E + 1], [E + 2], [1]
+  int32_t *gather;      // [P] pair ids sorted by (expert, row)
+  int *n_units;         // [2] gate/up and down units
+  int4 *units_g, *units_d;
+  void *xg;             // [P][d] bf16 x rows in sorted order
+  uint16_t *h;          // [P][d_ff] bf16
+  float *ys;            // [P][d] fp32, by pair id
+  unsigned *err;
+  int32_t *u_idx, *u_nw;
+};
+
 struct AcceptParams {
   const void *logits;   // [k+1][V]
   const int32_t *draft; // [k]
@@ -344,6 +365,8 @@ cudaError_t launch_fused_bs(const FusedParams &p, int fmt, const FusedPlan &plan
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);
+// batched verify (batch.cu); `why` receives a reason when a tensor map cannot be built
+cudaError_t launch_batch(const BatchParams &p, const dfv_moe_layer *L, cudaStream_t s, char *why, size_t why_len);
 // device address of the fixed acceptance scratch array on the current device
 cudaError_t accept_noalloc_scratch(void **out);
 int accept_noalloc_max_chunks();

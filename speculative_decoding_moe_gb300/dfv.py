@@ -25,7 +25,7 @@ EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_pro
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
            "dfv_accept_workspace_size", "dfv_accept_greedy", "dfv_selftest_bounded_waits", "dfv_selftest_mma",
-           "dfv_selftest_tcgen05")
+           "dfv_selftest_tcgen05", "dfv_moe_batch_workspace_size", "dfv_moe_batch_forward")
 
 
 class DfvError(RuntimeError):
@@ -76,6 +76,9 @@ def _load():
         L.dfv_selftest_bounded_waits.argtypes = [P, S, P]
         L.dfv_selftest_mma.argtypes = [I, P, P, P, P]
         L.dfv_selftest_tcgen05.argtypes = [P, P, I, I, P, P, P]
+        L.dfv_moe_batch_workspace_size.restype = S
+        L.dfv_moe_batch_workspace_size.argtypes = [P, I]
+        L.dfv_moe_batch_forward.argtypes = [P, P, I, I, P, P, P, P, S, P]
         L.dfv_set_path.argtypes = [I]
         L.dfv_set_staging.restype = I
         L.dfv_set_staging.argtypes = [I]
@@ -175,6 +178,25 @@ def moe_block_forward(layer: Layer, hidden: torch.Tensor, ws: torch.Tensor, out:
     return out
 
 
+def batch_workspace_size(layer: Layer, n_rows_max: int) -> int:
+    return int(_load().dfv_moe_batch_workspace_size(layer.ref, int(n_rows_max)))
+
+
+def moe_batch_forward(layer: Layer, hidden: torch.Tensor, n_blocks: int, ws: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, topk_idx: Optional[torch.Tensor] = None,
+                      n_woken: Optional[torch.Tensor] = None, stream=None):
+    """n_blocks verify blocks of k = rows / n_blocks positions through one layer."""
+    T = hidden.shape[0]
+    if T % n_blocks:
+        raise ValueError("rows %d are not n_blocks=%d blocks of equal size" % (T, n_blocks))
+    if out is None:
+        out = torch.empty_like(hidden)
+    st = _load().dfv_moe_batch_forward(layer.ref, _p(hidden), n_blocks, T // n_blocks, _p(out), _p(topk_idx),
+                                       _p(n_woken), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dfv_moe_batch_forward")
+    return out
+
+
 def moe_block_forward_host(layer: Layer, hidden_host: torch.Tensor, out_host: torch.Tensor, ws: torch.Tensor,
                            stream=None):
     """hidden_host / out_host: CPU tensors (pinned for asynchronous copies)."""
@@ -262,7 +284,7 @@ def selftest_tcgen05(a: torch.Tensor, b: torch.Tensor, stream=None):
     d = torch.full((128, b.shape[0]), float("nan"), dtype=torch.float32, device=a.device)
     st = torch.zeros(1, dtype=torch.int32, device=a.device)
     _check(_load().dfv_selftest_tcgen05(_p(a), _p(b), b.shape[0], a.shape[1], _p(d), _p(st), _stream(stream)),
-           "dfv_selftest_tcgen05")
+           "dfv_selftest_tcgen05", "dfv_moe_batch_workspace_size", "dfv_moe_batch_forward")
     return d, st
 
 
