@@ -541,6 +541,8 @@ def run_gpu(args):
            "d2h_bytes_per_step": N_LAYERS * ho.numel() * ho.element_size(), "ms_per_step": e2e_ms,
            "api": "dfv_moe_block_forward_host per layer, pinned host buffers"}
 
+    bt = None if args.no_batch else batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls,
+                                                   exp_bytes, router_bytes)
     mx = None if args.no_mxfp4 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
     q8 = None if args.no_q8 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw, fmt="q8")
     sh = None if args.no_shared else shared_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
@@ -568,7 +570,7 @@ def run_gpu(args):
         "kernel_path": {"fused": fused_used, "why_not": dfv.fused_unavailable_reason()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
-        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "mxfp4": mx, "q8": q8, "shared_expert": sh,
+        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "batch": bt, "mxfp4": mx, "q8": q8, "shared_expert": sh,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -576,6 +578,81 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls, exp_bytes, router_bytes):
+    """Batched verify: 32 blocks of k=16 (512 rows) through the same 40
+    Qwen3-A3B-like layers, expert contractions on tcgen05.  Bytes count each
+    woken expert once per layer (the batch shares the weights) plus the
+    router; FLOPs count 2 * rows * K * 3 * d * d_ff per layer.  Also timed:
+    the same rows as 32 single-block calls per layer (legacy mma.sync path,
+    weights streamed once per block)."""
+    progress("batched verify")
+    shape = inputs.A3B
+    n_blocks, k = 32, KBLOCK
+    T = n_blocks * k
+    x = inputs.make_hidden(T, shape.d, "bf16", seed=61 + 100 * rank, device=dev)
+    out = torch.empty_like(x)
+    bws = dfv.alloc_workspace(dfv.batch_workspace_size(Ls[0], T), device=dev)
+    nws = torch.zeros(N_LAYERS, dtype=torch.int32, device=dev)
+
+    def fn():
+        for l in range(N_LAYERS):
+            dfv.moe_batch_forward(Ls[l], x, n_blocks, bws, out=out, n_woken=nws[l:l + 1])
+
+    ms = graph_time(fn, args.warmup, args.steps, barrier)
+    W = nws.to(torch.int64).cpu()
+    nbytes = float(W.sum().item() * exp_bytes + N_LAYERS * router_bytes)
+    flops = 2.0 * T * shape.top_k * 3 * shape.d * shape.d_ff * N_LAYERS
+    # per-phase events over the 40 layers (stream launches)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(N_LAYERS)]
+    tot = [0.0, 0.0, 0.0]
+    reps = 3
+    for r in range(reps + 1):
+        for l in range(N_LAYERS):
+            dfv.profile_set_events(evs[l])
+            dfv.moe_batch_forward(Ls[l], x, n_blocks, bws, out=out)
+        dfv.profile_set_events(None)
+        torch.cuda.synchronize()
+        if r:
+            for l in range(N_LAYERS):
+                for i in range(3):
+                    tot[i] += evs[l][i].elapsed_time(evs[l][i + 1])
+    ph = [t / (reps * N_LAYERS) for t in tot]
+    Wm = float(W.double().mean().item())
+    gate_bytes = Wm * 2 * shape.d_ff * shape.d * 2
+    down_bytes = Wm * shape.d * shape.d_ff * 2
+    gate_flops = 2.0 * T * shape.top_k * 2 * shape.d * shape.d_ff
+    # the same rows as single-block calls (mma.sync path), 40 layers
+    ws1 = dfv.alloc_workspace(dfv.workspace_size(Ls[0], k), device=dev)
+    o1 = torch.empty(k, shape.d, dtype=torch.bfloat16, device=dev)
+    xb = [x[b * k:(b + 1) * k].contiguous() for b in range(n_blocks)]
+
+    def fn_single():
+        for l in range(N_LAYERS):
+            for b in range(n_blocks):
+                dfv.moe_block_forward(Ls[l], xb[b], ws1, out=o1)
+
+    ms_single = graph_time(fn_single, 2, max(3, args.steps // 5))
+    tf_sus = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
+    return {
+        "config": "32 blocks x k=16 (512 rows), Qwen3-A3B-like layer x 40 (d=2048, E=128, top-8, d_ff=768, bf16)",
+        "ms_per_pass": ms, "layer_us": ms * 1e3 / N_LAYERS, "woken_mean": Wm,
+        "value_gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": nbytes / (ms * 1e-3) / 1e9 / peak_bw,
+        "tflops": flops / (ms * 1e-3) / 1e12,
+        "rows_per_s": T * 1.0 / (ms * 1e-3) * N_LAYERS / N_LAYERS,
+        "phase_us": {"routing_gather": ph[0] * 1e3, "gate_up": ph[1] * 1e3, "down_combine": ph[2] * 1e3},
+        "roofline": {"bound": "hbm", "kernel": "tc_group_kernel<gate/up> (tcgen05, one launch per layer)",
+                     "achieved": gate_bytes / (ph[1] * 1e-3) / 1e9, "peak": peak_bw, "unit": "GB/s",
+                     "frac": gate_bytes / (ph[1] * 1e-3) / 1e9 / peak_bw, "traffic": None,
+                     "per_launch_us": ph[1] * 1e3, "algorithmic_bytes_per_launch": gate_bytes,
+                     "tensor_tflops": gate_flops / (ph[1] * 1e-3) / 1e12,
+                     "tensor_frac_of_sustained": gate_flops / (ph[1] * 1e-3) / 1e12 / tf_sus if tf_sus else None},
+        "down_gbs": down_bytes / (ph[2] * 1e-3) / 1e9,
+        "single_block_calls": {"ms_per_pass": ms_single, "layer_us": ms_single * 1e3 / N_LAYERS,
+                               "speedup_of_batched": ms_single / ms},
+        "device_error": dfv.read_device_error(bws),
+    }
 
 
 def mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw, fmt="mxfp4"):
@@ -763,6 +840,7 @@ def main():
     ap.add_argument("--no-mxfp4", action="store_true", help="skip the mxfp4-expert section")
     ap.add_argument("--no-shared", action="store_true", help="skip the shared-expert section")
     ap.add_argument("--no-q8", action="store_true", help="skip the 8-bit-expert section")
+    ap.add_argument("--no-batch", action="store_true", help="skip the batched-verify section")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=40, help="layers per step (profiling runs only)")
     args = ap.parse_args()

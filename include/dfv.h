@@ -294,7 +294,11 @@ int dfv_profile_set_events(void *const *events, int n_events);
 int dfv_set_path(int path);
 
 /* Path the last layer call from this host thread took: 1 fused, 0
- * multi-kernel, -1 none yet. */
+ * multi-kernel, 2 batched verify (dfv_moe_batch_forward), -1 none yet.
+ * With profiling events set, a batched call records events[0] before its
+ * routing launches, events[1] after the routing and the token gather,
+ * events[2] after the gate/up contraction and events[3] after the down
+ * contraction and the combine. */
 int dfv_last_layer_path(void);
 
 /*

@@ -268,7 +268,9 @@ BatchWs batch_layout(const dfv_moe_layer *L, int tmax, void *base) {
   BatchWs b = {};
   const size_t E = L->n_experts, K = L->top_k, d = L->d, I = L->d_ff, ns = L->n_shared ? 1 : 0;
   const size_t T = ((size_t)tmax + 31) / 32 * 32, P = T * K + ns * T;
-  const size_t units = (E + 1) * ((I > d ? I : d) / 128) * 2;
+  // units: per woken expert, row tiles x passes of <= 128 tokens; the passes
+  // over all experts number at most (E + 1) + P / 128
+  const size_t units = ((E + 1) + P / 128 + 1) * ((I > d ? I : d) / 128);
   size_t off = 0;
   auto take = [&](size_t bytes) -> void * {
     void *q = base ? (void *)((char *)base + off) : nullptr;
@@ -545,11 +547,17 @@ int dfv_moe_batch_forward(const dfv_moe_layer *layer, const void *hidden, int n_
   p.u_idx = opt_topk_idx;
   p.u_nw = opt_n_woken;
   char why[256] = {0};
-  cudaError_t e = dfv::launch_batch(p, layer, (cudaStream_t)stream, why, sizeof why);
-  if (e != cudaSuccess) {
-    if (why[0]) return fail(DFV_ERR_CUDA, "batched verify: %s", why);
-    return cuda_fail(e, "batched verify launch");
+  cudaStream_t s = (cudaStream_t)stream;
+  mark(0, s);
+  for (int phase = 0; phase < 3; ++phase) {
+    cudaError_t e = dfv::launch_batch(p, layer, phase, s, why, sizeof why);
+    if (e != cudaSuccess) {
+      if (why[0]) return fail(DFV_ERR_CUDA, "batched verify: %s", why);
+      return cuda_fail(e, "batched verify launch");
+    }
+    mark(phase + 1, s);
   }
+  g_last_path = 2;
   return DFV_OK;
 }
 

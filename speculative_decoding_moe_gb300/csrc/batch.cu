@@ -16,17 +16,18 @@
 //            sorted by (expert, row) from the masks, the shared expert
 //            appended, and the work units of the two contractions
 //   gather   the x row of every sorted pair, copied to Xg[position]
-//   gateup   per unit (woken expert, 128 d_ff rows, <= 256 of its tokens):
+//   gateup   per unit (woken expert, 128 d_ff rows, <= 128 of its tokens):
 //            Dg = Wg_tile . Xg^T and Du = Wu_tile . Xg^T in TMEM (M = 128
 //            weight rows, N = the tokens padded to 16, K = d in 64-column
 //            stages), H[position][i] = bf16(silu(Dg) * Du)
-//   down     per unit (woken expert, 128 d rows, <= 256 tokens):
+//   down     per unit (woken expert, 128 d rows, <= 128 tokens):
 //            D = Wd_tile . H^T, Ys[pair][r] = w_pair * D
 //   combine  out[t] = bf16(sum over slots s of Ys[t*K+s] (+ Ys[T*K+t]))
 // Each contraction kernel is persistent (one CTA per SM, units round robin):
 // warp 0 streams weight and token tiles with TMA into a ring of stages, one
 // thread of warp 1 issues the MMAs and commits each stage back to the
-// producer, warps 2-5 read the accumulators out of TMEM.  Every wait is
+// producer, warps 2-5 read the accumulators out of TMEM; two TMEM buffers let
+// the MMAs of one unit run while the epilogue reads the last.  Every wait is
 // bounded (2 s) and reports through the workspace error word.
 #include <cstdio>
 #include <cstring>
@@ -49,7 +50,7 @@ constexpr int kBExpTile = 32;    // router: experts per CTA
 constexpr int kTcThreads = 192;  // contraction kernels: producer, MMA, 4 epilogue warps
 constexpr int kTcK = 64;         // K elements per stage (one 128-byte swizzle row)
 constexpr int kTcM = 128;        // weight rows per unit
-constexpr int kTcNMax = 256;     // tokens per unit (TMEM: two accumulators of 256 columns)
+constexpr int kTcNMax = 128;     // tokens per unit (TMEM: two buffers of one or two accumulators)
 constexpr int kTcBoxN = 16;      // token rows per TMA box
 
 // tcgen05 kernels' parameters (tensor maps first: 64-byte aligned in the
@@ -90,40 +91,51 @@ __global__ void __launch_bounds__(512) batch_logits_kernel(BatchParams p) {
   __syncthreads();
   // warp w: experts e0 + w, e0 + w + 16, each dot product in the order the
   // single-block kernels use (lane l: 16-byte pieces l, l+32, ... in chunks
-  // of 256 pieces, words in order, then an xor butterfly)
+  // of 256 pieces, words in order, then an xor butterfly); a chunk of the
+  // router row is loaded once and used for all the tile's rows
   for (int j = warp; j < ne; j += 16) {
     const int e = e0 + j;
     const uint16_t *wr = reinterpret_cast<const uint16_t *>(p.wr) + (size_t)e * d;
+    float acc[kBRowTile];
+#pragma unroll
+    for (int t = 0; t < kBRowTile; ++t) acc[t] = 0.f;
 #pragma unroll 1
-    for (int t = 0; t < nt; ++t) {
-      const uint16_t *xr = xs + (size_t)t * d;
-      float acc = 0.f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < cpr; c0 += 256) {
-        uint4 wv[8];
+    for (int c0 = 0; c0 < cpr; c0 += 256) {
+      uint4 wv[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c0 + lane + 32 * i;
-          wv[i] = c < cpr ? __ldg(reinterpret_cast<const uint4 *>(wr + (size_t)c * 8)) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c0 + lane + 32 * i;
-          if (c < cpr) {
-            const uint4 xv = *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8);
-            const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
-            const uint32_t w4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              acc = fmaf(bf16_lo(x4[h]), bf16_lo(w4[h]), acc);
-              acc = fmaf(bf16_hi(x4[h]), bf16_hi(w4[h]), acc);
-            }
-          }
-        }
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + lane + 32 * i;
+        wv[i] = c < cpr ? __ldg(reinterpret_cast<const uint4 *>(wr + (size_t)c * 8)) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) p.logits[(size_t)(t0 + t) * E + e] = acc;
+      for (int t = 0; t < kBRowTile; ++t) {
+        if (t < nt) {
+          const uint16_t *xr = xs + (size_t)t * d;
+          float a_ = acc[t];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = c0 + lane + 32 * i;
+            if (c < cpr) {
+              const uint4 xv = *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8);
+              const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
+              const uint32_t w4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                a_ = fmaf(bf16_lo(x4[h]), bf16_lo(w4[h]), a_);
+                a_ = fmaf(bf16_hi(x4[h]), bf16_hi(w4[h]), a_);
+              }
+            }
+          }
+          acc[t] = a_;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kBRowTile; ++t) {
+      float a_ = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a_ += __shfl_xor_sync(0xffffffffu, a_, o);
+      if (lane == 0 && t < nt) p.logits[(size_t)(t0 + t) * E + e] = a_;
     }
   }
 }
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(512) batch_tables_kernel(BatchParams p) {
       p.gather[T * K + t] = T * K + t;
       p.topk_w[T * K + t] = 1.f;
     }
-  // units: per woken expert, row tiles x passes of <= 256 tokens
+  // units: per woken expert, row tiles x passes of <= 128 tokens
   const int tg = p.I / kTcM, td = p.d / kTcM;
   if (tid == 0) {
     int ug = 0, ud = 0;
@@ -319,14 +331,15 @@ __device__ __forceinline__ void tma2_plain(uint32_t dst, const CUtensorMap *map,
 // DUAL: gate/up (two weight operands, H = silu(D1) * D2); else down.
 template <bool DUAL>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_constant__ TcParams p) {
-  constexpr int kStages = DUAL ? 3 : 4;
+  constexpr int kStages = DUAL ? 4 : 6;
   constexpr uint32_t kABytes = kTcM * kTcK * 2;             // 16 KB per weight tile
   constexpr uint32_t kBOff = (DUAL ? 2 : 1) * kABytes;       // token tile after the weight tile(s)
-  constexpr uint32_t kStage = kBOff + kTcNMax * kTcK * 2;    // + 32 KB of token rows
-  constexpr uint32_t kCols = DUAL ? 512 : 256;               // TMEM columns
+  constexpr uint32_t kStage = kBOff + kTcNMax * kTcK * 2;    // + 16 KB of token rows
+  constexpr uint32_t kBuf = (DUAL ? 2 : 1) * kTcNMax;        // TMEM columns of one accumulator buffer
+  constexpr uint32_t kCols = 2 * kBuf;                       // two buffers: MMAs of one unit, epilogue of the last
   extern __shared__ __align__(1024) unsigned char tsm_raw[];
   unsigned char *tsm = tsm_raw + ((1024u - (smem_u32(tsm_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) unsigned long long s_full[kStages], s_empty[kStages], s_tfull, s_tempty, s_drain;
+  __shared__ __align__(8) unsigned long long s_full[kStages], s_empty[kStages], s_tfull[2], s_tempty[2], s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   pdl_trigger();
@@ -338,8 +351,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&s_empty[s]), 1);
     }
-    mbar_init(smem_u32(&s_tfull), 1);
-    mbar_init(smem_u32(&s_tempty), 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&s_tfull[b]), 1);
+      mbar_init(smem_u32(&s_tempty[b]), 4);
+    }
     mbar_init(smem_u32(&s_drain), 1);
     mbar_init_fence();
   }
@@ -396,9 +411,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
         const int4 un = p.units[u];
         const int npad = (un.w + 15) & ~15;
         const uint32_t idesc = idesc_bf16(kTcM, npad);
-        // the epilogue of the previous unit has read TMEM
-        if (tcount > 0 &&
-            !mbar_wait(smem_u32(&s_tempty), (tcount - 1) & 1, p.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) {
+        const int buf = tcount & 1;
+        const uint32_t dbuf = tmem + (uint32_t)buf * kBuf;
+        // the epilogue has read this buffer's previous unit (two units ago)
+        if (tcount >= 2 && !mbar_wait(smem_u32(&s_tempty[buf]), ((tcount >> 1) - 1) & 1, p.err,
+                                      DFV_DEVERR_STAGE_WAIT, &s_abort)) {
           ok = false;
           break;
         }
@@ -414,13 +431,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
           for (int kk = 0; kk < kTcK / 16; ++kk) {
             const uint64_t bd = sdesc_k128(st + kBOff) + (uint64_t)(2 * kk);
             const uint32_t acc = (kc > 0 || kk > 0) ? 1u : 0u;
-            tc_mma(tmem, sdesc_k128(st) + (uint64_t)(2 * kk), bd, idesc, acc);
-            if (DUAL) tc_mma(tmem + kTcNMax, sdesc_k128(st + kABytes) + (uint64_t)(2 * kk), bd, idesc, acc);
+            tc_mma(dbuf, sdesc_k128(st) + (uint64_t)(2 * kk), bd, idesc, acc);
+            if (DUAL) tc_mma(dbuf + kTcNMax, sdesc_k128(st + kABytes) + (uint64_t)(2 * kk), bd, idesc, acc);
           }
           tc_commit(smem_u32(&s_empty[cs]));  // the stage is free once these MMAs have read it
           if (++cs == kStages) { cs = 0; cph ^= 1; }
         }
-        if (ok) tc_commit(smem_u32(&s_tfull));
+        if (ok) tc_commit(smem_u32(&s_tfull[buf]));
       }
       // every MMA issued has completed before TMEM is released
       tc_commit(smem_u32(&s_drain));
@@ -436,7 +453,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
     for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++tcount) {
       const int4 un = p.units[u];
       // every lane observes the accumulator barrier itself before it reads TMEM
-      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_tfull), tcount & 1, p.err,
+      const int buf = tcount & 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_tfull[buf]), (tcount >> 1) & 1, p.err,
                                                          DFV_DEVERR_STAGE_WAIT, &s_abort));
       if (!got) {
         ok = false;
@@ -445,7 +463,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
       tc_fence_after();
       const int pos0 = p.off[un.x] + un.z;
       const int col = un.y * kTcM + row;  // output column of this thread
-      const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+      const uint32_t lane_addr = tmem + (uint32_t)buf * kBuf + ((uint32_t)(quad * 32) << 16);
       for (int c0 = 0; c0 < un.w; c0 += 16) {
         float v1[16];
         tmem_ld16(lane_addr + (uint32_t)c0, v1);
@@ -467,7 +485,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_tempty));
+      if (lane == 0) mbar_arrive(smem_u32(&s_tempty[buf]));
     }
   }
   tc_fence_before();
@@ -477,7 +495,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
 
 template <bool DUAL>
 constexpr size_t tc_smem() {
-  return 1024 + (size_t)(DUAL ? 3 : 4) * ((DUAL ? 2 : 1) * kTcM * kTcK * 2 + kTcNMax * kTcK * 2);
+  return 1024 + (size_t)(DUAL ? 4 : 6) * ((DUAL ? 2 : 1) * kTcM * kTcK * 2 + kTcNMax * kTcK * 2);
 }
 
 bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
@@ -515,27 +533,31 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
 
 }  // namespace
 
-// Host: the seven launches of one batched layer.  The caller has validated
-// the shapes (bf16, d % 128 == 0, d_ff % 128 == 0, d <= 8192, T <= Tmax <= 512).
-cudaError_t launch_batch(const BatchParams &p, const dfv_moe_layer *L, cudaStream_t s, char *why, size_t why_len) {
+// Host: the launches of one batched layer, in three phases (0: routing and
+// gather, 1: gate/up, 2: down and combine) so that a caller can record events
+// between them.  The caller has validated the shapes (bf16, d % 128 == 0,
+// d_ff % 128 == 0, d <= 8192, T <= Tmax <= 512).
+cudaError_t launch_batch(const BatchParams &p, const dfv_moe_layer *L, int phase, cudaStream_t s, char *why,
+                         size_t why_len) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int T = p.T, E = p.E, d = p.d, I = p.I;
-  const size_t lsmem = (size_t)kBRowTile * d * 2;
-  e = cudaFuncSetAttribute(batch_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsmem);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(batch_logits_kernel, dim3((T + kBRowTile - 1) / kBRowTile, (E + kBExpTile - 1) / kBExpTile),
-                 dim3(512), lsmem, s, p);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(batch_topk_kernel, dim3((T + 15) / 16), dim3(512), 0, s, p);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(batch_tables_kernel, dim3(1), dim3(512), 0, s, p);
-  if (e != cudaSuccess) return e;
   const int P = T * p.K + p.ns * T;
-  e = launch_pdl(batch_gather_kernel, dim3(P < 4 * sms ? P : 4 * sms), dim3(256), 0, s, p);
-  if (e != cudaSuccess) return e;
+  if (phase == 0) {
+    const size_t lsmem = (size_t)kBRowTile * d * 2;
+    e = cudaFuncSetAttribute(batch_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lsmem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(batch_logits_kernel, dim3((T + kBRowTile - 1) / kBRowTile, (E + kBExpTile - 1) / kBExpTile),
+                   dim3(512), lsmem, s, p);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(batch_topk_kernel, dim3((T + 15) / 16), dim3(512), 0, s, p);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(batch_tables_kernel, dim3(1), dim3(512), 0, s, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(batch_gather_kernel, dim3(P < 4 * sms ? P : 4 * sms), dim3(256), 0, s, p);
+  }
   // contraction tensor maps (weights cached per layer; token maps per workspace)
   TcParams g = {}, dn = {};
   const int Et = E + p.ns;
@@ -563,12 +585,14 @@ cudaError_t launch_batch(const BatchParams &p, const dfv_moe_layer *L, cudaStrea
   dn.a_rows = d;
   dn.kdim = I;
   dn.ncols = d;
-  e = cudaFuncSetAttribute(tc_group_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem<true>());
-  if (e != cudaSuccess) return e;
+  if (phase == 1) {
+    e = cudaFuncSetAttribute(tc_group_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc_smem<true>());
+    if (e != cudaSuccess) return e;
+    return launch_pdl(tc_group_kernel<true>, dim3(sms), dim3(kTcThreads), tc_smem<true>(), s, g);
+  }
   e = cudaFuncSetAttribute(tc_group_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc_smem<false>());
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(tc_group_kernel<true>, dim3(sms), dim3(kTcThreads), tc_smem<true>(), s, g);
   if (e != cudaSuccess) return e;
   e = launch_pdl(tc_group_kernel<false>, dim3(sms), dim3(kTcThreads), tc_smem<false>(), s, dn);
   if (e != cudaSuccess) return e;

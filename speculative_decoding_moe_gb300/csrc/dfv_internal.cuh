@@ -365,8 +365,10 @@ cudaError_t launch_fused_bs(const FusedParams &p, int fmt, const FusedPlan &plan
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);
-// batched verify (batch.cu); `why` receives a reason when a tensor map cannot be built
-cudaError_t launch_batch(const BatchParams &p, const dfv_moe_layer *L, cudaStream_t s, char *why, size_t why_len);
+// batched verify (batch.cu), phase 0 routing + gather, 1 gate/up, 2 down + combine;
+// `why` receives a reason when a tensor map cannot be built
+cudaError_t launch_batch(const BatchParams &p, const dfv_moe_layer *L, int phase, cudaStream_t s, char *why,
+                         size_t why_len);
 // device address of the fixed acceptance scratch array on the current device
 cudaError_t accept_noalloc_scratch(void **out);
 int accept_noalloc_max_chunks();

@@ -284,7 +284,7 @@ def selftest_tcgen05(a: torch.Tensor, b: torch.Tensor, stream=None):
     d = torch.full((128, b.shape[0]), float("nan"), dtype=torch.float32, device=a.device)
     st = torch.zeros(1, dtype=torch.int32, device=a.device)
     _check(_load().dfv_selftest_tcgen05(_p(a), _p(b), b.shape[0], a.shape[1], _p(d), _p(st), _stream(stream)),
-           "dfv_selftest_tcgen05", "dfv_moe_batch_workspace_size", "dfv_moe_batch_forward")
+           "dfv_selftest_tcgen05")
     return d, st
 
 

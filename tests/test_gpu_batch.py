@@ -111,9 +111,9 @@ def test_batch_a3b_against_oracle_and_single_blocks(dfv, a3b, n_blocks):
         assert (a - r).abs().max().item() <= TOL * r.abs().max().item()
 
 
-def test_batch_repeated_blocks_and_more_than_256_tokens_per_expert(dfv):
+def test_batch_repeated_blocks_and_more_than_128_tokens_per_expert(dfv):
     """32 blocks of one repeated row each at top-1 over 4 experts: experts get
-    more than 256 tokens, so their units run in two passes."""
+    more than 128 tokens (up to 512), so their units run in several passes."""
     shape = inputs.LayerShape(d=256, n_experts=4, top_k=1, d_ff=128)
     lw = inputs.make_layer(shape, seed=808)
     ol = oracle_layer(lw)
