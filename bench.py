@@ -541,6 +541,8 @@ def run_gpu(args):
            "d2h_bytes_per_step": N_LAYERS * ho.numel() * ho.element_size(), "ms_per_step": e2e_ms,
            "api": "dfv_moe_block_forward_host per layer, pinned host buffers"}
 
+    stk = None if args.no_stack else stack_section(args, dev, rank, barrier, dfv, inputs, peak_bw, Ls, exp_bytes,
+                                                    router_bytes, ws, shape)
     bt = None if args.no_batch else batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls,
                                                    exp_bytes, router_bytes)
     mx = None if args.no_mxfp4 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
@@ -570,7 +572,7 @@ def run_gpu(args):
         "kernel_path": {"fused": fused_used, "why_not": dfv.fused_unavailable_reason()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
-        "sweep": sweep, "stack40_accept": stack, "weight_gen_s": t_gen, "batch": bt, "mxfp4": mx, "q8": q8, "shared_expert": sh,
+        "sweep": sweep, "stack40": stk, "stack40_accept": stack, "weight_gen_s": t_gen, "batch": bt, "mxfp4": mx, "q8": q8, "shared_expert": sh,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -578,6 +580,50 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def stack_section(args, dev, rank, barrier, dfv, inputs, peak_bw, Ls, exp_bytes, router_bytes, ws, shape):
+    """The 40-layer pre-norm residual stack through dfv_moe_stack_forward at k = 16
+    (verify) and k = 1 (decode): one persistent launch for all layers against
+    one launch per layer.  Bytes are each layer's woken experts (reported by the
+    call) plus its router."""
+    res = {"config": "Qwen3-A3B-like layer x %d (d=2048, E=128, top-8, d_ff=768, bf16), pre-norm residual stack"
+                     % N_LAYERS}
+    outs = {}
+    for k in (KBLOCK, 1):
+        x0 = inputs.make_hidden(k, shape.d, "bf16", seed=9 + 100 * rank + k, device=dev)
+        xs = x0.clone()
+        nw = torch.zeros(N_LAYERS, dtype=torch.int32, device=dev)
+
+        def fn():
+            xs.copy_(x0)
+            dfv.moe_stack_forward(Ls, xs, ws, n_woken=nw)
+
+        row = {}
+        for name, mode in (("persistent", 2), ("per_layer", 0)):
+            progress("stack k=%d %s" % (k, name))
+            dfv.set_stack_launch(mode)
+            try:
+                ms = graph_time(fn, max(3, args.warmup), max(5, args.steps // 2), barrier)
+                fn()
+                torch.cuda.synchronize()
+                path = dfv.last_layer_path()
+            finally:
+                dfv.set_stack_launch(1)
+            outs[(k, name)] = xs.clone()
+            W = nw.to(torch.int64).cpu()
+            nbytes = float(W.sum().item() * exp_bytes + N_LAYERS * router_bytes)
+            row[name] = {"ms": ms, "layer_us": ms * 1e3 / N_LAYERS, "gbs": achieved_gbs(nbytes, ms),
+                         "frac_of_measured_hbm": achieved_gbs(nbytes, ms) / peak_bw, "path": path,
+                         "woken_mean": float(W.double().mean().item()), "bytes": nbytes}
+        row["identical"] = bool(torch.equal(outs[(k, "persistent")], outs[(k, "per_layer")]))
+        res["k%d" % k] = row
+    for name in ("persistent", "per_layer"):
+        a, b = res["k%d" % KBLOCK][name], res["k1"][name]
+        res["verify_decode_" + name] = {"latency_ratio": a["ms"] / b["ms"], "woken_byte_ratio": a["bytes"] / b["bytes"],
+                                        "quotient": (a["bytes"] / b["bytes"]) / (a["ms"] / b["ms"])}
+    res["device_error"] = dfv.read_device_error(ws)
+    return res
 
 
 def batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls, exp_bytes, router_bytes):

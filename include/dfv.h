@@ -220,9 +220,24 @@ int dfv_moe_block_forward_host(const dfv_moe_layer *layer, const void *hidden_ho
  *   layers  host array of n_layers layer descriptors (BF16, MXFP4 or Q8 experts,
  *           BF16 router), all with the same d
  *   x       [k, d] bf16 device buffer, input and output
+ *   opt_n_woken  NULL, or an int32 device array [n_layers]: per layer, the
+ *           number of distinct routed experts the block woke
+ * Layers are applied in order; each one's routing depends on the previous
+ * one's output ("Speculating on a Strix Halo (part 2)", section "The
+ * verification cog": every layer pays its own fixed cost, which is what the
+ * decode step of one token feels).  When every layer has bf16 experts and
+ * router and the same shape (d, d_ff, experts, top-k, shared expert, weight
+ * renormalisation), and the single-launch kernel fits the shape, the layers
+ * can run as ONE persistent cooperative launch per 48 layers: grid barriers
+ * separate the layers, the next layer's router rows are fetched towards L2
+ * while the current one drains, and no launch or set-up is paid in between
+ * (see dfv_set_stack_launch).  Otherwise one launch (or one multi-kernel
+ * sequence) per layer.  Both give the same bits.  The workspace is sized for
+ * the largest layer with dfv_moe_workspace_size; one error word covers the
+ * whole call.
  */
 int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, int k, float eps,
-                          void *ws, size_t ws_bytes, void *stream);
+                          int32_t *opt_n_woken, void *ws, size_t ws_bytes, void *stream);
 
 /* Bytes of workspace dfv_moe_batch_forward needs for up to n_rows_max rows
  * (n_blocks * k) of a layer (0 on invalid arguments). */
@@ -293,8 +308,23 @@ int dfv_profile_set_events(void *const *events, int n_events);
  */
 int dfv_set_path(int path);
 
+/*
+ * How dfv_moe_stack_forward launches a stack whose layers allow the persistent
+ * kernel, for later calls from this host thread (no counterpart on the
+ * method's pages): 0 one launch per layer (chained programmatically); 1
+ * (default) one persistent launch per 48 layers for blocks of k <= 8, one
+ * launch per layer above (with 16 tokens the persistent kernel's down loop
+ * spills registers and runs slower than the per-layer kernel); 2 one
+ * persistent launch per 48 layers for every k.  The result is the same bit
+ * for bit.  Returns DFV_ERR_INVALID_ARG for a mode outside 0..2.
+ */
+int dfv_set_stack_launch(int mode);
+
 /* Path the last layer call from this host thread took: 1 fused, 0
- * multi-kernel, 2 batched verify (dfv_moe_batch_forward), -1 none yet.
+ * multi-kernel, 2 batched verify (dfv_moe_batch_forward), 3 persistent stack
+ * launch (dfv_moe_stack_forward), -1 none yet.  With profiling events set, a
+ * persistent stack call records events[0] before and events[1..3] after each
+ * of its launches.
  * With profiling events set, a batched call records events[0] before its
  * routing launches, events[1] after the routing and the token gather,
  * events[2] after the gate/up contraction and events[3] after the down

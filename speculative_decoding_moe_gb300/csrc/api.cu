@@ -298,6 +298,92 @@ BatchWs batch_layout(const dfv_moe_layer *L, int tmax, void *base) {
 }
 
 thread_local bool g_fused_enabled = true;
+thread_local int g_stack_mode = 1;  // 0 per layer, 1 persistent for k <= 8, 2 persistent
+
+// A residual stack of bf16 layers of one shape as persistent launches of up
+// to kMaxStackLayers layers each.  Returns -1 when the layers or the device do
+// not allow it (the caller then launches layer by layer), else a DFV status.
+int run_stack_persistent(const dfv_moe_layer *Ls, int n_layers, void *x, int k, float eps, int32_t *u_nw,
+                         void *ws, cudaStream_t s) {
+  const dfv_moe_layer &L0 = Ls[0];
+  for (int l = 0; l < n_layers; ++l) {
+    const dfv_moe_layer &L = Ls[l];
+    if (L.w_dtype != DFV_BF16 || L.r_dtype != DFV_BF16 || L.d != L0.d || L.d_ff != L0.d_ff ||
+        L.n_experts != L0.n_experts || L.top_k != L0.top_k || (L.n_shared != 0) != (L0.n_shared != 0) ||
+        (L.norm_topk != 0) != (L0.norm_topk != 0))
+      return -1;
+  }
+  dfv::FusedPlan plan;
+  if (!dfv::fused_plan(k, L0.d, L0.d_ff, L0.n_experts, &plan)) return -1;
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int grid;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_tuple(dev, k <= 8 ? 1 : 2, plan.smem);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+      char why[256] = {0};
+      const int gmax = dfv::fused_stack_max_grid(plan, k, why, sizeof why);
+      if (gmax <= 0 && g_fused_why.empty()) g_fused_why = why;
+      it = cache.emplace(key, gmax).first;
+    }
+    grid = it->second;
+  }
+  if (grid <= 0) return -1;
+  // the parameter block carries every layer's tensor maps
+  static thread_local dfv::StackParams sp;
+  sp = dfv::StackParams{};
+  dfv::FusedParams &fp = sp.p;
+  fp.x = x;
+  fp.residual = x;
+  fp.out = x;
+  fp.k = k;
+  fp.d = L0.d;
+  fp.I = L0.d_ff;
+  fp.E = L0.n_experts;
+  fp.K = L0.top_k;
+  fp.norm_topk = L0.norm_topk ? 1 : 0;
+  fp.ns = L0.n_shared ? 1 : 0;
+  fp.fuse_norm = 1;
+  fp.swz_x = (L0.d % 64 == 0) ? 4 : 0;
+  fp.eps = eps;
+  fp.ws = layout(&L0, k, ws);
+  for (int l0 = 0; l0 < n_layers; l0 += dfv::kMaxStackLayers) {
+    const int n = n_layers - l0 < dfv::kMaxStackLayers ? n_layers - l0 : dfv::kMaxStackLayers;
+    // every layer of a launch takes the same staging mode: the lowest any
+    // layer's maps allow
+    int mode = g_max_staging;
+    for (int pass = 0; pass < 2; ++pass) {
+      int lo = mode;
+      for (int i = 0; i < n; ++i) {
+        int m = 0;
+        dfv::stack_layer_maps(&sp.L[i], &Ls[l0 + i], plan, mode, &m);
+        lo = m < lo ? m : lo;
+      }
+      if (lo == mode) break;
+      mode = lo;
+    }
+    fp.tma_mode = mode;
+    fp.u_nw = u_nw ? u_nw + l0 : nullptr;
+    g_last_staging = mode;
+    sp.n_layers = n;
+    mark(0, s);
+    cudaError_t e = dfv::launch_fused_stack(sp, plan, grid, s, true);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      e = dfv::launch_fused_stack(sp, plan, grid, s, false);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "persistent stack launch");
+    mark(1, s);
+    mark(2, s);
+    mark(3, s);
+  }
+  g_last_path = 3;
+  return DFV_OK;
+}
 
 int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, const void *residual,
               bool fuse_norm, float eps, int32_t *u_idx, int32_t *u_nw, const dfv::Workspace &w, cudaStream_t s) {
@@ -488,8 +574,8 @@ int dfv_moe_block_forward_host(const dfv_moe_layer *layer, const void *hidden_ho
   return DFV_OK;
 }
 
-int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, int k, float eps, void *ws,
-                          size_t ws_bytes, void *stream) {
+int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, int k, float eps,
+                          int32_t *opt_n_woken, void *ws, size_t ws_bytes, void *stream) {
   if (!layers || n_layers < 1) return fail(DFV_ERR_INVALID_ARG, "no layers");
   if (k < 1 || k > DFV_MAX_BLOCK) return fail(DFV_ERR_INVALID_ARG, "k=%d outside 1..%d", k, DFV_MAX_BLOCK);
   if (!x || !aligned(x, 16)) return fail(DFV_ERR_INVALID_ARG, "x NULL or not 16-byte aligned");
@@ -500,9 +586,14 @@ int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, in
     if (layers[l].d != layers[0].d) return fail(DFV_ERR_INVALID_ARG, "layer %d: d differs from layer 0", l);
     if ((st = check_ws(&layers[l], k, ws, ws_bytes))) return fail(st, "layer %d: %s", l, g_detail.c_str());
   }
+  if (g_fused_enabled && (g_stack_mode == 2 || (g_stack_mode == 1 && k <= 8))) {
+    const int st = run_stack_persistent(layers, n_layers, x, k, eps, opt_n_woken, ws, (cudaStream_t)stream);
+    if (st >= 0) return st;
+  }
   for (int l = 0; l < n_layers; ++l) {
     const dfv::Workspace w = layout(&layers[l], k, ws);
-    int st = run_layer(&layers[l], x, DFV_BF16, k, x, x, true, eps, nullptr, nullptr, w, (cudaStream_t)stream);
+    int st = run_layer(&layers[l], x, DFV_BF16, k, x, x, true, eps, nullptr, opt_n_woken ? opt_n_woken + l : nullptr,
+                       w, (cudaStream_t)stream);
     if (st) return st;
   }
   return DFV_OK;
@@ -572,6 +663,12 @@ int dfv_set_staging(int max_mode) {
 }
 
 int dfv_last_staging(void) { return g_last_staging; }
+
+int dfv_set_stack_launch(int mode) {
+  if (mode < 0 || mode > 2) return fail(DFV_ERR_INVALID_ARG, "stack launch mode must be 0, 1 or 2");
+  g_stack_mode = mode;
+  return DFV_OK;
+}
 
 int dfv_set_path(int path) {
   if (path != 0 && path != 1) return fail(DFV_ERR_INVALID_ARG, "path must be 0 (multi-kernel) or 1 (fused)");

@@ -108,6 +108,20 @@ struct FusedPlan {
   size_t smem;
 };
 
+// One layer of a persistent stack launch (bf16 experts): what changes from
+// layer to layer when every layer has the same shape.  The tensor maps sit in
+// the kernel parameters, where TMA copies and prefetch.tensormap read them.
+struct StackLayer {
+  CUtensorMap tm_wg, tm_wu;
+  const void *wr, *wg, *wu, *wd;
+};
+constexpr int kMaxStackLayers = 48;  // layers per launch (parameter space: 48 x 384 bytes)
+struct StackParams {
+  FusedParams p;  // shape, plan, workspace, the residual stream (x = out = residual)
+  int n_layers;
+  StackLayer L[kMaxStackLayers];
+};
+
 // Batched verify (batch.cu): T = n_blocks * k rows through one bf16 layer.
 struct BatchParams {
   const void *x;        // [T][d] bf16 rows
@@ -226,6 +240,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)_
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// Retire an mbarrier no thread waits on and no copy completes on any more,
+// before it is initialised again.
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -353,6 +372,9 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
 bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
 int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
 cudaError_t launch_fused(const FusedParams &p, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
+int fused_stack_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);
+cudaError_t launch_fused_stack(const StackParams &sp, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
+bool stack_layer_maps(StackLayer *sl, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode, int *mode);
 // fills p->tm_wg / tm_wu and p->tma_mode (<= max_mode) for a bf16 layer (mode 0 when no tensor map fits)
 void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode);
 // single-launch layer with block-scaled experts, fmt = DFV_MXFP4 or DFV_Q8

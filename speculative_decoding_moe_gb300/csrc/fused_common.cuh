@@ -19,6 +19,7 @@ constexpr int kMaxChunksP2 = 2;   // 32-column chunks per consumer warp per gate
 
 __device__ __forceinline__ int fpad(int bytes) { return (bytes % 128 == 0) ? bytes + 64 : bytes; }
 
+
 __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -62,11 +63,11 @@ __device__ bool grid_sync(const FusedParams &p, unsigned nb) {
 // The router rows of this CTA's experts b, b+G, ... start towards L2.  They are
 // weights no kernel writes, so this may run before griddepcontrol.wait, while
 // the previous launch drains; nothing else does.
-__device__ __forceinline__ void prefetch_router_rows(const FusedParams &p) {
+__device__ __forceinline__ void prefetch_router_rows(const void *wr, int E, int d) {
   const int e = blockIdx.x + (int)threadIdx.x * gridDim.x;
-  if (threadIdx.x < 8 && e < p.E)
-    prefetch_l2(reinterpret_cast<const char *>(p.wr) + (size_t)e * p.d * 2, (uint32_t)p.d * 2);
+  if (threadIdx.x < 8 && e < E) prefetch_l2(reinterpret_cast<const char *>(wr) + (size_t)e * d * 2, (uint32_t)d * 2);
 }
+__device__ __forceinline__ void prefetch_router_rows(const FusedParams &p) { prefetch_router_rows(p.wr, p.E, p.d); }
 
 // Arrive on named barrier `id` (n threads in all) without waiting.
 __device__ __forceinline__ void bar_arrive_n(int id, int n) {
@@ -110,6 +111,7 @@ struct RouteSmem {
 // them after each store it cannot prove distinct).
 struct RouteArgs {
   int k, d, E, K, fuse_norm, norm_topk, ns;
+  unsigned gb;              // grid barriers the launch completed before this layer
   float eps;
   const uint16_t *wr;       // router [E][d] bf16
   const uint16_t *xs;       // x rows [k][d] bf16 (shared memory, or p.x)
@@ -138,6 +140,7 @@ __device__ __forceinline__ RouteArgs route_args(const FusedParams &p, const Rout
   RouteArgs a;
   a.k = p.k; a.d = p.d; a.E = p.E; a.K = p.K;
   a.fuse_norm = p.fuse_norm; a.norm_topk = p.norm_topk; a.ns = p.ns ? 1 : 0;
+  a.gb = 0;
   a.eps = p.eps;
   a.wr = reinterpret_cast<const uint16_t *>(p.wr);
   a.xs = xs;
@@ -310,7 +313,7 @@ __device__ __forceinline__ void route_p1(const RouteArgs &r, AfterScan &&after_s
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // ---- grid barrier 1: every CTA's logits are published
   bar_sync_n(kBarAll, kFC);
-  if (tid == 0 && !grid_sync_raw(r.sync, r.err, 1)) *r.abort = 1;
+  if (tid == 0 && !grid_sync_raw(r.sync, r.err, r.gb + 1)) *r.abort = 1;
   bar_sync_n(kBarAll, kFC);
 
   // Warp t: top-K of row t (lane holds experts lane + 32 q), then the routing

@@ -71,10 +71,125 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int
       : "memory");
 }
 
+// The kernel body.  STACK: `nl` layers of one shape in a row over the residual
+// stream p.x (= p.out = p.residual), the weights of layer l in SL[l]; between
+// layers a grid barrier (every row of x is combined) and the ring's mbarriers
+// are armed afresh.  Without STACK, one layer with the weights in p.
+// What the down phase reads besides the thread's own indexes.
+struct DownArgs {
+  const uint16_t *hbf;       // h rounded to bf16, [k*K][d_ff] by sorted pair position
+  float *ys;                 // weighted expert outputs, by pair id
+  unsigned *err;             // workspace error word
+  const int *off, *gat;      // per woken expert: first sorted position; sorted pair ids
+  const float *w;            // routing weight of each pair
+  float *red;                // cross-warp reduction scratch [16][NT][32][4]
+  volatile int *abort;
+  uint32_t sbase, slot, full0, empty0, extra;  // ring, its barriers, the extra stage
+  int SH, S, lo_d, hi_d, tiles_d, I, d;        // reserved and usable stages, this CTA's units
+};
+
+// P3: down = (woken expert, 16 d rows) units lo_d..hi_d-1 of this CTA,
+// expert-major; two groups of 8 consumer warps take alternate units, reduce
+// within the group and write w[t,s] * y to ys[pair].  Each group owns the
+// ring stages of its parity.  Returns the updated stage phase bits; *dead is
+// set when a wait gave up.
 template <int NT>
-__global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant__ FusedParams p) {
+__device__ __forceinline__ uint32_t down_phase(const DownArgs &A, uint32_t cbits, int *dead_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int I = A.I, d = A.d, S = A.S, SH = A.SH, tiles_d = A.tiles_d;
+  const uint32_t full0 = A.full0, empty0 = A.empty0;
+  const uint16_t *hbf = A.hbf;
+  const int *s_off = A.off, *s_gat = A.gat;
+  const float *s_w = A.w;
+  bool dead = *dead_out != 0;
+  auto slot_addr = [&](int st) -> uint32_t { return st < SH ? A.sbase + (uint32_t)st * A.slot : A.extra; };
+  const int grp = warp >> 3, wg = warp & 7;
+  const int C = I / 32;
+  const int d0 = wg * C / 8, d1 = (wg + 1) * C / 8;
+  const int rsd = I * 2;
+  float *redg = A.red + grp * 8 * NT * 32 * 4;  // this group's [8][NT][32][4]
+  int cur_d = -1, eoff = 0, em = 0;
+  int gs = grp;  // this group's next stage (the group owns the stages of its parity)
+  uint4 bh[3][NT];  // B fragments: h of the current expert's tokens (bf16), reused across its tiles
+  // unit lo_d + j belongs to group j & 1
+  for (int u = A.lo_d + grp; u < A.hi_d; u += 2) {
+    const int s = gs;
+    gs = (gs + 2 < S) ? gs + 2 : grp;
+    const int wi = u / tiles_d, r0 = (u - wi * tiles_d) * 16;
+    if (wi != cur_d) {
+      // straight from L2, issued before the stage wait so the latencies overlap
+      cur_d = wi;
+      eoff = s_off[wi];
+      em = s_off[wi + 1] - eoff;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          bh[j][nt] = make_uint4(0u, 0u, 0u, 0u);
+          const int row = nt * 8 + g, ch = d0 + j;
+          if (!dead && ch < d1 && row < em)
+            bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hbf + (size_t)(eoff + row) * I + ch * 32 + c * 8));
+        }
+      }
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+    if (!dead && !mbar_wait_fast(full0 + 8 * s, (cbits >> s) & 1u, A.err, DFV_DEVERR_STAGE_WAIT, A.abort))
+      dead = true;
+    cbits ^= 1u << s;
+    // A fragments chunk by chunk, each straight into its MMAs (holding all
+    // three chunks' fragments would cost 16 more registers, and the stage
+    // is released only a few MMAs later)
+    if (!dead) {
+      const uint32_t st = slot_addr(s);
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        if (d0 + j < d1) {
+          const uint32_t q16 = ((d0 + j) * 4 + c) * 16;
+          const uint4 a0 = lds128(st + g * rsd + q16);
+          const uint4 a1 = lds128(st + (g + 8) * rsd + q16);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (nt * 8 < em) {
+              mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bh[j][nt].x, bh[j][nt].y);
+              mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bh[j][nt].z, bh[j][nt].w);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_n(empty0 + 8 * s, 2);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
+          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    bar_sync_n(kBarGroup + grp, 256);
+    const int gt = tid & 255;
+    if (gt < NT * 128 && !dead) {
+      const int q4 = gt & 3, ln = (gt >> 2) & 31, nt = gt >> 7;
+      const int tok = nt * 8 + 2 * (ln & 3) + (q4 & 1);
+      if (tok < em) {
+        float y = 0.f;
+        for (int w = 0; w < 8; ++w) y += redg[((w * NT + nt) * 32 + ln) * 4 + q4];
+        const int pair = s_gat[eoff + tok];
+        A.ys[(size_t)pair * d + r0 + (ln >> 2) + ((q4 & 2) ? 8 : 0)] = s_w[pair] * y;
+      }
+    }
+    bar_sync_n(kBarGroup + grp, 256);
+  }
+  *dead_out = dead ? 1 : 0;
+  return cbits;
+}
+
+template <int NT, bool STACK>
+__device__ __forceinline__ void fused_body(const FusedParams &p, const StackLayer *SL, int nl) {
   pdl_trigger();
-  prefetch_router_rows(p);
+  prefetch_router_rows(STACK ? SL[0].wr : p.wr, p.E, p.d);
   pdl_wait();  // before this only the router-row prefetch touches global memory
   extern __shared__ __align__(128) unsigned char smem[];
   const int k = p.k, d = p.d, I = p.I, K = p.K, ks = p.ks, nsl = p.nsl;
@@ -112,30 +227,71 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
   // the k rows of x are copied into the staged-x rows (idle until gate/up),
   // which always hold at least k rows
   const uint32_t xbar = smem_u32(&s_xbar);
-  if (tid == 0) {
-    s_abort = 0;
-    s_bad = 0;
+  auto init_bars = [&] {
     for (int s = 0; s <= SH; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kFW);
     }
     mbar_init(xbar, 1);
     mbar_init_fence();
+  };
+  if (tid == 0) {
+    s_abort = 0;
+    s_bad = 0;
+    init_bars();
   }
   __syncthreads();
 
   const bool consumer = warp < kFW;
+#pragma unroll 1
+  for (int l = 0; l < nl; ++l) {
+  // (the layer's weights are read from the parameters where they are used)
+  const unsigned gb = 4u * (unsigned)l;  // grid barriers completed before this layer
+  if (STACK && l > 0) {
+    // layer boundary: every CTA's combine has written its rows of x (the
+    // writes are fenced for the async proxy, which copies x in next), and
+    // every wait and copy on this CTA's mbarriers is over (the producer
+    // drained its stages and the x copy), so they are armed afresh
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+      if (!grid_sync(p, gb)) s_abort = 1;
+      if (!s_abort) {
+        for (int s = 0; s <= SH; ++s) {
+          mbar_inval(full0 + 8 * s);
+          mbar_inval(empty0 + 8 * s);
+        }
+        mbar_inval(xbar);
+        init_bars();
+      }
+      s_bad = 0;
+    }
+    __syncthreads();
+    if (s_abort) {
+      // a CTA that gave up passes the later layers' grid barriers without
+      // work (the others see the abort flag or time out)
+      if (tid == 0)
+        for (unsigned b = 1; b <= 3; ++b) grid_sync(p, gb + b);
+      continue;
+    }
+  }
   if (!consumer && lane == 0) {
+    if (STACK) asm volatile("fence.proxy.async.global;" ::: "memory");
     stage_x_rows(p, sbase + SH * slot, xbar);
     if (p.tma_mode) {
-      prefetch_tensormap(&p.tm_wg);
-      prefetch_tensormap(&p.tm_wu);
+      prefetch_tensormap(STACK ? &SL[l].tm_wg : &p.tm_wg);
+      prefetch_tensormap(STACK ? &SL[l].tm_wu : &p.tm_wu);
     }
   }
   // ------------------------------------------------------------------ P0, P1: routing
   if (consumer) {
     const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_tmask, s_inv, &s_nw, &s_abort, &s_bad};
-    const RouteArgs ra = route_args(p, rs, reinterpret_cast<const uint16_t *>(scratch), xbar);
+    RouteArgs ra = route_args(p, rs, reinterpret_cast<const uint16_t *>(scratch), xbar);
+    if (STACK) {
+      ra.wr = reinterpret_cast<const uint16_t *>(SL[l].wr);
+      ra.u_nw = p.u_nw ? p.u_nw + l : nullptr;  // one count per layer
+    }
+    ra.gb = gb;
     route_p0(ra);
     route_p1(ra, [&] {
       // (warp 0, lane 0, right after the woken list is known; the producer
@@ -189,9 +345,11 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       // ring's async-proxy writes
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       const uint64_t pol = l2_evict_first();  // expert weights are read once per launch
-      const uint16_t *wg = reinterpret_cast<const uint16_t *>(p.wg);
-      const uint16_t *wu = reinterpret_cast<const uint16_t *>(p.wu);
-      const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
+      const uint16_t *wg = reinterpret_cast<const uint16_t *>(STACK ? SL[l].wg : p.wg);
+      const uint16_t *wu = reinterpret_cast<const uint16_t *>(STACK ? SL[l].wu : p.wu);
+      const uint16_t *wd = reinterpret_cast<const uint16_t *>(STACK ? SL[l].wd : p.wd);
+      const CUtensorMap *const tmg = STACK ? &SL[l].tm_wg : &p.tm_wg;
+      const CUtensorMap *const tmu = STACK ? &SL[l].tm_wu : &p.tm_wu;
       // Stage phases are tracked per stage (bit s of pbits: parity of the next
       // fill's phase on stage s), because gate/up fills go round the whole
       // ring while down fills go round the stages of their consumer group.
@@ -212,12 +370,12 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
           const uint32_t fb = full0 + 8 * s, dst = slot_addr(s);
           mbar_expect_tx(fb, 16u * ks * 2);
           if (p.tma_mode == 2) {  // [ks/256][8 rows][256]: one box per matrix
-            tma_3d_hint(dst, &p.tm_wg, 0, e * I + i0, sl * (ks / 256), fb, pol);
-            tma_3d_hint(dst + up_off, &p.tm_wu, 0, e * I + i0, sl * (ks / 256), fb, pol);
+            tma_3d_hint(dst, tmg, 0, e * I + i0, sl * (ks / 256), fb, pol);
+            tma_3d_hint(dst + up_off, tmu, 0, e * I + i0, sl * (ks / 256), fb, pol);
           } else if (p.tma_mode == 1) {  // the same layout from 256-column boxes
             for (int b = 0; b < ks / 256; ++b) {
-              tma_2d_hint(dst + b * 4096, &p.tm_wg, sl * ks + b * 256, e * I + i0, fb, pol);
-              tma_2d_hint(dst + up_off + b * 4096, &p.tm_wu, sl * ks + b * 256, e * I + i0, fb, pol);
+              tma_2d_hint(dst + b * 4096, tmg, sl * ks + b * 256, e * I + i0, fb, pol);
+              tma_2d_hint(dst + up_off + b * 4096, tmu, sl * ks + b * 256, e * I + i0, fb, pol);
             }
           } else {  // one padded row per copy
             for (int r = 0; r < 8; ++r) {
@@ -246,6 +404,16 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
         const uint32_t fb = full0 + 8 * s;
         mbar_expect_tx(fb, 16u * I * 2);
         bulk_g2s_hint(slot_addr(s), wd + ((size_t)s_woken[wi] * d + (size_t)tl * 16) * I, 16u * I * 2, fb, pol);
+      }
+      if (STACK && l + 1 < nl) {
+        // the next layer's router rows (this CTA's experts) and gate/up maps
+        // start towards L2 and the descriptor cache while this layer drains
+        const char *nwr = reinterpret_cast<const char *>(SL[l + 1].wr);
+        for (int e = blockIdx.x; e < p.E; e += G) prefetch_l2(nwr + (size_t)e * d * 2, (uint32_t)d * 2);
+        if (p.tma_mode) {
+          prefetch_tensormap(&SL[l + 1].tm_wg);
+          prefetch_tensormap(&SL[l + 1].tm_wu);
+        }
       }
       // no copy may land after the CTA exits: wait for the last fill of every stage
       volatile int never = 0;
@@ -287,7 +455,9 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
         bar_sync_n(kBarAll, kFC);
         for (int idx = tid; idx < m * cpr; idx += kFC) {
           const int j = idx / cpr, q = idx % cpr, t = s_tok[j];
-          uint4 v = *reinterpret_cast<const uint4 *>(xg + (size_t)t * d + q * 8);
+          // (a stack's later layers read rows other CTAs combined: from L2)
+          const uint4 *src = reinterpret_cast<const uint4 *>(xg + (size_t)t * d + q * 8);
+          uint4 v = STACK ? __ldcg(src) : *src;
           if (p.fuse_norm) {
             const float inv = s_inv[t];
             uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -369,97 +539,22 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       bar_sync_n(kBarAll, kFC);
     }
     // ---- grid barrier 2: every h row is written
-    if (tid == 0 && !grid_sync(p, 2)) s_abort = 1;
+    if (tid == 0 && !grid_sync(p, gb + 2)) s_abort = 1;
     bar_sync_n(kBarAll, kFC);
     dead = dead || s_abort != 0;
 
     // ---------------------------------------------------------------- P3: down
-    const int grp = warp >> 3, wg = warp & 7;
-    const int C = I / 32;
-    const int d0 = wg * C / 8, d1 = (wg + 1) * C / 8;
-    const int rsd = I * 2;
-    float *redg = red + grp * 8 * NT * 32 * 4;  // this group's [8][NT][32][4]
-    int jd = 0, cur_d = -1, eoff = 0, em = 0;
-    int gs = grp;  // this group's next stage (the group owns the stages of its parity)
-    uint4 bh[3][NT];  // B fragments: h of the current expert's tokens (bf16), reused across its tiles
-    for (int u = lo_d; u < hi_d; ++u, ++jd) {
-      if ((jd & 1) != grp) continue;
-      const int s = gs;
-      gs = (gs + 2 < S) ? gs + 2 : grp;
-      const int wi = u / tiles_d, r0 = (u - wi * tiles_d) * 16;
-      if (wi != cur_d) {
-        // straight from L2, issued before the stage wait so the latencies overlap
-        cur_d = wi;
-        eoff = s_off[wi];
-        em = s_off[wi + 1] - eoff;
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            bh[j][nt] = make_uint4(0u, 0u, 0u, 0u);
-            const int row = nt * 8 + g, ch = d0 + j;
-            if (!dead && ch < d1 && row < em)
-              bh[j][nt] = __ldcg(reinterpret_cast<const uint4 *>(hbf + (size_t)(eoff + row) * I + ch * 32 + c * 8));
-          }
-        }
-      }
-      float acc[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-      if (!dead && !mbar_wait_fast(full0 + 8 * s, (cbits >> s) & 1u, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort))
-        dead = true;
-      cbits ^= 1u << s;
-      uint4 a0[3], a1[3];
-      if (!dead) {
-        const uint32_t st = slot_addr(s);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          if (d0 + j < d1) {
-            const uint32_t q16 = ((d0 + j) * 4 + c) * 16;
-            a0[j] = lds128(st + g * rsd + q16);
-            a1[j] = lds128(st + (g + 8) * rsd + q16);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_n(empty0 + 8 * s, 2);  // released before the MMAs
-      if (!dead) {
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          if (d0 + j < d1) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              if (nt * 8 < em) {
-                mma_bf16(acc[nt], a0[j].x, a1[j].x, a0[j].y, a1[j].y, bh[j][nt].x, bh[j][nt].y);
-                mma_bf16(acc[nt], a0[j].z, a1[j].z, a0[j].w, a1[j].w, bh[j][nt].z, bh[j][nt].w);
-              }
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        *reinterpret_cast<float4 *>(redg + ((wg * NT + nt) * 32 + lane) * 4) =
-            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-      bar_sync_n(kBarGroup + grp, 256);
-      const int gt = tid & 255;
-      if (gt < NT * 128 && !dead) {
-        const int q4 = gt & 3, ln = (gt >> 2) & 31, nt = gt >> 7;
-        const int tok = nt * 8 + 2 * (ln & 3) + (q4 & 1);
-        if (tok < em) {
-          float y = 0.f;
-          for (int w = 0; w < 8; ++w) y += redg[((w * NT + nt) * 32 + ln) * 4 + q4];
-          const int pair = s_gat[eoff + tok];
-          p.ws.ys[(size_t)pair * d + r0 + (ln >> 2) + ((q4 & 2) ? 8 : 0)] = s_w[pair] * y;
-        }
-      }
-      bar_sync_n(kBarGroup + grp, 256);
+    {
+      const DownArgs da = {hbf, p.ws.ys, p.ws.err, s_off, s_gat, s_w, red, &s_abort,
+                           sbase, slot, full0, empty0, sbase + (uint32_t)SH * slot + 8u * rsx,
+                           SH, S, lo_d, hi_d, tiles_d, I, d};
+      int dd = dead ? 1 : 0;
+      cbits = down_phase<NT>(da, cbits, &dd);
+      dead = dd != 0;
     }
     // ---- grid barrier 3: every ys row is written
     bar_sync_n(kBarAll, kFC);
-    if (tid == 0 && !grid_sync(p, 3)) s_abort = 1;
+    if (tid == 0 && !grid_sync(p, gb + 3)) s_abort = 1;
     bar_sync_n(kBarAll, kFC);
     dead = dead || s_abort != 0;
 
@@ -479,6 +574,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       }
     }
   }
+  }  // layers
 
   // exit ticket: the last CTA out resets the grid-barrier count for the next launch
   __syncthreads();
@@ -488,6 +584,17 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant
       atomicExch(p.ws.sync + 1, 0u);
     }
   }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant__ FusedParams p) {
+  fused_body<NT, false>(p, nullptr, 1);
+}
+
+// All layers of a residual stack in one persistent launch.
+template <int NT>
+__global__ void __launch_bounds__(kFT, 1) moe_stack_kernel(const __grid_constant__ StackParams sp) {
+  fused_body<NT, true>(sp.p, sp.L, sp.n_layers);
 }
 
 // ----------------------------------------------------------------------------
@@ -591,23 +698,33 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
   p->tm_wu = m.wu;
 }
 
+// Tensor maps and weight pointers of one layer of a stack launch; *mode is the
+// staging mode the maps serve (every layer of a launch must share it).
+bool stack_layer_maps(StackLayer *sl, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode, int *mode) {
+  FusedParams tmp = {};
+  fused_tensor_maps(&tmp, L, plan, max_mode);
+  sl->tm_wg = tmp.tm_wg;
+  sl->tm_wu = tmp.tm_wu;
+  sl->wr = L->w_router;
+  sl->wg = L->w_gate;
+  sl->wu = L->w_up;
+  sl->wd = L->w_down;
+  *mode = tmp.tma_mode;
+  return true;
+}
+
+namespace {
 // A cooperative launch (the grid barriers need every CTA resident), chained
 // to the previous kernel programmatically when `pdl`: CTAs may start while it
 // drains, and do nothing before griddepcontrol.wait.
-cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
-  FusedParams p = p0;
-  p.ks = plan.ks;
-  p.nsl = plan.nsl;
-  p.slot = plan.slot;
-  p.scratch = plan.scratch;
-  p.ring = plan.ring;
-  auto kern = p.k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+template <class Kern, class Params>
+cudaError_t launch_coop(Kern kern, const Params &p, size_t smem, int grid, cudaStream_t s, bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kFT);
-  cfg.dynamicSmemBytes = plan.smem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -619,7 +736,10 @@ cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid,
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
+// SM count when `kern` fits one CTA per SM with the plan's shared memory, else
+// 0 with the reason in `why`.
+template <class Kern>
+int coop_max_grid(Kern kern, const FusedPlan &plan, char *why, size_t why_len) {
   int dev = 0, sms = 0, per = 0;
   cudaGetDevice(&dev);
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -627,7 +747,6 @@ int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
     snprintf(why, why_len, "SM count query: %s", cudaGetErrorString(e));
     return 0;
   }
-  auto kern = k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -644,6 +763,35 @@ int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
     return 0;
   }
   return sms;
+}
+
+void apply_plan(FusedParams &f, const FusedPlan &plan) {
+  f.ks = plan.ks;
+  f.nsl = plan.nsl;
+  f.slot = plan.slot;
+  f.scratch = plan.scratch;
+  f.ring = plan.ring;
+}
+}  // namespace
+
+cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
+  FusedParams p = p0;
+  apply_plan(p, plan);
+  return launch_coop(p.k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>, p, plan.smem, grid, s, pdl);
+}
+
+cudaError_t launch_fused_stack(const StackParams &sp0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
+  StackParams sp = sp0;
+  apply_plan(sp.p, plan);
+  return launch_coop(sp.p.k <= 8 ? moe_stack_kernel<1> : moe_stack_kernel<2>, sp, plan.smem, grid, s, pdl);
+}
+
+int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
+  return coop_max_grid(k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>, plan, why, why_len);
+}
+
+int fused_stack_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
+  return coop_max_grid(k <= 8 ? moe_stack_kernel<1> : moe_stack_kernel<2>, plan, why, why_len);
 }
 
 }  // namespace dfv

@@ -25,7 +25,8 @@ EXPORTS = ("dfv_version", "dfv_status_string", "dfv_last_error_detail", "dfv_pro
            "dfv_moe_workspace_size",
            "dfv_route_topk", "dfv_moe_block_forward", "dfv_moe_block_forward_host", "dfv_moe_stack_forward",
            "dfv_accept_workspace_size", "dfv_accept_greedy", "dfv_selftest_bounded_waits", "dfv_selftest_mma",
-           "dfv_selftest_tcgen05", "dfv_moe_batch_workspace_size", "dfv_moe_batch_forward")
+           "dfv_selftest_tcgen05", "dfv_moe_batch_workspace_size", "dfv_moe_batch_forward",
+           "dfv_set_stack_launch")
 
 
 class DfvError(RuntimeError):
@@ -66,7 +67,7 @@ def _load():
         L.dfv_route_topk.argtypes = [P, P, I, I, P, P, P, P, P, P, P, S, P]
         L.dfv_moe_block_forward.argtypes = [P, P, I, I, P, P, P, P, S, P]
         L.dfv_moe_block_forward_host.argtypes = [P, P, I, I, P, P, S, P]
-        L.dfv_moe_stack_forward.argtypes = [P, I, P, I, ctypes.c_float, P, S, P]
+        L.dfv_moe_stack_forward.argtypes = [P, I, P, I, ctypes.c_float, P, P, S, P]
         L.dfv_accept_workspace_size.restype = S
         L.dfv_accept_workspace_size.argtypes = [I, I]
         L.dfv_accept_greedy.argtypes = [P, I, I, I, P, P, P, P, S, P]
@@ -80,6 +81,7 @@ def _load():
         L.dfv_moe_batch_workspace_size.argtypes = [P, I]
         L.dfv_moe_batch_forward.argtypes = [P, P, I, I, P, P, P, P, S, P]
         L.dfv_set_path.argtypes = [I]
+        L.dfv_set_stack_launch.argtypes = [I]
         L.dfv_set_staging.restype = I
         L.dfv_set_staging.argtypes = [I]
         L.dfv_last_staging.restype = I
@@ -207,10 +209,15 @@ def moe_block_forward_host(layer: Layer, hidden_host: torch.Tensor, out_host: to
     return out_host
 
 
-def moe_stack_forward(layers: Sequence[Layer], x: torch.Tensor, ws: torch.Tensor, eps: float = 1e-6, stream=None):
+def moe_stack_forward(layers: Sequence[Layer], x: torch.Tensor, ws: torch.Tensor, eps: float = 1e-6, stream=None,
+                      n_woken: Optional[torch.Tensor] = None):
+    """x <- the stack applied to x (in place).  n_woken: optional int32 [len(layers)]
+    device tensor that receives each layer's routed woken-expert count."""
     arr = (CLayer * len(layers))(*[L.c for L in layers])
-    st = _load().dfv_moe_stack_forward(arr, len(layers), _p(x), x.shape[0], float(eps), _p(ws), ws.numel(),
-                                       _stream(stream))
+    if n_woken is not None and (n_woken.dtype != torch.int32 or n_woken.numel() < len(layers)):
+        raise ValueError("n_woken must be int32 with one entry per layer")
+    st = _load().dfv_moe_stack_forward(arr, len(layers), _p(x), x.shape[0], float(eps), _p(n_woken), _p(ws),
+                                       ws.numel(), _stream(stream))
     _check(st, "dfv_moe_stack_forward")
     return x
 
@@ -302,8 +309,15 @@ def set_path(fused: bool):
     _check(_load().dfv_set_path(1 if fused else 0), "dfv_set_path")
 
 
+def set_stack_launch(mode):
+    """Stacks whose layers allow it: 0 (or False) one launch per layer; 1 (default) one persistent
+    launch per 48 layers for k <= 8; 2 (or True) one persistent launch per 48 layers for every k."""
+    m = {False: 0, True: 2}.get(mode, mode) if isinstance(mode, bool) else int(mode)
+    _check(_load().dfv_set_stack_launch(m), "dfv_set_stack_launch")
+
+
 def last_layer_path() -> int:
-    """1 if the last layer call from this thread ran the fused kernel, 0 if multi-kernel."""
+    """Path of the last layer call from this thread: 1 fused, 0 multi-kernel, 2 batched, 3 persistent stack."""
     return int(_load().dfv_last_layer_path())
 
 

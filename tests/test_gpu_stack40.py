@@ -13,7 +13,7 @@ Strix Halo", sections "Speculative decoding" and "What the pieces cost"; part
   check: with a near-tie either expert set is a legitimate outcome of the
   summation order.
 * The one-call stack over all 40 layers equals the layer-by-layer calls bit
-  for bit.
+  for bit in every launch mode (bf16: also as one persistent launch).
 * Acceptance: logits[17, 151936] bf16 ~N(0, 2) with drafts planted from the
   oracle's argmax at Geometric(0.3) accepted lengths; tau and the committed
   tokens must equal the oracle's.
@@ -109,11 +109,23 @@ def test_stack40_teacher_forced_then_accept(dfv, shape_name):
     assert excluded <= N_LAYERS * K_BLOCK // 4
     assert dfv.read_device_error(ws) == 0
 
-    # the one-call stack equals the layer-by-layer calls
+    # the one-call stack equals the layer-by-layer calls, in every launch mode
+    # (bf16 layers: mode 2 is one persistent launch for all 40 layers)
     xs = x0.clone()
     dfv.moe_stack_forward(Ls, xs, ws)
     torch.cuda.synchronize()
     assert torch.equal(xs, x)
+    for mode, want in ((2, 3 if shape_name == "bf16" else 1), (0, 1)):
+        dfv.set_stack_launch(mode)
+        try:
+            xp = x0.clone()
+            dfv.moe_stack_forward(Ls, xp, ws)
+            torch.cuda.synchronize()
+            path = dfv.last_layer_path()
+        finally:
+            dfv.set_stack_launch(1)
+        assert path == want
+        assert torch.equal(xp, x)
     del Ls, lws
 
     # acceptance on the full vocabulary after the stack
