@@ -303,7 +303,9 @@ __device__ __forceinline__ void route_p0(const RouteArgs &r) {
 // equals), routing weights, per-expert token masks, woken union and pair
 // offsets (one warp's scan over the experts), the (expert, token)-sorted pair
 // list (a pair's position is its expert's offset plus the number of earlier
-// rows that chose the expert), then the shared expert (when p.ns).  The tables
+// rows that chose the expert), then the shared expert (when p.ns).  Lane 0 of
+// warp 0 calls after_scan(most rows any routed expert took) as soon as the
+// woken list and the offsets are in shared memory.  The tables
 // are checked before anything indexes with them.  CTA 0 also publishes the
 // decision to the workspace and the routed part to the caller's copies.  Not
 // inlined, like route_p0.
@@ -381,6 +383,10 @@ __device__ __forceinline__ void route_p1(const RouteArgs &r, AfterScan &&after_s
       nf += cnt[i] > 0;
       nc += cnt[i];
     }
+    int cmax = 0;  // most rows any routed expert took
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cmax = max(cmax, cnt[i]);
+    cmax = (int)__reduce_max_sync(0xffffffffu, (unsigned)cmax);
     int fi = nf, ci = nc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -410,7 +416,7 @@ __device__ __forceinline__ void route_p1(const RouteArgs &r, AfterScan &&after_s
       *r.nw = *r.abort ? 0 : nW;  // a CTA that gave up at the grid barrier takes no units
     }
     __syncwarp();
-    if (lane == 0) after_scan();
+    if (lane == 0) after_scan(cmax);
     __syncwarp();
     // the woken list and the offsets are all the producer needs: release it
     bar_arrive_n(kBarProducer, 64);

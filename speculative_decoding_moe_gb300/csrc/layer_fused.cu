@@ -293,17 +293,14 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
     }
     ra.gb = gb;
     route_p0(ra);
-    route_p1(ra, [&] {
+    route_p1(ra, [&](int mmax) {
       // (warp 0, lane 0, right after the woken list is known; the producer
       // reads both words) with at most 8 tokens per gate/up entry the
       // staged-x rows 8..15 are unused: they become one more ring stage.  A
       // shared expert with more than 8 tokens then enters gate/up as two
       // entries (its rows 0-7 and 8-15), which reads its gate/up rows twice
-      // but keeps that stage.
-      int mmax = 0;
+      // but keeps that stage.  mmax: most tokens any routed expert took.
       const int nw0 = s_nw;
-      const int nr = nw0 - ((p.ns && nw0 > 0) ? 1 : 0);  // routed experts
-      for (int i = 0; i < nr; ++i) mmax = max(mmax, s_off[i + 1] - s_off[i]);
       const bool extra = NT == 2 && (uint32_t)p.scratch >= 8u * rsx + slot && SH < kMaxRing;
       const bool split = extra && p.ns && nw0 > 0 && k > 8 && mmax <= 8;
       if (p.ns && nw0 > 0 && !split) mmax = max(mmax, k);

@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
     const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_tmask, s_inv, &s_nw, &s_abort, &s_bad};
     const RouteArgs ra = route_args(p, rs, reinterpret_cast<const uint16_t *>(scratch), xbar);
     route_p0(ra);
-    route_p1(ra, [] {});
+    route_p1(ra, [](int) {});
   } else {
     bar_sync_n(kBarProducer, 64);  // released as soon as the woken list is known
   }
