@@ -44,12 +44,19 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # reports traffic null.
 KERNEL_SOURCES = {
     "moe_fused_kernel": ["layer_fused.cu", "fused_common.cuh", "dfv_internal.cuh"],
+    "moe_fused_kernel_shared": ["layer_fused.cu", "fused_common.cuh", "dfv_internal.cuh"],
     "moe_fused_bs_kernel_mxfp4": ["layer_fused_bs.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
     "moe_fused_bs_kernel_q8": ["layer_fused_bs.cu", "fused_common.cuh", "mxfp4_common.cuh", "dfv_internal.cuh"],
+    "tc_group_kernel_gateup": ["batch.cu", "tc05.cuh", "dfv_internal.cuh"],
 }
-NCU_TRAFFIC = {  # kernel -> (source hash, dram read+write bytes, algorithmic bytes of that launch)
-    "moe_fused_kernel": ("2f82a8ae8f35161b", 728471040 + 7303680, 77 * 9437184 + 524288),
-
+# kernel -> (source hash, dram read+write bytes of one captured launch, algorithmic bytes of that launch);
+# the captures and their commands are summarised under profiles/ (one file per kernel and workload)
+NCU_TRAFFIC = {
+    "moe_fused_kernel": ("4ee57a88780eaf78", 727388672 + 4438016, 77 * 9437184 + 524288),
+    "moe_fused_kernel_shared": ("4ee57a88780eaf78", 647236096 + 4615936, 102 * 6291456 + 1048576),
+    "moe_fused_bs_kernel_mxfp4": ("b59e471700dfdc74", 171706112 + 4334848, 102 * 1671168 + 1048576),
+    "moe_fused_bs_kernel_q8": ("b59e471700dfdc74", 342171648 + 4303616, 102 * 3342336 + 1048576),
+    "tc_group_kernel_gateup": ("b930ce98180039b0", 822154240 + 3593472, 128 * 6291456),
 }
 
 
@@ -416,6 +423,7 @@ def run_gpu(args):
 
     # ---- headline: k=16 verify pass over 40 layers (CUDA graph replay)
     progress("headline k=16")
+    torch.cuda.nvtx.range_push("headline")
     fn16, nw16 = make_pass(KBLOCK)
     sampler = ClockSampler(local)
     steps16 = []
@@ -424,6 +432,8 @@ def run_gpu(args):
     bytes16, W16 = pass_bytes(nw16)
     ms_max = max_over_ranks(ms16, dev)
     value = achieved_gbs(world * bytes16, ms_max)
+
+    torch.cuda.nvtx.range_pop()
 
     # ---- decode: k=1 pass, same layers
     progress("decode k=1")
@@ -541,13 +551,23 @@ def run_gpu(args):
            "d2h_bytes_per_step": N_LAYERS * ho.numel() * ho.element_size(), "ms_per_step": e2e_ms,
            "api": "dfv_moe_block_forward_host per layer, pinned host buffers"}
 
-    stk = None if args.no_stack else stack_section(args, dev, rank, barrier, dfv, inputs, peak_bw, Ls, exp_bytes,
-                                                    router_bytes, ws, shape)
-    bt = None if args.no_batch else batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls,
-                                                   exp_bytes, router_bytes)
-    mx = None if args.no_mxfp4 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
-    q8 = None if args.no_q8 else mxfp4_section(args, dev, rank, barrier, dfv, inputs, peak_bw, fmt="q8")
-    sh = None if args.no_shared else shared_section(args, dev, rank, barrier, dfv, inputs, peak_bw)
+    # each section in its own NVTX range, so a profiler can select one (ncu --nvtx --nvtx-include "q8/")
+    def section(name, skip, fn, *a, **kw):
+        if skip:
+            return None
+        torch.cuda.nvtx.range_push(name)
+        try:
+            return fn(*a, **kw)
+        finally:
+            torch.cuda.nvtx.range_pop()
+
+    stk = section("stack40", args.no_stack, stack_section, args, dev, rank, barrier, dfv, inputs, peak_bw, Ls,
+                  exp_bytes, router_bytes, ws, shape)
+    bt = section("batch", args.no_batch, batch_section, args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls,
+                 exp_bytes, router_bytes)
+    mx = section("mxfp4", args.no_mxfp4, mxfp4_section, args, dev, rank, barrier, dfv, inputs, peak_bw)
+    q8 = section("q8", args.no_q8, mxfp4_section, args, dev, rank, barrier, dfv, inputs, peak_bw, fmt="q8")
+    sh = section("shared_expert", args.no_shared, shared_section, args, dev, rank, barrier, dfv, inputs, peak_bw)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -690,7 +710,8 @@ def batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls, exp
         "phase_us": {"routing_gather": ph[0] * 1e3, "gate_up": ph[1] * 1e3, "down_combine": ph[2] * 1e3},
         "roofline": {"bound": "hbm", "kernel": "tc_group_kernel<gate/up> (tcgen05, one launch per layer)",
                      "achieved": gate_bytes / (ph[1] * 1e-3) / 1e9, "peak": peak_bw, "unit": "GB/s",
-                     "frac": gate_bytes / (ph[1] * 1e-3) / 1e9 / peak_bw, "traffic": None,
+                     "frac": gate_bytes / (ph[1] * 1e-3) / 1e9 / peak_bw,
+                     "traffic": ncu_traffic("tc_group_kernel_gateup", gate_bytes),
                      "per_launch_us": ph[1] * 1e3, "algorithmic_bytes_per_launch": gate_bytes,
                      "tensor_tflops": gate_flops / (ph[1] * 1e-3) / 1e12,
                      "tensor_frac_of_sustained": gate_flops / (ph[1] * 1e-3) / 1e12 / tf_sus if tf_sus else None},
@@ -866,8 +887,8 @@ def shared_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
         "roofline": {"bound": "hbm", "kernel": "moe_fused_kernel<2> (k=16)" if fused else "multi-launch",
                      "achieved": layer_bytes / (per_launch_ms * 1e-3) / 1e9, "peak": peak_bw, "unit": "GB/s",
                      "frac": layer_bytes / (per_launch_ms * 1e-3) / 1e9 / peak_bw,
-                     "traffic": None, "per_launch_us": per_launch_ms * 1e3,
-                     "algorithmic_bytes_per_launch": layer_bytes},
+                     "traffic": ncu_traffic("moe_fused_kernel_shared", layer_bytes) if fused else None,
+                     "per_launch_us": per_launch_ms * 1e3, "algorithmic_bytes_per_launch": layer_bytes},
         "device_error": dfv.read_device_error(ws),
     }
     del layers, Ls
