@@ -642,6 +642,10 @@ def stack_section(args, dev, rank, barrier, dfv, inputs, peak_bw, Ls, exp_bytes,
         a, b = res["k%d" % KBLOCK][name], res["k1"][name]
         res["verify_decode_" + name] = {"latency_ratio": a["ms"] / b["ms"], "woken_byte_ratio": a["bytes"] / b["bytes"],
                                         "quotient": (a["bytes"] / b["bytes"]) / (a["ms"] / b["ms"])}
+    # the default launch mode: one launch per layer at k = 16, persistent at k = 1
+    a, b = res["k%d" % KBLOCK]["per_layer"], res["k1"]["persistent"]
+    res["verify_decode_default_mode"] = {"latency_ratio": a["ms"] / b["ms"], "woken_byte_ratio": a["bytes"] / b["bytes"],
+                                         "quotient": (a["bytes"] / b["bytes"]) / (a["ms"] / b["ms"])}
     res["device_error"] = dfv.read_device_error(ws)
     return res
 
@@ -700,6 +704,32 @@ def batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls, exp
                 dfv.moe_block_forward(Ls[l], xb[b], ws1, out=o1)
 
     ms_single = graph_time(fn_single, 2, max(3, args.steps // 5))
+
+    # the small-M contraction choice: one block of 16 rows through the tcgen05
+    # path (M = 128 weight rows per tile, N = the expert's rows) against the
+    # single-launch kernel's mma.sync (M = 16, N = 8 tokens per tile)
+    def fn_one_tc():
+        for l in range(N_LAYERS):
+            dfv.moe_batch_forward(Ls[l], xb[0], 1, bws, out=o1)
+
+    def fn_one_mma():
+        for l in range(N_LAYERS):
+            dfv.moe_block_forward(Ls[l], xb[0], ws1, out=o1)
+
+    ms_one_tc = graph_time(fn_one_tc, 2, max(3, args.steps // 5))
+    ms_one_mma = graph_time(fn_one_mma, 2, max(3, args.steps // 5))
+    tot1 = [0.0, 0.0, 0.0]
+    for r in range(reps + 1):
+        for l in range(N_LAYERS):
+            dfv.profile_set_events(evs[l])
+            dfv.moe_batch_forward(Ls[l], xb[0], 1, bws, out=o1)
+        dfv.profile_set_events(None)
+        torch.cuda.synchronize()
+        if r:
+            for l in range(N_LAYERS):
+                for i in range(3):
+                    tot1[i] += evs[l][i].elapsed_time(evs[l][i + 1])
+    ph1 = [t / (reps * N_LAYERS) for t in tot1]
     tf_sus = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
     return {
         "config": "32 blocks x k=16 (512 rows), Qwen3-A3B-like layer x 40 (d=2048, E=128, top-8, d_ff=768, bf16)",
@@ -718,6 +748,10 @@ def batch_section(args, dev, rank, barrier, dfv, inputs, peaks, peak_bw, Ls, exp
         "down_gbs": down_bytes / (ph[2] * 1e-3) / 1e9,
         "single_block_calls": {"ms_per_pass": ms_single, "layer_us": ms_single * 1e3 / N_LAYERS,
                                "speedup_of_batched": ms_single / ms},
+        "one_block_16_rows": {"tcgen05_path_layer_us": ms_one_tc * 1e3 / N_LAYERS,
+                              "mma_sync_single_launch_layer_us": ms_one_mma * 1e3 / N_LAYERS,
+                              "tcgen05_phase_us": {"routing_gather": ph1[0] * 1e3, "gate_up": ph1[1] * 1e3,
+                                                   "down_combine": ph1[2] * 1e3}},
         "device_error": dfv.read_device_error(bws),
     }
 

@@ -298,7 +298,7 @@ BatchWs batch_layout(const dfv_moe_layer *L, int tmax, void *base) {
 }
 
 thread_local bool g_fused_enabled = true;
-thread_local int g_stack_mode = 1;  // 0 per layer, 1 persistent for k <= 8, 2 persistent
+thread_local int g_stack_mode = 1;  // 0 per layer, 1 persistent for eager calls with k <= 8, 2 persistent
 
 // A residual stack of bf16 layers of one shape as persistent launches of up
 // to kMaxStackLayers layers each.  Returns -1 when the layers or the device do
@@ -586,7 +586,14 @@ int dfv_moe_stack_forward(const dfv_moe_layer *layers, int n_layers, void *x, in
     if (layers[l].d != layers[0].d) return fail(DFV_ERR_INVALID_ARG, "layer %d: d differs from layer 0", l);
     if ((st = check_ws(&layers[l], k, ws, ws_bytes))) return fail(st, "layer %d: %s", l, g_detail.c_str());
   }
-  if (g_fused_enabled && (g_stack_mode == 2 || (g_stack_mode == 1 && k <= 8))) {
+  bool persistent = g_stack_mode == 2;
+  if (g_stack_mode == 1 && k <= 8) {
+    // measured: inside a CUDA graph, per-layer launches chained programmatically
+    // are faster than the persistent kernel's layer-boundary grid barrier
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    persistent = cudaStreamIsCapturing((cudaStream_t)stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone;
+  }
+  if (g_fused_enabled && persistent) {
     const int st = run_stack_persistent(layers, n_layers, x, k, eps, opt_n_woken, ws, (cudaStream_t)stream);
     if (st >= 0) return st;
   }

@@ -311,7 +311,8 @@ def set_path(fused: bool):
 
 def set_stack_launch(mode):
     """Stacks whose layers allow it: 0 (or False) one launch per layer; 1 (default) one persistent
-    launch per 48 layers for k <= 8; 2 (or True) one persistent launch per 48 layers for every k."""
+    launch per 48 layers for eager calls with k <= 8 (per layer inside a CUDA graph); 2 (or True)
+    one persistent launch per 48 layers for every k."""
     m = {False: 0, True: 2}.get(mode, mode) if isinstance(mode, bool) else int(mode)
     _check(_load().dfv_set_stack_launch(m), "dfv_set_stack_launch")
 

@@ -126,8 +126,8 @@ def test_persistent_repeated_calls_one_workspace(dfv):
 
 
 def test_default_mode_persistent_up_to_8_tokens(dfv):
-    """The default launch mode takes the persistent kernel for k <= 8 and one
-    launch per layer above; every mode gives the same bits."""
+    """The default launch mode takes the persistent kernel for eager calls with
+    k <= 8 and one launch per layer above; every mode gives the same bits."""
     lws, Ls = _layers(dfv, SMALL, 3, seed=7450)
     ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], 16))
     for k, want in ((1, 3), (8, 3), (9, 1), (16, 1)):
@@ -204,3 +204,27 @@ def test_stack_kernel_teacher_forced_against_oracle(dfv, k):
         dfv.set_stack_launch(1)
     assert excluded <= n_layers * k // 4
     assert dfv.read_device_error(ws) == 0
+
+
+def test_default_mode_launches_per_layer_inside_a_graph(dfv):
+    """Captured in a CUDA graph, the default mode launches per layer even at
+    k = 1 (chained launches are the faster choice there); the replay equals
+    the eager persistent call."""
+    lws, Ls = _layers(dfv, SMALL, 3, seed=7480)
+    ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], 16))
+    x0 = inputs.make_hidden(1, SMALL.d, "bf16", seed=7481, device="cuda")
+    ref = x0.clone()
+    dfv.moe_stack_forward(Ls, ref, ws)
+    torch.cuda.synchronize()
+    assert dfv.last_layer_path() == 3
+    x = x0.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dfv.moe_stack_forward(Ls, x, ws, stream=s)
+    assert dfv.last_layer_path() == 1
+    x.copy_(x0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(x, ref)
