@@ -47,3 +47,18 @@ def moe_forward_with(lib, layer: oracle.Layer, x: np.ndarray) -> np.ndarray:
     if rc:
         raise ValueError("orc_moe_forward failed (%d)" % rc)
     return out
+
+
+def matmul_with(lib, dtype: int, a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """orc_matmul of a (possibly mutated) oracle library (operands as in oracle.matmul)."""
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.orc_matmul.argtypes = [I, P, P, I, I, I, P]
+    M, L = a.shape
+    N = b.shape[1]
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b)
+    out = np.empty((M, N), dtype=np.float64)
+    rc = lib.orc_matmul(int(dtype), a.ctypes.data_as(P), b.ctypes.data_as(P), M, L, N, out.ctypes.data_as(P))
+    if rc:
+        raise ValueError("orc_matmul failed (%d)" % rc)
+    return out

@@ -113,6 +113,21 @@ def test_signed_zero_mma_exact_in_the_oracle(fmt, neg_zero_row):
         assert int(d[int(i), int(j):int(j) + 1].view(np.uint32)[0]) == int(bits)
 
 
+@pytest.mark.parametrize("mistake", ["skips column 12", "transposes B"])
+def test_signed_zero_case_catches_planted_matmul_mistakes(mistake):
+    """Planted in a copy of the oracle's matrix product, each mistake misses
+    the printed bits: skipping the one non-zero term leaves 0, a transposed B
+    puts the column of (j+1)/16 values on the wrong axis."""
+    from tests import _mutants
+    loop = "for (int l = 0; l < L; ++l) acc += a[(size_t)i * L + l] * b[(size_t)l * N + j];"
+    bad = {"skips column 12": "for (int l = 0; l < L; ++l) if (l != 12) acc += a[(size_t)i * L + l] * b[(size_t)l * N + j];",
+           "transposes B": "for (int l = 0; l < L; ++l) acc += a[(size_t)i * L + l] * b[(size_t)j * N + l];"}[mistake]
+    lib = _mutants.build_mutant(loop, bad)
+    a, b = signed_zero_operands(None, "f16")
+    d = _mutants.matmul_with(lib, oracle.F16, _bits(a), _bits(b)).astype(np.float32)
+    assert any(d[int(i), int(j)] != value for i, j, value, _ in SIGNED_ZERO)
+
+
 def test_signed_zero_fixture_bits_are_the_printed_values():
     for i, j, value, bits in SIGNED_ZERO:
         assert np.float32(value).view(np.uint32) == int(bits)
