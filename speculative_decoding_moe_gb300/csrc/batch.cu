@@ -45,13 +45,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len);
 
 namespace {
 
-constexpr int kBRowTile = 16;    // router: rows per CTA
+constexpr int kBRowTile = 8;     // router: rows per CTA
 constexpr int kBExpTile = 32;    // router: experts per CTA
 constexpr int kTcThreads = 192;  // contraction kernels: producer, MMA, 4 epilogue warps
 constexpr int kTcK = 64;         // K elements per stage (one 128-byte swizzle row)
 constexpr int kTcM = 128;        // weight rows per unit
 constexpr int kTcNMax = 128;     // tokens per unit (TMEM: two buffers of one or two accumulators)
 constexpr int kTcBoxN = 16;      // token rows per TMA box
+constexpr int kTcEpiBar = 1;     // named barrier of the four epilogue warps
 
 // tcgen05 kernels' parameters (tensor maps first: 64-byte aligned in the
 // kernel parameter space)
@@ -208,9 +209,13 @@ __global__ void __launch_bounds__(512) batch_tables_kernel(BatchParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ int s_cnt[kMaxExperts + 1], s_eoff[kMaxExperts + 1], s_wsum[16], s_csum[16];
   __shared__ int s_nw, s_ug[kMaxExperts + 2], s_ud[kMaxExperts + 2];
+  __shared__ unsigned short s_pref[kMaxExperts][DFV_MAX_BATCH_ROWS / 32];  // rows of earlier mask words
   int cnt = 0;
   if (tid < E)
-    for (int w = 0; w < (T + 31) / 32; ++w) cnt += __popc(p.tmask[(size_t)tid * mw + w]);
+    for (int w = 0; w < (T + 31) / 32; ++w) {
+      s_pref[tid][w] = (unsigned short)cnt;
+      cnt += __popc(p.tmask[(size_t)tid * mw + w]);
+    }
   const int flag = cnt > 0;
   int fi = flag, ci = cnt;
 #pragma unroll
@@ -246,9 +251,7 @@ __global__ void __launch_bounds__(512) batch_tables_kernel(BatchParams p) {
   // sorted pairs: pair t*K+s of expert e lands at eoff[e] + (rows before t that chose e)
   for (int q = tid; q < T * K; q += blockDim.x) {
     const int t = q / K, e = p.topk_idx[q];
-    const unsigned *tm = p.tmask + (size_t)e * mw;
-    int rank = __popc(tm[t >> 5] & ((1u << (t & 31)) - 1u));
-    for (int w = 0; w < (t >> 5); ++w) rank += __popc(tm[w]);
+    const int rank = s_pref[e][t >> 5] + __popc(p.tmask[(size_t)e * mw + (t >> 5)] & ((1u << (t & 31)) - 1u));
     p.gather[s_eoff[e] + rank] = q;
   }
   if (ns)
@@ -258,19 +261,32 @@ __global__ void __launch_bounds__(512) batch_tables_kernel(BatchParams p) {
     }
   // units: per woken expert, row tiles x passes of <= 128 tokens
   const int tg = p.I / kTcM, td = p.d / kTcM;
-  if (tid == 0) {
+  if (warp == 0) {
+    // each woken expert's first gate/up and down unit: exclusive scans of its
+    // unit counts, 32 experts at a time
     int ug = 0, ud = 0;
-    for (int wi = 0; wi < nWt; ++wi) {
-      s_ug[wi] = ug;
-      s_ud[wi] = ud;
-      const int passes = (s_cnt[wi] + kTcNMax - 1) / kTcNMax;
-      ug += tg * passes;
-      ud += td * passes;
+    for (int base = 0; base < nWt; base += 32) {
+      const int wi = base + lane;
+      const int passes = wi < nWt ? (s_cnt[wi] + kTcNMax - 1) / kTcNMax : 0;
+      int ig = tg * passes, id = td * passes;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ig, o), b = __shfl_up_sync(0xffffffffu, id, o);
+        if (lane >= o) { ig += a; id += b; }
+      }
+      if (wi < nWt) {
+        s_ug[wi] = ug + ig - tg * passes;
+        s_ud[wi] = ud + id - td * passes;
+      }
+      ug += __shfl_sync(0xffffffffu, ig, 31);
+      ud += __shfl_sync(0xffffffffu, id, 31);
     }
-    s_ug[nWt] = ug;
-    s_ud[nWt] = ud;
-    p.n_units[0] = ug;
-    p.n_units[1] = ud;
+    if (lane == 0) {
+      s_ug[nWt] = ug;
+      s_ud[nWt] = ud;
+      p.n_units[0] = ug;
+      p.n_units[1] = ud;
+    }
   }
   __syncthreads();
   for (int wi = warp; wi < nWt; wi += 16) {
@@ -305,13 +321,22 @@ __global__ void __launch_bounds__(256) batch_combine_kernel(BatchParams p) {
   pdl_trigger();
   pdl_wait();
   const int T = p.T, K = p.K, d = p.d;
-  const size_t n = (size_t)T * d;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / d), r = (int)(i % d);
-    float s = 0.f;
-    for (int sl = 0; sl < K; ++sl) s += p.ys[(size_t)(t * K + sl) * d + r];
-    if (p.ns) s += p.ys[(size_t)(T * K + t) * d + r];
-    reinterpret_cast<__nv_bfloat16 *>(p.out)[i] = __float2bfloat16_rn(s);
+  // four consecutive outputs per thread (d % 128 == 0), each summed in slot order
+  const size_t n4 = (size_t)T * d / 4;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i * 4 / d), r = (int)(i * 4 % d);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 0; sl < K; ++sl) {
+      const float4 v = *reinterpret_cast<const float4 *>(p.ys + (size_t)(t * K + sl) * d + r);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    if (p.ns) {
+      const float4 v = *reinterpret_cast<const float4 *>(p.ys + (size_t)(T * K + t) * d + r);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    const uint32_t lo = (uint32_t)f32_to_bf16_bits(s.x) | ((uint32_t)f32_to_bf16_bits(s.y) << 16);
+    const uint32_t hi = (uint32_t)f32_to_bf16_bits(s.z) | ((uint32_t)f32_to_bf16_bits(s.w) << 16);
+    reinterpret_cast<uint2 *>(p.out)[i] = make_uint2(lo, hi);
   }
 }
 
@@ -342,6 +367,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
   __shared__ __align__(8) unsigned long long s_full[kStages], s_empty[kStages], s_tfull[2], s_tempty[2], s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  __shared__ int s_pair[kTcNMax];    // down: pair id of each token column of the unit
+  __shared__ float s_wt[kTcNMax];    // down: its routing weight
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(tsm);
@@ -450,18 +477,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
     const int row = quad * 32 + lane;   // weight row of the tile this thread reads
     int tcount = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++tcount) {
+    // after a wait gives up, the loop still runs to the end without touching
+    // TMEM, so the four warps meet at every named barrier
+    for (int u = blockIdx.x; u < U; u += gridDim.x, ++tcount) {
       const int4 un = p.units[u];
+      const int pos0 = p.off[un.x] + un.z;
+      if (!DUAL) {
+        // the unit's pair ids and weights, fetched while its MMAs run (the
+        // previous unit's columns are all stored before they are replaced)
+        const int et = tid - 64;  // epilogue thread 0..127
+        bar_sync_n(kTcEpiBar, 128);
+        if (et < un.w) {
+          const int q = p.gather[pos0 + et];
+          s_pair[et] = q;
+          s_wt[et] = p.w[q];
+        }
+        bar_sync_n(kTcEpiBar, 128);
+      }
       // every lane observes the accumulator barrier itself before it reads TMEM
       const int buf = tcount & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_tfull[buf]), (tcount >> 1) & 1, p.err,
-                                                         DFV_DEVERR_STAGE_WAIT, &s_abort));
-      if (!got) {
-        ok = false;
-        break;
-      }
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_tfull[buf]), (tcount >> 1) & 1, p.err,
+                                                     DFV_DEVERR_STAGE_WAIT, &s_abort));
+      if (!ok) continue;
       tc_fence_after();
-      const int pos0 = p.off[un.x] + un.z;
       const int col = un.y * kTcM + row;  // output column of this thread
       const uint32_t lane_addr = tmem + (uint32_t)buf * kBuf + ((uint32_t)(quad * 32) << 16);
       for (int c0 = 0; c0 < un.w; c0 += 16) {
@@ -477,10 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_group_kernel(const __grid_co
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < un.w) {
-              const int pair = p.gather[pos0 + c0 + j];
-              p.ys[(size_t)pair * p.ncols + col] = p.w[pair] * v1[j];
-            }
+            if (c0 + j < un.w) p.ys[(size_t)s_pair[c0 + j] * p.ncols + col] = s_wt[c0 + j] * v1[j];
         }
       }
       tc_fence_before();
@@ -596,7 +631,7 @@ cudaError_t launch_batch(const BatchParams &p, const dfv_moe_layer *L, int phase
   if (e != cudaSuccess) return e;
   e = launch_pdl(tc_group_kernel<false>, dim3(sms), dim3(kTcThreads), tc_smem<false>(), s, dn);
   if (e != cudaSuccess) return e;
-  return launch_pdl(batch_combine_kernel, dim3(2 * sms), dim3(256), 0, s, p);
+  return launch_pdl(batch_combine_kernel, dim3(4 * sms), dim3(256), 0, s, p);
 }
 
 }  // namespace dfv
