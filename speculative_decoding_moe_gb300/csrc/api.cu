@@ -461,7 +461,9 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
     if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
     mark(2, s);
     e = dfv::launch_ffn_tma(fp, L->w_dtype, 1, plan, units_d < sms ? units_d : sms, s, true);
-    if (e != cudaSuccess) return cuda_fail(e, "expert down/combine launch");
+    if (e != cudaSuccess) return cuda_fail(e, "expert down launch");
+    e = dfv::launch_ffn_tma(fp, L->w_dtype, 2, plan, sms, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     mark(3, s);
     return DFV_OK;
   }

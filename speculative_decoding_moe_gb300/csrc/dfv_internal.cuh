@@ -384,6 +384,7 @@ bool fused_bs_plan(int fmt, int k, int d, int I, int E, FusedPlan *plan);
 bool fused_bs_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, size_t why_len);
 int fused_bs_max_grid(const FusedPlan &plan, int fmt, int k, char *why, size_t why_len);
 cudaError_t launch_fused_bs(const FusedParams &p, int fmt, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl);
+// phase 0 gate/up, 1 down (writes ys), 2 combine
 cudaError_t launch_ffn_tma(const FfnParams &p, int w_dtype, int phase, const TmaPlan &plan, int grid, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_accept(const AcceptParams &p, cudaStream_t s);

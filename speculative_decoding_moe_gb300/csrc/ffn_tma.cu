@@ -13,8 +13,13 @@
 //     bulk copies (cp.async.bulk, the untiled TMA) of the weight rows;
 //   * warps 0-7 consume: wait on "full", run the m16n8k16 MMAs from shared
 //     memory, release the stage on its "empty" mbarrier, and do the per-unit
-//     epilogues (cross-warp reduction, SwiGLU, weighted scatter, combine)
-//     while the producer keeps the next stages loading.
+//     epilogues (cross-warp reduction, SwiGLU, weighted scatter) while the
+//     producer keeps the next stages loading;
+//   * a third launch combines: every output summed over its slots in slot
+//     order (no per-unit ticket on the down kernel's path).
+//
+// h enters the down contraction rounded to bf16, as in the single-launch
+// kernel.
 //
 // Every weight byte of a woken expert crosses HBM once.  Row pieces land in
 // shared memory with a row stride of 64 mod 128 bytes, so the fragment loads
@@ -188,27 +193,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gateup_tma_kernel(FfnParams p)
 }
 
 // ----------------------------------------------------------------------------
-// down + combine.  Unit = (woken expert, rs rows of d); stage = those rows over
-// the full d_ff.  Consumers: 2 row-tiles of 16 x 4 k-quarters (rs = 32) or
-// 1 x 8 (rs = 16).  h of the expert's tokens is staged as a bf16 hi/lo pair.
-// Shared memory: stages[S][rs][rsd] | hh[NT*8][rsh] | hl[NT*8][rsh] |
-// red[8][NT][32][4] f32 | full[S] | empty[S]
+// down.  Unit = (woken expert, rs rows of d); stage = those rows over the full
+// d_ff.  Consumers: 2 row-tiles of 16 x 4 k-quarters (rs = 32) or 1 x 8
+// (rs = 16).  h of the expert's tokens is staged in bf16; w[t,s] * y goes to
+// ys[pair], and the combine launch sums it.
+// Shared memory: stages[S][rs][rsd] | h[NT*8][rsh] | red[8][NT][32][4] f32 |
+// full[S] | empty[S]
 template <int NT>
 __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(128) unsigned char smem[];
-  const int d = p.d, I = p.I, K = p.K, S = p.stages, RS = p.rs;
+  const int d = p.d, I = p.I, S = p.stages, RS = p.rs;
   const int rsd = pad_to_64mod128(I * 2);
   const int rsh = pad_to_64mod128(I * 2);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t stage_bytes = (uint32_t)RS * rsd;
   const uint32_t hhb = sbase + S * stage_bytes;
-  const uint32_t hlb = hhb + NT * 8 * rsh;
-  float *red = reinterpret_cast<float *>(smem + S * stage_bytes + (size_t)2 * NT * 8 * rsh);
+  float *red = reinterpret_cast<float *>(smem + S * stage_bytes + (size_t)NT * 8 * rsh);
   const uint32_t full0 = smem_u32(red + kConsumerWarps * NT * 32 * 4);
   const uint32_t empty0 = full0 + 8 * S;
-  __shared__ unsigned s_last;
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -267,17 +271,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
         const float4 *src = reinterpret_cast<const float4 *>(p.ws.h + (size_t)(off + j) * I + q * 8);
         const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
         const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint32_t h2[4], l2[4];
+        uint32_t h2[4];
 #pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          const __nv_bfloat16 a = __float2bfloat16_rn(v[2 * q2]), b = __float2bfloat16_rn(v[2 * q2 + 1]);
-          const __nv_bfloat16 la = __float2bfloat16_rn(v[2 * q2] - __bfloat162float(a));
-          const __nv_bfloat16 lb = __float2bfloat16_rn(v[2 * q2 + 1] - __bfloat162float(b));
-          h2[q2] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-          l2[q2] = (uint32_t)__bfloat16_as_ushort(la) | ((uint32_t)__bfloat16_as_ushort(lb) << 16);
-        }
+        for (int q2 = 0; q2 < 4; ++q2)
+          h2[q2] = (uint32_t)f32_to_bf16_bits(v[2 * q2]) | ((uint32_t)f32_to_bf16_bits(v[2 * q2 + 1]) << 16);
         *reinterpret_cast<uint4 *>(smem + (hhb - sbase) + (size_t)j * rsh + q * 16) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-        *reinterpret_cast<uint4 *>(smem + (hlb - sbase) + (size_t)j * rsh + q * 16) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
       }
       bar_sync_n(kBarConsumers, kConsumers);
     }
@@ -299,15 +297,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
         for (int nt = 0; nt < NT; ++nt) {
           if (nt * 8 < m) {
             const int row = nt * 8 + g;
-            uint4 bh = make_uint4(0u, 0u, 0u, 0u), bl = bh;
-            if (row < m) {
-              bh = lds128(hhb + row * rsh + q16);
-              bl = lds128(hlb + row * rsh + q16);
-            }
+            uint4 bh = make_uint4(0u, 0u, 0u, 0u);
+            if (row < m) bh = lds128(hhb + row * rsh + q16);
             mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bh.x, bh.y);
             mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bh.z, bh.w);
-            mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bl.x, bl.y);
-            mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bl.z, bl.w);
           }
         }
       }
@@ -331,19 +324,24 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
         p.ws.ys[(size_t)pair * d + row] = p.ws.topk_w[pair] * y;
       }
     }
-    // ticket for this row tile; the last unit to finish it runs the combine
-    bar_sync_n(kBarConsumers, kConsumers);
-    if (tid == 0) {
-      __threadfence();
-      s_last = (!s_abort && atomicAdd(p.ws.down_cnt + dt, 1u) == (unsigned)(nW - 1)) ? 1u : 0u;
-    }
-    bar_sync_n(kBarConsumers, kConsumers);
-    if (s_last) {
-      __threadfence();
-      combine_rows(p.residual, p.out, p.ws.ys, p.k, K, p.ns, d, p.act, r0, rows, tid, kConsumers);
-      bar_sync_n(kBarConsumers, kConsumers);
-      if (tid == 0) p.ws.down_cnt[dt] = 0u;
-    }
+    bar_sync_n(kBarConsumers, kConsumers);  // red is free for the next unit
+  }
+}
+
+// out[t] = residual[t] + sum over slots s of ys[t*K+s] (slot order) + the
+// shared slot, every (t, r) once, after the down launch wrote every ys row.
+__global__ void __launch_bounds__(256) combine_kernel(FfnParams p) {
+  pdl_trigger();
+  pdl_wait();
+  const int n = p.k * p.d;
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthr = gridDim.x * blockDim.x;
+  for (int idx = tid; idx < n; idx += nthr) {
+    const int t = idx / p.d, r = idx - t * p.d;
+    float s = 0.f;
+    for (int sl = 0; sl < p.K; ++sl) s += __ldcg(p.ws.ys + (size_t)(t * p.K + sl) * p.d + r);
+    if (p.ns) s += __ldcg(p.ws.ys + (size_t)(p.k * p.K + t) * p.d + r);
+    if (p.residual) s = load_act(p.residual, (size_t)t * p.d + r, p.act) + s;
+    store_act(p.out, (size_t)t * p.d + r, p.act, s);
   }
 }
 
@@ -373,7 +371,7 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan) {
   }
   if (Sg < 2) return false;
   // down: rs rows of the full d_ff per stage
-  const size_t hb = (size_t)2 * NT * 8 * pad_host(I * 2);
+  const size_t hb = (size_t)NT * 8 * pad_host(I * 2);
   int rs = 32, Sd = 0;
   size_t smd = 0;
   for (; rs >= 16; rs /= 2) {
@@ -424,6 +422,19 @@ cudaError_t launch_ffn_tma(const FfnParams &p0, int w_dtype, int phase, const Tm
     p.stages = plan.stages_g;
     return p.k <= 8 ? launch_tma(gateup_tma_kernel<1>, grid, plan.smem_g, p, s, pdl)
                     : launch_tma(gateup_tma_kernel<2>, grid, plan.smem_g, p, s, pdl);
+  }
+  if (phase == 2) {
+    cudaLaunchConfig_t cfg = {};
+    const int n = p.k * p.d;
+    cfg.gridDim = dim3((n + 255) / 256 < 4 * grid ? (n + 255) / 256 : 4 * grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
   }
   p.stages = plan.stages_d;
   return p.k <= 8 ? launch_tma(down_tma_kernel<1>, grid, plan.smem_d, p, s, pdl)
