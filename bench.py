@@ -476,8 +476,10 @@ def run_gpu(args):
     fused_ms = ph[0] + ph[1] + ph[2]
     fused_gbs = layer_bytes / (fused_ms * 1e-3) / 1e9
     dfv.set_path(False)
+    torch.cuda.nvtx.range_push("multi_kernel")
     phm = per_phase()
     ms16_multi = graph_time(fn16, 2, max(3, args.steps // 4))
+    torch.cuda.nvtx.range_pop()
     dfv.set_path(True)
     gate_bytes = float(W16.sum().item()) * (2 * shape.d_ff * shape.d * 2) / N_LAYERS
     down_bytes = float(W16.sum().item()) * (shape.d * shape.d_ff * 2) / N_LAYERS

@@ -127,12 +127,42 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   const int k = p.k, d = p.d, E = p.E, K = p.K;
   const int e = blockIdx.x;
 
+  // bf16 activations: the k rows' pieces of one column chunk are all loaded
+  // before any arithmetic, so their latencies overlap (the sums below keep
+  // the generic path's order exactly)
+  const bool xbf = p.act == DFV_BF16;
+  auto load_rows = [&](int c, uint4 (&xv)[kMaxBlock]) {
+#pragma unroll
+    for (int t = 0; t < kMaxBlock; ++t)
+      xv[t] = t < k ? __ldcg(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.x) +
+                                                             (size_t)t * d + (size_t)c * 8))
+                    : make_uint4(0u, 0u, 0u, 0u);
+  };
+  auto unpack = [](const uint4 &v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+  };
+
   // ---- 1. RMSNorm scale per row (fixed-order sums)
   if (p.fuse_norm) {
     float ss[kMaxBlock];
 #pragma unroll
     for (int t = 0; t < kMaxBlock; ++t) ss[t] = 0.f;
     for (int c = tid; c < d / 8; c += kRouterThreads) {
+      if (xbf) {
+        uint4 xv[kMaxBlock];
+        load_rows(c, xv);
+#pragma unroll
+        for (int t = 0; t < kMaxBlock; ++t) {
+          if (t < k) {
+            float f[8];
+            unpack(xv[t], f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ss[t] = fmaf(f[q], f[q], ss[t]);
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int t = 0; t < kMaxBlock; ++t) {
         if (t < k) {
@@ -155,6 +185,29 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   for (int c = tid; c < d / 8; c += kRouterThreads) {
     float w[8];
     load8(p.wr, (size_t)e * d + c * 8, p.rdt, w);
+    if (xbf) {
+      uint4 xv[kMaxBlock];
+      load_rows(c, xv);
+#pragma unroll
+      for (int t = 0; t < kMaxBlock; ++t) {
+        if (t < k) {
+          float f[8];
+          unpack(xv[t], f);
+          if (p.fuse_norm) {
+            const float inv = s_inv[t];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] = round_act(f[q] * inv, DFV_BF16);
+            if (e == 0) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) store_act(p.ws.xn, (size_t)t * d + c * 8 + q, DFV_BF16, f[q]);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[t] = fmaf(f[q], w[q], acc[t]);
+        }
+      }
+      continue;
+    }
 #pragma unroll
     for (int t = 0; t < kMaxBlock; ++t) {
       if (t < k) {
