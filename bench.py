@@ -570,6 +570,7 @@ def run_gpu(args):
     mx = section("mxfp4", args.no_mxfp4, mxfp4_section, args, dev, rank, barrier, dfv, inputs, peak_bw)
     q8 = section("q8", args.no_q8, mxfp4_section, args, dev, rank, barrier, dfv, inputs, peak_bw, fmt="q8")
     sh = section("shared_expert", args.no_shared, shared_section, args, dev, rank, barrier, dfv, inputs, peak_bw)
+    wd = section("wide", args.no_wide, wide_section, args, dev, rank, barrier, dfv, inputs, peak_bw)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -594,7 +595,7 @@ def run_gpu(args):
         "kernel_path": {"fused": fused_used, "why_not": dfv.fused_unavailable_reason()},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": N_LAYERS * args.steps, "clocks": clocks,
-        "sweep": sweep, "stack40": stk, "stack40_accept": stack, "weight_gen_s": t_gen, "batch": bt, "mxfp4": mx, "q8": q8, "shared_expert": sh,
+        "sweep": sweep, "stack40": stk, "stack40_accept": stack, "weight_gen_s": t_gen, "batch": bt, "mxfp4": mx, "q8": q8, "shared_expert": sh, "wide_layers": wd,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -931,6 +932,47 @@ def shared_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
     return res
 
 
+def wide_section(args, dev, rank, barrier, dfv, inputs, peak_bw):
+    """Layers wider than the single-launch bf16 kernel takes (d_ff > 768), on
+    the general router + gate/up + down + combine path: 8 distinct layers per
+    shape (more than L2 holds), k = 16 and k = 1, graph replay.  Bytes are
+    each layer's woken experts plus its router."""
+    shapes = [("OLMoE-like: d=2048, E=64, top-8, d_ff=1024", inputs.LayerShape(d=2048, n_experts=64, top_k=8, d_ff=1024)),
+              ("Qwen1.5-MoE-like: d=2048, E=60, top-4, d_ff=1408",
+               inputs.LayerShape(d=2048, n_experts=60, top_k=4, d_ff=1408)),
+              ("Qwen3-235B-like: d=4096, E=128, top-8, d_ff=1536",
+               inputs.LayerShape(d=4096, n_experts=128, top_k=8, d_ff=1536))]
+    nl = 8
+    res = []
+    for name, shape in shapes:
+        progress("wide layers: " + name)
+        layers = [inputs.make_layer(shape, seed=2000 + 10 * rank + l, device=dev) for l in range(nl)]
+        Ls = [dfv.Layer(w) for w in layers]
+        ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], KBLOCK), device=dev)
+        eb, rb = layers[0].expert_bytes(), layers[0].router_bytes()
+        row = {"shape": name, "layers": nl}
+        for k in (KBLOCK, 1):
+            x = inputs.make_hidden(k, shape.d, "bf16", seed=2100 + k, device=dev)
+            out = torch.empty_like(x)
+            nws = torch.zeros(nl, dtype=torch.int32, device=dev)
+
+            def fn():
+                for l in range(nl):
+                    dfv.moe_block_forward(Ls[l], x, ws, out=out, n_woken=nws[l:l + 1])
+
+            ms = graph_time(fn, max(3, args.warmup), max(5, args.steps // 2), barrier)
+            W = nws.to(torch.int64).cpu()
+            nbytes = float(W.sum().item() * eb + nl * rb)
+            row["k%d" % k] = {"layer_us": ms * 1e3 / nl, "gbs": achieved_gbs(nbytes, ms),
+                              "frac_of_measured_hbm": achieved_gbs(nbytes, ms) / peak_bw,
+                              "woken_mean": float(W.double().mean().item()), "path": dfv.last_layer_path()}
+        row["device_error"] = dfv.read_device_error(ws)
+        res.append(row)
+        del layers, Ls, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -942,6 +984,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-mxfp4", action="store_true", help="skip the mxfp4-expert section")
     ap.add_argument("--no-shared", action="store_true", help="skip the shared-expert section")
+    ap.add_argument("--no-wide", action="store_true", help="skip the section of layers wider than the fused kernel takes")
     ap.add_argument("--no-q8", action="store_true", help="skip the 8-bit-expert section")
     ap.add_argument("--no-batch", action="store_true", help="skip the batched-verify section")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
