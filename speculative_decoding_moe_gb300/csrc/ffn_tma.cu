@@ -370,18 +370,23 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan) {
     if (smg <= kSmemBudget) break;
   }
   if (Sg < 2) return false;
-  // down: rs rows of the full d_ff per stage
+  // down: rs rows of the full d_ff per stage.  rs sets how a row's sum splits
+  // over the warps, so it is chosen for the largest block (two token tiles)
+  // and is the same for every k: a block's rows then equal single-token calls
+  // bit for bit.  The stage count then uses this block's own buffers.
+  const size_t redb2 = (size_t)kConsumerWarps * 2 * 32 * 16, hb2 = (size_t)2 * 8 * pad_host(I * 2);
+  int rs = 32;
+  for (; rs >= 16; rs /= 2)
+    if ((size_t)2 * rs * pad_host(I * 2) + hb2 + redb2 + 32 <= kSmemBudget) break;
+  if (rs < 16) return false;
   const size_t hb = (size_t)NT * 8 * pad_host(I * 2);
-  int rs = 32, Sd = 0;
+  int Sd = 4;
   size_t smd = 0;
-  for (; rs >= 16; rs /= 2) {
-    for (Sd = 4; Sd >= 2; --Sd) {
-      smd = (size_t)Sd * rs * pad_host(I * 2) + hb + redb + 16 * Sd;
-      if (smd <= kSmemBudget) break;
-    }
-    if (Sd >= 2) break;
+  for (; Sd >= 2; --Sd) {
+    smd = (size_t)Sd * rs * pad_host(I * 2) + hb + redb + 16 * Sd;
+    if (smd <= kSmemBudget) break;
   }
-  if (rs < 16 || Sd < 2) return false;
+  if (Sd < 2) return false;
   plan->ks = ks;
   plan->nslices = nsl;
   plan->stages_g = Sg;

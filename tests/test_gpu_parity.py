@@ -125,6 +125,39 @@ def test_bf16_wide_rows(dfv, path, shape, k, mode):
             assert torch.equal(row[0], out[t])
 
 
+WIDE_FF = [
+    # d, E, K, I: expert intermediates wider than the single-launch kernel
+    # takes (d_ff > 768), on the general path: ragged unit counts, top-2/4
+    (512, 16, 4, 1024),
+    (2048, 12, 4, 1408),
+    (4096, 8, 2, 1536),
+]
+
+
+@pytest.mark.parametrize("shape", WIDE_FF)
+@pytest.mark.parametrize("k,mode", [(16, "repeated"), (9, "independent"), (1, "independent")])
+def test_bf16_wide_intermediate_general_path(dfv, shape, k, mode):
+    d, E, K, I = shape
+    lw = inputs.make_layer(inputs.LayerShape(d=d, n_experts=E, top_k=K, d_ff=I), seed=I + 7 * k, device="cuda")
+    ol = oracle_layer(lw.to("cpu"))
+    L = dfv.Layer(lw)
+    x = hidden_without_near_ties(ol, k, "bf16", seed=I + k, mode=mode)
+    xg = x.cuda()
+    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
+    _check_routing(dfv, L, ol, xg, ws)
+    out = dfv.moe_block_forward(L, xg, ws)
+    torch.cuda.synchronize()
+    assert dfv.last_layer_path() == 0  # the single-launch kernel does not take d_ff > 768
+    assert dfv.read_device_error(ws) == 0
+    ref = oracle.moe_forward(ol, np_of(x), nthreads=oracle.num_threads_available())
+    assert _max_rel_err(_gpu_out_np(out), ref) <= TOL_BF16
+    if k > 1:
+        for t in (0, k - 1):
+            row = dfv.moe_block_forward(L, xg[t:t + 1].contiguous(), ws)
+            torch.cuda.synchronize()
+            assert torch.equal(row[0], out[t])
+
+
 @pytest.mark.parametrize("k", [1, 4])
 def test_tiny_fp32_config(dfv, k):
     lw = inputs.make_layer(inputs.TINY, seed=1)
