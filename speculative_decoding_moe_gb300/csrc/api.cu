@@ -431,11 +431,15 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
   const int maxW = (L->n_experts < k * L->top_k ? L->n_experts : k * L->top_k) + fp.ns;  // + the shared expert
   if (L->w_dtype == DFV_MXFP4) {
     // codes widened in registers: gate/up units of (expert, 8 * 4/ks rows),
-    // ks the smallest split of d whose units still fill two CTAs per SM
+    // ks the smallest split of d whose units still fill two CTAs per SM.  ks
+    // sets how each row's sum splits over d, so it is chosen for the largest
+    // block and is the same for every k (a block's rows then equal
+    // single-token calls bit for bit)
     const int sms = sm_count();
     if (sms <= 0) return fail(DFV_ERR_CUDA, "cannot query the SM count");
+    const int maxW16 = (L->n_experts < DFV_MAX_BLOCK * L->top_k ? L->n_experts : DFV_MAX_BLOCK * L->top_k) + fp.ns;
     int ks = 1;
-    while (ks < 4 && maxW * (L->d_ff / (8 * (4 / ks))) < 2 * sms) ks *= 2;
+    while (ks < 4 && maxW16 * (L->d_ff / (8 * (4 / ks))) < 2 * sms) ks *= 2;
     fp.ks = ks;
     const int units_g = maxW * (L->d_ff / (8 * (4 / ks)));
     const int units_d = maxW * (L->d / dfv::kDownTile);

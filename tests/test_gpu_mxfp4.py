@@ -304,6 +304,30 @@ def test_mxfp4_block_rows_equal_single_token_calls_fused(dfv, mx_full):
     assert dfv.read_device_error(ws) == 0
 
 
+@pytest.mark.parametrize("shape", [(2048, 256, 8, 512), (1024, 16, 4, 256), (2560, 8, 2, 1024)])
+def test_mxfp4_block_rows_equal_single_token_calls_multi_launch(dfv, shape):
+    """Multi-launch path: row t of a 16-row block is bit-identical to the k=1
+    call on that row.  The gate/up split of d is chosen for the largest block
+    whatever k is, so every row's sums run in one order."""
+    d, E, K, I = shape
+    lw = inputs.make_layer(inputs.LayerShape(d=d, n_experts=E, top_k=K, d_ff=I, w_dtype="mxfp4"), seed=d + E,
+                           device="cuda")
+    L = dfv.Layer(lw)
+    x = inputs.make_hidden(16, d, "bf16", seed=37, device="cuda")
+    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
+    dfv.set_path(False)
+    try:
+        blk = dfv.moe_block_forward(L, x, ws).clone()
+        _check_path(dfv, "multi")
+        for t in (0, 7, 8, 15):
+            row = dfv.moe_block_forward(L, x[t:t + 1].contiguous(), ws)
+            torch.cuda.synchronize()
+            assert torch.equal(row[0], blk[t]), t
+    finally:
+        dfv.set_path(True)
+    assert dfv.read_device_error(ws) == 0
+
+
 def test_mxfp4_fused_and_multikernel_paths_agree(dfv, mx_full):
     lw, ol, L = mx_full
     x = inputs.make_hidden(16, 2048, "bf16", seed=32, device="cuda")
