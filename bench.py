@@ -52,11 +52,11 @@ KERNEL_SOURCES = {
 # kernel -> (source hash, dram read+write bytes of one captured launch, algorithmic bytes of that launch);
 # the captures and their commands are summarised under profiles/ (one file per kernel and workload)
 NCU_TRAFFIC = {
-    "moe_fused_kernel": ("4ee57a88780eaf78", 727388672 + 4438016, 77 * 9437184 + 524288),
-    "moe_fused_kernel_shared": ("4ee57a88780eaf78", 647236096 + 4615936, 102 * 6291456 + 1048576),
-    "moe_fused_bs_kernel_mxfp4": ("b59e471700dfdc74", 171706112 + 4334848, 102 * 1671168 + 1048576),
-    "moe_fused_bs_kernel_q8": ("b59e471700dfdc74", 342171648 + 4303616, 102 * 3342336 + 1048576),
-    "tc_group_kernel_gateup": ("b930ce98180039b0", 822154240 + 3593472, 128 * 6291456),
+    "moe_fused_kernel": ("47c0d6932ba0aa4f", 727388928 + 4576256, 77 * 9437184 + 524288),
+    "moe_fused_kernel_shared": ("47c0d6932ba0aa4f", 647156992 + 5047808, 102 * 6291456 + 1048576),
+    "moe_fused_bs_kernel_mxfp4": ("4ff3029a6d2892a0", 171713792 + 4430080, 102 * 1671168 + 1048576),
+    "moe_fused_bs_kernel_q8": ("4ff3029a6d2892a0", 342168064 + 4563712, 102 * 3342336 + 1048576),
+    "tc_group_kernel_gateup": ("90e973b082322786", 822155776 + 3629568, 128 * 6291456),
 }
 
 
@@ -651,15 +651,33 @@ def stack_section(args, dev, rank, barrier, dfv, inputs, peak_bw, Ls, exp_bytes,
                          "frac_of_measured_hbm": achieved_gbs(nbytes, ms) / peak_bw, "path": path,
                          "woken_mean": float(W.double().mean().item()), "bytes": nbytes}
         row["identical"] = bool(torch.equal(outs[(k, "persistent")], outs[(k, "per_layer")]))
+        # eager calls (no graph): each launch pays the host's launch cost, which
+        # is what the default mode's choice of the persistent kernel at k <= 8 saves
+        eager = {}
+        for name, mode in (("persistent", 2), ("per_layer", 0), ("default", 1)):
+            progress("stack k=%d eager %s" % (k, name))
+            dfv.set_stack_launch(mode)
+            try:
+                if barrier:
+                    barrier()
+                ms_e = max_over_ranks(stream_time(fn, max(3, args.warmup), max(5, args.steps // 2)), dev)
+                path = dfv.last_layer_path()
+            finally:
+                dfv.set_stack_launch(1)
+            eager[name] = {"ms": ms_e, "layer_us": ms_e * 1e3 / N_LAYERS, "path": path,
+                           "gbs": achieved_gbs(row["per_layer"]["bytes"], ms_e)}
+        row["eager"] = eager
         res["k%d" % k] = row
     for name in ("persistent", "per_layer"):
         a, b = res["k%d" % KBLOCK][name], res["k1"][name]
         res["verify_decode_" + name] = {"latency_ratio": a["ms"] / b["ms"], "woken_byte_ratio": a["bytes"] / b["bytes"],
                                         "quotient": (a["bytes"] / b["bytes"]) / (a["ms"] / b["ms"])}
-    # the default launch mode: one launch per layer at k = 16, persistent at k = 1
-    a, b = res["k%d" % KBLOCK]["per_layer"], res["k1"]["persistent"]
-    res["verify_decode_default_mode"] = {"latency_ratio": a["ms"] / b["ms"], "woken_byte_ratio": a["bytes"] / b["bytes"],
-                                         "quotient": (a["bytes"] / b["bytes"]) / (a["ms"] / b["ms"])}
+    # the default launch mode on eager calls: one launch per layer at k = 16,
+    # persistent at k = 1 (inside a graph it launches per layer at every k)
+    a, b = res["k%d" % KBLOCK]["eager"]["default"], res["k1"]["eager"]["default"]
+    wb = res["k%d" % KBLOCK]["per_layer"]["bytes"] / res["k1"]["per_layer"]["bytes"]
+    res["verify_decode_default_mode_eager"] = {"latency_ratio": a["ms"] / b["ms"], "woken_byte_ratio": wb,
+                                               "quotient": wb / (a["ms"] / b["ms"])}
     res["device_error"] = dfv.read_device_error(ws)
     return res
 
