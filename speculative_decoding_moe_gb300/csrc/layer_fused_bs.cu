@@ -23,20 +23,21 @@
 // (512 mxfp4 codes or 256 8-bit codes) and the 16 bytes of scales that cover
 // them.  Codes arrive as tensor-map boxes of 64 bytes x rows with the 64-byte
 // swizzle, so that ldmatrix reads eight rows of a 16-byte chunk without bank
-// conflicts.  ldmatrix hands lane (g, c) bytes 4c..4c+3 of each chunk of row
-// g: for mxfp4 eight codes of one 32-element block, for 8-bit four codes of
-// half a block.  Every MMA (m16n8k16, fp16 operands, fp32 accumulate; A =
-// weights, B = tokens) therefore sums over the elements of one scale block
-// only, and the block's scale multiplies the fp32 result: for every E8M0
-// exponent 0..254 and every binary16 scale the products are exact, and only
-// the fp32 sums round.  The token rows (x for gate/up, h for down) sit in
-// shared memory as fp16, each multiplied by the power of two 2^sh that puts
-// its largest magnitude in [1, 2), so the accumulators hold about the true
-// sums (no overflow short of the fp32 range itself) and 2^-sh brings them
-// back; bf16 elements down to 2^-17 of their row's largest stay exact, and
-// smaller ones round at 2^-25 of it; for 8-bit weights the 32 elements of each block are stored in the
-// order the MMA's k slots take them, so one 16-byte load feeds two MMAs in
-// both formats.
+// conflicts; one 3-D copy brings the four boxes of a stage (the producer is a
+// single thread, and one copy per box capped the stream rate).  ldmatrix hands
+// lane (g, c) bytes 4c..4c+3 of each chunk of row g: for mxfp4 eight codes of
+// one 32-element block, for 8-bit four codes of half a block.  Every MMA
+// (m16n8k16, fp16 operands, fp32 accumulate; A = weights, B = tokens) therefore
+// sums over the elements of one scale block only, and the block's scale
+// multiplies the fp32 result: for every E8M0 exponent 0..254 and every binary16
+// scale the products are exact, and only the fp32 sums round.  The token rows
+// (x for gate/up, h for down) sit in shared memory as fp16, each multiplied by
+// the power of two 2^sh that puts its largest magnitude in [1, 2), so the
+// accumulators hold about the true sums (no overflow short of the fp32 range
+// itself) and 2^-sh brings them back; bf16 elements down to 2^-17 of their
+// row's largest stay exact, and smaller ones round at 2^-25 of it; for 8-bit
+// weights the 32 elements of each block are stored in the order the MMA's k
+// slots take them, so one 16-byte load feeds two MMAs in both formats.
 //
 //   P0, P1  routing, shared with the bf16 single-launch kernel (route_p0,
 //       route_p1, on the k rows of x the producer copies into the staged-x
@@ -324,11 +325,9 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
               const int wi = u / tiles_g;
               const int row = s_woken[wi] * I + (u - wi * tiles_g) * kBsRowsG;
               mbar_expect_tx(fb, kBsStage);
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                tma2(dst + b * (kBsRowsG * kBsBox), &p.tm_wg, q * kBsRowBytes + b * kBsBox, row, fb, pol);
-                tma2(dst + kUpOff + b * (kBsRowsG * kBsBox), &p.tm_wu, q * kBsRowBytes + b * kBsBox, row, fb, pol);
-              }
+              // the stage's four 64-byte boxes of 32 rows in one copy each
+              tma_3d_hint(dst, &p.tm_wg, 0, row, q * 4, fb, pol);
+              tma_3d_hint(dst + kUpOff, &p.tm_wu, 0, row, q * 4, fb, pol);
               tma2(dst + kScOff, &p.tm_sg, q * 16, row, fb, pol);
               tma2(dst + kScUpOff, &p.tm_su, q * 16, row, fb, pol);
             } else {
@@ -351,10 +350,11 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
             if (u < hi_d) {
               const int wi = u / tiles_d;
               const int row = s_woken[wi] * d + (u - wi * tiles_d) * kBsRowsD;
-              const int nb = min(4, (rowb_d - q * kBsRowBytes) / kBsBox);
-              mbar_expect_tx(fb, (uint32_t)(nb * kBsRowsD * kBsBox + kBsRowsD * srs_d));
-              for (int b = 0; b < nb; ++b)
-                tma2(dst + b * (kBsRowsD * kBsBox), &p.tm_wd, q * kBsRowBytes + b * kBsBox, row, fb, pol);
+              // one copy of the stage's min(4, boxes per row) boxes (the shapes
+              // the plan takes have no partial last stage)
+              const int bz = min(4, rowb_d / kBsBox);
+              mbar_expect_tx(fb, (uint32_t)(bz * kBsRowsD * kBsBox + kBsRowsD * srs_d));
+              tma_3d_hint(dst, &p.tm_wd, 0, row, q * 4, fb, pol);
               if (nqd == 1)
                 bulk_g2s_hint(dst + kScOff, p.sd + (size_t)row * srow_d, (uint32_t)(kBsRowsD * srow_d), fb, pol);
               else
@@ -786,6 +786,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len) {
 }
 
 namespace {
+// 3-D uint8 map over [rows][cols] bytes seen as [cols / 64][rows][64]: one box
+// is min(4, cols / 64) consecutive 64-byte chunks of `by` rows, landing as
+// that many [by][64] boxes with the 64-byte swizzle.
+bool encode_3d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t by, char *why,
+               size_t why_len) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(why, why_len);
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols, 64};
+  const cuuint32_t box[3] = {64, by, (cuuint32_t)(cols / 64 < 4 ? cols / 64 : 4)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(why, why_len, "block-scaled: tensor map encode failed (%d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
 bool encode_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
                CUtensorMapSwizzle swizzle, char *why, size_t why_len) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(why, why_len);
@@ -862,12 +883,11 @@ bool fused_bs_tensor_maps(FusedParams *p, const dfv_moe_layer *L, char *why, siz
   Maps m;
   memset(&m, 0, sizeof m);
   const bool multi = I * cbn / cbd > (uint64_t)kBsRowBytes;  // down rows of more than one stage
-  if (!encode_2d(&m.wg, L->w_gate, d * cbn / cbd, rows_g, kBsBox, kBsRowsG, CU_TENSOR_MAP_SWIZZLE_64B, why, why_len) ||
-      !encode_2d(&m.wu, L->w_up, d * cbn / cbd, rows_g, kBsBox, kBsRowsG, CU_TENSOR_MAP_SWIZZLE_64B, why, why_len) ||
+  if (!encode_3d(&m.wg, L->w_gate, d * cbn / cbd, rows_g, kBsRowsG, why, why_len) ||
+      !encode_3d(&m.wu, L->w_up, d * cbn / cbd, rows_g, kBsRowsG, why, why_len) ||
       !encode_2d(&m.sg, L->s_gate, d / 32 * sb, rows_g, 16, kBsRowsG, CU_TENSOR_MAP_SWIZZLE_NONE, why, why_len) ||
       !encode_2d(&m.su, L->s_up, d / 32 * sb, rows_g, 16, kBsRowsG, CU_TENSOR_MAP_SWIZZLE_NONE, why, why_len) ||
-      !encode_2d(&m.wd, L->w_down, I * cbn / cbd, rows_d, kBsBox, kBsRowsD, CU_TENSOR_MAP_SWIZZLE_64B, why,
-                 why_len) ||
+      !encode_3d(&m.wd, L->w_down, I * cbn / cbd, rows_d, kBsRowsD, why, why_len) ||
       (multi &&
        !encode_2d(&m.sd, L->s_down, I / 32 * sb, rows_d, 16, kBsRowsD, CU_TENSOR_MAP_SWIZZLE_NONE, why, why_len)))
     return false;

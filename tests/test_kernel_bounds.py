@@ -223,10 +223,12 @@ def check_bs_layer(fmt, k, d, I, E, K, idx, ns):
     assert scu_off + 31 * 16 + 16 <= BS_STAGE  # lds128 of the last up-scale row
     nq = d // F["CPS"]
     assert cb(d) == nq * BS_ROW_BYTES
-    for q in (0, nq - 1):  # TMA x coordinates: 16-byte aligned, boxes inside the row
-        for b in range(4):
-            x = q * BS_ROW_BYTES + b * BS_BOX
-            assert x % 16 == 0 and x + BS_BOX <= cb(d)
+    # the code maps are 3-D, [row bytes / 64][rows][64]: one copy of 4 boxes per stage,
+    # at chunk coordinate z = 4 q (x = 0, so the 16-byte rule holds), all inside the row
+    chunks_g = cb(d) // BS_BOX
+    assert cb(d) % BS_BOX == 0 and min(4, chunks_g) == 4
+    for q in (0, nq - 1):
+        assert 4 * q + 4 <= chunks_g
         assert (q * 16) % 16 == 0 and q * 16 + 16 <= d // 32 * F["SB"]
     # ---- down stage: [nb boxes][64][64] codes | [64][srs] scales
     rowb = cb(I)
@@ -234,13 +236,15 @@ def check_bs_layer(fmt, k, d, I, E, K, idx, ns):
     srow = I // 32 * F["SB"]
     srs = srow if nqd == 1 else 16
     assert (srow * 64) % 16 == 0 and (nqd == 1 or srow % 16 == 0)  # bulk size / tensor-map stride
+    chunks_d = rowb // BS_BOX
+    bz = min(4, chunks_d)  # the down map's box depth; the copy's byte count is bz full boxes
+    assert rowb % BS_BOX == 0
     for q in range(nqd):
         nb = min(4, (rowb - q * BS_ROW_BYTES) // BS_BOX)
         assert 1 <= nb <= 4 and (rowb - q * BS_ROW_BYTES) % BS_BOX == 0
-        assert nb * BS_ROWS_D * BS_BOX <= BS_CODES and BS_CODES + BS_ROWS_D * srs <= BS_STAGE
-        for b in range(nb):
-            x = q * BS_ROW_BYTES + b * BS_BOX
-            assert x % 16 == 0 and x + BS_BOX <= rowb
+        assert nb == bz  # no partial last stage: every copy lands whole boxes that are read
+        assert 4 * q + bz <= chunks_d  # the copy's chunks lie inside the row
+        assert bz * BS_ROWS_D * BS_BOX <= BS_CODES and BS_CODES + BS_ROWS_D * srs <= BS_STAGE
         for itb in range(nb):
             for wq in range(4):
                 for lane in (0, 7, 31):
