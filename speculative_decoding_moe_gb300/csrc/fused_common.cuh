@@ -297,19 +297,147 @@ __device__ __forceinline__ void route_p0(const RouteArgs &r) {
   }
 }
 
+// Top-K of logit row t, by one warp (lane l holds experts l + 32 q): largest
+// logit first, lowest id among equals; then the routing weights.  Returns, in
+// lane s < K, the s-th selected expert; its weight is z / den.
+__device__ __forceinline__ void route_row(const RouteArgs &r, int t, int lane, int &sel_id, float &z, float &den) {
+  const int E = r.E, K = r.K;
+  uint32_t key[8];
+  float val[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    val[q] = (e < E) ? __ldcg(r.logits + (size_t)t * E + e) : 0.f;
+    key[q] = (e < E) ? max(float_key(val[q]), 1u) : 0u;
+  }
+  sel_id = 0;
+  float sel_val = 0.f;
+  for (int s = 0; s < K; ++s) {
+    // every lane rescans its eight keys each round (no divergent update)
+    uint32_t bk = 0;
+    int bq = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (key[q] > bk) { bk = key[q]; bq = q; }
+    float bv = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q == bq) bv = val[q];
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bk == m) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31));
+    if ((int)(win & 31) == lane) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q == (int)(win >> 5)) key[q] = 0u;
+    }
+    if (lane == s) { sel_id = (int)win; sel_val = wv; }
+  }
+  const float m0 = __shfl_sync(0xffffffffu, sel_val, 0);
+  z = (lane < K) ? expf(sel_val - m0) : 0.f;
+  den = 0.f;
+  if (r.norm_topk) {
+    den = z;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (lane + 32 * q < E) den += expf(val[q] - m0);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+}
+
+// Writes the routing decision in the calling CTA's tables to the workspace
+// (CTA 0) and the routed part to the caller's copies.
+__device__ __forceinline__ void route_publish(const RouteArgs &r) {
+  const int k = r.k, K = r.K, tid = threadIdx.x;
+  const int nP = k * K + r.ns * k;
+  if (blockIdx.x == 0) {
+    const int nW = *r.nw;
+    for (int q = tid; q < k * K; q += kFC) {
+      r.topk_idx[q] = r.idx[q];
+      if (r.u_idx) r.u_idx[q] = r.idx[q];
+    }
+    for (int q = tid; q < nP; q += kFC) {
+      r.topk_w[q] = r.w[q];
+      r.gather[q] = r.gat[q];
+    }
+    for (int i = tid; i < nW; i += kFC) { r.woken[i] = r.s_woken[i]; r.offsets[i] = r.off[i]; }
+    if (tid == 0) {
+      r.offsets[nW] = r.off[nW];
+      *r.n_woken = nW;
+      if (r.u_nw) *r.u_nw = nW - r.ns;  // the caller's count: routed experts only
+    }
+  }
+}
+
+// P1 of a single-token block (k = 1), by warp 0 alone: its K experts are the
+// woken ones, one pair each, so the tables are the selection sorted by id
+// (each selected expert's rank among the K is its woken position, its pair
+// position and its offset).  The same tables as the general path builds,
+// without the per-expert masks, the scan and their block barriers.
+template <class AfterScan>
+__device__ __forceinline__ void route_p1_single(const RouteArgs &r, AfterScan &&after_scan) {
+  const int E = r.E, K = r.K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (warp == 0) {
+    int sel_id;
+    float z, den;
+    route_row(r, 0, lane, sel_id, z, den);
+    int rank = 0;  // selected ids are distinct: the rank is the woken position
+    for (int j = 0; j < K; ++j) rank += (__shfl_sync(0xffffffffu, sel_id, j) < sel_id) ? 1 : 0;
+    const bool in = lane < K;
+    const unsigned seen = __reduce_or_sync(0xffffffffu, in ? 1u << rank : 0u);
+    const bool bad = __any_sync(0xffffffffu, in && (sel_id < 0 || sel_id >= E)) || seen != (1u << K) - 1u;
+    if (in) {
+      r.idx[lane] = sel_id;
+      r.w[lane] = z / den;
+      r.s_woken[rank] = sel_id;
+      r.off[rank] = rank;
+      r.gat[rank] = lane;  // pair t * K + s of row 0 is s
+    }
+    if (lane == 0) {
+      int nW = K;
+      r.off[K] = K;
+      if (r.ns) {
+        // the shared expert: the last woken expert, selected by row 0 with weight 1
+        r.s_woken[K] = E;
+        r.off[K + 1] = K + 1;
+        r.idx[K] = E;
+        r.w[K] = 1.f;
+        r.gat[K] = K;
+        ++nW;
+      }
+      if (bad) {
+        *r.bad = 1;
+        atomicOr(r.err, DFV_DEVERR_ROUTING);
+        *r.abort = 1;
+      }
+      *r.nw = *r.abort ? 0 : nW;
+    }
+    __syncwarp();
+    if (lane == 0) after_scan(1);  // every routed expert took the one row
+    __syncwarp();
+    bar_arrive_n(kBarProducer, 64);
+  }
+  bar_sync_n(kBarAll, kFC);
+  route_publish(r);
+}
+
 // grid barrier 1 + P1, run by the kFW consumer warps of every CTA.  Every CTA
 // derives the whole routing decision itself from the published logits:
-// top-K per row (warp per row, redux max/min: largest logit, lowest id among
-// equals), routing weights, per-expert token masks, woken union and pair
-// offsets (one warp's scan over the experts), the (expert, token)-sorted pair
-// list (a pair's position is its expert's offset plus the number of earlier
-// rows that chose the expert), then the shared expert (when p.ns).  Lane 0 of
-// warp 0 calls after_scan(most rows any routed expert took) as soon as the
-// woken list and the offsets are in shared memory.  The tables
+// top-K per row (warp per row, route_row), per-expert token masks, woken
+// union and pair offsets (one warp's scan over the experts), the (expert,
+// token)-sorted pair list (a pair's position is its expert's offset plus the
+// number of earlier rows that chose the expert), then the shared expert (when
+// p.ns).  Lane 0 of warp 0 calls after_scan(most rows any routed expert took)
+// as soon as the woken list and the offsets are in shared memory.  The tables
 // are checked before anything indexes with them.  CTA 0 also publishes the
-// decision to the workspace and the routed part to the caller's copies.  Not
-// inlined, like route_p0.
-template <class AfterScan>
+// decision to the workspace and the routed part to the caller's copies.
+// SINGLE (a kernel instantiated for single-token blocks only, k = 1) takes
+// route_p1_single instead; the other instantiations do not carry that code.
+template <bool SINGLE, class AfterScan>
 __device__ __forceinline__ void route_p1(const RouteArgs &r, AfterScan &&after_scan) {
   const int k = r.k, E = r.E, K = r.K;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -317,54 +445,17 @@ __device__ __forceinline__ void route_p1(const RouteArgs &r, AfterScan &&after_s
   bar_sync_n(kBarAll, kFC);
   if (tid == 0 && !grid_sync_raw(r.sync, r.err, r.gb + 1)) *r.abort = 1;
   bar_sync_n(kBarAll, kFC);
+  if constexpr (SINGLE) {
+    route_p1_single(r, after_scan);
+    return;
+  }
 
-  // Warp t: top-K of row t (lane holds experts lane + 32 q), then the routing
-  // weights in parallel over the K lanes.
+  // Warp t: top-K of row t, then the per-expert token masks.
   if (warp < k) {
     const int t = warp;
-    uint32_t key[8];
-    float val[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = lane + 32 * q;
-      val[q] = (e < E) ? __ldcg(r.logits + (size_t)t * E + e) : 0.f;
-      key[q] = (e < E) ? max(float_key(val[q]), 1u) : 0u;
-    }
-    int sel_id = 0;
-    float sel_val = 0.f;
-    for (int s = 0; s < K; ++s) {
-      uint32_t bk = 0;
-      int bq = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (key[q] > bk) { bk = key[q]; bq = q; }
-      float bv = 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q == bq) bv = val[q];
-      const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-      const uint32_t cand = (bk == m) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu;
-      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-      const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31));
-      if ((int)(win & 31) == lane) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q == (int)(win >> 5)) key[q] = 0u;
-      }
-      if (lane == s) { sel_id = (int)win; sel_val = wv; }
-    }
-    const float m0 = __shfl_sync(0xffffffffu, sel_val, 0);
-    const float z = (lane < K) ? expf(sel_val - m0) : 0.f;
-    float den = 0.f;
-    if (r.norm_topk) {
-      den = z;
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (lane + 32 * q < E) den += expf(val[q] - m0);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    int sel_id;
+    float z, den;
+    route_row(r, t, lane, sel_id, z, den);
     if (lane < K) {
       r.idx[t * K + lane] = sel_id;
       r.w[t * K + lane] = z / den;
@@ -464,23 +555,7 @@ __device__ __forceinline__ void route_p1(const RouteArgs &r, AfterScan &&after_s
     if (tid == 0) atomicOr(r.err, DFV_DEVERR_ROUTING);
     *r.abort = 1;
   }
-  if (blockIdx.x == 0) {
-    const int nW = *r.nw;
-    for (int q = tid; q < k * K; q += kFC) {
-      r.topk_idx[q] = r.idx[q];
-      if (r.u_idx) r.u_idx[q] = r.idx[q];
-    }
-    for (int q = tid; q < nP; q += kFC) {
-      r.topk_w[q] = r.w[q];
-      r.gather[q] = r.gat[q];
-    }
-    for (int i = tid; i < nW; i += kFC) { r.woken[i] = r.s_woken[i]; r.offsets[i] = r.off[i]; }
-    if (tid == 0) {
-      r.offsets[nW] = r.off[nW];
-      *r.n_woken = nW;
-      if (r.u_nw) *r.u_nw = nW - ns;  // the caller's count: routed experts only
-    }
-  }
+  route_publish(r);
 }
 
 }  // namespace

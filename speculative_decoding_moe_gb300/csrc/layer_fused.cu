@@ -186,7 +186,7 @@ __device__ __forceinline__ uint32_t down_phase(const DownArgs &A, uint32_t cbits
   return cbits;
 }
 
-template <int NT, bool STACK>
+template <int NT, bool STACK, bool SINGLE>
 __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLayer *SL, int nl) {
   pdl_trigger();
   prefetch_router_rows(STACK ? SL[0].wr : p.wr, p.E, p.d);
@@ -293,7 +293,7 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
     }
     ra.gb = gb;
     route_p0(ra);
-    route_p1(ra, [&](int mmax) {
+    route_p1<SINGLE>(ra, [&](int mmax) {
       // (warp 0, lane 0, right after the woken list is known; the producer
       // reads both words) with at most 8 tokens per gate/up entry the
       // staged-x rows 8..15 are unused: they become one more ring stage.  A
@@ -583,15 +583,25 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
   }
 }
 
-template <int NT>
+// NT: token tiles of 8 (k <= 8: 1); SINGLE: instantiated for k = 1 only.
+template <int NT, bool SINGLE>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_kernel(const __grid_constant__ FusedParams p) {
-  fused_body<NT, false>(p, nullptr, 1);
+  fused_body<NT, false, SINGLE>(p, nullptr, 1);
 }
 
 // All layers of a residual stack in one persistent launch.
-template <int NT>
+template <int NT, bool SINGLE>
 __global__ void __launch_bounds__(kFT, 1) moe_stack_kernel(const __grid_constant__ StackParams sp) {
-  fused_body<NT, true>(sp.p, sp.L, sp.n_layers);
+  fused_body<NT, true, SINGLE>(sp.p, sp.L, sp.n_layers);
+}
+
+// the instantiation for a block of k rows
+template <bool STACK>
+auto fused_kernel_for(int k) {
+  if constexpr (STACK)
+    return k == 1 ? moe_stack_kernel<1, true> : k <= 8 ? moe_stack_kernel<1, false> : moe_stack_kernel<2, false>;
+  else
+    return k == 1 ? moe_fused_kernel<1, true> : k <= 8 ? moe_fused_kernel<1, false> : moe_fused_kernel<2, false>;
 }
 
 // ----------------------------------------------------------------------------
@@ -774,21 +784,21 @@ void apply_plan(FusedParams &f, const FusedPlan &plan) {
 cudaError_t launch_fused(const FusedParams &p0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
   FusedParams p = p0;
   apply_plan(p, plan);
-  return launch_coop(p.k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>, p, plan.smem, grid, s, pdl);
+  return launch_coop(fused_kernel_for<false>(p.k), p, plan.smem, grid, s, pdl);
 }
 
 cudaError_t launch_fused_stack(const StackParams &sp0, const FusedPlan &plan, int grid, cudaStream_t s, bool pdl) {
   StackParams sp = sp0;
   apply_plan(sp.p, plan);
-  return launch_coop(sp.p.k <= 8 ? moe_stack_kernel<1> : moe_stack_kernel<2>, sp, plan.smem, grid, s, pdl);
+  return launch_coop(fused_kernel_for<true>(sp.p.k), sp, plan.smem, grid, s, pdl);
 }
 
 int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
-  return coop_max_grid(k <= 8 ? moe_fused_kernel<1> : moe_fused_kernel<2>, plan, why, why_len);
+  return coop_max_grid(fused_kernel_for<false>(k), plan, why, why_len);
 }
 
 int fused_stack_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len) {
-  return coop_max_grid(k <= 8 ? moe_stack_kernel<1> : moe_stack_kernel<2>, plan, why, why_len);
+  return coop_max_grid(fused_kernel_for<true>(k), plan, why, why_len);
 }
 
 }  // namespace dfv

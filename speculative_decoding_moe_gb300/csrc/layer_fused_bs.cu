@@ -208,7 +208,8 @@ __device__ __forceinline__ void q8_permute(uint32_t (&w)[4]) {
   w[3] = h ? b[3] : b[1];
 }
 
-template <int FMT, int NT>
+// NT: token tiles of 8 (k <= 8: 1); SINGLE: instantiated for k = 1 only.
+template <int FMT, int NT, bool SINGLE>
 __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_constant__ FusedParams p) {
   using F = Fmt<FMT>;
   pdl_trigger();
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
     const RouteSmem rs = {s_idx, s_w, s_woken, s_off, s_eoff, s_gat, s_tmask, s_inv, &s_nw, &s_abort, &s_bad};
     const RouteArgs ra = route_args(p, rs, reinterpret_cast<const uint16_t *>(scratch), xbar);
     route_p0(ra);
-    route_p1(ra, [](int) {});
+    route_p1<SINGLE>(ra, [](int) {});
   } else {
     bar_sync_n(kBarProducer, 64);  // released as soon as the woken list is known
   }
@@ -754,8 +755,9 @@ size_t bs_smem(int d, int I, size_t *scratch_out) {
 
 template <int FMT>
 void *bs_kernel(int k) {
-  return k <= 8 ? reinterpret_cast<void *>(moe_fused_bs_kernel<FMT, 1>)
-                : reinterpret_cast<void *>(moe_fused_bs_kernel<FMT, 2>);
+  return k == 1   ? reinterpret_cast<void *>(moe_fused_bs_kernel<FMT, 1, true>)
+         : k <= 8 ? reinterpret_cast<void *>(moe_fused_bs_kernel<FMT, 1, false>)
+                  : reinterpret_cast<void *>(moe_fused_bs_kernel<FMT, 2, false>);
 }
 void *bs_kernel(int fmt, int k) { return fmt == DFV_Q8 ? bs_kernel<kFmtQ8>(k) : bs_kernel<kFmtMx>(k); }
 
