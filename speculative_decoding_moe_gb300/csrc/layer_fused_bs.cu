@@ -484,7 +484,8 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
         const uint32_t xq0 = (uint32_t)(q * (F::CPS / 8) + c) * 16;
         const uint32_t x0e = xb0 + xq0 + ((t0 & 1) ? 64u : 0u), x0o = xb0 + xq0 - ((t0 & 1) ? 64u : 0u);
         const uint32_t x1e = xb1 + xq0 + ((t1 & 1) ? 64u : 0u), x1o = xb1 + xq0 - ((t1 & 1) ? 64u : 0u);
-#pragma unroll 1
+        // unrolled by two: the next box's ldmatrix overlaps this box's MMAs
+#pragma unroll 2
         for (int itb = 0; itb < 4; ++itb) {  // one box = four 16-byte chunks per row
           uint32_t cg[4], cu[4];
           ldsm_x4(sw64(st + itb * (kBsRowsG * kBsBox), wq * 8 + lrow, lchunk), cg);
