@@ -52,10 +52,10 @@ KERNEL_SOURCES = {
 # kernel -> (source hash, dram read+write bytes of one captured launch, algorithmic bytes of that launch);
 # the captures and their commands are summarised under profiles/ (one file per kernel and workload)
 NCU_TRAFFIC = {
-    "moe_fused_kernel": ("47c0d6932ba0aa4f", 727388928 + 4576256, 77 * 9437184 + 524288),
-    "moe_fused_kernel_shared": ("47c0d6932ba0aa4f", 647156992 + 5047808, 102 * 6291456 + 1048576),
-    "moe_fused_bs_kernel_mxfp4": ("4ff3029a6d2892a0", 171713792 + 4430080, 102 * 1671168 + 1048576),
-    "moe_fused_bs_kernel_q8": ("4ff3029a6d2892a0", 342168064 + 4563712, 102 * 3342336 + 1048576),
+    "moe_fused_kernel": ("8b776246db0a5417", 727389696 + 4304128, 77 * 9437184 + 524288),
+    "moe_fused_kernel_shared": ("8b776246db0a5417", 647156736 + 4783104, 102 * 6291456 + 1048576),
+    "moe_fused_bs_kernel_mxfp4": ("4ac4cd864c4cb72c", 171705600 + 4300800, 102 * 1671168 + 1048576),
+    "moe_fused_bs_kernel_q8": ("4ac4cd864c4cb72c", 342160896 + 4527872, 102 * 3342336 + 1048576),
     "tc_group_kernel_gateup": ("90e973b082322786", 822155776 + 3629568, 128 * 6291456),
 }
 
