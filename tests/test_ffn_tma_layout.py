@@ -1,0 +1,102 @@
+"""CPU model of the multi-launch bf16 gate/up kernel's staging (ffn_tma.cu):
+each stage's gate and up matrices arrive as one 3-D tensor copy of 8 rows x
+ks columns in 128-byte segments with the 128-byte swizzle, and MMA row g reads
+stored row (g >> 1) | ((g & 1) << 2).  Checked for every d, d_ff the plan
+takes: the consumer's fragment address fetches exactly the row piece the MMA
+expects, the eight 16-byte loads of each quarter-warp hit distinct bank
+groups, the h row each MMA row writes is its stored row (a permutation of the
+unit's 8 rows), and the stages stay 1024-aligned inside the plan's shared
+memory."""
+from __future__ import annotations
+
+import pytest
+
+CONSUMER_WARPS, SMEM_BUDGET = 8, 220 * 1024
+
+
+def pad(b):
+    return b + 64 if b % 128 == 0 else b
+
+
+def tma_plan(k, d, I):
+    """The gate/up part of ffn_tma.cu's tma_plan (ks, stage count, smem)."""
+    NT = 1 if k <= 8 else 2
+    C = d // 32
+    nsl = (d + 1023) // 1024
+    while nsl <= C and C % nsl:
+        nsl += 1
+    if nsl > C:
+        return None
+    ks = d // nsl
+    xg = NT * 8 * pad(d * 2)
+    redb = CONSUMER_WARPS * NT * 32 * 16
+    for Sg in (4, 3, 2):
+        smg = 1024 + Sg * 16 * pad(ks * 2) + xg + redb + 16 * Sg
+        if smg <= SMEM_BUDGET:
+            return dict(ks=ks, nsl=nsl, S=Sg, smem=smg, xg=xg, redb=redb, NT=NT)
+    return None
+
+
+def swizzle128(z, r, b):
+    """Where the tensor copy puts byte b (0..127) of row r (0..7) of segment z:
+    the 16-byte chunk index is XORed with the row inside each 1024-byte atom."""
+    return z * 1024 + r * 128 + ((((b >> 4) ^ r) << 4) | (b & 15))
+
+
+def stored_row(g):
+    return (g >> 1) | ((g & 1) << 2)
+
+
+def consumer_offset(g, c, ch):
+    pr = stored_row(g)
+    return (ch >> 1) * 1024 + pr * 128 + ((((ch & 1) * 4 + c) ^ pr) << 4)
+
+
+@pytest.mark.parametrize("d", [512, 1024, 1536, 2048, 4096])
+def test_swizzled_gateup_fragment_addresses(d):
+    P = tma_plan(16, d, 1024)
+    assert P is not None
+    ks = P["ks"]
+    assert ks % 64 == 0 and ks // 64 <= 256  # the map's box {64, 8, ks / 64}
+    # inverse of the copy's placement for one matrix of a stage
+    where = {}
+    for z in range(ks // 64):
+        for r in range(8):
+            for b in range(0, 128, 16):
+                where[swizzle128(z, r, b)] = (r, z * 64 + b // 2)  # (stored row, first column)
+    assert len(where) == 8 * ks // 8  # every 16-byte piece lands once
+    cps = ks // 32
+    for w in range(CONSUMER_WARPS):
+        c0, c1 = w * cps // CONSUMER_WARPS, (w + 1) * cps // CONSUMER_WARPS
+        for ch in range(c0, c1):
+            offs = []
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                o = consumer_offset(g, c, ch)
+                assert o % 16 == 0 and 0 <= o and o + 16 <= 8 * ks * 2
+                # the MMA wants row g's columns ch*32 + c*8 .. +7 of stored row pr
+                assert where[o] == (stored_row(g), ch * 32 + c * 8)
+                offs.append(o)
+            for q in range(4):  # a quarter-warp's eight 16-byte loads: distinct bank groups
+                groups = {(o // 16) % 8 for o in offs[8 * q:8 * q + 8]}
+                assert len(groups) == 8
+
+
+def test_stored_rows_are_a_permutation():
+    assert sorted(stored_row(g) for g in range(8)) == list(range(8))
+    # the quarter-warp pairs: MMA rows 2i and 2i+1 read stored rows i and i + 4
+    assert all(stored_row(2 * i) == i and stored_row(2 * i + 1) == i + 4 for i in range(4))
+
+
+@pytest.mark.parametrize("k", [1, 8, 16])
+@pytest.mark.parametrize("d", [512, 1024, 1536, 2048, 4096])
+def test_swizzled_stages_fit_and_align(k, d):
+    P = tma_plan(k, d, 1024)
+    if P is None:
+        return
+    ks, S = P["ks"], P["S"]
+    stage = 32 * ks  # gate then up, unpadded
+    assert stage % 1024 == 0 and (16 * ks) % 1024 == 0  # each matrix's box starts 1024-aligned
+    assert stage <= 16 * pad(ks * 2)  # no more than the padded layout the plan reserves
+    # aligned base (up to 1023 bytes of slack) + stages + x rows + reduction + barriers
+    assert 1023 + S * stage + P["xg"] + P["redb"] + 16 * S <= P["smem"] <= SMEM_BUDGET
