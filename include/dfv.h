@@ -339,12 +339,15 @@ int dfv_last_layer_path(void);
 /*
  * How the single-launch bf16 kernel fetches its gate/up stages, for later
  * layer calls from this host thread (no counterpart on the method's pages):
- * the highest mode allowed: 2 one 3-D tensor-map copy per weight matrix and
- * stage (a view of the matrix with its column blocks as the outer dimension),
- * 1 (default) one 2-D tensor-map copy per 256 columns, 0 one 1-D bulk copy per
- * weight row.  A mode the driver or the shape does not allow falls back to the
- * next lower one.  All modes compute the same result bit for bit.
- * Returns DFV_ERR_INVALID_ARG for a mode outside 0..2.
+ * the highest mode allowed: 3 (default) one 3-D tensor-map copy per weight
+ * matrix and stage in 128-byte segments with the 128-byte swizzle (d and the
+ * stage width multiples of 64), 2 one 3-D tensor-map copy per matrix and stage
+ * in 256-column blocks, 1 one 2-D tensor-map copy per 256 columns, 0 one 1-D
+ * bulk copy per weight row.  A mode the driver or the shape does not allow
+ * falls back to the next lower one.  All modes compute the same result bit for
+ * bit.  Mode 0 also makes the multi-launch bf16 path use one bulk copy per
+ * weight row for its gate/up stages (its swizzled copies otherwise).
+ * Returns DFV_ERR_INVALID_ARG for a mode outside 0..3.
  */
 int dfv_set_staging(int max_mode);
 

@@ -23,7 +23,7 @@ thread_local cudaEvent_t g_events[4];
 thread_local bool g_profile = false;
 thread_local int g_last_path = -1;
 std::string g_fused_why;  // why the fused path is unavailable (first failure)
-thread_local int g_max_staging = 1;   // highest gate/up staging mode of the bf16 fused kernel
+thread_local int g_max_staging = 3;   // highest gate/up staging mode of the bf16 fused kernel
 thread_local int g_last_staging = -1;
 
 inline void mark(int i, cudaStream_t s) {
@@ -671,7 +671,7 @@ int dfv_last_layer_path(void) { return g_last_path; }
 const char *dfv_fused_unavailable_reason(void) { return g_fused_why.c_str(); }
 
 int dfv_set_staging(int max_mode) {
-  if (max_mode < 0 || max_mode > 2) return fail(DFV_ERR_INVALID_ARG, "staging mode must be 0, 1 or 2");
+  if (max_mode < 0 || max_mode > 3) return fail(DFV_ERR_INVALID_ARG, "staging mode must be 0, 1, 2 or 3");
   g_max_staging = max_mode;
   return DFV_OK;
 }

@@ -24,11 +24,13 @@
 //       always-on shared expert (same section) joins them as the last woken
 //       expert (id E), selected by every row with weight 1 (pairs k*K + t).
 //   P2  gate/up: unit = (woken expert, 8 d_ff rows).  The producer streams
-//       stages of 8 gate + 8 up rows x `ks` columns into an mbarrier ring
-//       (2-D tensor-map boxes of 256 columns by default; a 3-D box per matrix,
-//       or one bulk copy per row, on request); the 16 consumer warps split the
-//       columns, run
-//       m16n8k16 MMAs (gate rows = M 0-7, up rows = M 8-15, tokens = N) and
+//       stages of 8 gate + 8 up rows x `ks` columns into an mbarrier ring (by
+//       default one 3-D tensor copy per matrix in 128-byte segments with the
+//       128-byte swizzle; 256-column boxes, or one bulk copy per row, on
+//       request); the 16 consumer warps split the columns, run m16n8k16 MMAs
+//       (gate rows = M 0-7, up rows = M 8-15, tokens = N; with the swizzle,
+//       MMA row g is stored row (g >> 1) | ((g & 1) << 2), which keeps a
+//       quarter-warp's fragment loads free of bank conflicts) and
 //       reduce across warps in fixed order; h = silu(g) * u is written in
 //       bf16.  The producer then runs ahead into P3's weights.
 //       -- grid barrier 2 (consumers only) --
@@ -191,13 +193,16 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
   pdl_trigger();
   prefetch_router_rows(STACK ? SL[0].wr : p.wr, p.E, p.d);
   pdl_wait();  // before this only the router-row prefetch touches global memory
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // 1024-aligned: the 128-byte swizzle of staging mode 3 repeats every 1024 bytes
+  unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int k = p.k, d = p.d, I = p.I, K = p.K, ks = p.ks, nsl = p.nsl;
   const int G = gridDim.x;
   const int rsg = fpad(ks * 2);        // gate/up stage row stride (64 mod 128: conflict-free)
   const int rsx = d * 2;               // staged x row stride (16B chunks XOR-swizzled)
-  // gate/up stage layout: padded rows (mode 0) or [ks/256][8 rows][512 B] blocks
-  // from tensor copies (modes 1, 2); up rows follow the gate rows
+  // gate/up stage layout: padded rows (mode 0), [ks/256][8 rows][512 B] blocks
+  // from tensor copies (modes 1, 2), or [ks/64][8 rows][128 B] segments with
+  // the 128-byte swizzle (mode 3); up rows follow the gate rows
   const uint32_t row_b = p.tma_mode ? 512u : (uint32_t)rsg;
   const uint32_t blk_b = p.tma_mode ? 4096u : 512u;
   const uint32_t up_off = p.tma_mode ? 8u * ks * 2 : 8u * rsg;
@@ -366,7 +371,10 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
           used |= 1u << s;
           const uint32_t fb = full0 + 8 * s, dst = slot_addr(s);
           mbar_expect_tx(fb, 16u * ks * 2);
-          if (p.tma_mode == 2) {  // [ks/256][8 rows][256]: one box per matrix
+          if (p.tma_mode == 3) {  // [ks/64][8 rows][128 B], swizzled: one box per matrix
+            tma_3d_hint(dst, tmg, 0, e * I + i0, sl * (ks / 64), fb, pol);
+            tma_3d_hint(dst + up_off, tmu, 0, e * I + i0, sl * (ks / 64), fb, pol);
+          } else if (p.tma_mode == 2) {  // [ks/256][8 rows][256]: one box per matrix
             tma_3d_hint(dst, tmg, 0, e * I + i0, sl * (ks / 256), fb, pol);
             tma_3d_hint(dst + up_off, tmu, 0, e * I + i0, sl * (ks / 256), fb, pol);
           } else if (p.tma_mode == 1) {  // the same layout from 256-column boxes
@@ -426,6 +434,7 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
   } else {
     // ---------------------------------------------------------------- P2: gate/up
     const int g = lane >> 2, c = lane & 3;
+    const uint32_t pr = (uint32_t)((g >> 1) | ((g & 1) << 2));  // stored row of MMA row g (mode 3)
     const int cps = ks / 32;
     const int c0 = warp * cps / kFW, c1 = (warp + 1) * cps / kFW;
     const uint16_t *xg = reinterpret_cast<const uint16_t *>(p.x);
@@ -488,7 +497,12 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
           for (int j = 0; j < kMaxChunksP2; ++j) {
             if (c0 + j < c1) {
               const int ch = c0 + j;  // 32-column chunk within the stage
-              const uint32_t o = g * row_b + (ch >> 3) * blk_b + (ch & 7) * 64 + c * 16;
+              // mode 3: MMA row g reads stored row pr (rows 0,4,1,5,...), so the
+              // two rows of a quarter-warp's loads sit in opposite halves of
+              // the swizzle: no bank conflicts
+              const uint32_t o = p.tma_mode == 3
+                                     ? (ch >> 1) * 1024u + pr * 128u + ((((ch & 1) * 4 + c) ^ pr) << 4)
+                                     : g * row_b + (ch >> 3) * blk_b + (ch & 7) * 64 + c * 16;
               ag[j] = lds128(st + o);
               au[j] = lds128(st + up_off + o);
             }
@@ -529,7 +543,8 @@ __device__ __forceinline__ void fused_body(const FusedParams &p, const StackLaye
             gs += red[((w * NT + nt) * 32 + ln) * 4 + q];
             us += red[((w * NT + nt) * 32 + ln) * 4 + q + 2];
           }
-          const size_t o = (size_t)(off + tok) * I + i0 + (ln >> 2);
+          const int gr = ln >> 2;  // MMA row; mode 3 stores it as row (gr >> 1) | ((gr & 1) << 2)
+          const size_t o = (size_t)(off + tok) * I + i0 + (p.tma_mode == 3 ? ((gr >> 1) | ((gr & 1) << 2)) : gr);
           hbf[o] = __bfloat16_as_ushort(__float2bfloat16_rn(silu(gs) * us));
         }
       }
@@ -619,7 +634,7 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   const size_t gslot = (size_t)16 * pad(ks * 2);
   const size_t dslot = (size_t)16 * I * 2;
   size_t slot = gslot > dslot ? gslot : dslot;
-  slot = (slot + 127) & ~(size_t)127;
+  slot = (slot + 1023) & ~(size_t)1023;  // stage bases 1024-aligned (the mode-3 swizzle)
   // staged x: NT * 8 rows.  k > 8: rows 8..15 double as one more ring stage
   // when no expert has more than 8 tokens, so they span at least one full slot
   size_t scratch = (size_t)NT * 8 * d * 2;
@@ -632,7 +647,7 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   const size_t budget = 220 * 1024;
   int ring = 0;
   for (int r = kMaxRing - 1; r >= 4; --r) {
-    if (r * slot + scratch + redb + 16 * kMaxRing <= budget) { ring = r; break; }
+    if (1024 + r * slot + scratch + redb + 16 * kMaxRing <= budget) { ring = r; break; }
   }
   if (ring < 4) return false;
   plan->ks = ks;
@@ -640,15 +655,17 @@ bool fused_plan(int k, int d, int I, int E, FusedPlan *plan) {
   plan->slot = (int)slot;
   plan->scratch = (int)scratch;
   plan->ring = ring;
-  plan->smem = ring * slot + scratch + redb + 16 * kMaxRing;
+  plan->smem = 1024 + ring * slot + scratch + redb + 16 * kMaxRing;
   return true;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len);
 
 void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &plan, int max_mode) {
-  // the gate/up stage of 8 rows x ks columns as one 3-D box ([ks/256][8][256]),
-  // else as ks/256 2-D boxes of 8 x 256; cached per (weights, shape)
+  // the gate/up stage of 8 rows x ks columns as one swizzled 3-D box
+  // ([ks/64][8][64], 128-byte swizzle: mode 3), one 3-D box ([ks/256][8][256]:
+  // mode 2) or ks/256 2-D boxes of 8 x 256 (mode 1), the highest that max_mode
+  // and the shape allow; cached per (weights, shape)
   struct Maps {
     int mode;
     CUtensorMap wg, wu;
@@ -657,7 +674,7 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
   static std::map<std::tuple<const void *, const void *, int, int, int, int, int>, Maps> cache;
   p->tma_mode = 0;
   const int d = L->d, I = L->d_ff, E = L->n_experts + (L->n_shared ? 1 : 0), ks = plan.ks;  // the shared expert is the last
-  if (d % 256 || ks % 256 || max_mode <= 0) return;
+  if (d % 64 || ks % 64 || max_mode <= 0) return;
   const auto key = std::make_tuple(L->w_gate, L->w_up, d, I, E, ks, max_mode);
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -692,9 +709,20 @@ void fused_tensor_maps(FusedParams *p, const dfv_moe_layer *L, const FusedPlan &
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    if (max_mode >= 2 && enc3(&m.wg, L->w_gate) && enc3(&m.wu, L->w_up))
+    auto enc3s = [&](CUtensorMap *map, const void *base) {
+      const cuuint64_t dims[3] = {64, rows, (cuuint64_t)d / 64};
+      const cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
+      const cuuint32_t box[3] = {64, 8, (cuuint32_t)ks / 64};
+      const cuuint32_t es[3] = {1, 1, 1};
+      return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (max_mode >= 3 && ks / 64 <= 256 && enc3s(&m.wg, L->w_gate) && enc3s(&m.wu, L->w_up))
+      m.mode = 3;
+    else if (d % 256 == 0 && ks % 256 == 0 && max_mode >= 2 && enc3(&m.wg, L->w_gate) && enc3(&m.wu, L->w_up))
       m.mode = 2;
-    else if (enc2(&m.wg, L->w_gate) && enc2(&m.wu, L->w_up))
+    else if (d % 256 == 0 && ks % 256 == 0 && enc2(&m.wg, L->w_gate) && enc2(&m.wu, L->w_up))
       m.mode = 1;
   }
   std::lock_guard<std::mutex> lock(mu);

@@ -296,7 +296,7 @@ def selftest_tcgen05(a: torch.Tensor, b: torch.Tensor, stream=None):
 
 
 def set_staging(max_mode: int):
-    """Highest gate/up staging mode of the single-launch bf16 kernel (2, 1 or 0)."""
+    """Highest gate/up staging mode of the single-launch bf16 kernel (3, the default, 2, 1 or 0)."""
     _check(_load().dfv_set_staging(int(max_mode)), "dfv_set_staging")
 
 

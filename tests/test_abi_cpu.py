@@ -131,9 +131,10 @@ def test_device_error_bits_match_the_header(lib):
 
 def test_staging_mode_is_validated(lib):
     L = lib.lib()
-    assert L.dfv_set_staging(3) == 1
+    assert L.dfv_set_staging(4) == 1
     assert L.dfv_set_staging(-1) == 1
     assert L.dfv_set_staging(2) == 0
+    assert L.dfv_set_staging(3) == 0  # the default again
     assert L.dfv_last_staging() == -1
 
 

@@ -361,11 +361,11 @@ def test_fused_and_multikernel_paths_agree(dfv, a3b):
     assert dfv.read_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_fused_staging_modes_agree(dfv, a3b, mode):
     """Every gate/up staging mode of the single-launch kernel (row copies, 2-D
-    tensor boxes, one 3-D box) computes the same output bit for bit, and each
-    matches the oracle."""
+    tensor boxes, one 3-D box, one swizzled 3-D box with permuted MMA rows)
+    computes the same output bit for bit, and each matches the oracle."""
     lw, ol, L = a3b
     x = hidden_without_near_ties(ol, 16, "bf16", seed=41)
     xg = x.cuda()
@@ -373,17 +373,17 @@ def test_fused_staging_modes_agree(dfv, a3b, mode):
     dfv.set_path(True)
     outs = {}
     try:
-        for m in (2, mode):
+        for m in (3, mode):
             dfv.set_staging(m)
             outs[m] = dfv.moe_block_forward(L, xg, ws).clone()
             torch.cuda.synchronize()
             assert dfv.last_layer_path() == 1, dfv.fused_unavailable_reason()
             assert dfv.last_staging() <= m
     finally:
-        dfv.set_staging(1)  # the library's default
+        dfv.set_staging(3)  # the library's default
     if mode > 0:
         assert dfv.last_staging() in (mode, mode - 1)
-    assert torch.equal(outs[mode], outs[2])
+    assert torch.equal(outs[mode], outs[3])
     assert dfv.read_device_error(ws) == 0
     ref = oracle.moe_forward(ol, np_of(x), nthreads=oracle.num_threads_available())
     assert _max_rel_err(_gpu_out_np(outs[mode]), ref) <= TOL_BF16

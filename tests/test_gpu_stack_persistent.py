@@ -73,7 +73,7 @@ def test_persistent_equals_per_layer_launches(dfv, shape_name, k):
     assert dfv.read_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_persistent_every_staging_mode(dfv, mode):
     lws, Ls = _layers(dfv, SMALL, 5, seed=7200)
     ws = dfv.alloc_workspace(dfv.workspace_size(Ls[0], 16))
@@ -84,7 +84,7 @@ def test_persistent_every_staging_mode(dfv, mode):
         got, path = _run(dfv, Ls, x0, ws, True)
         used = dfv.last_staging()
     finally:
-        dfv.set_staging(1)
+        dfv.set_staging(3)
     assert path == 3 and used <= mode
     assert torch.equal(got, ref)
 

@@ -37,18 +37,19 @@ def fused_plan(k, d, I, E):
     if ks // 32 > FW * MAX_CHUNKS_P2:
         return None
     slot = max(16 * pad(ks * 2), 16 * I * 2)
-    slot = (slot + 127) & ~127
+    slot = (slot + 1023) & ~1023  # stage bases 1024-aligned (the mode-3 swizzle)
     scratch = NT * 8 * d * 2
     if NT == 2 and 8 * d * 2 + slot > scratch:
         scratch = 8 * d * 2 + slot
     scratch = max(scratch, k * E * 4, k * 8 * 16 * 4)
     scratch = (scratch + 127) & ~127
     redb = FW * NT * 32 * 16
-    ring = next((r for r in range(MAX_RING - 1, 3, -1) if r * slot + scratch + redb + 16 * MAX_RING <= SMEM_BUDGET), 0)
+    ring = next((r for r in range(MAX_RING - 1, 3, -1)
+                 if 1024 + r * slot + scratch + redb + 16 * MAX_RING <= SMEM_BUDGET), 0)
     if ring < 4:
         return None
     return dict(NT=NT, nsl=nsl, ks=ks, slot=slot, scratch=scratch, ring=ring, redb=redb,
-                smem=ring * slot + scratch + redb + 16 * MAX_RING)
+                smem=1024 + ring * slot + scratch + redb + 16 * MAX_RING)
 
 
 def tables(idx, k, K, E, ns):
@@ -77,11 +78,16 @@ def check_layer(k, d, I, E, K, idx, ns, tma):
     if P is None:
         return None
     NT, ks, nsl, slot, SH = P["NT"], P["ks"], P["nsl"], P["slot"], P["ring"]
-    if tma and (d % 256 or ks % 256):
+    if tma == 3 and (d % 64 or ks % 64):
+        tma = 1
+    if tma in (1, 2) and (d % 256 or ks % 256):
         tma = 0
     rsx, rsg = d * 2, pad(ks * 2)
     row_b, blk_b = (512, 4096) if tma else (rsg, 512)
     up_off = 8 * ks * 2 if tma else 8 * rsg
+    if tma == 3:
+        # swizzled segments: every stage base (ring slots and the staged-x stage) 1024-aligned
+        assert slot % 1024 == 0 and (8 * rsx) % 1024 == 0 and up_off % 1024 == 0
     assert P["smem"] + 5632 <= SMEM_MAX  # dynamic + the kernel's static 5.5 KB (routing tables)
     woken, off, gat = tables(idx, k, K, E, ns)
     nW, nP = len(woken), k * K + ns * k
@@ -119,7 +125,12 @@ def check_layer(k, d, I, E, K, idx, ns, tma):
             assert c1 - c0 <= MAX_CHUNKS_P2
             if c1 > c0:
                 ch = c1 - 1
-                o_frag = 7 * row_b + (ch >> 3) * blk_b + (ch & 7) * 64 + 3 * 16
+                if tma == 3:  # the largest offset over the MMA rows and lane columns
+                    o_frag = max((ch >> 1) * 1024 + ((g >> 1) | ((g & 1) << 2)) * 128
+                                 + ((((ch & 1) * 4 + c) ^ ((g >> 1) | ((g & 1) << 2))) << 4)
+                                 for g in range(8) for c in range(4))
+                else:
+                    o_frag = 7 * row_b + (ch >> 3) * blk_b + (ch & 7) * 64 + 3 * 16
                 assert o_frag + 16 <= up_off and up_off + o_frag + 16 <= min(slot, 2 * up_off)
         # B fragments: x chunk index of the last slice, XOR swizzle within the row
         swz = 4 if d % 64 == 0 else 0
@@ -159,7 +170,7 @@ def test_fused_bf16_indices_stay_in_their_buffers(d, I):
         for k in (1, 8, 9, 16):
             for idx in _draws(k, E, K, rnd):
                 for ns in (0, 1):
-                    for tma in (1, 0):
+                    for tma in (3, 1, 0):
                         S = check_layer(k, d, I, E, K, idx, ns, tma)
                         if S is not None:
                             checked += 1
