@@ -66,7 +66,7 @@ struct RouterParams {
 struct FfnParams {
   // TMA-staged bf16 gate/up: tma_mode 1, one 3-D box per matrix and stage
   // ([ks/64][8 rows][128 B], 128-byte swizzle); 0, one bulk copy per row piece
-  CUtensorMap tm_wg, tm_wu;
+  CUtensorMap tm_wg, tm_wu, tm_wd;  // tm_wd: down rows [d_ff/64][rs rows][128 B] swizzled
   int tma_mode;
   const void *x;        // [k][d] rows the experts see (bf16 / f32)
   const void *wg, *wu, *wd;
@@ -372,7 +372,7 @@ struct TmaPlan {
   size_t smem_g, smem_d;
 };
 bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
-void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks);
+void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks, int rs);
 // Fused single-launch layer (bf16): plan, grid (0 = cannot run) and launch.
 bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
 int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);

@@ -10,9 +10,10 @@
 //   * warp 8 is the producer: one thread walks the CTA's units and, for each
 //     stage of a ring in shared memory, waits for the stage to be free, posts
 //     the expected byte count on the stage's "full" mbarrier and issues the
-//     copies: for gate/up one 3-D tensor copy per matrix (its 8 rows as
-//     128-byte segments with the 128-byte swizzle), for down 1-D bulk copies
-//     (cp.async.bulk) of the weight rows;
+//     copies: one 3-D tensor copy per gate/up matrix (its 8 rows) and per down
+//     unit (its rs rows), as 128-byte segments with the 128-byte swizzle (1-D
+//     bulk copies per row piece, into padded rows, when the maps cannot be
+//     made);
 //   * warps 0-7 consume: wait on "full", run the m16n8k16 MMAs from shared
 //     memory, release the stage on its "empty" mbarrier, and do the per-unit
 //     epilogues (cross-warp reduction, SwiGLU, weighted scatter) while the
@@ -23,15 +24,14 @@
 // h enters the down contraction rounded to bf16, as in the single-launch
 // kernel.
 //
-// Every weight byte of a woken expert crosses HBM once.  The down rows land in
-// shared memory with a row stride of 64 mod 128 bytes, so the fragment loads
-// of two neighbouring rows fall on disjoint bank halves.  The gate/up stages
-// get the same property from the swizzle: MMA row g reads stored row
-// (g >> 1) | ((g & 1) << 2), so the two rows of a quarter-warp's loads are r
-// and r + 4, whose 16-byte chunks the swizzle puts in opposite halves of the
-// banks.  One copy per matrix instead of one per row piece took the
-// single-token layers 6-13% faster and the Qwen3-235B-like layer at k = 16
-// from 645 to 605 us.  Every mbarrier wait
+// Every weight byte of a woken expert crosses HBM once.  In the swizzled
+// stages MMA row g (and g + 8) reads stored row (g >> 1) | ((g & 1) << 2) (and
+// that + 8), so the two rows of a quarter-warp's fragment loads are r and
+// r + 4, whose 16-byte chunks the swizzle puts in opposite halves of the
+// banks; the padded rows (a stride of 64 mod 128 bytes) get the same from the
+// padding.  One copy per matrix and per down unit, instead of one per row
+// piece, took the A3B layer at k = 16 from 201 to 181 us and the single-token
+// layers 6-13% faster.  Every mbarrier wait
 // is bounded (2 s); a timeout sets a bit in the workspace error word, the CTA
 // stops, and the producer waits (bounded) for its copies in flight first.
 #include <map>
@@ -228,18 +228,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gateup_tma_kernel(const __grid
 // d_ff.  Consumers: 2 row-tiles of 16 x 4 k-quarters (rs = 32) or 1 x 8
 // (rs = 16).  h of the expert's tokens is staged in bf16; w[t,s] * y goes to
 // ys[pair], and the combine launch sums it.
-// Shared memory: stages[S][rs][rsd] | h[NT*8][rsh] | red[8][NT][32][4] f32 |
-// full[S] | empty[S]
+// Shared memory (1024-aligned): stages[S] | h[NT*8][rsh] | red[8][NT][32][4]
+// f32 | full[S] | empty[S]; a stage is [d_ff/64][rs][128 B] swizzled
+// (tma_mode 1) or [rs][rsd] padded rows (tma_mode 0).
 template <int NT>
-__global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
+__global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(const __grid_constant__ FfnParams p) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int d = p.d, I = p.I, S = p.stages, RS = p.rs;
   const int rsd = pad_to_64mod128(I * 2);
   const int rsh = pad_to_64mod128(I * 2);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t stage_bytes = (uint32_t)RS * rsd;
+  // stage layout: padded rows (tma_mode 0), or [I/64][RS rows][128 B] with the
+  // 128-byte swizzle from one tensor copy (tma_mode 1)
+  const uint32_t stage_bytes = p.tma_mode ? (uint32_t)RS * I * 2 : (uint32_t)RS * rsd;
   const uint32_t hhb = sbase + S * stage_bytes;
   float *red = reinterpret_cast<float *>(smem + S * stage_bytes + (size_t)NT * 8 * rsh);
   const uint32_t full0 = smem_u32(red + kConsumerWarps * NT * 32 * 4);
@@ -265,6 +269,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
+      const uint64_t pol = l2_evict_first();  // expert weights are read once per launch
       int it = 0;
       for (int u = lo; u < hi; ++u, ++it) {
         const int e = p.ws.woken[u / tiles], r0 = (u % tiles) * RS;
@@ -272,8 +277,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
         const int s = it % S;
         if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) break;
         const uint32_t fb = full0 + 8 * s, dst = sbase + s * stage_bytes;
-        mbar_expect_tx(fb, (uint32_t)rows * I * 2);
-        for (int r = 0; r < rows; ++r) bulk_g2s(dst + r * rsd, wd + ((size_t)e * d + r0 + r) * I, I * 2, fb);
+        if (p.tma_mode) {  // one box of RS rows (rows past d are zero-filled and counted)
+          mbar_expect_tx(fb, (uint32_t)RS * I * 2);
+          tma_3d_hint(dst, &p.tm_wd, 0, e * d + r0, 0, fb, pol);
+        } else {
+          mbar_expect_tx(fb, (uint32_t)rows * I * 2);
+          for (int r = 0; r < rows; ++r) bulk_g2s(dst + r * rsd, wd + ((size_t)e * d + r0 + r) * I, I * 2, fb);
+        }
       }
       drain_stages(full0, it, S, p.ws.err);
     }
@@ -281,6 +291,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
   }
 
   const int g = lane >> 2, c = lane & 3;
+  // swizzled stages: MMA rows g and g + 8 of a row tile read stored rows pr and
+  // 8 + pr (rows 0,4,1,5,...), so a quarter-warp's two rows sit in opposite
+  // halves of the swizzle
+  const uint32_t pr = (uint32_t)((g >> 1) | ((g & 1) << 2));
   const int rtiles = RS / 16;                   // row tiles per unit (2 or 1)
   const int kparts = kConsumerWarps / rtiles;   // k parts (4 or 8)
   const int rw = warp % rtiles, kq = warp / rtiles;
@@ -322,8 +336,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
     if (!dead && rw * 16 < rows) {
       for (int ch = c0; ch < c1; ++ch) {
         const uint32_t q16 = (ch * 4 + c) * 16;
-        const uint4 a0 = lds128(st + (rw * 16 + g) * rsd + q16);
-        const uint4 a1 = lds128(st + (rw * 16 + g + 8) * rsd + q16);
+        uint32_t o0, o1;
+        if (p.tma_mode) {
+          const uint32_t x = (uint32_t)(ch * 4 + c);
+          o0 = (x >> 3) * (uint32_t)(RS * 128) + (rw * 16 + pr) * 128u + (((x & 7u) ^ pr) << 4);
+          o1 = o0 + 1024u;
+        } else {
+          o0 = (rw * 16 + g) * rsd + q16;
+          o1 = (rw * 16 + g + 8) * rsd + q16;
+        }
+        const uint4 a0 = lds128(st + o0);
+        const uint4 a1 = lds128(st + o1);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (nt * 8 < m) {
@@ -346,7 +369,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) down_tma_kernel(FfnParams p) {
     // y[row][tok] = sum over k parts (fixed order); weighted by the pair's routing weight
     for (int idx = tid; idx < rtiles * NT * 128; idx += kConsumers) {
       const int q4 = idx & 3, ln = (idx >> 2) & 31, nt = (idx >> 7) % NT, rt = idx / (128 * NT);
-      const int row = r0 + rt * 16 + (ln >> 2) + ((q4 & 2) ? 8 : 0);
+      const int gr = ln >> 2;
+      const int row = r0 + rt * 16 + (p.tma_mode ? ((gr >> 1) | ((gr & 1) << 2)) : gr) + ((q4 & 2) ? 8 : 0);
       const int tok = nt * 8 + 2 * (ln & 3) + (q4 & 1);
       if (tok < m && row < d) {
         float y = 0.f;
@@ -385,20 +409,21 @@ constexpr size_t kSmemBudget = 220 * 1024;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len);
 
-// The gate/up maps of the TMA-staged kernel: each matrix viewed as
-// [d/64][E*I rows][64 columns] (128-byte rows, 128-byte swizzle), box {64, 8,
-// ks/64}; cached per (weights, shape).  Mode 0 when they cannot be encoded.
-void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks) {
+// The maps of the TMA-staged kernels, 128-byte rows with the 128-byte swizzle:
+// gate and up viewed as [d/64][E*I rows][64 columns], box {64, 8, ks/64}; down
+// as [d_ff/64][E*d rows][64 columns], box {64, rs, d_ff/64}; cached per
+// (weights, shape).  Mode 0 when any of them cannot be encoded.
+void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks, int rs) {
   struct Maps {
     int mode;
-    CUtensorMap wg, wu;
+    CUtensorMap wg, wu, wd;
   };
   static std::mutex mu;
-  static std::map<std::tuple<const void *, const void *, int, int, int, int>, Maps> cache;
+  static std::map<std::tuple<const void *, const void *, const void *, int, int, int, int, int>, Maps> cache;
   p->tma_mode = 0;
   const int d = L->d, I = L->d_ff, E = L->n_experts + (L->n_shared ? 1 : 0), kst = ks;
   if (d % 64 || ks % 64 || ks / 64 > 256) return;
-  const auto key = std::make_tuple(L->w_gate, L->w_up, d, I, E, kst);
+  const auto key = std::make_tuple(L->w_gate, L->w_up, L->w_down, d, I, E, kst, rs);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -406,6 +431,7 @@ void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks) {
       p->tma_mode = it->second.mode;
       p->tm_wg = it->second.wg;
       p->tm_wu = it->second.wu;
+      p->tm_wd = it->second.wd;
       return;
     }
   }
@@ -422,7 +448,18 @@ void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks) {
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    if (enc(&m.wg, L->w_gate) && enc(&m.wu, L->w_up)) m.mode = 1;
+    // the down rows: [d_ff/64][rs rows][64 columns], box {64, rs, d_ff/64}
+    auto encd = [&](CUtensorMap *map, const void *base) {
+      const cuuint64_t dims[3] = {64, (cuuint64_t)E * d, (cuuint64_t)I / 64};
+      const cuuint64_t strides[2] = {(cuuint64_t)I * 2, 128};
+      const cuuint32_t box[3] = {64, (cuuint32_t)rs, (cuuint32_t)I / 64};
+      const cuuint32_t es[3] = {1, 1, 1};
+      return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (I % 64 == 0 && I / 64 <= 256 && enc(&m.wg, L->w_gate) && enc(&m.wu, L->w_up) && encd(&m.wd, L->w_down))
+      m.mode = 1;
   }
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
@@ -430,6 +467,7 @@ void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks) {
   p->tma_mode = m.mode;
   p->tm_wg = m.wg;
   p->tm_wu = m.wu;
+  p->tm_wd = m.wd;
 }
 
 bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan) {
@@ -463,7 +501,7 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan) {
   int Sd = 4;
   size_t smd = 0;
   for (; Sd >= 2; --Sd) {
-    smd = (size_t)Sd * rs * pad_host(I * 2) + hb + redb + 16 * Sd;
+    smd = 1024 + (size_t)Sd * rs * pad_host(I * 2) + hb + redb + 16 * Sd;
     if (smd <= kSmemBudget) break;
   }
   if (Sd < 2) return false;

@@ -100,3 +100,48 @@ def test_swizzled_stages_fit_and_align(k, d):
     assert stage <= 16 * pad(ks * 2)  # no more than the padded layout the plan reserves
     # aligned base (up to 1023 bytes of slack) + stages + x rows + reduction + barriers
     assert 1023 + S * stage + P["xg"] + P["redb"] + 16 * S <= P["smem"] <= SMEM_BUDGET
+
+
+def down_plan(I):
+    """The down part of ffn_tma.cu's tma_plan: rows per unit (chosen for two token tiles)."""
+    redb2, hb2 = CONSUMER_WARPS * 2 * 32 * 16, 2 * 8 * pad(I * 2)
+    for rs in (32, 16):
+        if 2 * rs * pad(I * 2) + hb2 + redb2 + 32 <= SMEM_BUDGET:
+            return rs
+    return None
+
+
+def down_offset(rw, g, c, ch, rs, upper):
+    """The down consumer's swizzled fragment offset: row tile rw, MMA row g (+ 8
+    when upper), lane column c, 32-column chunk ch."""
+    pr = stored_row(g)
+    x = ch * 4 + c
+    o0 = (x >> 3) * (rs * 128) + (rw * 16 + pr) * 128 + (((x & 7) ^ pr) << 4)
+    return o0 + (1024 if upper else 0)
+
+
+@pytest.mark.parametrize("I", [768, 1024, 1408, 1536])
+def test_swizzled_down_fragment_addresses(I):
+    rs = down_plan(I)
+    assert rs is not None and I % 64 == 0 and I // 64 <= 256
+    rtiles, kparts = rs // 16, CONSUMER_WARPS // (rs // 16)
+    where = {}
+    for z in range(I // 64):  # the box {64, rs, I/64} as rs-row segments, swizzled per 8-row atom
+        for r in range(rs):
+            for b in range(0, 128, 16):
+                off = z * rs * 128 + r * 128 + ((((b >> 4) ^ (r & 7)) << 4))
+                where[off] = (r, z * 64 + b // 2)
+    assert len(where) == rs * I // 8 and (rs * 128) % 1024 == 0
+    C = I // 32
+    for w in range(CONSUMER_WARPS):
+        rw, kq = w % rtiles, w // rtiles
+        for ch in range(kq * C // kparts, (kq + 1) * C // kparts):
+            for upper in (0, 1):
+                offs = []
+                for lane in range(32):
+                    g, c = lane >> 2, lane & 3
+                    o = down_offset(rw, g, c, ch, rs, upper)
+                    assert where[o] == (rw * 16 + 8 * upper + stored_row(g), ch * 32 + c * 8)
+                    offs.append(o)
+                for q in range(4):
+                    assert len({(o // 16) % 8 for o in offs[8 * q:8 * q + 8]}) == 8
