@@ -52,11 +52,11 @@ KERNEL_SOURCES = {
 # kernel -> (source hash, dram read+write bytes of one captured launch, algorithmic bytes of that launch);
 # the captures and their commands are summarised under profiles/ (one file per kernel and workload)
 NCU_TRAFFIC = {
-    "moe_fused_kernel": ("8b776246db0a5417", 727389696 + 4304128, 77 * 9437184 + 524288),
-    "moe_fused_kernel_shared": ("8b776246db0a5417", 647156736 + 4783104, 102 * 6291456 + 1048576),
-    "moe_fused_bs_kernel_mxfp4": ("4ac4cd864c4cb72c", 171705600 + 4300800, 102 * 1671168 + 1048576),
-    "moe_fused_bs_kernel_q8": ("4ac4cd864c4cb72c", 342160896 + 4527872, 102 * 3342336 + 1048576),
-    "tc_group_kernel_gateup": ("90e973b082322786", 822155776 + 3629568, 128 * 6291456),
+    "moe_fused_kernel": ("a3be62effd88e793", 727385856 + 4414208, 77 * 9437184 + 524288),
+    "moe_fused_kernel_shared": ("a3be62effd88e793", 647198208 + 4800512, 102 * 6291456 + 1048576),
+    "moe_fused_bs_kernel_mxfp4": ("9694464e59221471", 171706112 + 4454400, 102 * 1671168 + 1048576),
+    "moe_fused_bs_kernel_q8": ("9694464e59221471", 342162944 + 4792064, 102 * 3342336 + 1048576),
+    "tc_group_kernel_gateup": ("b97ea086aa1c0f1c", 822155776 + 3629568, 128 * 6291456),
 }
 
 
