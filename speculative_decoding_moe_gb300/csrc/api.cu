@@ -465,7 +465,8 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
     e = dfv::launch_ffn_tma(fp, L->w_dtype, 0, plan, units_g < sms ? units_g : sms, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
     mark(2, s);
-    e = dfv::launch_ffn_tma(fp, L->w_dtype, 1, plan, units_d < sms ? units_d : sms, s, true);
+    const int gd = plan.down_per_sm * sms;
+    e = dfv::launch_ffn_tma(fp, L->w_dtype, 1, plan, units_d < gd ? units_d : gd, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "expert down launch");
     e = dfv::launch_ffn_tma(fp, L->w_dtype, 2, plan, sms, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");

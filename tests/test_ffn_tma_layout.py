@@ -103,12 +103,32 @@ def test_swizzled_stages_fit_and_align(k, d):
 
 
 def down_plan(I):
-    """The down part of ffn_tma.cu's tma_plan: rows per unit (chosen for two token tiles)."""
+    """The down part of ffn_tma.cu's tma_plan: rows per unit, chosen for two token tiles
+    (16 rows and two CTAs per SM when half the budget holds two stages, else 32 or 16 rows)."""
     redb2, hb2 = CONSUMER_WARPS * 2 * 32 * 16, 2 * 8 * pad(I * 2)
+    if 1024 + 2 * 16 * pad(I * 2) + hb2 + redb2 + 32 <= SMEM_BUDGET // 2 + 1024:
+        return 16
     for rs in (32, 16):
         if 2 * rs * pad(I * 2) + hb2 + redb2 + 32 <= SMEM_BUDGET:
             return rs
     return None
+
+
+@pytest.mark.parametrize("I", [768, 1024, 1408, 1536])
+@pytest.mark.parametrize("k", [1, 16])
+def test_down_plan_fits_its_ctas_per_sm(I, k):
+    """Two CTAs per SM only where both fit: the stages, h rows, reduction buffer and
+    alignment slack of one CTA within half of the budget (and 227 KB per SM)."""
+    rs = down_plan(I)
+    two = 1024 + 2 * 16 * pad(I * 2) + 2 * 8 * pad(I * 2) + CONSUMER_WARPS * 2 * 32 * 16 + 32 <= SMEM_BUDGET // 2 + 1024
+    NT = 1 if k <= 8 else 2
+    hb, redb = NT * 8 * pad(I * 2), CONSUMER_WARPS * NT * 32 * 16
+    budget = SMEM_BUDGET // 2 + 1024 if two else SMEM_BUDGET
+    S = next(S for S in (4, 3, 2) if 1024 + S * rs * pad(I * 2) + hb + redb + 16 * S <= budget)
+    smem = 1024 + S * rs * pad(I * 2) + hb + redb + 16 * S
+    assert S >= 2 and smem <= budget
+    if two:
+        assert rs == 16 and 2 * (smem + 1024) <= 228 * 1024  # + the per-CTA reserve
 
 
 def down_offset(rw, g, c, ch, rs, upper):
