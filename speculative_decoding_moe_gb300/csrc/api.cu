@@ -462,7 +462,8 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
     const int units_g = maxW * (L->d_ff / dfv::kGateTile);
     const int units_d = maxW * ((L->d + plan.rs - 1) / plan.rs);
     if (g_max_staging > 0) dfv::ffn_tensor_maps(&fp, L, plan.ks, plan.rs);  // else mode 0: bulk copies
-    e = dfv::launch_ffn_tma(fp, L->w_dtype, 0, plan, units_g < sms ? units_g : sms, s, true);
+    const int gg = plan.gate_per_sm * sms;
+    e = dfv::launch_ffn_tma(fp, L->w_dtype, 0, plan, units_g < gg ? units_g : gg, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
     mark(2, s);
     const int gd = plan.down_per_sm * sms;

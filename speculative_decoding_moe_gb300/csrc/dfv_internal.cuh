@@ -368,6 +368,7 @@ int mxfp4_grid_limit(int k, int d, int I, int which);
 cudaError_t launch_ffn_mxfp4(const FfnParams &p, int phase, int grid, cudaStream_t s, bool pdl);
 // TMA-staged expert FFN: geometry for a layer shape, 0 if it does not fit.
 struct TmaPlan {
+  int gate_per_sm;  // gate/up CTAs per SM (1 or 2)
   int down_per_sm;  // down CTAs per SM (1 or 2)
   int ks, nslices, stages_g, rs, stages_d;
   size_t smem_g, smem_d;

@@ -20,12 +20,17 @@
 
 namespace dfv {
 
-constexpr int kRouterThreads = 256;
-constexpr int kRouterWarps = kRouterThreads / 32;
+// The GEMV and the row norms run on the first kGemvThreads threads, in a
+// fixed summation order.  A launch has 256 threads for k <= 8 and 512 above,
+// so the top-K tail gives every row of a block its own warp; the arithmetic
+// of a row is the same in both.
+constexpr int kGemvThreads = 256;
+constexpr int kGemvWarps = kGemvThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Fixed-order block sum of v[0..n): warp butterfly, then warps in index order.
-// Result in out[0..n) (shared), visible after the trailing __syncthreads.
+// Fixed-order block sum of v[0..n) over the GEMV warps: warp butterfly, then
+// warps in index order.  Result in out[0..n) (shared), visible after the
+// trailing __syncthreads.
 template <int N>
 __device__ __forceinline__ void block_sum_rows(float (&v)[N], int n, float (*red)[N], float *out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -38,7 +43,7 @@ __device__ __forceinline__ void block_sum_rows(float (&v)[N], int n, float (*red
       v[t] = a;
     }
   }
-  if (lane == 0) {
+  if (lane == 0 && warp < kGemvWarps) {
 #pragma unroll
     for (int t = 0; t < N; ++t)
       if (t < n) red[warp][t] = v[t];
@@ -46,7 +51,7 @@ __device__ __forceinline__ void block_sum_rows(float (&v)[N], int n, float (*red
   __syncthreads();
   if (threadIdx.x < n) {
     float a = 0.f;
-    for (int w = 0; w < kRouterWarps; ++w) a += red[w][threadIdx.x];
+    for (int w = 0; w < kGemvWarps; ++w) a += red[w][threadIdx.x];
     out[threadIdx.x] = a;
   }
   __syncthreads();
@@ -114,11 +119,19 @@ __device__ void topk_row(const float *lg, int E, int K, int32_t *idx_out, float 
   }
 }
 
+template <int kRouterThreads>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) {
+  constexpr int kRouterWarps = kRouterThreads / 32;
   pdl_trigger();
+  // this CTA's router row does not depend on the previous launch: start its
+  // fetch into L2 before waiting for that launch to finish
+  if (threadIdx.x == 0) {
+    const size_t rb = (size_t)p.d * (p.rdt == DFV_BF16 ? 2 : 4);
+    prefetch_l2(reinterpret_cast<const char *>(p.wr) + (size_t)blockIdx.x * rb, (uint32_t)rb);
+  }
   pdl_wait();  // x may be the previous layer's output
 
-  __shared__ float s_red[kRouterWarps][kMaxBlock];
+  __shared__ float s_red[kGemvWarps][kMaxBlock];
   __shared__ float s_inv[kMaxBlock];
   __shared__ float s_dot[kMaxBlock];
   __shared__ unsigned s_last;
@@ -148,7 +161,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
     float ss[kMaxBlock];
 #pragma unroll
     for (int t = 0; t < kMaxBlock; ++t) ss[t] = 0.f;
-    for (int c = tid; c < d / 8; c += kRouterThreads) {
+    for (int c = tid < kGemvThreads ? tid : d; c < d / 8; c += kGemvThreads) {
       if (xbf) {
         uint4 xv[kMaxBlock];
         load_rows(c, xv);
@@ -182,7 +195,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   float acc[kMaxBlock];
 #pragma unroll
   for (int t = 0; t < kMaxBlock; ++t) acc[t] = 0.f;
-  for (int c = tid; c < d / 8; c += kRouterThreads) {
+  for (int c = tid < kGemvThreads ? tid : d; c < d / 8; c += kGemvThreads) {
     float w[8];
     load8(p.wr, (size_t)e * d + c * 8, p.rdt, w);
     if (xbf) {
@@ -255,19 +268,24 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   for (int t = warp; t < k; t += kRouterWarps) {
     topk_row(s_lg + t * E, E, K, s_idx + t * K, s_sel + t * K);
     __syncwarp();
-    if (lane == 0) {
-      // routing weights: softmax restricted to the K selected (renormalised),
-      // or the full softmax probability of each selected expert
-      const float m0 = s_sel[t * K];
-      float z[kMaxTopK], zs = 0.f;
-      for (int s = 0; s < K; ++s) { z[s] = expf(s_sel[t * K + s] - m0); zs += z[s]; }
-      float denom = zs;
-      if (!p.norm_topk) {
-        denom = 0.f;
-        for (int j = 0; j < E; ++j) denom += expf(s_lg[t * E + j] - m0);
-      }
-      for (int s = 0; s < K; ++s) s_sel[t * K + s] = z[s] / denom;
+    // routing weights: softmax restricted to the K selected (renormalised),
+    // or the full softmax probability of each selected expert.  Lane s takes
+    // selection s; the denominator is the warp's butterfly sum of the lanes'
+    // terms (lane l's term sums experts l, l + 32, ... in that order)
+    const float m0 = s_sel[t * K];
+    const float z = lane < K ? expf(s_sel[t * K + lane] - m0) : 0.f;
+    float den = 0.f;
+    if (p.norm_topk) {
+      den = z;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (lane + 32 * q < E) den += expf(s_lg[t * E + lane + 32 * q] - m0);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+    __syncwarp();
+    if (lane < K) s_sel[t * K + lane] = z / den;
   }
   __syncthreads();
 
@@ -341,7 +359,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
 cudaError_t launch_router(const RouterParams &p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.E);
-  cfg.blockDim = dim3(kRouterThreads);
+  const bool wide = p.k > 8;
+  cfg.blockDim = dim3(wide ? 512 : 256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -349,7 +368,7 @@ cudaError_t launch_router(const RouterParams &p, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, router_kernel, p);
+  return wide ? cudaLaunchKernelEx(&cfg, router_kernel<512>, p) : cudaLaunchKernelEx(&cfg, router_kernel<256>, p);
 }
 
 }  // namespace dfv

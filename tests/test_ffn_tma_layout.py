@@ -18,8 +18,11 @@ def pad(b):
     return b + 64 if b % 128 == 0 else b
 
 
+HALF = SMEM_BUDGET // 2 + 1024
+
+
 def tma_plan(k, d, I):
-    """The gate/up part of ffn_tma.cu's tma_plan (ks, stage count, smem)."""
+    """The gate/up part of ffn_tma.cu's tma_plan (ks, CTAs per SM, stage count, smem)."""
     NT = 1 if k <= 8 else 2
     C = d // 32
     nsl = (d + 1023) // 1024
@@ -27,13 +30,23 @@ def tma_plan(k, d, I):
         nsl += 1
     if nsl > C:
         return None
-    ks = d // nsl
+    ks, per_sm = d // nsl, 1
+    xg2, redb2 = 2 * 8 * pad(d * 2), CONSUMER_WARPS * 2 * 32 * 16
+
+    def two_fit(w):
+        return 1024 + 2 * 16 * pad(w * 2) + xg2 + redb2 + 32 <= HALF
+
+    if two_fit(ks):
+        per_sm = 2
+    elif ks > 512 and d % 512 == 0 and two_fit(512):
+        ks, nsl, per_sm = 512, d // 512, 2
     xg = NT * 8 * pad(d * 2)
     redb = CONSUMER_WARPS * NT * 32 * 16
+    budget = HALF if per_sm == 2 else SMEM_BUDGET
     for Sg in (4, 3, 2):
         smg = 1024 + Sg * 16 * pad(ks * 2) + xg + redb + 16 * Sg
-        if smg <= SMEM_BUDGET:
-            return dict(ks=ks, nsl=nsl, S=Sg, smem=smg, xg=xg, redb=redb, NT=NT)
+        if smg <= budget:
+            return dict(ks=ks, nsl=nsl, S=Sg, smem=smg, xg=xg, redb=redb, NT=NT, per_sm=per_sm)
     return None
 
 
@@ -100,6 +113,25 @@ def test_swizzled_stages_fit_and_align(k, d):
     assert stage <= 16 * pad(ks * 2)  # no more than the padded layout the plan reserves
     # aligned base (up to 1023 bytes of slack) + stages + x rows + reduction + barriers
     assert 1023 + S * stage + P["xg"] + P["redb"] + 16 * S <= P["smem"] <= SMEM_BUDGET
+    if P["per_sm"] == 2:
+        assert P["smem"] <= HALF and 2 * (P["smem"] + 1024) <= 228 * 1024  # + the per-CTA reserve
+
+
+@pytest.mark.parametrize("d", [512, 1024, 1536, 2048, 3072, 4096])
+def test_gateup_slice_depends_on_the_shape_only(d):
+    """A block's rows equal single-token calls only if every k splits a row's sum
+    the same way: the slice width (and so the warps' column chunks) is the same for
+    k = 1..16; two CTAs per SM exactly where the two-token-tile plan fits half the
+    budget (d = 2048 with 512-column slices), one elsewhere (d = 4096)."""
+    plans = [tma_plan(k, d, 768) for k in (1, 2, 8, 9, 16)]
+    assert all(P is not None for P in plans)
+    assert len({(P["ks"], P["nsl"], P["per_sm"]) for P in plans}) == 1
+    P = plans[-1]
+    assert P["ks"] * P["nsl"] == d and P["ks"] % 32 == 0 and P["ks"] <= 1024
+    if d == 2048:
+        assert (P["ks"], P["per_sm"]) == (512, 2)
+    if d == 4096:
+        assert (P["ks"], P["per_sm"]) == (1024, 1)
 
 
 def down_plan(I):
