@@ -108,26 +108,34 @@ __global__ void __launch_bounds__(512) batch_logits_kernel(BatchParams p) {
         const int c = c0 + lane + 32 * i;
         wv[i] = c < cpr ? __ldg(reinterpret_cast<const uint4 *>(wr + (size_t)c * 8)) : make_uint4(0u, 0u, 0u, 0u);
       }
+      // piece by piece: the piece's router elements are widened once and
+      // used for every row of the tile (each row still sums its pieces in
+      // order, words in order, low half first)
 #pragma unroll
-      for (int t = 0; t < kBRowTile; ++t) {
-        if (t < nt) {
-          const uint16_t *xr = xs + (size_t)t * d;
-          float a_ = acc[t];
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < cpr) {
+          const uint32_t w4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+          float wf[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int c = c0 + lane + 32 * i;
-            if (c < cpr) {
-              const uint4 xv = *reinterpret_cast<const uint4 *>(xr + (size_t)c * 8);
+          for (int h = 0; h < 4; ++h) {
+            wf[2 * h] = bf16_lo(w4[h]);
+            wf[2 * h + 1] = bf16_hi(w4[h]);
+          }
+#pragma unroll
+          for (int t = 0; t < kBRowTile; ++t) {
+            if (t < nt) {
+              const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)t * d + (size_t)c * 8);
               const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
-              const uint32_t w4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+              float a_ = acc[t];
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
-                a_ = fmaf(bf16_lo(x4[h]), bf16_lo(w4[h]), a_);
-                a_ = fmaf(bf16_hi(x4[h]), bf16_hi(w4[h]), a_);
+                a_ = fmaf(bf16_lo(x4[h]), wf[2 * h], a_);
+                a_ = fmaf(bf16_hi(x4[h]), wf[2 * h + 1], a_);
               }
+              acc[t] = a_;
             }
           }
-          acc[t] = a_;
         }
       }
     }
@@ -209,13 +217,26 @@ __global__ void __launch_bounds__(512) batch_tables_kernel(BatchParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ int s_cnt[kMaxExperts + 1], s_eoff[kMaxExperts + 1], s_wsum[16], s_csum[16];
   __shared__ int s_nw, s_ug[kMaxExperts + 2], s_ud[kMaxExperts + 2];
-  __shared__ unsigned short s_pref[kMaxExperts][DFV_MAX_BATCH_ROWS / 32];  // rows of earlier mask words
+  // rows of earlier mask words and the token masks, one padded row per
+  // expert (odd word strides: a warp's lookups for different experts spread
+  // over the banks)
+  __shared__ unsigned short s_pref[kMaxExperts][DFV_MAX_BATCH_ROWS / 32 + 2];
+  __shared__ unsigned s_mask[kMaxExperts][DFV_MAX_BATCH_ROWS / 32 + 1];
   int cnt = 0;
-  if (tid < E)
-    for (int w = 0; w < (T + 31) / 32; ++w) {
+  if (tid < E) {
+    // all of the expert's mask words in flight at once, then kept in shared memory
+    constexpr int kMW = DFV_MAX_BATCH_ROWS / 32;
+    const int nw = (T + 31) / 32;
+    unsigned mv[kMW];
+#pragma unroll
+    for (int w = 0; w < kMW; ++w) mv[w] = w < nw ? p.tmask[(size_t)tid * mw + w] : 0u;
+#pragma unroll
+    for (int w = 0; w < kMW; ++w) {
       s_pref[tid][w] = (unsigned short)cnt;
-      cnt += __popc(p.tmask[(size_t)tid * mw + w]);
+      s_mask[tid][w] = mv[w];
+      cnt += __popc(mv[w]);
     }
+  }
   const int flag = cnt > 0;
   int fi = flag, ci = cnt;
 #pragma unroll
@@ -248,11 +269,24 @@ __global__ void __launch_bounds__(512) batch_tables_kernel(BatchParams p) {
   }
   __syncthreads();
   const int nWt = s_nw;
-  // sorted pairs: pair t*K+s of expert e lands at eoff[e] + (rows before t that chose e)
-  for (int q = tid; q < T * K; q += blockDim.x) {
-    const int t = q / K, e = p.topk_idx[q];
-    const int rank = s_pref[e][t >> 5] + __popc(p.tmask[(size_t)e * mw + (t >> 5)] & ((1u << (t & 31)) - 1u));
-    p.gather[s_eoff[e] + rank] = q;
+  // sorted pairs: pair t*K+s of expert e lands at eoff[e] + (rows before t
+  // that chose e); eight pairs per thread with their expert ids loaded at once
+  for (int q0 = 0; q0 < T * K; q0 += 8 * 512) {
+    int ev[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = q0 + j * 512 + tid;
+      ev[j] = q < T * K ? p.topk_idx[q] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = q0 + j * 512 + tid;
+      if (q < T * K) {
+        const int t = q / K, e = ev[j];
+        const int rank = s_pref[e][t >> 5] + __popc(s_mask[e][t >> 5] & ((1u << (t & 31)) - 1u));
+        p.gather[s_eoff[e] + rank] = q;
+      }
+    }
   }
   if (ns)
     for (int t = tid; t < T; t += blockDim.x) {
@@ -289,17 +323,23 @@ __global__ void __launch_bounds__(512) batch_tables_kernel(BatchParams p) {
     }
   }
   __syncthreads();
-  for (int wi = warp; wi < nWt; wi += 16) {
-    const int m = s_cnt[wi], passes = (m + kTcNMax - 1) / kTcNMax;
-    for (int i = lane; i < tg * passes; i += 32) {
-      const int ps = i / tg, mt = i % tg;
-      p.units_g[s_ug[wi] + i] = make_int4(wi, mt, ps * kTcNMax, min(kTcNMax, m - ps * kTcNMax));
+  // every thread writes units: unit u of a contraction belongs to the woken
+  // expert wi with first[wi] <= u < first[wi + 1] (binary search)
+  auto write_units = [&](const int *first, int per, int4 *units) {
+    const int total = first[nWt];
+    for (int u = tid; u < total; u += blockDim.x) {
+      int lo = 0, hi = nWt;  // first[lo] <= u < first[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (first[mid] <= u) lo = mid; else hi = mid;
+      }
+      const int wi = lo, i = u - first[wi], m = s_cnt[wi];
+      const int ps = i / per, mt = i - ps * per;
+      units[u] = make_int4(wi, mt, ps * kTcNMax, min(kTcNMax, m - ps * kTcNMax));
     }
-    for (int i = lane; i < td * passes; i += 32) {
-      const int ps = i / td, mt = i % td;
-      p.units_d[s_ud[wi] + i] = make_int4(wi, mt, ps * kTcNMax, min(kTcNMax, m - ps * kTcNMax));
-    }
-  }
+  };
+  write_units(s_ug, tg, p.units_g);
+  write_units(s_ud, td, p.units_d);
 }
 
 // Xg[position] = x[row of the pair at that position]
