@@ -52,11 +52,11 @@ KERNEL_SOURCES = {
 # kernel -> (source hash, dram read+write bytes of one captured launch, algorithmic bytes of that launch);
 # the captures and their commands are summarised under profiles/ (one file per kernel and workload)
 NCU_TRAFFIC = {
-    "moe_fused_kernel": ("a3be62effd88e793", 727385856 + 4414208, 77 * 9437184 + 524288),
-    "moe_fused_kernel_shared": ("a3be62effd88e793", 647198208 + 4800512, 102 * 6291456 + 1048576),
-    "moe_fused_bs_kernel_mxfp4": ("9694464e59221471", 171706112 + 4454400, 102 * 1671168 + 1048576),
-    "moe_fused_bs_kernel_q8": ("9694464e59221471", 342162944 + 4792064, 102 * 3342336 + 1048576),
-    "tc_group_kernel_gateup": ("b97ea086aa1c0f1c", 822155776 + 3629568, 128 * 6291456),
+    "moe_fused_kernel": ("c19e2c6b8fa07d1d", 727464704 + 4395776, 77 * 9437184 + 524288),
+    "moe_fused_kernel_shared": ("c19e2c6b8fa07d1d", 647158528 + 4748800, 102 * 6291456 + 1048576),
+    "moe_fused_bs_kernel_mxfp4": ("a0f32e96cd9be945", 171703040 + 4625920, 102 * 1671168 + 1048576),
+    "moe_fused_bs_kernel_q8": ("a0f32e96cd9be945", 342161408 + 4780800, 102 * 3342336 + 1048576),
+    "tc_group_kernel_gateup": ("ac9079195f87f791", 822142208 + 3482624, 128 * 6291456),
 }
 
 
