@@ -54,8 +54,8 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     "moe_fused_kernel": ("c19e2c6b8fa07d1d", 727464704 + 4395776, 77 * 9437184 + 524288),
     "moe_fused_kernel_shared": ("c19e2c6b8fa07d1d", 647158528 + 4748800, 102 * 6291456 + 1048576),
-    "moe_fused_bs_kernel_mxfp4": ("a0f32e96cd9be945", 171703040 + 4625920, 102 * 1671168 + 1048576),
-    "moe_fused_bs_kernel_q8": ("a0f32e96cd9be945", 342161408 + 4780800, 102 * 3342336 + 1048576),
+    "moe_fused_bs_kernel_mxfp4": ("3bfa5f16616c3b09", 171722752 + 4392960, 102 * 1671168 + 1048576),
+    "moe_fused_bs_kernel_q8": ("3bfa5f16616c3b09", 342162944 + 4491520, 102 * 3342336 + 1048576),
     "tc_group_kernel_gateup": ("ac9079195f87f791", 822142208 + 3482624, 128 * 6291456),
 }
 

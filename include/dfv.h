@@ -80,14 +80,10 @@ typedef enum { DFV_F32 = 0, DFV_BF16 = 1, DFV_MXFP4 = 2, DFV_Q8 = 3, DFV_F16 = 4
 #define DFV_DEVERR_SLOT_WAIT 0x2u    /* the producer gave up waiting for a free stage */
 #define DFV_DEVERR_DRAIN_WAIT 0x4u   /* copies still in flight at exit after a timeout */
 #define DFV_DEVERR_GRID_WAIT 0x8u    /* a CTA gave up waiting at a grid-wide barrier */
-/* An mxfp4 scale byte outside [113, 140] was met on the multi-kernel path
- * (layers whose shape the single-launch kernel does not take: see
- * dfv_moe_layer).  That path widens each code to fp16 and multiplies it by its
- * block's scale 2^(s-127) in fp16, exact only inside that range (with the OCP
- * choice of a block's scale, 2^(floor(log2 amax) - 2), blocks whose largest
- * magnitude lies in [2^-12, 2^16)); outside it the call's outputs are invalid
- * and this bit says so.  The single-launch kernel applies every scale to fp32
- * partial sums and is exact for every scale 0..254; it never sets the bit. */
+/* Reserved; no kernel sets it.  It once flagged mxfp4 scale bytes outside the
+ * range that a scale folded into fp16 codes keeps exact.  Every mxfp4 path
+ * (single launch and multi-launch) now multiplies each 32-element block's
+ * fp32 partial sum by its scale 2^(s-127), exact for every scale 0..254. */
 #define DFV_DEVERR_SCALE_RANGE 0x10u
 #define DFV_DEVERR_REDUCE_WAIT 0x20u /* a warp gave up waiting for a free partial-sum buffer */
 /* A single-launch kernel found its own routing tables inconsistent (an expert

@@ -128,14 +128,6 @@ struct Fmt<kFmtQ8> {
   }
 };
 
-// Power-of-two exponent that brings a row's largest magnitude amax into [1, 2).
-__device__ __forceinline__ int row_shift1(float amax) {
-  if (!(amax > 0.f) || !(amax < INFINITY)) return 0;
-  int ex;
-  frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
-  return min(max(1 - ex, -126), 126);
-}
-
 // 16-byte chunk q of staged token row r sits at chunk q ^ ((r & 1) << 2):
 // the quarter-warp reading chunks Q..Q+3 of rows 2i and 2i+1 then spans all
 // 32 banks.
@@ -405,7 +397,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
       mb = __reduce_max_sync(0xffffffffu, max(mb & 0xffffu, mb >> 16));
       float amax = __uint_as_float(mb << 16);
       if (p.fuse_norm) amax = rnd_bf16(amax * inv);  // rounding is monotone: the max of the rounded row
-      const int sh = row_shift1(amax);
+      const int sh = row_shift(amax);
       const float sc = exp2i(sh);
 #pragma unroll 1
       for (int q0 = 0; q0 < cpr; q0 += 32) {  // cpr is a multiple of 64
@@ -599,7 +591,7 @@ __global__ void __launch_bounds__(kFT, 1) moe_fused_bs_kernel(const __grid_const
               for (int i = 0; i < 4; ++i)
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j][i].x), fabsf(v[j][i].y)),
                                          fmaxf(fabsf(v[j][i].z), fabsf(v[j][i].w))));
-              const int sh = row_shift1(warp_max(amax));
+              const int sh = row_shift(warp_max(amax));
               const float sc = exp2i(sh);
 #pragma unroll
               for (int cq = 0; cq < 2; ++cq) {

@@ -1,7 +1,8 @@
-// mxfp4_common.cuh -- widening of mxfp4 weights (E2M1 codes + E8M0 block
-// scales) to fp16 MMA operands, and the fp16 staging of activation rows with a
-// per-row power-of-two scale.  Shared by the multi-launch (ffn_mxfp4.cu) and
-// the single-launch (layer_fused_mxfp4.cu) mxfp4 kernels.
+// mxfp4_common.cuh -- widening of mxfp4 codes (E2M1) to fp16 MMA operands,
+// and the fp16 staging of activation rows with a per-row power-of-two scale.
+// Shared by the multi-launch (ffn_mxfp4.cu) and the single-launch block-scaled
+// (layer_fused_bs.cu) kernels; both apply each block's E8M0 scale to the fp32
+// partial sum of that block's MMAs.
 //
 // OCP Microscaling Formats (MX) v1.0, as used by the MI355X / vLLM write-up
 // (allbreaknews.com/?p=4397), section "Why Quantize the Target Model on Top?":
@@ -14,15 +15,6 @@
 
 namespace dfv {
 namespace {
-
-// Streaming 16-byte load, not kept in L1 (every weight byte is used once).
-__device__ __forceinline__ uint4 ldg_codes(const void *p) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
-  return r;
-}
 
 // One scale byte (kept in L1: the four chunks of a sector share it).
 __device__ __forceinline__ uint32_t ldg_scale(const uint8_t *p) {
@@ -40,25 +32,6 @@ __device__ __forceinline__ void e2m1_word(uint32_t w, uint32_t (&r)[4]) {
       : "r"(w));
 }
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// E8M0 byte s -> fp16x2 {2^(s-127), 2^(s-127)}: for s in [113, 140] the scale
-// is a normal fp16 number whose exponent field is s - 112, so one multiply-add
-// builds both halves ((s - 112) * 0x04000400, written modulo 2^32).  There the
-// product of any E2M1 value with the scale is exact in fp16 (at most 6 * 2^13,
-// at least 2^-15, a subnormal on the 2^-24 grid).  `range` keeps the largest
-// s - 113 seen (unsigned): above kScaleRangeMax a scale outside [113, 140] was
-// used and the kernel reports DFV_DEVERR_SCALE_RANGE.
-constexpr uint32_t kScaleRangeMax = 27;
-__device__ __forceinline__ uint32_t e8m0_half2(uint32_t s, uint32_t &range) {
-  range = max(range, s - 113u);
-  return s * 0x04000400u + 0x3FFE4000u;
-}
-
 __device__ __forceinline__ void mma_f16x(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -67,22 +40,21 @@ __device__ __forceinline__ void mma_f16x(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Shared-memory position of 16-byte chunk q of token row j: the XOR spreads the
-// eight lanes of a quarter-warp (rows j, j+1; lanes c = 0..3) over 8 banks groups.
-__device__ __forceinline__ int swz(int q, int j) { return q ^ (((q >> 3) & 1) | ((j & 1) << 1)); }
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
-// Power-of-two exponent that brings the row maximum amax into [2^14, 2^15).
+// Power-of-two exponent that brings a row's largest magnitude amax into
+// [1, 2): a block's fp32 partial sum then stays near the true sum, so its
+// scale 2^(s-127) cannot push it past the fp32 range short of the true
+// result itself.
 __device__ __forceinline__ int row_shift(float amax) {
   if (!(amax > 0.f) || !(amax < INFINITY)) return 0;
   int ex;
   frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
-  return min(max(15 - ex, -126), 126);
+  return min(max(1 - ex, -126), 126);
 }
 
 __device__ __forceinline__ float exp2i(int s) { return __int_as_float((127 + s) << 23); }
@@ -90,14 +62,6 @@ __device__ __forceinline__ float exp2i(int s) { return __int_as_float((127 + s) 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-// Widen one word of codes and apply the block scale: r[b] = fp16x2 of byte b
-// times 2^(s-127) (exact inside the scale range e8m0_half2 checks).
-__device__ __forceinline__ void mx_decode_word(uint32_t w, uint32_t s2, uint32_t (&r)[4]) {
-  e2m1_word(w, r);
-#pragma unroll
-  for (int b = 0; b < 4; ++b) r[b] = hmul2(r[b], s2);
 }
 
 }  // namespace

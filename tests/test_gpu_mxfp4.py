@@ -118,16 +118,10 @@ def test_decode_every_code_and_scale_one_hot(dfv, path, d, I, scale_exp):
         assert _max_rel_err(got[t:t + 1], ref[t:t + 1]) <= TOL_DECODE, t
 
 
-@pytest.mark.parametrize("d,I", [(512, 256), (2048, 512), (1024, 128)])
-def test_fused_decode_exact_for_every_scale(dfv, d, I):
-    """The single-launch kernel applies each block's scale to fp32 partial
-    sums, so every E8M0 exponent is exact as long as the values stay inside
-    the fp32 range (above 251 the largest E2M1 codes, 6 * 2^125, would leave
-    it at any input).  Gate scales are drawn over 0..251 and each up scale is
-    251 minus its gate scale (g * u stays near 1, so h is finite and normal);
-    each down row r has one scale s_r spread over 20..219.  With one-hot rows every output is a short sum; each output is
-    divided by 2^(s_r - 127) before the comparison, so rows of every
-    magnitude are held to the same bar."""
+def _wide_scale_layer(d, I):
+    """One expert, K = 1: gate scales drawn over 0..251 and each up scale 251
+    minus its gate scale (g * u stays near 1, so h is finite and normal); each
+    down row r has one scale s_r spread over 20..219."""
     s = _shape(d, 1, 1, I)
     lw = inputs.make_layer(s, seed=d + 3 * I)
     g = torch.Generator().manual_seed(d + I)
@@ -136,15 +130,22 @@ def test_fused_decode_exact_for_every_scale(dfv, d, I):
     srow = (20 + (torch.arange(d) * 37) % 200).to(torch.uint8)
     lw.s_down = srow.view(1, d, 1).expand(lw.s_down.shape).contiguous()
     assert int(lw.s_gate.min()) == 0 and int(lw.s_gate.max()) == 251
+    return lw, srow
+
+
+def _check_every_scale(dfv, lw, srow, d, I, fused):
     ol = oracle_layer(lw)
     k = 16
     x = _one_hot_rows(k, d, seed=d + 1)
-    dfv.set_path(True)
-    L = dfv.Layer(lw.to("cuda"))
-    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
-    out = dfv.moe_block_forward(L, x.cuda(), ws)
-    torch.cuda.synchronize()
-    _check_path(dfv, "fused", d, I)
+    dfv.set_path(fused)
+    try:
+        L = dfv.Layer(lw.to("cuda"))
+        ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
+        out = dfv.moe_block_forward(L, x.cuda(), ws)
+        torch.cuda.synchronize()
+        _check_path(dfv, "fused" if fused else "multi", d, I)
+    finally:
+        dfv.set_path(True)
     assert dfv.read_device_error(ws) == 0
     ref = oracle.moe_forward(ol, np_of(x))
     norm = np.exp2(srow.double().numpy() - 127.0)
@@ -155,27 +156,27 @@ def test_fused_decode_exact_for_every_scale(dfv, d, I):
         assert _max_rel_err(got[t:t + 1], refn[t:t + 1]) <= TOL_DECODE, t
 
 
-@pytest.mark.parametrize("bad_scale", [112, 141])
-@pytest.mark.parametrize("d", [128, 512])
-def test_scale_outside_exact_range_sets_device_error_on_the_multi_launch_path(dfv, bad_scale, d):
-    """The multi-launch mxfp4 kernels scale codes in fp16, exact for scales in
-    [113, 140]; outside it they report DFV_DEVERR_SCALE_RANGE (d_ff = 64 is a
-    shape only they take)."""
-    path = "multi"
-    dfv.set_path(False)
-    s = _shape(d, 4, 2, 64)
-    lw = inputs.make_layer(s, seed=3)
-    lw.s_gate[0, 0, 0] = bad_scale
-    lw.s_gate[1:, 0, 0] = bad_scale
-    lw.s_down[:, 5, 1] = bad_scale
-    L = dfv.Layer(lw.to("cuda"))
-    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
-    x = inputs.make_hidden(16, d, "bf16", seed=4, device="cuda")
-    dfv.moe_block_forward(L, x, ws)
-    torch.cuda.synchronize()
-    _check_path(dfv, path, d, 64)
-    dfv.set_path(True)
-    assert dfv.read_device_error(ws) & dfv.DEVERR_SCALE_RANGE
+@pytest.mark.parametrize("d,I", [(512, 256), (2048, 512), (1024, 128)])
+def test_fused_decode_exact_for_every_scale(dfv, d, I):
+    """The single-launch kernel applies each block's scale to fp32 partial
+    sums, so every E8M0 exponent is exact as long as the values stay inside
+    the fp32 range (above 251 the largest E2M1 codes, 6 * 2^125, would leave
+    it at any input).  With one-hot rows every output is a short sum; each
+    output is divided by 2^(s_r - 127) before the comparison, so rows of every
+    magnitude are held to the same bar."""
+    lw, srow = _wide_scale_layer(d, I)
+    _check_every_scale(dfv, lw, srow, d, I, fused=True)
+
+
+@pytest.mark.parametrize("d,I", [(512, 256), (2048, 512), (320, 64), (1024, 192), (4096, 1536)])
+def test_multi_launch_decode_exact_for_every_scale(dfv, d, I):
+    """The multi-launch mxfp4 kernels also scale each 32-element block's fp32
+    partial sum (a quad's lanes hold one block per MMA pair), so they are exact
+    for every scale too and set no device error.  d = 320 and d_ff = 64 or 192
+    end in half chunks of 64 codes; d = 4096 is wider than the single launch
+    takes."""
+    lw, srow = _wide_scale_layer(d, I)
+    _check_every_scale(dfv, lw, srow, d, I, fused=False)
 
 
 SMALL = [
