@@ -461,7 +461,7 @@ int run_layer(const dfv_moe_layer *L, const void *x, int act, int k, void *out, 
     if (sms <= 0) return fail(DFV_ERR_CUDA, "cannot query the SM count");
     const int units_g = maxW * (L->d_ff / dfv::kGateTile);
     const int units_d = maxW * ((L->d + plan.rs - 1) / plan.rs);
-    if (g_max_staging > 0) dfv::ffn_tensor_maps(&fp, L, plan.ks, plan.rs);  // else mode 0: bulk copies
+    if (g_max_staging > 0) dfv::ffn_tensor_maps(&fp, L, plan.ks, plan.rs, plan.dsl);  // else mode 0: bulk copies
     const int gg = plan.gate_per_sm * sms;
     e = dfv::launch_ffn_tma(fp, L->w_dtype, 0, plan, units_g < gg ? units_g : gg, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");

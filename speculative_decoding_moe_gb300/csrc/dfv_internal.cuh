@@ -369,12 +369,13 @@ cudaError_t launch_ffn_mxfp4(const FfnParams &p, int phase, int grid, cudaStream
 // TMA-staged expert FFN: geometry for a layer shape, 0 if it does not fit.
 struct TmaPlan {
   int gate_per_sm;  // gate/up CTAs per SM (1 or 2)
+  int dsl;          // down stages per unit: 1, or 2 when a stage holds half of d_ff
   int down_per_sm;  // down CTAs per SM (1 or 2)
   int ks, nslices, stages_g, rs, stages_d;
   size_t smem_g, smem_d;
 };
 bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan);
-void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks, int rs);
+void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks, int rs, int dsl);
 // Fused single-launch layer (bf16): plan, grid (0 = cannot run) and launch.
 bool fused_plan(int k, int d, int I, int E, FusedPlan *plan);
 int fused_max_grid(const FusedPlan &plan, int k, char *why, size_t why_len);

@@ -233,24 +233,28 @@ __global__ void __launch_bounds__(kTmaThreads, 2) gateup_tma_kernel(const __grid
 // (rs = 16).  Where half the shared-memory budget holds two 16-row stages
 // (d_ff up to 1024), two CTAs share an SM: 18 warps instead of 9 hide the
 // stage and L2 latencies (the A3B layer at k = 16 went from 180.8 to 167.7
-// us, the OLMoE-like one from 162.0 to 153.0 us).  h of the expert's tokens is staged in bf16; w[t,s] * y goes to
+// us, the OLMoE-like one from 162.0 to 153.0 us).  Wider d_ff (a multiple of
+// 128) keeps two CTAs per SM with DS = 2 stages per unit, each holding half of
+// d_ff (Qwen1.5-MoE-like layer 145.5 -> 134.7 us, Qwen3-235B-like 597.4 ->
+// 552.9 us); each warp then takes an eighth of every half.  h of the expert's tokens is staged in bf16; w[t,s] * y goes to
 // ys[pair], and the combine launch sums it.
 // Shared memory (1024-aligned): stages[S] | h[NT*8][rsh] | red[8][NT][32][4]
 // f32 | full[S] | empty[S]; a stage is [d_ff/64][rs][128 B] swizzled
 // (tma_mode 1) or [rs][rsd] padded rows (tma_mode 0).
-template <int NT>
+template <int NT, int DS>
 __global__ void __launch_bounds__(kTmaThreads, 2) down_tma_kernel(const __grid_constant__ FfnParams p) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int d = p.d, I = p.I, S = p.stages, RS = p.rs;
-  const int rsd = pad_to_64mod128(I * 2);
+  const int Ih = I / DS;  // d_ff columns per stage
+  const int rsd = pad_to_64mod128(Ih * 2);
   const int rsh = pad_to_64mod128(I * 2);
   const uint32_t sbase = smem_u32(smem);
-  // stage layout: padded rows (tma_mode 0), or [I/64][RS rows][128 B] with the
-  // 128-byte swizzle from one tensor copy (tma_mode 1)
-  const uint32_t stage_bytes = p.tma_mode ? (uint32_t)RS * I * 2 : (uint32_t)RS * rsd;
+  // stage layout: padded rows (tma_mode 0), or [Ih/64][RS rows][128 B] with the
+  // 128-byte swizzle from one tensor copy (tma_mode 1); a unit takes DS stages
+  const uint32_t stage_bytes = p.tma_mode ? (uint32_t)RS * Ih * 2 : (uint32_t)RS * rsd;
   const uint32_t hhb = sbase + S * stage_bytes;
   float *red = reinterpret_cast<float *>(smem + S * stage_bytes + (size_t)NT * 8 * rsh);
   const uint32_t full0 = smem_u32(red + kConsumerWarps * NT * 32 * 4);
@@ -278,18 +282,25 @@ __global__ void __launch_bounds__(kTmaThreads, 2) down_tma_kernel(const __grid_c
       const uint16_t *wd = reinterpret_cast<const uint16_t *>(p.wd);
       const uint64_t pol = l2_evict_first();  // expert weights are read once per launch
       int it = 0;
-      for (int u = lo; u < hi; ++u, ++it) {
+      bool ok = true;
+      for (int u = lo; u < hi && ok; ++u) {
         const int e = p.ws.woken[u / tiles], r0 = (u % tiles) * RS;
         const int rows = min(RS, d - r0);
-        const int s = it % S;
-        if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) break;
-        const uint32_t fb = full0 + 8 * s, dst = sbase + s * stage_bytes;
-        if (p.tma_mode) {  // one box of RS rows (rows past d are zero-filled and counted)
-          mbar_expect_tx(fb, (uint32_t)RS * I * 2);
-          tma_3d_hint(dst, &p.tm_wd, 0, e * d + r0, 0, fb, pol);
-        } else {
-          mbar_expect_tx(fb, (uint32_t)rows * I * 2);
-          for (int r = 0; r < rows; ++r) bulk_g2s(dst + r * rsd, wd + ((size_t)e * d + r0 + r) * I, I * 2, fb);
+        for (int sl = 0; sl < DS; ++sl, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, p.ws.err, DFV_DEVERR_SLOT_WAIT, &s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * s, dst = sbase + s * stage_bytes;
+          if (p.tma_mode) {  // one box of RS rows (rows past d are zero-filled and counted)
+            mbar_expect_tx(fb, (uint32_t)RS * Ih * 2);
+            tma_3d_hint(dst, &p.tm_wd, 0, e * d + r0, sl * (Ih / 64), fb, pol);
+          } else {
+            mbar_expect_tx(fb, (uint32_t)rows * Ih * 2);
+            for (int r = 0; r < rows; ++r)
+              bulk_g2s(dst + r * rsd, wd + ((size_t)e * d + r0 + r) * I + (size_t)sl * Ih, Ih * 2, fb);
+          }
         }
       }
       drain_stages(full0, it, S, p.ws.err);
@@ -305,12 +316,12 @@ __global__ void __launch_bounds__(kTmaThreads, 2) down_tma_kernel(const __grid_c
   const int rtiles = RS / 16;                   // row tiles per unit (2 or 1)
   const int kparts = kConsumerWarps / rtiles;   // k parts (4 or 8)
   const int rw = warp % rtiles, kq = warp / rtiles;
-  const int C = I / 32;
-  const int c0 = kq * C / kparts, c1 = (kq + 1) * C / kparts;
+  const int Cs = Ih / 32;  // 32-column chunks per stage
+  const int c0 = kq * Cs / kparts, c1 = (kq + 1) * Cs / kparts;
   const int cpr = I / 8;
   int cur = -1, m = 0, off = 0, it = 0;
   bool dead = false;  // after a failed wait: keep the barrier schedule, skip the work
-  for (int u = lo; u < hi; ++u, ++it) {
+  for (int u = lo; u < hi; ++u) {
     const int wi = u / tiles, dt = u % tiles, r0 = dt * RS;
     const int rows = min(RS, d - r0);
     if (wi != cur) {
@@ -337,37 +348,39 @@ __global__ void __launch_bounds__(kTmaThreads, 2) down_tma_kernel(const __grid_c
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
 
-    const int s = it % S;
-    if (!dead && !mbar_wait(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
-    const uint32_t st = sbase + s * stage_bytes;
-    if (!dead && rw * 16 < rows) {
-      for (int ch = c0; ch < c1; ++ch) {
-        const uint32_t q16 = (ch * 4 + c) * 16;
-        uint32_t o0, o1;
-        if (p.tma_mode) {
-          const uint32_t x = (uint32_t)(ch * 4 + c);
-          o0 = (x >> 3) * (uint32_t)(RS * 128) + (rw * 16 + pr) * 128u + (((x & 7u) ^ pr) << 4);
-          o1 = o0 + 1024u;
-        } else {
-          o0 = (rw * 16 + g) * rsd + q16;
-          o1 = (rw * 16 + g + 8) * rsd + q16;
-        }
-        const uint4 a0 = lds128(st + o0);
-        const uint4 a1 = lds128(st + o1);
+    for (int sl = 0; sl < DS; ++sl, ++it) {
+      const int s = it % S;
+      if (!dead && !mbar_wait(full0 + 8 * s, (it / S) & 1, p.ws.err, DFV_DEVERR_STAGE_WAIT, &s_abort)) dead = true;
+      const uint32_t st = sbase + s * stage_bytes;
+      if (!dead && rw * 16 < rows) {
+        for (int ch = c0; ch < c1; ++ch) {
+          const uint32_t ql = (uint32_t)(ch * 4 + c);                  // 16-byte piece within the stage
+          const uint32_t q16 = (uint32_t)((sl * Cs + ch) * 4 + c) * 16;  // and within the h row
+          uint32_t o0, o1;
+          if (p.tma_mode) {
+            o0 = (ql >> 3) * (uint32_t)(RS * 128) + (rw * 16 + pr) * 128u + (((ql & 7u) ^ pr) << 4);
+            o1 = o0 + 1024u;
+          } else {
+            o0 = (rw * 16 + g) * rsd + ql * 16;
+            o1 = (rw * 16 + g + 8) * rsd + ql * 16;
+          }
+          const uint4 a0 = lds128(st + o0);
+          const uint4 a1 = lds128(st + o1);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          if (nt * 8 < m) {
-            const int row = nt * 8 + g;
-            uint4 bh = make_uint4(0u, 0u, 0u, 0u);
-            if (row < m) bh = lds128(hhb + row * rsh + q16);
-            mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bh.x, bh.y);
-            mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bh.z, bh.w);
+          for (int nt = 0; nt < NT; ++nt) {
+            if (nt * 8 < m) {
+              const int row = nt * 8 + g;
+              uint4 bh = make_uint4(0u, 0u, 0u, 0u);
+              if (row < m) bh = lds128(hhb + row * rsh + q16);
+              mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, bh.x, bh.y);
+              mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, bh.z, bh.w);
+            }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
       *reinterpret_cast<float4 *>(red + ((warp * NT + nt) * 32 + lane) * 4) =
@@ -420,17 +433,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char *why, size_t why_len);
 // gate and up viewed as [d/64][E*I rows][64 columns], box {64, 8, ks/64}; down
 // as [d_ff/64][E*d rows][64 columns], box {64, rs, d_ff/64}; cached per
 // (weights, shape).  Mode 0 when any of them cannot be encoded.
-void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks, int rs) {
+void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks, int rs, int dsl) {
   struct Maps {
     int mode;
     CUtensorMap wg, wu, wd;
   };
   static std::mutex mu;
-  static std::map<std::tuple<const void *, const void *, const void *, int, int, int, int, int>, Maps> cache;
+  static std::map<std::tuple<const void *, const void *, const void *, int, int, int, int, int, int>, Maps> cache;
   p->tma_mode = 0;
   const int d = L->d, I = L->d_ff, E = L->n_experts + (L->n_shared ? 1 : 0), kst = ks;
   if (d % 64 || ks % 64 || ks / 64 > 256) return;
-  const auto key = std::make_tuple(L->w_gate, L->w_up, L->w_down, d, I, E, kst, rs);
+  const auto key = std::make_tuple(L->w_gate, L->w_up, L->w_down, d, I, E, kst, rs, dsl);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -455,17 +468,18 @@ void ffn_tensor_maps(FfnParams *p, const dfv_moe_layer *L, int ks, int rs) {
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    // the down rows: [d_ff/64][rs rows][64 columns], box {64, rs, d_ff/64}
+    // the down rows: [d_ff/64][rs rows][64 columns], box {64, rs, d_ff/64/dsl}
     auto encd = [&](CUtensorMap *map, const void *base) {
       const cuuint64_t dims[3] = {64, (cuuint64_t)E * d, (cuuint64_t)I / 64};
       const cuuint64_t strides[2] = {(cuuint64_t)I * 2, 128};
-      const cuuint32_t box[3] = {64, (cuuint32_t)rs, (cuuint32_t)I / 64};
+      const cuuint32_t box[3] = {64, (cuuint32_t)rs, (cuuint32_t)(I / 64 / dsl)};
       const cuuint32_t es[3] = {1, 1, 1};
       return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    if (I % 64 == 0 && I / 64 <= 256 && enc(&m.wg, L->w_gate) && enc(&m.wu, L->w_up) && encd(&m.wd, L->w_down))
+    if (I % (64 * dsl) == 0 && I / 64 <= 256 && enc(&m.wg, L->w_gate) && enc(&m.wu, L->w_up) &&
+        encd(&m.wd, L->w_down))
       m.mode = 1;
   }
   std::lock_guard<std::mutex> lock(mu);
@@ -518,20 +532,24 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan) {
   // two-token-tile buffers (the choice depends on the shape only, not on k);
   // else one CTA per SM with 32-row units when they fit
   const size_t hb2 = (size_t)2 * 8 * pad_host(I * 2);
-  int rs = 16, per_sm = 2;
+  int rs = 16, per_sm = 2, dsl = 1;
   size_t budget = half;
   if (1024 + (size_t)2 * rs * pad_host(I * 2) + hb2 + redb2 + 32 > half) {
-    per_sm = 1;
-    budget = kSmemBudget;
-    for (rs = 32; rs >= 16; rs /= 2)
-      if ((size_t)2 * rs * pad_host(I * 2) + hb2 + redb2 + 32 <= kSmemBudget) break;
-    if (rs < 16) return false;
+    if (I % 128 == 0 && 1024 + (size_t)2 * rs * pad_host(I) + hb2 + redb2 + 32 <= half) {
+      dsl = 2;  // half of d_ff per stage keeps two CTAs per SM
+    } else {
+      per_sm = 1;
+      budget = kSmemBudget;
+      for (rs = 32; rs >= 16; rs /= 2)
+        if ((size_t)2 * rs * pad_host(I * 2) + hb2 + redb2 + 32 <= kSmemBudget) break;
+      if (rs < 16) return false;
+    }
   }
   const size_t hb = (size_t)NT * 8 * pad_host(I * 2);
   int Sd = 4;
   size_t smd = 0;
   for (; Sd >= 2; --Sd) {
-    smd = 1024 + (size_t)Sd * rs * pad_host(I * 2) + hb + redb + 16 * Sd;
+    smd = 1024 + (size_t)Sd * rs * pad_host(I * 2 / dsl) + hb + redb + 16 * Sd;
     if (smd <= budget) break;
   }
   if (Sd < 2) return false;
@@ -542,6 +560,7 @@ bool tma_plan(int w_dtype, int k, int d, int I, TmaPlan *plan) {
   plan->stages_d = Sd;
   plan->down_per_sm = per_sm;
   plan->gate_per_sm = gper;
+  plan->dsl = dsl;
   plan->smem_g = smg;
   plan->smem_d = smd;
   return true;
@@ -592,8 +611,11 @@ cudaError_t launch_ffn_tma(const FfnParams &p0, int w_dtype, int phase, const Tm
     return cudaLaunchKernelEx(&cfg, combine_kernel, p);
   }
   p.stages = plan.stages_d;
-  return p.k <= 8 ? launch_tma(down_tma_kernel<1>, grid, plan.smem_d, p, s, pdl)
-                  : launch_tma(down_tma_kernel<2>, grid, plan.smem_d, p, s, pdl);
+  if (plan.dsl == 2)
+    return p.k <= 8 ? launch_tma(down_tma_kernel<1, 2>, grid, plan.smem_d, p, s, pdl)
+                    : launch_tma(down_tma_kernel<2, 2>, grid, plan.smem_d, p, s, pdl);
+  return p.k <= 8 ? launch_tma(down_tma_kernel<1, 1>, grid, plan.smem_d, p, s, pdl)
+                  : launch_tma(down_tma_kernel<2, 1>, grid, plan.smem_d, p, s, pdl);
 }
 
 }  // namespace dfv

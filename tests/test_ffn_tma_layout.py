@@ -135,14 +135,20 @@ def test_gateup_slice_depends_on_the_shape_only(d):
 
 
 def down_plan(I):
-    """The down part of ffn_tma.cu's tma_plan: rows per unit, chosen for two token tiles
-    (16 rows and two CTAs per SM when half the budget holds two stages, else 32 or 16 rows)."""
+    """The down part of ffn_tma.cu's tma_plan, chosen for two token tiles:
+    (rows per unit, CTAs per SM, stages per unit).  16 rows and two CTAs per SM when
+    half the budget holds two full-d_ff stages; else, for d_ff a multiple of 128,
+    two CTAs per SM with two half-d_ff stages per unit; else one CTA per SM with 32
+    or 16 rows."""
+    half = SMEM_BUDGET // 2 + 1024
     redb2, hb2 = CONSUMER_WARPS * 2 * 32 * 16, 2 * 8 * pad(I * 2)
-    if 1024 + 2 * 16 * pad(I * 2) + hb2 + redb2 + 32 <= SMEM_BUDGET // 2 + 1024:
-        return 16
+    if 1024 + 2 * 16 * pad(I * 2) + hb2 + redb2 + 32 <= half:
+        return 16, 2, 1
+    if I % 128 == 0 and 1024 + 2 * 16 * pad(I) + hb2 + redb2 + 32 <= half:
+        return 16, 2, 2
     for rs in (32, 16):
         if 2 * rs * pad(I * 2) + hb2 + redb2 + 32 <= SMEM_BUDGET:
-            return rs
+            return rs, 1, 1
     return None
 
 
@@ -150,17 +156,19 @@ def down_plan(I):
 @pytest.mark.parametrize("k", [1, 16])
 def test_down_plan_fits_its_ctas_per_sm(I, k):
     """Two CTAs per SM only where both fit: the stages, h rows, reduction buffer and
-    alignment slack of one CTA within half of the budget (and 227 KB per SM)."""
-    rs = down_plan(I)
-    two = 1024 + 2 * 16 * pad(I * 2) + 2 * 8 * pad(I * 2) + CONSUMER_WARPS * 2 * 32 * 16 + 32 <= SMEM_BUDGET // 2 + 1024
+    alignment slack of one CTA within half of the budget (and 227 KB per SM).  The
+    plan depends on the shape only (k = 1 and 16 agree), and every measured shape
+    keeps two CTAs per SM: full-d_ff stages up to d_ff = 1024, half-d_ff above."""
+    rs, per_sm, dsl = down_plan(I)
     NT = 1 if k <= 8 else 2
     hb, redb = NT * 8 * pad(I * 2), CONSUMER_WARPS * NT * 32 * 16
-    budget = SMEM_BUDGET // 2 + 1024 if two else SMEM_BUDGET
-    S = next(S for S in (4, 3, 2) if 1024 + S * rs * pad(I * 2) + hb + redb + 16 * S <= budget)
-    smem = 1024 + S * rs * pad(I * 2) + hb + redb + 16 * S
+    budget = SMEM_BUDGET // 2 + 1024 if per_sm == 2 else SMEM_BUDGET
+    S = next(S for S in (4, 3, 2) if 1024 + S * rs * pad(I * 2 // dsl) + hb + redb + 16 * S <= budget)
+    smem = 1024 + S * rs * pad(I * 2 // dsl) + hb + redb + 16 * S
     assert S >= 2 and smem <= budget
-    if two:
-        assert rs == 16 and 2 * (smem + 1024) <= 228 * 1024  # + the per-CTA reserve
+    assert per_sm == 2 and rs == 16 and 2 * (smem + 1024) <= 228 * 1024  # + the per-CTA reserve
+    assert dsl == (1 if I <= 1024 else 2)
+    assert (rs * (I // dsl) * 2) % 1024 == 0  # swizzled stages stay 1024-aligned
 
 
 def down_offset(rw, g, c, ch, rs, upper):
@@ -174,26 +182,33 @@ def down_offset(rw, g, c, ch, rs, upper):
 
 @pytest.mark.parametrize("I", [768, 1024, 1408, 1536])
 def test_swizzled_down_fragment_addresses(I):
-    rs = down_plan(I)
-    assert rs is not None and I % 64 == 0 and I // 64 <= 256
+    """Every lane's fragment offset in a down stage holds the weight row and the
+    d_ff columns its MMA slot expects; with half-d_ff stages the columns of stage
+    sl start at sl * I / 2, and the token (h) piece the lane reads is the same
+    global column.  A quarter-warp's loads cover all eight 16-byte bank groups."""
+    rs, _, dsl = down_plan(I)
+    Ih = I // dsl
+    assert Ih % 64 == 0 and Ih // 64 <= 256
     rtiles, kparts = rs // 16, CONSUMER_WARPS // (rs // 16)
-    where = {}
-    for z in range(I // 64):  # the box {64, rs, I/64} as rs-row segments, swizzled per 8-row atom
-        for r in range(rs):
-            for b in range(0, 128, 16):
-                off = z * rs * 128 + r * 128 + ((((b >> 4) ^ (r & 7)) << 4))
-                where[off] = (r, z * 64 + b // 2)
-    assert len(where) == rs * I // 8 and (rs * 128) % 1024 == 0
-    C = I // 32
-    for w in range(CONSUMER_WARPS):
-        rw, kq = w % rtiles, w // rtiles
-        for ch in range(kq * C // kparts, (kq + 1) * C // kparts):
-            for upper in (0, 1):
-                offs = []
-                for lane in range(32):
-                    g, c = lane >> 2, lane & 3
-                    o = down_offset(rw, g, c, ch, rs, upper)
-                    assert where[o] == (rw * 16 + 8 * upper + stored_row(g), ch * 32 + c * 8)
-                    offs.append(o)
-                for q in range(4):
-                    assert len({(o // 16) % 8 for o in offs[8 * q:8 * q + 8]}) == 8
+    for sl in range(dsl):
+        where = {}
+        for z in range(Ih // 64):  # the box {64, rs, Ih/64} at z = sl * Ih/64, swizzled per 8-row atom
+            for r in range(rs):
+                for b in range(0, 128, 16):
+                    off = z * rs * 128 + r * 128 + ((((b >> 4) ^ (r & 7)) << 4))
+                    where[off] = (r, sl * Ih + z * 64 + b // 2)
+        assert len(where) == rs * Ih // 8 and (rs * 128) % 1024 == 0
+        Cs = Ih // 32
+        for w in range(CONSUMER_WARPS):
+            rw, kq = w % rtiles, w // rtiles
+            for ch in range(kq * Cs // kparts, (kq + 1) * Cs // kparts):
+                for upper in (0, 1):
+                    offs = []
+                    for lane in range(32):
+                        g, c = lane >> 2, lane & 3
+                        o = down_offset(rw, g, c, ch, rs, upper)
+                        h_piece = (sl * Cs + ch) * 4 + c  # 16-byte piece of the h row
+                        assert where[o] == (rw * 16 + 8 * upper + stored_row(g), h_piece * 8)
+                        offs.append(o)
+                    for q in range(4):
+                        assert len({(o // 16) % 8 for o in offs[8 * q:8 * q + 8]}) == 8
