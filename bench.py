@@ -52,11 +52,11 @@ KERNEL_SOURCES = {
 # kernel -> (source hash, dram read+write bytes of one captured launch, algorithmic bytes of that launch);
 # the captures and their commands are summarised under profiles/ (one file per kernel and workload)
 NCU_TRAFFIC = {
-    "moe_fused_kernel": ("c19e2c6b8fa07d1d", 727464704 + 4395776, 77 * 9437184 + 524288),
-    "moe_fused_kernel_shared": ("c19e2c6b8fa07d1d", 647158528 + 4748800, 102 * 6291456 + 1048576),
-    "moe_fused_bs_kernel_mxfp4": ("3bfa5f16616c3b09", 171722752 + 4392960, 102 * 1671168 + 1048576),
-    "moe_fused_bs_kernel_q8": ("3bfa5f16616c3b09", 342162944 + 4491520, 102 * 3342336 + 1048576),
-    "tc_group_kernel_gateup": ("ac9079195f87f791", 822142208 + 3482624, 128 * 6291456),
+    "moe_fused_kernel": ("8cafc0fbfcdc4fea", 727380480 + 4437504, 77 * 9437184 + 524288),
+    "moe_fused_kernel_shared": ("8cafc0fbfcdc4fea", 647156736 + 5038336, 102 * 6291456 + 1048576),
+    "moe_fused_bs_kernel_mxfp4": ("934bcf6738e1707c", 171702016 + 4564224, 102 * 1671168 + 1048576),
+    "moe_fused_bs_kernel_q8": ("934bcf6738e1707c", 342161920 + 4358144, 102 * 3342336 + 1048576),
+    "tc_group_kernel_gateup": ("39054c6688135d8c", 822216960 + 3193088, 128 * 6291456),
 }
 
 
