@@ -7,6 +7,8 @@ drawn without near-ties (gap between the K-th and (K+1)-th router logit at
 least 1e-3), so the routing decision is robust to summation order."""
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -209,6 +211,25 @@ def test_block_rows_equal_single_token_calls(dfv, a3b, path):
     for t in range(16):
         row = dfv.moe_block_forward(L, x[t:t + 1].contiguous(), ws)
         assert torch.equal(row[0], blk[t]), "row %d differs" % t
+
+
+@pytest.mark.parametrize("norm_topk", [1, 0])
+def test_route_topk_rows_equal_single_row_calls(dfv, norm_topk):
+    """The routing launch has 512 threads for k > 8 (a warp per row in its top-K
+    tail) and 256 for k <= 8; a row's experts and weights must not depend on
+    which one ran it, nor on the other rows of the block."""
+    s = dataclasses.replace(inputs.A3B, n_experts=256, d_ff=64, norm_topk=norm_topk)  # routing only
+    lw = inputs.make_layer(s, seed=21, device="cuda")
+    L = dfv.Layer(lw)
+    ws = dfv.alloc_workspace(dfv.workspace_size(L, 16))
+    x = inputs.make_hidden(16, s.d, "bf16", seed=22, device="cuda")
+    blk = dfv.route_topk(L, x, ws)
+    idx, w = blk["topk_idx"].clone(), blk["topk_w"].clone()
+    for k in (1, 8, 9):
+        part = dfv.route_topk(L, x[:k].contiguous(), ws)
+        assert torch.equal(part["topk_idx"], idx[:k]), k
+        assert torch.equal(part["topk_w"], w[:k]), k
+    assert dfv.read_device_error(ws) == 0
 
 
 def test_identical_rows_wake_one_set(dfv, a3b):
